@@ -1,0 +1,359 @@
+#!/usr/bin/env python
+"""Training-step throughput of the B300 GPT-2 library (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one whole training step -- forward of every layer, fused softmax +
+cross-entropy, zero_grad, backward of every layer, AdamW over the flat buffer -- on
+one fresh batch of the GPT-2 124M bf16 workload (B=16, T=1024, 16384 tokens, Zipf
+s=1.1 token stream, lr 6e-4, wd 0.1).  Weights are random-init from the seeded
+recipe; batches are synthetic and resident in HBM before timing starts.
+
+For N > 1 (torchrun) every rank trains its own replica on its own data (weak
+scaling, no collective): the data-parallel gradient exchange is not built, because
+every run of this library has one GPU.  ``--impl reference`` times the CPU oracle (the
+deliberately slow plain program) on the host cores, on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gpt2_124m_bf16_b16_t1024"
+METRIC = "GPT-2 124M train tokens/sec (fwd+bwd+AdamW) on 1 B300; MFU; kernel % roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ------------------------------------------------------------------------ model flops
+def mfu_flops_per_token(shape, T):
+    """6N + 12 L C T per token, N = real parameter count (V token rows)."""
+    C, L = shape.channels, shape.num_layers
+    N = (shape.vocab_size * C + shape.max_seq_len * C
+         + L * (12 * C * C + 13 * C) + 2 * C)
+    return 6.0 * N + 12.0 * L * C * T, N
+
+
+# ------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------ CPU oracle leg
+def oracle_tokens_per_s(w, sample_B, sample_T, steps, warmup=0, seed_offset=0):
+    """Time the CPU oracle (float32, as the pages' program) on a bounded sample of the
+    workload: `steps` whole training steps at (sample_B, sample_T)."""
+    import numpy as np
+    from oracle import gpt2_oracle as O
+    from step_gpt_train_03_b300 import synth
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    o = O.from_shape(w.shape, np.float32)
+    o.keep_preatt = False
+    o.load(synth.init_params(w.shape, w.seed))
+    batches = synth.zipf_batches(w.shape.vocab_size, sample_B, sample_T, warmup + steps, w.seed + 100 + seed_offset)
+    per = []
+    for i, (tok, tgt) in enumerate(batches):
+        t0 = time.perf_counter()
+        o.step(tok, tgt, w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, i + 1)
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            per.append(dt)
+    total = sum(per)
+    return sample_B * sample_T * len(per) / total, cores, total, per
+
+
+def reference_arm(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from step_gpt_train_03_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    sB, sT = 1, 512
+    tps, cores, total, per = oracle_tokens_per_s(w, sB, sT, args.steps, args.warmup)
+    sample = (f"{args.steps} timed whole steps (after {args.warmup} warm-up) of the fp32 CPU oracle "
+              f"on the {w.name} model at B={sB}, T={sT} ({sB * sT} tokens each)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / len(per),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Zipf s=1.1 token stream, random-init weights)",
+        "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.T, "parallelism": "none (CPU)"},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ our arm
+def ours(args):
+    import numpy as np
+    import torch
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    from step_gpt_train_03_b300 import build, synth
+    if rank == 0:
+        build.build()
+    barrier()
+    from step_gpt_train_03_b300 import gpt2lib as G
+
+    w = synth.WORKLOADS[args.workload]
+    B, T = w.B, w.T
+    BT = B * T
+    stream = torch.cuda.Stream()
+    m = G.GPT2(w.shape, B, T, "bf16", stream=stream)
+    m.load_params(synth.init_params(w.shape, w.seed))
+    n_batches = args.warmup + args.steps
+    host = synth.zipf_batches(w.shape.vocab_size, B, T, n_batches, w.seed + 7919 * rank)
+    toks = torch.as_tensor(np.stack([b[0] for b in host])).cuda()
+    tgts = torch.as_tensor(np.stack([b[1] for b in host])).cuda()
+    hp = (w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    torch.cuda.synchronize()
+
+    def step(i, t):
+        m.forward(toks[i], tgts[i], want_loss=False)
+        m.zero_grad()
+        m.backward()
+        m.update(*hp, t)
+
+    # warm-up, traced in full to get every kernel class's share of the step
+    G.profile_enable(None)
+    G.profile_reset()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, i + 1)
+    stream.synchronize()
+    m.check()
+    warm_prof = G.profile_read()
+    G.profile_reset()
+    shares = {k: v["ms"] for k, v in warm_prof.items()}
+    total_ms = sum(shares.values()) or 1.0
+    # the dominant kernel: the class family with the largest traced time
+    families = {"matmul": ["matmul_forward", "matmul_backward_dx", "matmul_backward_dw"]}
+    fam_ms = {"matmul": sum(shares[c] for c in families["matmul"])}
+    for c, v in shares.items():
+        if c not in families["matmul"]:
+            fam_ms[c] = v
+    dominant = max(fam_ms, key=fam_ms.get)
+    dom_classes = families.get(dominant, [dominant])
+    G.profile_enable(dom_classes)     # live tracing of the dominant kernel only
+
+    clocks = ClockSampler(local_rank)
+    launches0 = G.kernel_launches()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(args.warmup + i, args.warmup + i + 1)
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = G.kernel_launches() - launches0
+    ms = start.elapsed_time(end)
+    m.check()
+    live = G.profile_read()
+    G.profile_enable([])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = BT * args.steps * world / (ms / 1000.0)
+
+    # end-to-end through the public step call: pinned host tokens in, loss out, per step
+    e2e = None
+    if not args.no_e2e:
+        th = torch.as_tensor(np.stack([b[0] for b in host])).pin_memory()
+        gh = torch.as_tensor(np.stack([b[1] for b in host])).pin_memory()
+        m.set_stream(stream)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            m.step_host(th[args.warmup + i], gh[args.warmup + i], *hp, n_batches + i + 1)
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": BT * args.steps * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * BT * 4, "d2h_bytes_per_step": 4,
+               "call": "gpt2_step_host"}
+
+    if rank != 0:
+        return 0
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        src = "measured"
+    except OSError:
+        peaks = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+        src = "fallback"
+    d_ms = sum(live[c]["ms"] for c in dom_classes)
+    d_n = sum(live[c]["launches"] for c in dom_classes)
+    d_fl = sum(live[c]["flops"] for c in dom_classes)
+    d_by = sum(live[c]["bytes"] for c in dom_classes)
+    if d_fl > 0:
+        achieved = d_fl / (d_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{src} bf16 sustained (kernel timed inside a long step)",
+                "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
+                "share_of_traced_step": fam_ms[dominant] / total_ms}
+    else:
+        achieved = d_by / (d_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy bandwidth",
+                "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
+                "share_of_traced_step": fam_ms[dominant] / total_ms}
+    fpt, nparams = mfu_flops_per_token(w.shape, T)
+    step_s = ms / 1000.0 / args.steps
+    mfu = fpt * BT / step_s / 1e12
+    kernels = {k: {"ms_per_step": v["ms"] / max(args.warmup, 1),
+                   "share": v["ms"] / total_ms,
+                   "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
+                   "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["bytes"] and v["ms"] else None}
+               for k, v in warm_prof.items() if v["launches"]}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        sB, sT = 1, 1024
+        tps, cores, total, per = oracle_tokens_per_s(w, sB, sT, 1)
+        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"one whole step (fwd+bwd+AdamW) of the fp32 CPU oracle on the {w.name} model "
+                         f"at B={sB}, T={sT} ({sB * sT} tokens), {total:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Zipf s=1.1 int32 token stream, fresh batch per step; random-init weights)",
+        "config": {"workload": w.name, "model": "GPT-2 124M (L=12, C=768, NH=12, V=50257 padded to 50304)",
+                   "global_batch": B * world, "seq_len": T,
+                   "parallelism": "replicas only" if world > 1 else "single GPU",
+                   "precision": "bf16 weights/activations, fp32 master weights and AdamW state",
+                   "l2": "no flush: the step's working set (GBs of activations) is far larger than the 126 MB L2"},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "mfu": {"model_flops_per_step": fpt * BT, "num_parameters": nparams,
+                "tflops": mfu, "vs_measured_burst": mfu / peaks["bf16_tflops"],
+                "vs_measured_sustained": mfu / peaks["bf16_tflops_sustained"]},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,242 @@
+/*
+ * gpt2.h -- C ABI of the B300 (sm_103a) GPT-2 training-step library.
+ *
+ * The library runs the training step that the llm.c pages describe, on one GPU:
+ *   ujoy.net llm.c article, section "用C语言实现LLM" (implementing an LLM in C):
+ *     memory is allocated once, as one 1-D block, and every tensor points into it;
+ *     nothing is created or freed while training; each layer (encoder, layernorm,
+ *     matmul, self-attention, GELU, residual, softmax, cross-entropy) has a forward
+ *     and a backward pass written by hand, and the layers are chained together.
+ *   same article, section "训练过程" (training run): forward, backward and an Adam
+ *     update chained into one loop ("Adam lr 1e-4").
+ *   yinghuohong.cn llm.c article, section "脚动完成每一个层前向/反向流传": all memory
+ *     allocated at the start, constant footprint, weights and activations both point
+ *     into flat arrays.
+ *
+ * Conventions for every entry point
+ *   - Device pointers are plain CUDA device addresses on the current device; host
+ *     pointers are plain host addresses.  No PyTorch types cross this boundary.
+ *   - The caller owns every byte of device memory.  gpt2_build carves the one
+ *     workspace the caller passes; the library allocates no device memory at all
+ *     (it keeps a small host struct and, in bf16 mode, TMA descriptors).
+ *   - All work is enqueued on the handle's CUDA stream (set at build, changeable with
+ *     gpt2_set_stream) and is asynchronous unless stated otherwise.
+ *   - Every call returns a status code (GPT2_OK = 0).  Device-side faults the kernels
+ *     detect themselves (an out-of-range token id, a bounded wait that ran out, a
+ *     non-finite loss) are latched in a device error word and reported by the next
+ *     synchronising call (gpt2_forward with loss_out, gpt2_check).
+ *   - Matrices are row-major.  A linear layer's weight is stored (out, in) and computes
+ *     y = x W^T + b.  Activations are (B, T, C) row-major, token-major.
+ *
+ * Model (readings of the pages, pinned by the printed num_parameters 124439808 and
+ * num_activations 73323776): GPT-2 pre-LN blocks, learned position table, biases on
+ * every linear layer, LM head tied to the token table, layernorm eps 1e-5 (biased
+ * variance), tanh-form GELU, causal attention scaled by 1/sqrt(C/NH), mean
+ * cross-entropy over the V real vocabulary columns (padded columns are excluded and
+ * get zero gradient), AdamW with bias correction and decoupled weight decay on every
+ * parameter.
+ */
+#ifndef GPT2_B300_H
+#define GPT2_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int max_seq_len;        /* rows of the position table (maxT) */
+    int vocab_size;         /* V: real vocabulary */
+    int padded_vocab_size;  /* Vp >= V: rows of the token table; rows >= V stay zero */
+    int num_layers;         /* L */
+    int num_heads;          /* NH; channels % num_heads == 0 */
+    int channels;           /* C; a multiple of 64 */
+} GPT2Config;
+
+/* Arithmetic of the step.
+ * GPT2_FP32: fp32 activations and weights; every product and sum in fp32 (SIMT FMA).
+ * GPT2_BF16: bf16 weights (a shadow of the fp32 master copy), bf16 activations and
+ *            activation grads; matmuls and attention on the tcgen05 tensor cores with
+ *            fp32 accumulation; fp32 master weights, parameter grads, AdamW state,
+ *            layernorm statistics, softmax/loss arithmetic. */
+enum { GPT2_FP32 = 0, GPT2_BF16 = 1 };
+
+enum {
+    GPT2_OK = 0,
+    GPT2_EINVAL = 1,       /* bad argument: null pointer, size out of range, misalignment */
+    GPT2_ESTATE = 2,       /* call out of order, e.g. backward without a forward with targets */
+    GPT2_ECUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    GPT2_ETOKEN = 4,       /* a token or target id outside [0, V) (its rows were zeroed) */
+    GPT2_ENONFINITE = 5,   /* the mean loss was NaN or Inf */
+    GPT2_ETIMEOUT = 6,     /* a bounded device-side wait ran out; the kernel gave up */
+    GPT2_ENOMEM = 7,       /* the workspace passed to gpt2_build is too small */
+    GPT2_EUNSUPPORTED = 8  /* shape or precision this build does not implement */
+};
+
+/* Names of the 16 parameter tensors, in the order of the flat buffer:
+ *  0 wte (Vp,C)   1 wpe (maxT,C)
+ *  2 ln1w (L,C)   3 ln1b (L,C)   4 qkvw (L,3C,C)    5 qkvb (L,3C)
+ *  6 attprojw (L,C,C)   7 attprojb (L,C)   8 ln2w (L,C)   9 ln2b (L,C)
+ * 10 fcw (L,4C,C)  11 fcb (L,4C)  12 fcprojw (L,C,4C)  13 fcprojb (L,C)
+ * 14 lnfw (C)  15 lnfb (C)
+ * Each tensor starts on a 64-element boundary of the flat buffer; the gap elements are
+ * zero and stay zero. */
+#define GPT2_NUM_PARAM_TENSORS 16
+
+typedef struct GPT2 GPT2;
+
+/* Bytes of device workspace gpt2_build needs for this model, batch limits and
+ * precision.  Returns GPT2_EINVAL for an unsupported shape. */
+int gpt2_workspace_bytes(const GPT2Config* cfg, int max_B, int max_T, int precision,
+                         size_t* bytes);
+
+/* Carve `workspace` (device, >= gpt2_workspace_bytes, 1024-byte aligned) into the flat
+ * parameter, gradient, AdamW-moment and activation buffers and return a handle in *out.
+ * The parameters are zeroed; upload the initial weights into gpt2_params() and call
+ * gpt2_sync_params().  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * Synchronises the stream once.  The workspace must outlive the handle. */
+int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int precision,
+               void* workspace, size_t workspace_bytes, void* stream, GPT2** out);
+
+/* Release the host-side handle (the workspace stays the caller's). */
+void gpt2_free(GPT2* model);
+
+int gpt2_set_stream(GPT2* model, void* stream);
+
+/* Parameter counts: n_real counts the tensors with V token rows (the pages' count);
+ * n_flat is the length of the flat buffers (padded vocabulary and alignment gaps). */
+int gpt2_num_parameters(const GPT2* model, size_t* n_real, size_t* n_flat);
+
+/* Element offset of tensor `index` (0..15, order above) in the flat buffers, and its
+ * element count. */
+int gpt2_param_tensor(const GPT2* model, int index, size_t* offset, size_t* numel);
+
+/* Device pointers to the flat fp32 buffers (n_flat elements each). */
+float* gpt2_params(GPT2* model);     /* master weights; write the initial values here */
+float* gpt2_grads(GPT2* model);      /* parameter gradients */
+float* gpt2_adam_m(GPT2* model);
+float* gpt2_adam_v(GPT2* model);
+
+/* After writing gpt2_params(): refresh the bf16 shadow weights (bf16 mode; a no-op in
+ * fp32 mode) and clear the AdamW moments. */
+int gpt2_sync_params(GPT2* model);
+
+/* Forward pass of every layer over tokens (device int32, (B,T) row-major, ids in
+ * [0,V)).  With targets (device int32, (B,T)) it also computes the per-position
+ * cross-entropy, the mean loss, and -- fused with the softmax -- the gradient of the
+ * mean loss with respect to the logits, which backward consumes.  With
+ * targets == NULL only the logits are produced (gpt2_logits) and backward is refused.
+ * B <= max_B, 1 <= T <= min(max_T, max_seq_len).  The token ids are copied into the
+ * workspace, so the caller's buffers may be reused once the call returns.
+ * loss_out (host, nullable): if given, the call synchronises the stream and stores
+ * the mean loss (or -1 without targets); it then also returns any latched device
+ * error.  Without it, no synchronisation happens (the loss stays in gpt2_loss()). */
+int gpt2_forward(GPT2* model, const int32_t* tokens, const int32_t* targets, int B, int T,
+                 float* loss_out);
+
+/* Set every parameter gradient to zero. */
+int gpt2_zero_grad(GPT2* model);
+
+/* Backward pass of every layer in reverse order; adds d(mean loss)/d(param) into the
+ * gradient buffer.  Needs a preceding gpt2_forward with targets (else GPT2_ESTATE). */
+int gpt2_backward(GPT2* model);
+
+/* One AdamW step over the whole flat buffer:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;  mhat = m/(1-b1^t);  vhat = v/(1-b2^t)
+ *   p -= lr (mhat / (sqrt(vhat) + eps) + weight_decay p)
+ * then (bf16 mode) refresh the bf16 shadow.  t >= 1 is the 1-based step count. */
+int gpt2_update(GPT2* model, float lr, float beta1, float beta2, float eps,
+                float weight_decay, int t);
+
+/* One whole training step from HOST token buffers: copies tokens/targets (pinned host
+ * memory recommended) to the device, runs forward, zero_grad, backward and update, and
+ * copies the mean loss back into *loss_out (host).  Synchronises the stream. */
+int gpt2_step_host(GPT2* model, const int32_t* tokens_host, const int32_t* targets_host,
+                   int B, int T, float lr, float beta1, float beta2, float eps,
+                   float weight_decay, int t, float* loss_out);
+
+/* Device pointers into the last forward's outputs: the mean loss (1 float), the
+ * per-position losses (B*T floats) and the logits (B*T rows of Vp entries, fp32 or bf16
+ * by precision; overwritten by d loss/d logits when targets were given). */
+float* gpt2_loss(GPT2* model);
+float* gpt2_losses(GPT2* model);
+void* gpt2_logits(GPT2* model);
+
+/* Synchronise the stream and return (then clear) the latched device error, if any. */
+int gpt2_check(GPT2* model);
+
+const char* gpt2_strerror(int status);
+
+/* The cudaError_t of the most recent failed CUDA call on this thread (0 if none). */
+int gpt2_last_cuda_error(void);
+
+/* ---------------------------------------------------------------------------------
+ * Single-layer entry points (same kernels as the model; used for per-layer tests and
+ * by callers that chain layers themselves).  All pointers are device pointers;
+ * `stream` is a cudaStream_t.
+ * ------------------------------------------------------------------------------- */
+
+/* Layernorm forward over N rows of C (C % 8 == 0, C <= 2048), fp32; N == 0 is a no-op:
+ *   mean = sum(x)/C; rstd = 1/sqrt(sum((x-mean)^2)/C + 1e-5); out = (x-mean) rstd w + b.
+ * out (N,C), mean (N), rstd (N) are written. */
+int gpt2_layernorm_forward(float* out, float* mean, float* rstd, const float* inp,
+                           const float* weight, const float* bias, int N, int C,
+                           void* stream);
+
+/* Scratch bytes gpt2_layernorm_backward needs for N rows of C. */
+size_t gpt2_layernorm_backward_scratch_bytes(int N, int C);
+
+/* Layernorm backward, fp32.  dinp += dx (accumulates); dweight += sum_rows dout*xhat;
+ * dbias += sum_rows dout.  The column sums are deterministic (fixed-order two-stage
+ * reduction through `scratch`, device, >= gpt2_layernorm_backward_scratch_bytes). */
+int gpt2_layernorm_backward(float* dinp, float* dweight, float* dbias, const float* dout,
+                            const float* inp, const float* weight, const float* mean,
+                            const float* rstd, int N, int C, void* scratch,
+                            size_t scratch_bytes, void* stream);
+
+/* Matmul forward: out (M,N) = inp (M,K) * weight(N,K)^T + bias (N, nullable).
+ * precision GPT2_FP32: all float*; GPT2_BF16: out, inp, weight, bias are bf16 (bias
+ * nullable), fp32 accumulation. */
+int gpt2_matmul_forward(void* out, const void* inp, const void* weight, const void* bias,
+                        int M, int N, int K, int precision, void* stream);
+
+/* Matmul backward: dinp (M,K) = dout (M,N) * weight (N,K)  [overwrites];
+ * dweight (N,K, fp32) += dout^T * inp;  dbias (N, fp32, nullable) += column sums of
+ * dout.  dout/inp/weight/dinp are float or bf16 by precision.  `scratch` (device,
+ * >= gpt2_matmul_backward_scratch_bytes) holds the deterministic column-sum partials. */
+size_t gpt2_matmul_backward_scratch_bytes(int M, int N);
+int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, const void* dout,
+                         const void* inp, const void* weight, int M, int N, int K,
+                         int precision, void* scratch, size_t scratch_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Observability: kernel-launch counter and per-kernel-class tracing.
+ * Tracing brackets every layer launch with two CUDA events on the stream the kernels go
+ * to and attributes the elapsed device time and the launch's algorithmic work (flops of
+ * a contraction, bytes of a memory-bound layer) to one of gpt2_profile_num_classes()
+ * classes (names from gpt2_profile_class_name).  The event pool is created by the first
+ * gpt2_profile_enable(1); no device memory is used.
+ * ------------------------------------------------------------------------------- */
+
+/* Kernels this library has launched in this process so far. */
+long long gpt2_kernel_launches(void);
+
+/* Trace the classes whose bit is set in class_mask (bit i = class i); 0 switches off. */
+int gpt2_profile_enable(unsigned class_mask);
+/* Wait for the recorded events and fold their times into the per-class totals. */
+int gpt2_profile_collect(void);
+/* Collect, then zero the totals. */
+int gpt2_profile_reset(void);
+/* Totals of class `cls` since the last reset: device ms, bracketed launches, flops, bytes. */
+int gpt2_profile_read(int cls, double* ms, long long* scopes, double* flops, double* bytes);
+/* Brackets skipped because the event pool was exhausted (collect more often). */
+long long gpt2_profile_dropped(void);
+int gpt2_profile_num_classes(void);
+const char* gpt2_profile_class_name(int cls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_H */

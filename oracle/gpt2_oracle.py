@@ -300,6 +300,9 @@ class GPT2Oracle:
         self.g = self._views(self.flat_grad)
         self.acts = None
         self.batch = None
+        # the pre-softmax scores are part of the pages' activation list but the backward
+        # does not read them; large runs may drop them to save host memory
+        self.keep_preatt = True
 
     def _views(self, flat):
         out, off = {}, 0
@@ -341,6 +344,8 @@ class GPT2Oracle:
             g = gelu_forward(fch)
             fcproj = matmul_forward(g, p["fcprojw"][l], p["fcprojb"][l])
             res3 = residual_forward(res2, fcproj)
+            if not self.keep_preatt:
+                preatt = None
             for k_, v_ in (("ln1", ln1), ("ln1_mean", m1), ("ln1_rstd", r1), ("qkv", qkv),
                            ("atty", atty), ("preatt", preatt), ("att", att),
                            ("attproj", attproj), ("residual2", res2), ("ln2", ln2),

@@ -1,0 +1,803 @@
+// GPT-2 training step on one B300: the C ABI of include/gpt2.h.
+//
+// Structure (ujoy.net llm.c article, section "用C语言实现LLM"; yinghuohong.cn llm.c
+// article, section "脚动完成每一个层前向/反向流传"): one block of memory, passed in by
+// the caller, carved once into the flat parameter / gradient / AdamW buffers and the
+// activation buffers; nothing is allocated afterwards.  Each layer has a hand-written
+// forward and backward kernel; gpt2_forward / gpt2_backward chain them, gpt2_update
+// runs AdamW over the flat buffer (same article, section "训练过程": forward, backward
+// and update chained into one loop).
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#include <algorithm>
+
+#include "../../include/gpt2.h"
+#include "common.cuh"
+#include "kernels_mem.cuh"
+#include "gemm_simt.cuh"
+#include "attention_simt.cuh"
+#include "gemm_tc.h"
+#include "attention_flash.h"
+#include "runtime.h"
+
+#define CK(x)                                                   \
+    do {                                                        \
+        cudaError_t e_ = (x);                                   \
+        if (e_ != cudaSuccess) { g_last_cuda_error = e_; return GPT2_ECUDA; } \
+    } while (0)
+
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// ------------------------------------------------------------------ handle
+enum { P_WTE = 0, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB, P_LN2W, P_LN2B,
+       P_FCW, P_FCB, P_FCPROJW, P_FCPROJB, P_LNFW, P_LNFB };
+
+struct GPT2 {
+    GPT2Config cfg;
+    int maxB, maxT, prec;
+    int L, C, NH, V, Vp;
+    size_t poff[GPT2_NUM_PARAM_TENSORS], pnum[GPT2_NUM_PARAM_TENSORS];
+    size_t n_flat, n_real;
+    char* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+    // flat parameter buffers
+    float *params, *grads, *m, *v;
+    bf16* wbf;                         // bf16 shadow of params (bf16 mode)
+    // activations; element type is float (fp32 mode) or bf16 (bf16 mode)
+    void *encoded, *ln1, *qkv, *atty, *res2, *ln2, *fch, *fchg, *res3, *lnf, *logits;
+    float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd;
+    float *att;                        // fp32 path: (L, B, NH, T, T) probabilities
+    float *lse;                        // bf16 path: (L, B, NH, T) log-sum-exp of each row
+    float *losses, *loss;
+    // backward scratch
+    void *dresid, *dbufC, *dqkv, *dfch;
+    float *datt;                       // fp32 path: (B, NH, T, T) dS
+    float *attn_scratch;               // bf16 path: (B, NH, T) rowsum(dO * O)
+    float *partials;                   // column-sum / layernorm partials
+    size_t partials_floats;
+    float *enc_partial;                // (BT, C) encoder-backward partial sums
+    unsigned* sorted_keys;             // (BT)
+    int *tokens, *targets;             // staging copies of the last batch
+    unsigned* err;
+    // state
+    int B, T;
+    int have_fwd, have_targets;
+    // tensor-core plan (bf16 mode)
+    int use_tc;
+};
+
+static const size_t kAlign = 1024;
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static size_t act_elt(int prec) { return prec == GPT2_BF16 ? 2 : 4; }
+
+// Walk the workspace layout: with base == nullptr only sizes are computed.
+static size_t plan(GPT2* m, char* base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        off = align_up(off, kAlign);
+        char* p = base ? base + off : nullptr;
+        off += bytes;
+        return p;
+    };
+    const size_t BT = (size_t)m->maxB * m->maxT;
+    const size_t C = m->C, L = m->L, NH = m->NH, Vp = m->Vp;
+    const size_t es = act_elt(m->prec);
+    const size_t nf = m->n_flat;
+    m->params = (float*)take(nf * 4);
+    m->grads = (float*)take(nf * 4);
+    m->m = (float*)take(nf * 4);
+    m->v = (float*)take(nf * 4);
+    m->wbf = m->prec == GPT2_BF16 ? (bf16*)take(nf * 2) : nullptr;
+    m->encoded = take(BT * C * es);
+    m->ln1 = take(L * BT * C * es);
+    m->qkv = take(L * BT * 3 * C * es);
+    m->atty = take(L * BT * C * es);
+    m->res2 = take(L * BT * C * es);
+    m->ln2 = take(L * BT * C * es);
+    m->fch = take(L * BT * 4 * C * es);
+    m->fchg = take(L * BT * 4 * C * es);
+    m->res3 = take(L * BT * C * es);
+    m->lnf = take(BT * C * es);
+    m->logits = take(BT * Vp * es);
+    m->ln1_mean = (float*)take(L * BT * 4);
+    m->ln1_rstd = (float*)take(L * BT * 4);
+    m->ln2_mean = (float*)take(L * BT * 4);
+    m->ln2_rstd = (float*)take(L * BT * 4);
+    m->lnf_mean = (float*)take(BT * 4);
+    m->lnf_rstd = (float*)take(BT * 4);
+    const size_t attT = (size_t)m->maxB * NH * m->maxT;
+    if (m->prec == GPT2_FP32) {
+        m->att = (float*)take(L * attT * m->maxT * 4);
+        m->lse = nullptr;
+        m->datt = (float*)take(attT * m->maxT * 4);
+        m->attn_scratch = nullptr;
+    } else {
+        m->att = nullptr;
+        m->lse = (float*)take(L * attT * 4);
+        m->datt = nullptr;
+        m->attn_scratch = (float*)take(attT * 4);
+    }
+    m->losses = (float*)take(BT * 4);
+    m->loss = (float*)take(4);
+    m->dresid = take(BT * C * es);
+    m->dbufC = take(BT * C * es);
+    m->dqkv = take(BT * 3 * C * es);
+    m->dfch = take(BT * 4 * C * es);
+    // partials: layernorm backward (<= 1024 blocks x 2C) and column sums (<= 256 x 4C);
+    // the matmul backward on tensor cores may also use it for split-K partial tiles.
+    size_t pf = 1024 * 2 * C;
+    if (256 * 4 * C > pf) pf = 256 * 4 * C;
+    size_t tc_pf = gemm_tc_scratch_floats(BT, C);
+    if (tc_pf > pf) pf = tc_pf;
+    m->partials_floats = pf;
+    m->partials = (float*)take(pf * 4);
+    m->enc_partial = (float*)take(BT * C * 4);
+    m->sorted_keys = (unsigned*)take(BT * 4);
+    m->tokens = (int*)take(BT * 4);
+    m->targets = (int*)take(BT * 4);
+    m->err = (unsigned*)take(16);
+    return align_up(off, kAlign);
+}
+
+static int validate_cfg(const GPT2Config* c, int maxB, int maxT, int prec) {
+    if (!c) return GPT2_EINVAL;
+    if (prec != GPT2_FP32 && prec != GPT2_BF16) return GPT2_EINVAL;
+    if (c->num_layers < 1 || c->num_heads < 1 || c->channels < 64) return GPT2_EINVAL;
+    if (c->channels % 64 != 0 || c->channels % c->num_heads != 0) return GPT2_EINVAL;
+    if (c->channels > 2048) return GPT2_EUNSUPPORTED;
+    if (c->channels / c->num_heads > ATT_MAX_HS) return GPT2_EUNSUPPORTED;
+    if (c->vocab_size < 1 || c->padded_vocab_size < c->vocab_size) return GPT2_EINVAL;
+    if (c->padded_vocab_size % 64 != 0) return GPT2_EINVAL;
+    if (c->max_seq_len < 1 || maxB < 1 || maxT < 1 || maxT > c->max_seq_len) return GPT2_EINVAL;
+    const long long BT = (long long)maxB * maxT;
+    if (BT > 32768) return GPT2_EUNSUPPORTED;                       // encoder-backward sort
+    if ((long long)(c->padded_vocab_size + 1) * BT > 0xffffffffLL) return GPT2_EUNSUPPORTED;
+    return GPT2_OK;
+}
+
+static void fill_param_table(GPT2* m) {
+    const size_t C = m->C, L = m->L;
+    size_t num[GPT2_NUM_PARAM_TENSORS] = {
+        (size_t)m->Vp * C, (size_t)m->cfg.max_seq_len * C,
+        L * C, L * C, L * 3 * C * C, L * 3 * C, L * C * C, L * C,
+        L * C, L * C, L * 4 * C * C, L * 4 * C, L * C * 4 * C, L * C,
+        C, C};
+    size_t off = 0, real = 0;
+    for (int i = 0; i < GPT2_NUM_PARAM_TENSORS; i++) {
+        off = align_up(off, 64);
+        m->poff[i] = off;
+        m->pnum[i] = num[i];
+        off += num[i];
+        real += num[i];
+    }
+    m->n_flat = align_up(off, 64);
+    m->n_real = real - (size_t)(m->Vp - m->V) * C;
+}
+
+static void init_dims(GPT2* m, const GPT2Config* cfg, int maxB, int maxT, int prec) {
+    memset(m, 0, sizeof(*m));
+    m->cfg = *cfg;
+    m->maxB = maxB;
+    m->maxT = maxT;
+    m->prec = prec;
+    m->L = cfg->num_layers;
+    m->C = cfg->channels;
+    m->NH = cfg->num_heads;
+    m->V = cfg->vocab_size;
+    m->Vp = cfg->padded_vocab_size;
+    fill_param_table(m);
+}
+
+extern "C" int gpt2_workspace_bytes(const GPT2Config* cfg, int max_B, int max_T, int precision,
+                                    size_t* bytes) {
+    int st = validate_cfg(cfg, max_B, max_T, precision);
+    if (st) return st;
+    if (!bytes) return GPT2_EINVAL;
+    GPT2 tmp;
+    init_dims(&tmp, cfg, max_B, max_T, precision);
+    *bytes = plan(&tmp, nullptr);
+    return GPT2_OK;
+}
+
+static int launch_zero(cudaStream_t s, void* p, size_t bytes) {
+    // bytes is a multiple of 16 for every region this is used on
+    size_t n4 = bytes / 16;
+    if (n4 == 0) return GPT2_OK;
+    int grid = (int)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 8);
+    ProfScope ps(s, PC_MISC, 0, (double)bytes);
+    zero_kernel<<<grid, 256, 0, s>>>((float4*)p, n4);
+    rt_note_launches(1);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int precision,
+                          void* workspace, size_t workspace_bytes, void* stream, GPT2** out) {
+    int st = validate_cfg(cfg, max_B, max_T, precision);
+    if (st) return st;
+    if (!workspace || !out) return GPT2_EINVAL;
+    if (((uintptr_t)workspace) % kAlign != 0) return GPT2_EINVAL;
+    GPT2* m = (GPT2*)malloc(sizeof(GPT2));
+    if (!m) return GPT2_ENOMEM;
+    init_dims(m, cfg, max_B, max_T, precision);
+    size_t need = plan(m, nullptr);
+    if (workspace_bytes < need) { free(m); return GPT2_ENOMEM; }
+    plan(m, (char*)workspace);
+    m->ws = (char*)workspace;
+    m->ws_bytes = workspace_bytes;
+    m->stream = (cudaStream_t)stream;
+    m->use_tc = (precision == GPT2_BF16) ? gemm_tc_available() : 0;
+    if (cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             32768 * (int)sizeof(unsigned)) != cudaSuccess) {
+        free(m);
+        return GPT2_ECUDA;
+    }
+    int rc = launch_zero(m->stream, m->params, (size_t)m->n_flat * 4 * 4);   // params, grads, m, v
+    if (rc == GPT2_OK) rc = launch_zero(m->stream, m->err, 16);
+    if (rc == GPT2_OK && m->wbf) rc = launch_zero(m->stream, m->wbf, m->n_flat * 2);
+    if (rc == GPT2_OK && cudaStreamSynchronize(m->stream) != cudaSuccess) rc = GPT2_ECUDA;
+    if (rc != GPT2_OK) { free(m); return rc; }
+    *out = m;
+    return GPT2_OK;
+}
+
+extern "C" void gpt2_free(GPT2* m) { free(m); }
+
+extern "C" int gpt2_set_stream(GPT2* m, void* stream) {
+    if (!m) return GPT2_EINVAL;
+    m->stream = (cudaStream_t)stream;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_num_parameters(const GPT2* m, size_t* n_real, size_t* n_flat) {
+    if (!m) return GPT2_EINVAL;
+    if (n_real) *n_real = m->n_real;
+    if (n_flat) *n_flat = m->n_flat;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_param_tensor(const GPT2* m, int index, size_t* offset, size_t* numel) {
+    if (!m || index < 0 || index >= GPT2_NUM_PARAM_TENSORS) return GPT2_EINVAL;
+    if (offset) *offset = m->poff[index];
+    if (numel) *numel = m->pnum[index];
+    return GPT2_OK;
+}
+
+extern "C" float* gpt2_params(GPT2* m) { return m ? m->params : nullptr; }
+extern "C" float* gpt2_grads(GPT2* m) { return m ? m->grads : nullptr; }
+extern "C" float* gpt2_adam_m(GPT2* m) { return m ? m->m : nullptr; }
+extern "C" float* gpt2_adam_v(GPT2* m) { return m ? m->v : nullptr; }
+extern "C" float* gpt2_loss(GPT2* m) { return m ? m->loss : nullptr; }
+extern "C" float* gpt2_losses(GPT2* m) { return m ? m->losses : nullptr; }
+extern "C" void* gpt2_logits(GPT2* m) { return m ? m->logits : nullptr; }
+
+extern "C" int gpt2_sync_params(GPT2* m) {
+    if (!m) return GPT2_EINVAL;
+    if (m->wbf) {
+        f32_to_bf16_kernel<<<148 * 8, 256, 0, m->stream>>>(m->wbf, m->params, m->n_flat);
+        rt_note_launches(1);
+        CK(cudaGetLastError());
+    }
+    int rc = launch_zero(m->stream, m->m, m->n_flat * 4 * 2);   // m and v are adjacent
+    return rc;
+}
+
+// ------------------------------------------------------------------ layer launchers
+template <typename T>
+static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T* inp, const T* w,
+                      const T* b, int N, int C) {
+    constexpr int EPV = Vec<T>::N;
+    const int nv = ceil_div(C / EPV, 32);
+    dim3 grid(ceil_div(N, LN_WARPS));
+    ProfScope ps(s, PC_LAYERNORM_FWD, 0, 2.0 * N * C * sizeof(T) + 8.0 * N + 2.0 * C * sizeof(T));
+    rt_note_launches(1);
+    switch (nv) {
+#define LNF_CASE(k) case k: layernorm_forward_kernel<T, k><<<grid, LN_WARPS * 32, 0, s>>>(out, mean, rstd, inp, w, b, N, C); break;
+        LNF_CASE(1) LNF_CASE(2) LNF_CASE(3) LNF_CASE(4) LNF_CASE(5) LNF_CASE(6) LNF_CASE(7) LNF_CASE(8)
+        LNF_CASE(9) LNF_CASE(10) LNF_CASE(11) LNF_CASE(12) LNF_CASE(13) LNF_CASE(14) LNF_CASE(15) LNF_CASE(16)
+#undef LNF_CASE
+        default: return GPT2_EUNSUPPORTED;
+    }
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 4), 1024)); }
+
+template <typename T>
+static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
+                       const T* w, const float* mean, const float* rstd, int N, int C,
+                       float* partial, size_t partial_floats) {
+    constexpr int EPV = Vec<T>::N;
+    const int nv = ceil_div(C / EPV, 32);
+    const int G = ln_backward_grid(N);
+    if ((size_t)G * 2 * C > partial_floats) return GPT2_EINVAL;
+    const size_t smem = 2 * C * sizeof(float);
+    ProfScope ps(s, PC_LAYERNORM_BWD, 0, 4.0 * N * C * sizeof(T) + 8.0 * N + 3.0 * C * sizeof(T) + 8.0 * C);
+    rt_note_launches(2);
+    switch (nv) {
+#define LNB_CASE(k) case k: layernorm_backward_kernel<T, k><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
+        LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
+        LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
+#undef LNB_CASE
+        default: return GPT2_EUNSUPPORTED;
+    }
+    CK(cudaGetLastError());
+    layernorm_backward_reduce<<<ceil_div(2 * C, 256), 256, 0, s>>>(dw, db, partial, G, C);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+static void colsum_shape(int M, int N, int* R, int* rows) {
+    int r = std::max(1, std::min(256, ceil_div(M, 64)));
+    *rows = ceil_div(M, r);
+    *R = ceil_div(M, *rows);
+}
+
+template <typename T>
+static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* partial,
+                  size_t partial_floats) {
+    int R, rows;
+    colsum_shape(M, N, &R, &rows);
+    if ((size_t)R * N > partial_floats) return GPT2_EINVAL;
+    ProfScope ps(s, PC_BIAS_GRAD, 0, (double)M * N * sizeof(T) + 8.0 * N);
+    rt_note_launches(2);
+    colsum_partial_kernel<T><<<dim3(ceil_div(N, 256), R), 256, 0, s>>>(partial, x, M, N, rows);
+    CK(cudaGetLastError());
+    colsum_final_kernel<<<ceil_div(N, 256), 256, 0, s>>>(out, partial, R, N);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+// Linear-layer products.  W is (N, K) row-major for the forward (y = x W^T).
+template <typename T>
+static int mm_forward(GPT2* m, cudaStream_t s, T* out, const T* inp, const T* W, const T* bias,
+                      int M, int N, int K, int epi, void* aux) {
+    EpiArgs ep{out, bias, aux, (long)N};
+    ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
+    if constexpr (sizeof(T) == 2) {
+        if (m && m->use_tc) {
+            int rc = gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias,
+                                     M, N, K, epi, (bf16*)aux);
+            if (rc != GPT2_EUNSUPPORTED) return rc;
+        }
+    }
+    cudaError_t e;
+    rt_note_launches(1);
+    switch (epi) {
+        case EPI_STORE: e = launch_gemm_simt<T, true, true, EPI_STORE>(s, inp, K, W, K, M, N, K, ep); break;
+        case EPI_GELU: e = launch_gemm_simt<T, true, true, EPI_GELU>(s, inp, K, W, K, M, N, K, ep); break;
+        case EPI_RESID: e = launch_gemm_simt<T, true, true, EPI_RESID>(s, inp, K, W, K, M, N, K, ep); break;
+        default: return GPT2_EINVAL;
+    }
+    CK(e);
+    return GPT2_OK;
+}
+
+// dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation of dinp's layer)
+template <typename T>
+static int mm_backward_dx(GPT2* m, cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N,
+                          int K, int epi, const T* aux) {
+    EpiArgs ep{dinp, nullptr, (void*)aux, (long)K};
+    ProfScope ps(s, PC_MATMUL_BWD_DX, 2.0 * M * N * K, 0);
+    if constexpr (sizeof(T) == 2) {
+        if (m && m->use_tc) {
+            int rc = gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
+                                         (const bf16*)aux);
+            if (rc != GPT2_EUNSUPPORTED) return rc;
+        }
+    }
+    cudaError_t e;
+    rt_note_launches(1);
+    // C(m, k) = sum_n dout[m][n] W[n][k]: A K-contig over n (lda = N), B(k, n) = W[n*K + k]
+    if (epi == EPI_GELU_BWD) e = launch_gemm_simt<T, true, false, EPI_GELU_BWD>(s, dout, N, W, K, M, K, N, ep);
+    else e = launch_gemm_simt<T, true, false, EPI_STORE>(s, dout, N, W, K, M, K, N, ep);
+    CK(e);
+    return GPT2_OK;
+}
+
+// dW (N,K) += dout^T (N,M) inp (M,K)
+template <typename T>
+static int mm_backward_dw(GPT2* m, cudaStream_t s, float* dW, const T* dout, const T* inp, int M, int N,
+                          int K) {
+    EpiArgs ep{dW, nullptr, nullptr, (long)K};
+    ProfScope ps(s, PC_MATMUL_BWD_DW, 2.0 * M * N * K, 0);
+    if constexpr (sizeof(T) == 2) {
+        if (m && m->use_tc) {
+            int rc = gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, m->partials,
+                                         m->partials_floats);
+            if (rc != GPT2_EUNSUPPORTED) return rc;
+        }
+    }
+    // C(n, k) = sum_m dout[m][n] inp[m][k]: A(n, m) = dout[m*N + n], B(k, m) = inp[m*K + k]
+    rt_note_launches(1);
+    CK((launch_gemm_simt<T, false, false, EPI_ACC_F32>(s, dout, N, inp, K, N, K, M, ep)));
+    return GPT2_OK;
+}
+
+static double attn_fwd_flops(int B, int Tn, int C) {
+    // q k^T and P v over the causal half (keys j <= t): 2 products x 2 flops per MAC
+    return 4.0 * B * C * (double)Tn * (Tn + 1) / 2.0;
+}
+
+template <typename T>
+static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, int B, int Tn) {
+    const int C = m->C, NH = m->NH;
+    ProfScope ps(s, PC_ATTENTION_FWD, attn_fwd_flops(B, Tn, C), 0);
+    if constexpr (sizeof(T) == 2) {
+        float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
+        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH);
+    } else {
+        float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
+        int rows = B * NH * Tn;
+        attention_forward_simt<T><<<ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s>>>(out, att, qkv, B, Tn, C, NH);
+        rt_note_launches(1);
+        CK(cudaGetLastError());
+        return GPT2_OK;
+    }
+}
+
+template <typename T>
+static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const T* qkv, const T* out,
+                         int l, int B, int Tn) {
+    const int C = m->C, NH = m->NH;
+    // dV, dP, dQ, dK: four causal-half products (the recomputed S is not counted)
+    ProfScope ps(s, PC_ATTENTION_BWD, 2.0 * attn_fwd_flops(B, Tn, C), 0);
+    if constexpr (sizeof(T) == 2) {
+        const float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
+        return attention_flash_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out,
+                                     lse, m->attn_scratch, B, Tn, C, NH);
+    } else {
+        (void)out;
+        const float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
+        int rows = B * NH * Tn;
+        int grid = ceil_div(rows, ATT_WARPS);
+        rt_note_launches(3);
+        attention_backward_ds<T><<<grid, ATT_WARPS * 32, 0, s>>>(m->datt, att, dout, qkv, B, Tn, C, NH);
+        CK(cudaGetLastError());
+        attention_backward_dq<T><<<grid, ATT_WARPS * 32, 0, s>>>(dqkv, m->datt, qkv, B, Tn, C, NH);
+        CK(cudaGetLastError());
+        attention_backward_dkv<T><<<grid, ATT_WARPS * 32, 0, s>>>(dqkv, m->datt, att, qkv, dout, B, Tn, C, NH);
+        CK(cudaGetLastError());
+        return GPT2_OK;
+    }
+}
+
+#define RC(x)                          \
+    do {                               \
+        int rc_ = (x);                 \
+        if (rc_ != GPT2_OK) return rc_; \
+    } while (0)
+
+// ------------------------------------------------------------------ forward
+template <typename T>
+static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
+    cudaStream_t s = m->stream;
+    const int C = m->C, L = m->L, BT = B * Tn;
+    const size_t BTmax = (size_t)m->maxB * m->maxT;
+    const T* W = (sizeof(T) == 2) ? (const T*)m->wbf : (const T*)m->params;
+    auto P = [&](int i) { return W + m->poff[i]; };
+    T* encoded = (T*)m->encoded;
+    {
+        constexpr int EPV = Vec<T>::N;
+        size_t n = (size_t)BT * (C / EPV);
+        ProfScope ps(s, PC_ENCODER_FWD, 0, 3.0 * BT * C * sizeof(T) + 4.0 * BT);
+        rt_note_launches(1);
+        encoder_forward_kernel<T><<<(unsigned)ceil_div_sz(n, 256), 256, 0, s>>>(encoded, m->tokens, P(P_WTE), P(P_WPE), BT, Tn, C, m->V, m->err);
+        CK(cudaGetLastError());
+    }
+    const T* x = encoded;
+    for (int l = 0; l < L; l++) {
+        T* ln1 = (T*)m->ln1 + l * BTmax * C;
+        T* qkv = (T*)m->qkv + l * BTmax * 3 * C;
+        T* atty = (T*)m->atty + l * BTmax * C;
+        T* res2 = (T*)m->res2 + l * BTmax * C;
+        T* ln2 = (T*)m->ln2 + l * BTmax * C;
+        T* fch = (T*)m->fch + l * BTmax * 4 * C;
+        T* fchg = (T*)m->fchg + l * BTmax * 4 * C;
+        T* res3 = (T*)m->res3 + l * BTmax * C;
+        float* m1 = m->ln1_mean + l * BTmax; float* r1 = m->ln1_rstd + l * BTmax;
+        float* m2 = m->ln2_mean + l * BTmax; float* r2 = m->ln2_rstd + l * BTmax;
+        RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
+        RC(mm_forward<T>(m, s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr));
+        RC(attn_forward<T>(m, s, atty, qkv, l, B, Tn));
+        RC(mm_forward<T>(m, s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x));
+        RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
+        RC(mm_forward<T>(m, s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch));
+        RC(mm_forward<T>(m, s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2));
+        x = res3;
+    }
+    RC(ln_forward<T>(s, (T*)m->lnf, m->lnf_mean, m->lnf_rstd, x, P(P_LNFW), P(P_LNFB), BT, C));
+    RC(mm_forward<T>(m, s, (T*)m->logits, (const T*)m->lnf, P(P_WTE), (const T*)nullptr, BT, m->Vp, C, EPI_STORE, nullptr));
+    if (with_targets) {
+        {
+            ProfScope ps(s, PC_SOFTMAX_XENT, 0, 2.0 * BT * m->Vp * sizeof(T) + 12.0 * BT);
+            rt_note_launches(2);
+            softmax_xent_kernel<T><<<BT, XENT_THREADS, 0, s>>>((T*)m->logits, m->losses, m->targets, m->V, m->Vp, 1.0f / (float)BT, m->err);
+            CK(cudaGetLastError());
+            mean_loss_kernel<<<1, 1024, 0, s>>>(m->loss, m->losses, BT, m->err);
+            CK(cudaGetLastError());
+        }
+        // order the token positions by id now; the encoder backward consumes it
+        int NP = 1;
+        while (NP < BT) NP <<= 1;
+        ProfScope ps2(s, PC_ENCODER_BWD, 0, 8.0 * BT);
+        rt_note_launches(1);
+        encoder_sort_kernel<<<1, 1024, NP * sizeof(unsigned), s>>>(m->sorted_keys, m->tokens, BT, m->V, NP);
+        CK(cudaGetLastError());
+    }
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ backward
+template <typename T>
+static int backward_impl(GPT2* m) {
+    cudaStream_t s = m->stream;
+    const int B = m->B, Tn = m->T, C = m->C, L = m->L, BT = B * Tn;
+    const size_t BTmax = (size_t)m->maxB * m->maxT;
+    const T* W = (sizeof(T) == 2) ? (const T*)m->wbf : (const T*)m->params;
+    auto P = [&](int i) { return W + m->poff[i]; };
+    auto G = [&](int i) { return m->grads + m->poff[i]; };
+    T* dresid = (T*)m->dresid;
+    T* dbufC = (T*)m->dbufC;
+    T* dqkv = (T*)m->dqkv;
+    T* dfch = (T*)m->dfch;
+    const T* dlogits = (const T*)m->logits;
+    float* part = m->partials;
+    const size_t pf = m->partials_floats;
+    // LM head (tied): dlnf = dlogits wte; dwte += dlogits^T lnf
+    RC(mm_backward_dx<T>(m, s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr));
+    RC(mm_backward_dw<T>(m, s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C));
+    RC(launch_zero(s, dresid, (size_t)BT * C * sizeof(T)));
+    const T* xlast = (const T*)m->res3 + (L - 1) * BTmax * C;
+    RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf));
+    for (int l = L - 1; l >= 0; l--) {
+        const T* x_in = (l == 0) ? (const T*)m->encoded : (const T*)m->res3 + (l - 1) * BTmax * C;
+        const T* ln1 = (const T*)m->ln1 + l * BTmax * C;
+        const T* qkv = (const T*)m->qkv + l * BTmax * 3 * C;
+        const T* atty = (const T*)m->atty + l * BTmax * C;
+        const T* res2 = (const T*)m->res2 + l * BTmax * C;
+        const T* ln2 = (const T*)m->ln2 + l * BTmax * C;
+        const T* fch = (const T*)m->fch + l * BTmax * 4 * C;
+        const T* fchg = (const T*)m->fchg + l * BTmax * 4 * C;
+        const float* m1 = m->ln1_mean + l * BTmax; const float* r1 = m->ln1_rstd + l * BTmax;
+        const float* m2 = m->ln2_mean + l * BTmax; const float* r2 = m->ln2_rstd + l * BTmax;
+        // MLP output projection (dresid = d res3)
+        RC(mm_backward_dx<T>(m, s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch));
+        RC(mm_backward_dw<T>(m, s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C));
+        RC(colsum<T>(s, G(P_FCPROJB) + l * C, dresid, BT, C, part, pf));
+        // MLP input projection
+        RC(mm_backward_dx<T>(m, s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr));
+        RC(mm_backward_dw<T>(m, s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C));
+        RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf));
+        // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
+        RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf));
+        // attention output projection (dresid = d res2)
+        RC(mm_backward_dx<T>(m, s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr));
+        RC(mm_backward_dw<T>(m, s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C));
+        RC(colsum<T>(s, G(P_ATTPROJB) + l * C, dresid, BT, C, part, pf));
+        // attention
+        RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn));
+        // qkv projection
+        RC(mm_backward_dx<T>(m, s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr));
+        RC(mm_backward_dw<T>(m, s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C));
+        RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf));
+        // ln1 (dresid becomes d x_l)
+        RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf));
+    }
+    // encoder: deterministic scatter-add into dwte (ids sorted in the forward), dwpe
+    ProfScope ps(s, PC_ENCODER_BWD, 0, (double)BT * C * sizeof(T) + 8.0 * BT * C + 8.0 * Tn * C);
+    rt_note_launches(3);
+    encoder_backward_wte_partial<T><<<ceil_div(BT, ENC_CHUNK), 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, dresid, BT, C, m->V);
+    CK(cudaGetLastError());
+    encoder_backward_wte_final<<<BT, 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
+    CK(cudaGetLastError());
+    encoder_backward_wpe<T><<<ceil_div(Tn * C, 256), 256, 0, s>>>(G(P_WPE), dresid, B, Tn, C);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+static int read_error(GPT2* m) {
+    unsigned e = 0;
+    CK(cudaMemcpyAsync(&e, m->err, sizeof(unsigned), cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    if (e) {
+        CK(cudaMemsetAsync(m->err, 0, sizeof(unsigned), m->stream));
+        if (e & ERRBIT_TIMEOUT) return GPT2_ETIMEOUT;
+        if (e & ERRBIT_TOKEN) return GPT2_ETOKEN;
+        if (e & ERRBIT_NONFINITE) return GPT2_ENONFINITE;
+        return GPT2_ECUDA;
+    }
+    return GPT2_OK;
+}
+
+static int check_bt(GPT2* m, int B, int Tn) {
+    if (B < 1 || B > m->maxB || Tn < 1 || Tn > m->maxT || Tn > m->cfg.max_seq_len) return GPT2_EINVAL;
+    return GPT2_OK;
+}
+
+static int forward_dispatch(GPT2* m, int B, int Tn, bool with_targets) {
+    m->have_fwd = 0;
+    m->have_targets = 0;
+    int rc = (m->prec == GPT2_BF16) ? forward_impl<bf16>(m, B, Tn, with_targets)
+                                    : forward_impl<float>(m, B, Tn, with_targets);
+    if (rc != GPT2_OK) return rc;
+    m->B = B;
+    m->T = Tn;
+    m->have_fwd = 1;
+    m->have_targets = with_targets ? 1 : 0;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_forward(GPT2* m, const int32_t* tokens, const int32_t* targets, int B, int Tn,
+                            float* loss_out) {
+    if (!m || !tokens) return GPT2_EINVAL;
+    RC(check_bt(m, B, Tn));
+    const size_t BT = (size_t)B * Tn;
+    CK(cudaMemcpyAsync(m->tokens, tokens, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    if (targets) CK(cudaMemcpyAsync(m->targets, targets, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    RC(forward_dispatch(m, B, Tn, targets != nullptr));
+    if (loss_out) {
+        float l = -1.f;
+        if (targets) CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+        int rc = read_error(m);
+        *loss_out = l;
+        return rc;
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_zero_grad(GPT2* m) {
+    if (!m) return GPT2_EINVAL;
+    return launch_zero(m->stream, m->grads, m->n_flat * 4);
+}
+
+extern "C" int gpt2_backward(GPT2* m) {
+    if (!m) return GPT2_EINVAL;
+    if (!m->have_fwd || !m->have_targets) return GPT2_ESTATE;
+    int rc = (m->prec == GPT2_BF16) ? backward_impl<bf16>(m) : backward_impl<float>(m);
+    // the logits buffer now holds d loss/d logits and has been consumed
+    m->have_fwd = 0;
+    return rc;
+}
+
+extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float eps, float wd, int t) {
+    if (!m || t < 1) return GPT2_EINVAL;
+    double bc1 = 1.0 - pow((double)beta1, (double)t);
+    double bc2 = 1.0 - pow((double)beta2, (double)t);
+    size_t n4 = m->n_flat / 4;
+    int grid = (int)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 16);
+    ProfScope ps(m->stream, PC_ADAMW, 0, (double)m->n_flat * (m->wbf ? 30.0 : 28.0));
+    rt_note_launches(1);
+    adamw_kernel<<<grid, 256, 0, m->stream>>>(m->params, m->grads, m->m, m->v, m->wbf, n4, lr, beta1,
+                                              beta2, eps, wd, (float)bc1, (float)bc2);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_step_host(GPT2* m, const int32_t* tokens_host, const int32_t* targets_host, int B,
+                              int Tn, float lr, float beta1, float beta2, float eps, float wd, int t,
+                              float* loss_out) {
+    if (!m || !tokens_host || !targets_host || !loss_out) return GPT2_EINVAL;
+    RC(check_bt(m, B, Tn));
+    const size_t BT = (size_t)B * Tn;
+    CK(cudaMemcpyAsync(m->tokens, tokens_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
+    CK(cudaMemcpyAsync(m->targets, targets_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
+    RC(forward_dispatch(m, B, Tn, true));
+    RC(gpt2_zero_grad(m));
+    RC(gpt2_backward(m));
+    RC(gpt2_update(m, lr, beta1, beta2, eps, wd, t));
+    float l = -1.f;
+    CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+    int rc = read_error(m);
+    *loss_out = l;
+    return rc;
+}
+
+extern "C" int gpt2_check(GPT2* m) {
+    if (!m) return GPT2_EINVAL;
+    return read_error(m);
+}
+
+extern "C" int gpt2_last_cuda_error(void) { return (int)g_last_cuda_error; }
+
+extern "C" const char* gpt2_strerror(int st) {
+    switch (st) {
+        case GPT2_OK: return "ok";
+        case GPT2_EINVAL: return "invalid argument";
+        case GPT2_ESTATE: return "call out of order (backward needs a forward with targets)";
+        case GPT2_ECUDA: return "CUDA error";
+        case GPT2_ETOKEN: return "token or target id out of range";
+        case GPT2_ENONFINITE: return "non-finite loss";
+        case GPT2_ETIMEOUT: return "bounded device wait ran out";
+        case GPT2_ENOMEM: return "workspace too small";
+        case GPT2_EUNSUPPORTED: return "unsupported shape or precision";
+        default: return "unknown status";
+    }
+}
+
+// ------------------------------------------------------------------ single-layer API
+extern "C" int gpt2_layernorm_forward(float* out, float* mean, float* rstd, const float* inp,
+                                      const float* weight, const float* bias, int N, int C, void* stream) {
+    if (N < 0 || C < 8 || C % 8 || C > 2048) return GPT2_EINVAL;
+    if (N == 0) return GPT2_OK;
+    if (!out || !mean || !rstd || !inp || !weight || !bias) return GPT2_EINVAL;
+    return ln_forward<float>((cudaStream_t)stream, out, mean, rstd, inp, weight, bias, N, C);
+}
+
+extern "C" size_t gpt2_layernorm_backward_scratch_bytes(int N, int C) {
+    if (N <= 0 || C <= 0) return 0;
+    return (size_t)ln_backward_grid(N) * 2 * C * sizeof(float);
+}
+
+extern "C" int gpt2_layernorm_backward(float* dinp, float* dweight, float* dbias, const float* dout,
+                                       const float* inp, const float* weight, const float* mean,
+                                       const float* rstd, int N, int C, void* scratch,
+                                       size_t scratch_bytes, void* stream) {
+    if (N < 0 || C < 8 || C % 8 || C > 2048) return GPT2_EINVAL;
+    if (N == 0) return GPT2_OK;
+    if (!dinp || !dweight || !dbias || !dout || !inp || !weight || !mean || !rstd) return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < gpt2_layernorm_backward_scratch_bytes(N, C)) return GPT2_EINVAL;
+    return ln_backward<float>((cudaStream_t)stream, dinp, dweight, dbias, dout, inp, weight, mean, rstd,
+                              N, C, (float*)scratch, scratch_bytes / sizeof(float));
+}
+
+extern "C" int gpt2_matmul_forward(void* out, const void* inp, const void* weight, const void* bias,
+                                   int M, int N, int K, int precision, void* stream) {
+    if (!out || !inp || !weight || M < 0 || N <= 0 || K <= 0) return GPT2_EINVAL;
+    if (M == 0) return GPT2_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (precision == GPT2_FP32)
+        return mm_forward<float>(nullptr, s, (float*)out, (const float*)inp, (const float*)weight,
+                                 (const float*)bias, M, N, K, EPI_STORE, nullptr);
+    if (precision == GPT2_BF16) {
+        GPT2 shim;
+        memset(&shim, 0, sizeof(shim));
+        shim.use_tc = gemm_tc_available();
+        return mm_forward<bf16>(&shim, s, (bf16*)out, (const bf16*)inp, (const bf16*)weight,
+                                (const bf16*)bias, M, N, K, EPI_STORE, nullptr);
+    }
+    return GPT2_EINVAL;
+}
+
+extern "C" size_t gpt2_matmul_backward_scratch_bytes(int M, int N) {
+    int R, rows;
+    if (M <= 0 || N <= 0) return 0;
+    colsum_shape(M, N, &R, &rows);
+    size_t a = (size_t)R * N * sizeof(float);
+    size_t b = gemm_tc_scratch_floats(M, N) * sizeof(float);
+    return a > b ? a : b;
+}
+
+extern "C" int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, const void* dout,
+                                    const void* inp, const void* weight, int M, int N, int K,
+                                    int precision, void* scratch, size_t scratch_bytes, void* stream) {
+    if (!dinp || !dweight || !dout || !inp || !weight || M <= 0 || N <= 0 || K <= 0) return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < gpt2_matmul_backward_scratch_bytes(M, N)) return GPT2_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* part = (float*)scratch;
+    size_t pf = scratch_bytes / sizeof(float);
+    if (precision == GPT2_FP32) {
+        RC(mm_backward_dx<float>(nullptr, s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_STORE, nullptr));
+        RC(mm_backward_dw<float>(nullptr, s, dweight, (const float*)dout, (const float*)inp, M, N, K));
+        if (dbias) RC(colsum<float>(s, dbias, (const float*)dout, M, N, part, pf));
+        return GPT2_OK;
+    }
+    if (precision == GPT2_BF16) {
+        GPT2 shim;
+        memset(&shim, 0, sizeof(shim));
+        shim.use_tc = gemm_tc_available();
+        shim.partials = part;
+        shim.partials_floats = pf;
+        RC(mm_backward_dx<bf16>(&shim, s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_STORE, nullptr));
+        RC(mm_backward_dw<bf16>(&shim, s, dweight, (const bf16*)dout, (const bf16*)inp, M, N, K));
+        if (dbias) RC(colsum<bf16>(s, dbias, (const bf16*)dout, M, N, part, pf));
+        return GPT2_OK;
+    }
+    return GPT2_EINVAL;
+}

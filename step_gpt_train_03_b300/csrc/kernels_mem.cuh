@@ -1,0 +1,480 @@
+// Memory-bound layers of the training step: encoder, layernorm, fused softmax +
+// cross-entropy, AdamW, zeroing and the deterministic column reductions.
+//
+// Layer list: ujoy.net llm.c article, section "用C语言实现LLM" (encoder, layernorm,
+// matmul, self-attention, GELU, residual, softmax, cross-entropy, each with a
+// hand-written forward and backward).  Every reduction here runs in a fixed order, so
+// results are bitwise reproducible run to run (no floating-point atomics).
+#pragma once
+#include "common.cuh"
+
+// ============================================================== encoder
+// out[bt, :] = wte[tok[bt], :] + wpe[bt % T, :].  One thread per 16-byte packet.
+// An id outside [0, V) raises ERRBIT_TOKEN and yields a zero row.
+template <typename T>
+__global__ void encoder_forward_kernel(T* __restrict__ out, const int* __restrict__ tok,
+                                       const T* __restrict__ wte, const T* __restrict__ wpe,
+                                       int BT, int Tn, int C, int V, unsigned* err) {
+    constexpr int EPV = Vec<T>::N;
+    const int vpr = C / EPV;
+    size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)BT * vpr) return;
+    int bt = (int)(idx / vpr), cv = (int)(idx % vpr);
+    int t = bt % Tn;
+    int id = tok[bt];
+    Vec<T> o;
+    if (id < 0 || id >= V) {
+        if (cv == 0) raise_error(err, ERRBIT_TOKEN);
+#pragma unroll
+        for (int i = 0; i < EPV; i++) o.set(i, 0.f);
+    } else {
+        Vec<T> a = load_vec(wte + (size_t)id * C + cv * EPV);
+        Vec<T> b = load_vec(wpe + (size_t)t * C + cv * EPV);
+#pragma unroll
+        for (int i = 0; i < EPV; i++) o.set(i, a.get(i) + b.get(i));
+    }
+    store_vec(out + (size_t)bt * C + cv * EPV, o);
+}
+
+// Sort keys (id * BT + position) ascending in one CTA (bitonic network in shared
+// memory).  Invalid ids get key V*BT + position so they sort after every valid one.
+// Equal ids thus become contiguous runs ordered by position, which fixes the order of
+// the scatter-add sums below.  NP = next power of two >= BT, NP <= 32768.
+__global__ void encoder_sort_kernel(unsigned* __restrict__ sorted, const int* __restrict__ tok,
+                                    int BT, int V, int NP) {
+    extern __shared__ unsigned keys[];
+    for (int i = threadIdx.x; i < NP; i += blockDim.x) {
+        unsigned k = 0xffffffffu;
+        if (i < BT) {
+            int id = tok[i];
+            if (id < 0 || id >= V) id = V;
+            k = (unsigned)id * (unsigned)BT + (unsigned)i;
+        }
+        keys[i] = k;
+    }
+    __syncthreads();
+    for (int k = 2; k <= NP; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < NP; i += blockDim.x) {
+                int p = i ^ j;
+                if (p > i) {
+                    unsigned a = keys[i], b = keys[p];
+                    bool up = (i & k) == 0;
+                    if ((a > b) == up) { keys[i] = b; keys[p] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < BT; i += blockDim.x) sorted[i] = keys[i];
+}
+
+#define ENC_CHUNK 32
+// dwte[id, :] += sum of dout rows with that id, in position order.  Pass 1: each chunk
+// of ENC_CHUNK sorted positions walks its runs of equal id; a run whose id occurs
+// only inside this chunk is added straight into dwte (no other chunk touches that
+// row), a run of an id that spans chunks leaves its partial sum at the run's first
+// sorted index.
+template <typename T>
+__global__ void encoder_backward_wte_partial(float* __restrict__ dwte, float* __restrict__ partial,
+                                             const unsigned* __restrict__ sorted,
+                                             const T* __restrict__ dout, int BT, int C, int V) {
+    __shared__ unsigned sk[ENC_CHUNK + 2];
+    const int c0 = blockIdx.x * ENC_CHUNK;
+    const int n = min(ENC_CHUNK, BT - c0);
+    for (int i = threadIdx.x; i < n + 2; i += blockDim.x) {
+        int gi = c0 - 1 + i;
+        sk[i] = (gi >= 0 && gi < BT) ? sorted[gi] : 0xffffffffu;
+    }
+    __syncthreads();
+    const unsigned ubt = (unsigned)BT;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float acc = 0.f;
+        int run_start = 0;
+        for (int i = 0; i < n; i++) {
+            unsigned key = sk[i + 1];
+            unsigned id = key / ubt, pos = key % ubt;
+            acc += to_f32(dout[(size_t)pos * C + c]);
+            unsigned nxt = sk[i + 2];
+            bool last = (i == n - 1) || (nxt / ubt != id);
+            if (last) {
+                bool from_prev = (run_start == 0) && (c0 > 0) && (sk[0] / ubt == id);
+                bool into_next = (i == n - 1) && (c0 + n < BT) && (nxt / ubt == id);
+                if ((int)id < V) {
+                    if (!from_prev && !into_next) dwte[(size_t)id * C + c] += acc;
+                    else partial[(size_t)(c0 + run_start) * C + c] = acc;
+                }
+                acc = 0.f;
+                run_start = i + 1;
+            }
+        }
+    }
+}
+
+// Pass 2: for each id whose run spans chunks, add its partials (at the run start and at
+// every chunk boundary inside the run) in order.  One block per sorted index.
+__global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float* __restrict__ partial,
+                                           const unsigned* __restrict__ sorted, int BT, int C, int V) {
+    const int i = blockIdx.x;
+    const unsigned ubt = (unsigned)BT;
+    unsigned id = sorted[i] / ubt;
+    if ((int)id >= V) return;
+    if (i > 0 && sorted[i - 1] / ubt == id) return;        // not the start of a run
+    // end of the run: first index whose key reaches (id+1)*BT
+    unsigned lim = (id + 1) * ubt;
+    int lo = i, hi = BT;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (sorted[mid] < lim) lo = mid + 1; else hi = mid;
+    }
+    const int e = lo;
+    if (i / ENC_CHUNK == (e - 1) / ENC_CHUNK) return;     // handled in pass 1
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float s = partial[(size_t)i * C + c];
+        for (int b = (i / ENC_CHUNK + 1) * ENC_CHUNK; b < e; b += ENC_CHUNK)
+            s += partial[(size_t)b * C + c];
+        dwte[(size_t)id * C + c] += s;
+    }
+}
+
+// dwpe[t, :] += sum over b of dout[b, t, :], b in order.
+template <typename T>
+__global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restrict__ dout,
+                                     int B, int Tn, int C) {
+    size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)Tn * C) return;
+    int t = (int)(idx / C), c = (int)(idx % C);
+    float s = 0.f;
+    for (int b = 0; b < B; b++) s += to_f32(dout[((size_t)b * Tn + t) * C + c]);
+    dwpe[idx] += s;
+}
+
+// ============================================================== layernorm
+#define LN_EPS 1e-5f
+#define LN_WARPS 8
+// One warp per row; the row lives in registers (NV 16-byte packets per lane).
+// mean = sum(x)/C; var = sum((x-mean)^2)/C (two passes over registers); rstd =
+// 1/sqrt(var + eps); out = (x-mean)*rstd*w + b.
+template <typename T, int NV>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* __restrict__ rstd,
+                         const T* __restrict__ inp, const T* __restrict__ w,
+                         const T* __restrict__ b, int N, int C) {
+    constexpr int EPV = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const int nvec = C / EPV;
+    const T* x = inp + (size_t)row * C;
+    float v[NV][EPV];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        int vi = lane + 32 * i;
+        if (vi < nvec) {
+            Vec<T> p = load_vec(x + vi * EPV);
+#pragma unroll
+            for (int e = 0; e < EPV; e++) { v[i][e] = p.get(e); s += v[i][e]; }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPV; e++) v[i][e] = 0.f;
+        }
+    }
+    const float m = warp_sum(s) / (float)C;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        if (lane + 32 * i < nvec) {
+#pragma unroll
+            for (int e = 0; e < EPV; e++) { float d = v[i][e] - m; q += d * d; }
+        }
+    }
+    const float var = warp_sum(q) / (float)C;
+    const float r = 1.0f / sqrtf(var + LN_EPS);
+    T* o = out + (size_t)row * C;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        int vi = lane + 32 * i;
+        if (vi < nvec) {
+            Vec<T> wv = load_vec(w + vi * EPV), bv = load_vec(b + vi * EPV), ov;
+#pragma unroll
+            for (int e = 0; e < EPV; e++) ov.set(e, (v[i][e] - m) * r * wv.get(e) + bv.get(e));
+            store_vec(o + vi * EPV, ov);
+        }
+    }
+    if (lane == 0) { mean[row] = m; rstd[row] = r; }
+}
+
+// Backward.  With xhat = (x-mean)*rstd, g = dy*w:
+//   dinp += rstd * (g - mean(g) - xhat * mean(g*xhat))
+//   dw partial += dy*xhat, db partial += dy, per block over a fixed set of rows
+// Block j handles rows j*LN_WARPS + warp + k*gridDim.x*LN_WARPS; warps then combine in
+// warp order through shared memory and the block writes partial[j][0:2C].
+template <typename T, int NV>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
+                          const T* __restrict__ dout, const T* __restrict__ inp,
+                          const T* __restrict__ w, const float* __restrict__ mean,
+                          const float* __restrict__ rstd, int N, int C) {
+    constexpr int EPV = Vec<T>::N;
+    extern __shared__ float red[];   // 2C floats
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvec = C / EPV;
+    float wv[NV][EPV], dwa[NV][EPV], dba[NV][EPV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        int vi = lane + 32 * i;
+        Vec<T> p;
+        if (vi < nvec) p = load_vec(w + vi * EPV);
+#pragma unroll
+        for (int e = 0; e < EPV; e++) {
+            wv[i][e] = (vi < nvec) ? p.get(e) : 0.f;
+            dwa[i][e] = 0.f;
+            dba[i][e] = 0.f;
+        }
+    }
+    for (int row = blockIdx.x * LN_WARPS + warp; row < N; row += gridDim.x * LN_WARPS) {
+        const T* x = inp + (size_t)row * C;
+        const T* dy = dout + (size_t)row * C;
+        const float m = mean[row], r = rstd[row];
+        float xh[NV][EPV], g[NV][EPV], dyv[NV][EPV];
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            int vi = lane + 32 * i;
+            if (vi < nvec) {
+                Vec<T> xp = load_vec(x + vi * EPV), dp = load_vec(dy + vi * EPV);
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    xh[i][e] = (xp.get(e) - m) * r;
+                    dyv[i][e] = dp.get(e);
+                    g[i][e] = dyv[i][e] * wv[i][e];
+                    sg += g[i][e];
+                    sgx += g[i][e] * xh[i][e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; e++) { xh[i][e] = 0.f; dyv[i][e] = 0.f; g[i][e] = 0.f; }
+            }
+        }
+        const float mg = warp_sum(sg) / (float)C;
+        const float mgx = warp_sum(sgx) / (float)C;
+        T* dx = dinp + (size_t)row * C;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            int vi = lane + 32 * i;
+            if (vi < nvec) {
+                Vec<T> cur = load_vec(dx + vi * EPV), nv;
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    nv.set(e, cur.get(e) + r * (g[i][e] - mg - xh[i][e] * mgx));
+                    dwa[i][e] += dyv[i][e] * xh[i][e];
+                    dba[i][e] += dyv[i][e];
+                }
+                store_vec(dx + vi * EPV, nv);
+            }
+        }
+    }
+    // combine the warps in order 0..LN_WARPS-1
+    for (int wi = 0; wi < LN_WARPS; wi++) {
+        if (warp == wi) {
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                int vi = lane + 32 * i;
+                if (vi < nvec) {
+#pragma unroll
+                    for (int e = 0; e < EPV; e++) {
+                        int c = vi * EPV + e;
+                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; }
+                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float* pj = partial + (size_t)blockIdx.x * 2 * C;
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) pj[c] = red[c];
+}
+
+// dw[c] += sum_j partial[j][c]; db[c] += sum_j partial[j][C+c]  (j in order)
+__global__ void layernorm_backward_reduce(float* __restrict__ dw, float* __restrict__ db,
+                                          const float* __restrict__ partial, int G, int C) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= 2 * C) return;
+    float s = 0.f;
+    for (int j = 0; j < G; j++) s += partial[(size_t)j * 2 * C + c];
+    if (c < C) dw[c] += s; else db[c - C] += s;
+}
+
+// ============================================================== column sums (bias grads)
+// partial[r][n] = sum of x[m][n] over rows m of chunk r (in order); then
+// out[n] += sum_r partial[r][n] (in order).
+template <typename T>
+__global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x,
+                                      int M, int N, int rows_per_chunk) {
+    int n = blockIdx.x * blockDim.x + threadIdx.x;
+    int r = blockIdx.y;
+    if (n >= N) return;
+    int m0 = r * rows_per_chunk, m1 = min(M, m0 + rows_per_chunk);
+    float s = 0.f;
+    for (int m = m0; m < m1; m++) s += to_f32(x[(size_t)m * N + n]);
+    partial[(size_t)r * N + n] = s;
+}
+__global__ void colsum_final_kernel(float* __restrict__ out, const float* __restrict__ partial,
+                                    int R, int N) {
+    int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    float s = 0.f;
+    for (int r = 0; r < R; r++) s += partial[(size_t)r * N + n];
+    out[n] += s;
+}
+
+// ============================================================== softmax + cross-entropy
+// One block per row of logits (Vp entries).  Pass 1: online max / sum of exp over the V
+// real columns; lse = max + log(sum); loss = lse - z[target].  Pass 2 overwrites the row
+// with d(mean loss)/dz = (exp(z - lse) - [j == target]) * dloss for j < V and 0 for the
+// padded columns.  Without targets the kernel is not launched.
+#define XENT_THREADS 1024
+template <typename T>
+__global__ void __launch_bounds__(XENT_THREADS)
+softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
+                    const int* __restrict__ targets, int V, int Vp, float dloss, unsigned* err) {
+    constexpr int EPV = Vec<T>::N;
+    __shared__ float sm_m[32], sm_s[32];
+    __shared__ float sm_lse, sm_zt;
+    const int row = blockIdx.x;
+    T* z = logits + (size_t)row * Vp;
+    const int tgt_raw = targets[row];
+    const bool tgt_ok = tgt_raw >= 0 && tgt_raw < V;
+    const int tgt = tgt_ok ? tgt_raw : -1;
+    if (threadIdx.x == 0) {
+        if (!tgt_ok) raise_error(err, ERRBIT_TOKEN);
+        sm_zt = tgt_ok ? to_f32(z[tgt]) : 0.f;
+    }
+    const int nvec = Vp / EPV;
+    float mx = -INFINITY, sum = 0.f;
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        Vec<T> p = load_vec(z + (size_t)vi * EPV);
+        float vmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EPV; e++)
+            if (vi * EPV + e < V) vmax = fmaxf(vmax, p.get(e));
+        if (vmax == -INFINITY) continue;
+        float nm = fmaxf(mx, vmax);
+        float s = sum * expf(mx - nm);
+#pragma unroll
+        for (int e = 0; e < EPV; e++)
+            if (vi * EPV + e < V) s += expf(p.get(e) - nm);
+        mx = nm;
+        sum = s;
+    }
+    // combine (max, sum) pairs: within the warp, then across warps in order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float om = __shfl_xor_sync(0xffffffffu, mx, o), os = __shfl_xor_sync(0xffffffffu, sum, o);
+        float nm = fmaxf(mx, om);
+        float a = (mx == -INFINITY) ? 0.f : sum * expf(mx - nm);
+        float b = (om == -INFINITY) ? 0.f : os * expf(om - nm);
+        mx = nm;
+        sum = a + b;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sm_m[warp] = mx; sm_s[warp] = sum; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float M = -INFINITY, S = 0.f;
+        for (int wi = 0; wi < (int)(blockDim.x >> 5); wi++) {
+            float om = sm_m[wi], os = sm_s[wi];
+            float nm = fmaxf(M, om);
+            float a = (M == -INFINITY) ? 0.f : S * expf(M - nm);
+            float b = (om == -INFINITY) ? 0.f : os * expf(om - nm);
+            M = nm;
+            S = a + b;
+        }
+        float lse = M + logf(S);
+        sm_lse = lse;
+        losses[row] = tgt_ok ? (lse - sm_zt) : 0.f;
+    }
+    __syncthreads();
+    const float lse = sm_lse;
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        Vec<T> p = load_vec(z + (size_t)vi * EPV), o;
+#pragma unroll
+        for (int e = 0; e < EPV; e++) {
+            int j = vi * EPV + e;
+            float d = 0.f;
+            if (j < V) d = (expf(p.get(e) - lse) - (j == tgt ? 1.f : 0.f)) * dloss;
+            o.set(e, d);
+        }
+        store_vec(z + (size_t)vi * EPV, o);
+    }
+}
+
+// Mean of n per-position losses, fixed order: thread i sums i, i+1024, ...; then a tree.
+__global__ void __launch_bounds__(1024)
+mean_loss_kernel(float* __restrict__ loss, const float* __restrict__ losses, int n, unsigned* err) {
+    __shared__ float sm[32];
+    float s = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s += losses[i];
+    s = warp_sum(s);
+    if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = (threadIdx.x < (blockDim.x >> 5)) ? sm[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) {
+            float mval = v / (float)n;
+            if (!isfinite(mval)) raise_error(err, ERRBIT_NONFINITE);
+            *loss = mval;
+        }
+    }
+}
+
+// ============================================================== AdamW
+// One pass over the flat buffer (n a multiple of 4).  bc1 = 1 - b1^t, bc2 = 1 - b2^t.
+__global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
+                             float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ shadow,
+                             size_t n4, float lr, float b1, float b2, float eps, float wd,
+                             float bc1, float bc2) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float4 pp = reinterpret_cast<float4*>(p)[i];
+        float4 gg = __ldcs(reinterpret_cast<const float4*>(g) + i);
+        float4 mm = reinterpret_cast<float4*>(m)[i];
+        float4 vv = reinterpret_cast<float4*>(v)[i];
+        float* P = &pp.x; const float* G = &gg.x; float* Mm = &mm.x; float* Vv = &vv.x;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            Mm[e] = b1 * Mm[e] + (1.f - b1) * G[e];
+            Vv[e] = b2 * Vv[e] + (1.f - b2) * G[e] * G[e];
+            float mhat = Mm[e] / bc1;
+            float vhat = Vv[e] / bc2;
+            P[e] -= lr * (mhat / (sqrtf(vhat) + eps) + wd * P[e]);
+        }
+        reinterpret_cast<float4*>(p)[i] = pp;
+        reinterpret_cast<float4*>(m)[i] = mm;
+        reinterpret_cast<float4*>(v)[i] = vv;
+        if (shadow) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(pp.z, pp.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<unsigned*>(&lo);
+            pk.y = *reinterpret_cast<unsigned*>(&hi);
+            reinterpret_cast<uint2*>(shadow)[i] = pk;
+        }
+    }
+}
+
+// ============================================================== small utilities
+__global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        out[i] = __float2bfloat16_rn(in[i]);
+}
