@@ -196,6 +196,25 @@ int gpt2_layernorm_backward(float* dinp, float* dweight, float* dbias, const flo
                             const float* rstd, int N, int C, void* scratch,
                             size_t scratch_bytes, void* stream);
 
+/* Layernorm backward that allocates nothing and takes no scratch argument.  The pages
+ * have no counterpart; this exists for callers that cannot obtain device memory at
+ * all, such as a host program that passes this library only its input and output
+ * buffers, or one that commits all device memory at start-up and must not call
+ * cudaMalloc mid-step.  Same arguments and results as gpt2_layernorm_backward, whose
+ * kernels it runs, with the scratch taken from an array of GPT2_NOALLOC_SCRATCH_BYTES
+ * compiled into the library (held on every GPU that loads it, until the process
+ * exits).  Returns GPT2_EINVAL when gpt2_layernorm_backward_scratch_bytes(N, C) exceeds
+ * that size (for example C = 768 allows N <= 21824 rows, C = 2048 allows N <= 8192).
+ * The first call on each device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.  All calls
+ * share the one array, so calls that overlap on the GPU race: serialise them.  Nothing
+ * is carried over between calls (every partial sum read is rewritten first).  Calls no
+ * cudaMalloc, cudaFree or allocating routine. */
+#define GPT2_NOALLOC_SCRATCH_BYTES (4u << 20)
+int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias, const float* dout,
+                                    const float* inp, const float* weight, const float* mean,
+                                    const float* rstd, int N, int C, void* stream);
+
 /* Matmul forward: out (M,N) = inp (M,K) * weight(N,K)^T + bias (N, nullable).
  * precision GPT2_FP32: all float*; GPT2_BF16: out, inp, weight, bias are bf16 (bias
  * nullable), fp32 accumulation. */

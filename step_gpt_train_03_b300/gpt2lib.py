@@ -66,6 +66,7 @@ SIGNATURES = {
     "gpt2_layernorm_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
+    "gpt2_layernorm_backward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_matmul_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_matmul_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_matmul_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
@@ -318,6 +319,17 @@ def layernorm_backward(dinp, dweight, dbias, dout, inp, weight, mean, rstd, scra
                                       _ptr(weight), _ptr(mean), _ptr(rstd), N, C, _ptr(scratch),
                                       scratch.numel() * scratch.element_size(), _stream_handle(stream)),
           "gpt2_layernorm_backward")
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def layernorm_backward_noalloc(dinp, dweight, dbias, dout, inp, weight, mean, rstd, stream=None):
+    """gpt2_layernorm_backward_noalloc: the library's built-in scratch, no allocation."""
+    N, C = inp.shape
+    check(lib.gpt2_layernorm_backward_noalloc(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout),
+                                              _ptr(inp), _ptr(weight), _ptr(mean), _ptr(rstd), N, C,
+                                              _stream_handle(stream)), "gpt2_layernorm_backward_noalloc")
 
 
 def matmul_forward(out, inp, weight, bias, precision, stream=None):
