@@ -13,6 +13,7 @@
 #include "attention_flash.h"
 #include "../../include/gpt2.h"
 #include "runtime.h"
+#include "attention_mma.cuh"
 
 #define FA_WARPS 8
 #define FA_MAX_HS 128
@@ -209,6 +210,12 @@ int attention_flash_forward(cudaStream_t s, bf16* out, float* lse, const bf16* q
                             int NH) {
     const int hs = C / NH;
     if (hs > FA_MAX_HS) return GPT2_EUNSUPPORTED;
+    if (hs == AM_HS) {
+        dim3 grid((Tn + AMF_Q - 1) / AMF_Q, B * NH);
+        attention_forward_mma<<<grid, AMF_THREADS, 0, s>>>(out, lse, qkv, B, Tn, C, NH);
+        rt_note_launches(1);
+        return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
+    }
     const int rows = B * NH * Tn;
     const int grid = ceil_div(rows, FA_WARPS);
     rt_note_launches(1);
@@ -230,6 +237,12 @@ int attention_flash_backward(cudaStream_t s, bf16* dqkv, const bf16* dout, const
     const int grid = ceil_div(rows, FA_WARPS);
     rt_note_launches(3);
     fa_backward_D<<<grid, FA_WARPS * 32, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
+    if (hs == AM_HS) {
+        dim3 g2((Tn + AMB_ROWS - 1) / AMB_ROWS, B * NH);
+        attention_backward_dkv_mma<<<g2, AMB_THREADS, 0, s>>>(dqkv, dout, qkv, lse, scratch, B, Tn, C, NH);
+        attention_backward_dq_mma<<<g2, AMB_THREADS, 0, s>>>(dqkv, dout, qkv, lse, scratch, B, Tn, C, NH);
+        return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
+    }
     switch (ceil_div(hs, 32)) {
 #define FA_BWD_CASE(k)                                                                                 \
     case k:                                                                                            \

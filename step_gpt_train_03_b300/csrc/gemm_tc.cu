@@ -1,19 +1,536 @@
-// bf16 matmuls on the tcgen05 tensor cores.  (Placeholder until the kernel lands:
-// every entry reports GPT2_EUNSUPPORTED and the FMA kernel runs.)
+// bf16 matmuls of the linear layers on the sm_103a tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.
+//
+// ujoy.net llm.c article, section "用C语言实现LLM": the matmul layer's forward and
+// backward.  With the weight stored (out, in):
+//   forward  y  = x W^T (+ bias, GELU, residual in the epilogue)
+//   backward dx = dy W   (GELU backward in the epilogue),  dW += dy^T x
+// All three are D[m][n] = sum_k A(m,k) B(n,k) with each operand either K-major
+// (row r at ptr + r*ld, k contiguous) or MN-major (k-th row at ptr + k*ld, r
+// contiguous); the MMA reads both forms directly (instruction-descriptor major bits),
+// so no transposed copies are made.
+//
+// Kernel: persistent, one CTA per SM, 192 threads.
+//   warp 0      TMA producer: 128x64 A tile and BNx64 B tile per stage, 4-stage ring
+//   warp 1      TMEM owner and MMA issuer (one thread): 128xBN fp32 accumulator,
+//               two accumulators in TMEM so the epilogue of tile i overlaps tile i+1
+//   warps 2-5   epilogue: tcgen05.ld the accumulator rows, fuse bias / GELU /
+//               residual / GELU-backward / fp32 accumulate, store
+// Every mbarrier wait is bounded: on expiry the kernel raises the timeout bit in the
+// library's error word, the other roles see the abort flag and stop, in-flight copies
+// and MMAs are waited for (again bounded), TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_simt.cuh"
 #include "gemm_tc.h"
+#include "runtime.h"
 #include "../../include/gpt2.h"
 
-int gemm_tc_available() { return 0; }
-size_t gemm_tc_scratch_floats(size_t, size_t) { return 0; }
-int gemm_tc_forward(cudaStream_t, __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*,
-                    const __nv_bfloat16*, int, int, int, int, __nv_bfloat16*) {
+#define TC_BM 128
+#define TC_BK 64
+#define TC_STAGES 4
+#define TC_THREADS 192
+#define TC_EPI_PARTIAL 5          // fp32 split-K partial tile into scratch
+#define TC_WAIT_LIMIT (1ll << 31) // clock64 cycles (~1 s) before a wait gives up
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete.  Returns false (and sets the
+// CTA's abort flag and the global timeout bit) if it did not complete in time, or if
+// another role of this CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > TC_WAIT_LIMIT) {
+            *abort_flag = 1;
+            raise_error(err, ERRBIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start address, leading/stride byte offsets, the
+// sm_100 descriptor version (bit 46) and the 128-byte swizzle mode (bits 61-63 = 2).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16
+// (bits 7-9 and 10-12 = 1), major bits 15 (A) and 16 (B): 0 K-major, 1 MN-major;
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ kernel
+struct TcEpi {
+    void* out;          // bf16 (or fp32 for EPI_ACC_F32 / partial)
+    const bf16* bias;   // nullable
+    void* aux;          // GELU pre-activation out / residual in / pre-activation in
+    long ldo;           // row stride of out and aux (elements)
+};
+
+template <int BN>
+struct TcSmem {
+    static constexpr int A_BYTES = TC_BM * TC_BK * 2;
+    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_OFF = TC_STAGES * STAGE_BYTES;
+    // full[S], empty[S], acc_full[2], acc_empty[2], done, then tmem address + abort flag
+    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 5) * 8 + 16 + 1024;
+};
+
+template <int EPI>
+__device__ __forceinline__ void tc_epilogue_store(const TcEpi& ep, int grow, int col, int nvalid,
+                                                  const uint32_t (&r)[32], int M, int N) {
+    // 32 consecutive columns [col, col+32) of row grow; nvalid of them are < N
+    if (grow >= M || nvalid <= 0) return;
+    const size_t o = (size_t)grow * ep.ldo + col;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
+        float* out = reinterpret_cast<float*>(ep.out) + o;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            if (q * 4 >= nvalid) break;
+            float4 a = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if constexpr (EPI == EPI_ACC_F32) {
+                float4 b = *reinterpret_cast<const float4*>(out + 4 * q);
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+            }
+            *reinterpret_cast<float4*>(out + 4 * q) = a;
+        }
+        return;
+    } else {
+        if (ep.bias && EPI != EPI_GELU_BWD) {
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                if (q * 8 >= nvalid) break;
+                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+            }
+        }
+        bf16* out = reinterpret_cast<bf16*>(ep.out) + o;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (q * 8 >= nvalid) break;
+            Vec<bf16> res;
+            if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+                for (int e = 0; e < 8; e++) res.set(e, v[8 * q + e]);
+            } else if constexpr (EPI == EPI_GELU) {
+                Vec<bf16> pre;
+#pragma unroll
+                for (int e = 0; e < 8; e++) pre.set(e, v[8 * q + e]);
+                store_vec(reinterpret_cast<bf16*>(ep.aux) + o + 8 * q, pre);
+#pragma unroll
+                for (int e = 0; e < 8; e++) res.set(e, gelu_f(pre.get(e)));
+            } else if constexpr (EPI == EPI_RESID) {
+                Vec<bf16> rs = load_vec(reinterpret_cast<const bf16*>(ep.aux) + o + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 8; e++) res.set(e, rs.get(e) + v[8 * q + e]);
+            } else if constexpr (EPI == EPI_GELU_BWD) {
+                Vec<bf16> pre = load_vec(reinterpret_cast<const bf16*>(ep.aux) + o + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 8; e++) res.set(e, v[8 * q + e] * gelu_grad_f(pre.get(e)));
+            }
+            store_vec(out + 8 * q, res);
+        }
+    }
+}
+
+// D (M x N) over units = m_tiles x n_tiles x splits, n fastest.  Split s of a tile
+// covers k-blocks [s*kb_per, min(nkb, (s+1)*kb_per)); partial epilogues write tile
+// (s) of the scratch at out + s*M*ldo.
+template <int BN, int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+               int K, int splits, TcEpi ep, unsigned* err) {
+    using S = TcSmem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+    uint64_t* empty = full + TC_STAGES;
+    uint64_t* acc_full = empty + TC_STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* done = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (M + TC_BM - 1) / TC_BM, n_tiles = (N + BN - 1) / BN;
+    const int nkb = (K + TC_BK - 1) / TC_BK;
+    const int kb_per = (nkb + splits - 1) / splits;
+    const int units = m_tiles * n_tiles * splits;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TC_STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(2 * BN) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int sp = u % splits, tile = u / splits;
+                const int nt = tile % n_tiles, mt = tile / n_tiles;
+                const int kb0 = sp * kb_per, kb1 = min(nkb, kb0 + kb_per);
+                for (int kb = kb0; kb < kb1; kb++, it++) {
+                    const int s = it % TC_STAGES;
+                    const uint32_t ph = (it / TC_STAGES) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, err)) { ok = false; break; }
+                    uint8_t* a = smem + s * S::STAGE_BYTES;
+                    uint8_t* b = a + S::A_BYTES;
+                    mbar_expect_tx(&full[s], S::STAGE_BYTES);
+                    if (!A_MN) {
+                        tma_load_2d(a, &tmA, &full[s], kb * TC_BK, mt * TC_BM);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < TC_BM / 64; j++)
+                            tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * TC_BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(b, &tmB, &full[s], kb * TC_BK, nt * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++)
+                            tma_load_2d(b + j * 8192, &tmB, &full[s], nt * BN + j * 64, kb * TC_BK);
+                    }
+                }
+            }
+            // before leaving, every copy this thread started must have landed
+            for (int back = 0; back < TC_STAGES && back < it; back++) {
+                const int j = it - 1 - back;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&full[j % TC_STAGES], (j / TC_STAGES) & 1))
+                    if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(TC_BM, BN, A_MN, B_MN);
+            int it = 0, local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, local++) {
+                const int sp = u % splits;
+                const int kb0 = sp * kb_per, kb1 = min(nkb, kb0 + kb_per);
+                const int acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
+                if (!mbar_wait(&acc_empty[acc], aph ^ 1, abort_flag, err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = kb0; kb < kb1; kb++, it++) {
+                    const int s = it % TC_STAGES;
+                    const uint32_t ph = (it / TC_STAGES) & 1;
+                    if (!mbar_wait(&full[s], ph, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a = smem_u32(smem + s * S::STAGE_BYTES);
+                    const uint32_t b = a + S::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / 16; k++) {
+                        // K-major: 16 k-elements are 32 bytes inside each 128-byte row;
+                        // MN-major: 16 k-rows are two 1024-byte swizzle atoms
+                        const uint64_t ad = A_MN ? sdesc(a + k * 2048, 8192, 1024) : sdesc(a + k * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? sdesc(b + k * 2048, 8192, 1024) : sdesc(b + k * 32, 16, 1024);
+                        tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);     // the stage is free once these MMAs have read it
+                }
+                if (ok) tc_commit(&acc_full[acc]);
+            }
+            // all MMAs issued by this thread complete before the teardown
+            tc_commit(done);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(done, 0))
+                if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue warps 2..5
+        const int lane_grp = warp & 3;                 // TMEM lanes 32*lane_grp .. +31
+        const int row = lane_grp * 32 + lane;
+        int local = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, local++) {
+            const int sp = u % splits, tile = u / splits;
+            const int nt = tile % n_tiles, mt = tile / n_tiles;
+            const int acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
+            // one lane waits; the warp then proceeds converged (tcgen05.ld is warp-wide)
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(&acc_full[acc], aph, abort_flag, err) ? 1 : 0;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            if (!okw) break;
+            __syncwarp();
+            tc_fence_after();
+            const int grow = mt * TC_BM + row;
+            TcEpi e = ep;
+            if constexpr (EPI == TC_EPI_PARTIAL) e.out = reinterpret_cast<float*>(ep.out) + (size_t)sp * M * ep.ldo;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(lane_grp * 32) << 16) + acc * BN + c, r);
+                tmem_ld_wait();
+                const int col = nt * BN + c;
+                tc_epilogue_store<EPI>(e, grow, col, N - col, r, M, N);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    __syncwarp();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * BN)
+                     : "memory");
+}
+
+// out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic)
+__global__ void splitk_reduce_kernel(float* __restrict__ out, const float* __restrict__ part, size_t n4,
+                                     int splits) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 acc = reinterpret_cast<float4*>(out)[i];
+    for (int s = 0; s < splits; s++) {
+        float4 p = reinterpret_cast<const float4*>(part)[(size_t)s * n4 + i];
+        acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    reinterpret_cast<float4*>(out)[i] = acc;
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static int g_num_sms = 0;
+static int g_tc_ok = -1;
+static std::mutex g_tc_mutex;
+
+int gemm_tc_available() {
+    std::lock_guard<std::mutex> lock(g_tc_mutex);
+    if (g_tc_ok >= 0) return g_tc_ok;
+    g_tc_ok = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return 0;
+    if (prop.major != 10) return 0;
+    g_num_sms = prop.multiProcessorCount;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return 0;
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    g_tc_ok = 1;
+    return 1;
+}
+
+// Split-K is only used when a weight gradient has fewer 128x256 tiles than the GPU has
+// SMs, with at most 8 splits: its partials never exceed 8 x (SMs x one tile).
+#define TC_MAX_SPLITS 8
+#define TC_SPLIT_SM_BOUND 160
+size_t gemm_tc_scratch_floats(size_t M, size_t N) {
+    (void)M;
+    (void)N;
+    return (size_t)TC_MAX_SPLITS * TC_SPLIT_SM_BOUND * TC_BM * 256;
+}
+
+// 2-D bf16 tensor map: inner dimension `inner` (contiguous), outer `outer`, row pitch
+// `ld` elements; box {64, box_outer}; 128-byte swizzle; out-of-range reads give zero.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+template <int BN, int EPI, bool A_MN, bool B_MN>
+static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                     int splits, const TcEpi& ep, unsigned* err) {
+    using SM = TcSmem<BN>;
+    static bool attr_set = false;
+    auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN>;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::TOTAL) != cudaSuccess)
+            return GPT2_ECUDA;
+        attr_set = true;
+    }
+    const int units = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN) * splits;
+    const int grid = units < g_num_sms ? units : g_num_sms;
+    kern<<<grid, TC_THREADS, SM::TOTAL, s>>>(ta, tb, M, N, K, splits, ep, err);
+    rt_note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
+}
+
+int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, const bf16* bias, int M, int N,
+                    int K, int epi, bf16* aux, unsigned* err) {
+    if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
+    if (N % 8 || K % 8 || M < 1 || !aligned16(out) || !aligned16(inp) || !aligned16(W) ||
+        (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
+        return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, inp, K, M, K, TC_BM) || !make_map(&tb, W, K, N, K, 256)) return GPT2_EUNSUPPORTED;
+    TcEpi ep{out, bias, aux, (long)N};
+    switch (epi) {
+        case EPI_STORE: return launch_tc<256, EPI_STORE, false, false>(s, ta, tb, M, N, K, 1, ep, err);
+        case EPI_GELU: return launch_tc<256, EPI_GELU, false, false>(s, ta, tb, M, N, K, 1, ep, err);
+        case EPI_RESID: return launch_tc<256, EPI_RESID, false, false>(s, ta, tb, M, N, K, 1, ep, err);
+        default: return GPT2_EUNSUPPORTED;
+    }
+}
+
+int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16* W, int M, int N, int K, int epi,
+                        const bf16* aux, unsigned* err) {
+    // dinp (M x K) = dout (M x N) W (N x K): contraction over N; A = dout K-major,
+    // B(k_out, n) = W[n][k_out] is MN-major (k_out contiguous)
+    if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
+    if (N % 8 || K % 8 || M < 1 || !aligned16(dinp) || !aligned16(dout) || !aligned16(W) ||
+        (aux && !aligned16(aux)))
+        return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, dout, N, M, N, TC_BM) || !make_map(&tb, W, K, N, K, 64)) return GPT2_EUNSUPPORTED;
+    TcEpi ep{dinp, nullptr, (void*)aux, (long)K};
+    if (epi == EPI_GELU_BWD) return launch_tc<256, EPI_GELU_BWD, false, true>(s, ta, tb, M, K, N, 1, ep, err);
+    if (epi == EPI_STORE) return launch_tc<256, EPI_STORE, false, true>(s, ta, tb, M, K, N, 1, ep, err);
     return GPT2_EUNSUPPORTED;
 }
-int gemm_tc_backward_dx(cudaStream_t, __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*, int, int,
-                        int, int, const __nv_bfloat16*) {
-    return GPT2_EUNSUPPORTED;
+
+static int choose_splits(int tiles, int nkb) {
+    // with fewer tiles than SMs, fill the SMs: the split count with the best SM
+    // occupancy over whole waves, each split keeping at least 8 k-blocks
+    if (tiles >= g_num_sms || g_num_sms > TC_SPLIT_SM_BOUND) return 1;
+    int best = 1;
+    double best_eff = 0;
+    for (int sp = 1; sp <= TC_MAX_SPLITS; sp++) {
+        if (sp > 1 && nkb / sp < 8) break;
+        const int units = tiles * sp;
+        const int waves = (units + g_num_sms - 1) / g_num_sms;
+        const double eff = (double)units / (waves * g_num_sms);
+        if (eff > best_eff + 1e-9) { best_eff = eff; best = sp; }
+    }
+    return best;
 }
-int gemm_tc_backward_dw(cudaStream_t, float*, const __nv_bfloat16*, const __nv_bfloat16*, int, int, int,
-                        float*, size_t) {
-    return GPT2_EUNSUPPORTED;
+
+int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16* inp, int M, int N, int K,
+                        float* scratch, size_t scratch_floats, unsigned* err) {
+    // dW (N x K) += dout^T (N x M) inp (M x K): contraction over M; A(n, m) = dout[m][n]
+    // and B(k, m) = inp[m][k] are both MN-major
+    if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
+    if (N % 8 || K % 8 || M < 1 || !aligned16(dW) || !aligned16(dout) || !aligned16(inp))
+        return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, dout, N, M, N, 64) || !make_map(&tb, inp, K, M, K, 64)) return GPT2_EUNSUPPORTED;
+    const int tiles = ((N + TC_BM - 1) / TC_BM) * ((K + 255) / 256);
+    const int nkb = (M + TC_BK - 1) / TC_BK;
+    int splits = choose_splits(tiles, nkb);
+    if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch))) splits = 1;
+    if (splits == 1) {
+        TcEpi ep{dW, nullptr, nullptr, (long)K};
+        return launch_tc<256, EPI_ACC_F32, true, true>(s, ta, tb, N, K, M, 1, ep, err);
+    }
+    TcEpi ep{scratch, nullptr, nullptr, (long)K};
+    int rc = launch_tc<256, TC_EPI_PARTIAL, true, true>(s, ta, tb, N, K, M, splits, ep, err);
+    if (rc != GPT2_OK) return rc;
+    const size_t n4 = (size_t)N * K / 4;
+    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(dW, scratch, n4, splits);
+    rt_note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }

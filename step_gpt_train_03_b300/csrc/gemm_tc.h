@@ -1,6 +1,7 @@
 // bf16 matmuls of the linear layers on the tcgen05 tensor cores (TMA-fed, TMEM
 // accumulators).  Each call returns GPT2_EUNSUPPORTED for a shape it does not take, and
-// the caller then falls back to the FMA kernel.
+// the caller then falls back to the FMA kernel.  `err` (device, nullable) is the error
+// word a kernel sets if one of its bounded waits runs out.
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -17,12 +18,13 @@ size_t gemm_tc_scratch_floats(size_t M, size_t N);
 // pre-activation output (EPI_GELU) or the residual input (EPI_RESID).
 int gemm_tc_forward(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* inp,
                     const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, int N, int K, int epi,
-                    __nv_bfloat16* aux);
+                    __nv_bfloat16* aux, unsigned* err);
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation).
 int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16* dout,
-                        const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux);
+                        const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux,
+                        unsigned* err);
 
 // dW (N,K) fp32 += dout(M,N)^T inp (M,K).
 int gemm_tc_backward_dw(cudaStream_t s, float* dW, const __nv_bfloat16* dout, const __nv_bfloat16* inp,
-                        int M, int N, int K, float* scratch, size_t scratch_floats);
+                        int M, int N, int K, float* scratch, size_t scratch_floats, unsigned* err);

@@ -363,7 +363,7 @@ static int mm_forward(GPT2* m, cudaStream_t s, T* out, const T* inp, const T* W,
     if constexpr (sizeof(T) == 2) {
         if (m && m->use_tc) {
             int rc = gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias,
-                                     M, N, K, epi, (bf16*)aux);
+                                     M, N, K, epi, (bf16*)aux, m->err);
             if (rc != GPT2_EUNSUPPORTED) return rc;
         }
     }
@@ -388,7 +388,7 @@ static int mm_backward_dx(GPT2* m, cudaStream_t s, T* dinp, const T* dout, const
     if constexpr (sizeof(T) == 2) {
         if (m && m->use_tc) {
             int rc = gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
-                                         (const bf16*)aux);
+                                         (const bf16*)aux, m->err);
             if (rc != GPT2_EUNSUPPORTED) return rc;
         }
     }
@@ -410,7 +410,7 @@ static int mm_backward_dw(GPT2* m, cudaStream_t s, float* dW, const T* dout, con
     if constexpr (sizeof(T) == 2) {
         if (m && m->use_tc) {
             int rc = gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, m->partials,
-                                         m->partials_floats);
+                                         m->partials_floats, m->err);
             if (rc != GPT2_EUNSUPPORTED) return rc;
         }
     }
