@@ -307,7 +307,8 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
     return GPT2_OK;
 }
 
-static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 4), 1024)); }
+// two resident blocks per SM on a 148-SM part; each warp then walks ~7 rows at N = 16384
+static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 2), 296)); }
 
 template <typename T>
 static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
@@ -328,13 +329,14 @@ static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* d
         default: return GPT2_EUNSUPPORTED;
     }
     CK(cudaGetLastError());
-    layernorm_backward_reduce<<<ceil_div(2 * C, 256), 256, 0, s>>>(dw, db, partial, G, C);
+    column_reduce_kernel<<<ceil_div(2 * C, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(dw, db, C, partial, G, 2 * C);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
 
 static void colsum_shape(int M, int N, int* R, int* rows) {
-    int r = std::max(1, std::min(256, ceil_div(M, 64)));
+    (void)N;
+    int r = std::max(1, std::min(512, ceil_div(M, 32)));
     *rows = ceil_div(M, r);
     *R = ceil_div(M, *rows);
 }
@@ -347,9 +349,11 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
     if ((size_t)R * N > partial_floats) return GPT2_EINVAL;
     ProfScope ps(s, PC_BIAS_GRAD, 0, (double)M * N * sizeof(T) + 8.0 * N);
     rt_note_launches(2);
-    colsum_partial_kernel<T><<<dim3(ceil_div(N, 256), R), 256, 0, s>>>(partial, x, M, N, rows);
+    constexpr int EPV = Vec<T>::N;
+    if (N % EPV) colsum_partial_scalar_kernel<T><<<dim3(ceil_div(N, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
+    else colsum_partial_kernel<T><<<dim3(ceil_div(N / EPV, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
     CK(cudaGetLastError());
-    colsum_final_kernel<<<ceil_div(N, 256), 256, 0, s>>>(out, partial, R, N);
+    column_reduce_kernel<<<ceil_div(N, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(out, out, N, partial, R, N);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
@@ -518,7 +522,8 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         {
             ProfScope ps(s, PC_SOFTMAX_XENT, 0, 2.0 * BT * m->Vp * sizeof(T) + 12.0 * BT);
             rt_note_launches(2);
-            softmax_xent_kernel<T><<<BT, XENT_THREADS, 0, s>>>((T*)m->logits, m->losses, m->targets, m->V, m->Vp, 1.0f / (float)BT, m->err);
+            softmax_xent_kernel<T><<<BT, XENT_THREADS, 0, s>>>((T*)m->logits, m->losses, m->targets, m->V, m->Vp,
+                                                               1.0f / (float)BT, m->err);
             CK(cudaGetLastError());
             mean_loss_kernel<<<1, 1024, 0, s>>>(m->loss, m->losses, BT, m->err);
             CK(cudaGetLastError());

@@ -209,9 +209,11 @@ layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* _
 //   dinp += rstd * (g - mean(g) - xhat * mean(g*xhat))
 //   dw partial += dy*xhat, db partial += dy, per block over a fixed set of rows
 // Block j handles rows j*LN_WARPS + warp + k*gridDim.x*LN_WARPS; warps then combine in
-// warp order through shared memory and the block writes partial[j][0:2C].
+// warp order through shared memory and the block writes partial[j][0:2C].  The row's
+// x and dy stay packed (16-byte packets) in registers and xhat is recomputed in the
+// second pass, which keeps two blocks resident per SM.
 template <typename T, int NV>
-__global__ void __launch_bounds__(LN_WARPS * 32)
+__global__ void __launch_bounds__(LN_WARPS * 32, (NV * Vec<T>::N <= 24) ? 2 : 1)
 layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
                           const T* __restrict__ dout, const T* __restrict__ inp,
                           const T* __restrict__ w, const float* __restrict__ mean,
@@ -220,56 +222,58 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
     extern __shared__ float red[];   // 2C floats
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C / EPV;
-    float wv[NV][EPV], dwa[NV][EPV], dba[NV][EPV];
+    Vec<T> wv[NV];
+    float dwa[NV][EPV], dba[NV][EPV];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
-        int vi = lane + 32 * i;
-        Vec<T> p;
-        if (vi < nvec) p = load_vec(w + vi * EPV);
+        const int vi = lane + 32 * i;
+        if (vi < nvec) wv[i] = load_vec(w + vi * EPV);
 #pragma unroll
-        for (int e = 0; e < EPV; e++) {
-            wv[i][e] = (vi < nvec) ? p.get(e) : 0.f;
-            dwa[i][e] = 0.f;
-            dba[i][e] = 0.f;
-        }
+        for (int e = 0; e < EPV; e++) { dwa[i][e] = 0.f; dba[i][e] = 0.f; }
     }
     for (int row = blockIdx.x * LN_WARPS + warp; row < N; row += gridDim.x * LN_WARPS) {
         const T* x = inp + (size_t)row * C;
         const T* dy = dout + (size_t)row * C;
+        T* dx = dinp + (size_t)row * C;
         const float m = mean[row], r = rstd[row];
-        float xh[NV][EPV], g[NV][EPV], dyv[NV][EPV];
+        Vec<T> xp[NV], dp[NV], cur[NV];
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                xp[i] = load_vec(x + vi * EPV);
+                dp[i] = load_vec(dy + vi * EPV);
+                cur[i] = load_vec(dx + vi * EPV);
+            }
+        }
         float sg = 0.f, sgx = 0.f;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
-            int vi = lane + 32 * i;
-            if (vi < nvec) {
-                Vec<T> xp = load_vec(x + vi * EPV), dp = load_vec(dy + vi * EPV);
+            if (lane + 32 * i < nvec) {
 #pragma unroll
                 for (int e = 0; e < EPV; e++) {
-                    xh[i][e] = (xp.get(e) - m) * r;
-                    dyv[i][e] = dp.get(e);
-                    g[i][e] = dyv[i][e] * wv[i][e];
-                    sg += g[i][e];
-                    sgx += g[i][e] * xh[i][e];
+                    const float xh = (xp[i].get(e) - m) * r;
+                    const float d = dp[i].get(e);
+                    const float g = d * wv[i].get(e);
+                    sg += g;
+                    sgx += g * xh;
+                    dwa[i][e] += d * xh;
+                    dba[i][e] += d;
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPV; e++) { xh[i][e] = 0.f; dyv[i][e] = 0.f; g[i][e] = 0.f; }
             }
         }
         const float mg = warp_sum(sg) / (float)C;
         const float mgx = warp_sum(sgx) / (float)C;
-        T* dx = dinp + (size_t)row * C;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
-            int vi = lane + 32 * i;
+            const int vi = lane + 32 * i;
             if (vi < nvec) {
-                Vec<T> cur = load_vec(dx + vi * EPV), nv;
+                Vec<T> nv;
 #pragma unroll
                 for (int e = 0; e < EPV; e++) {
-                    nv.set(e, cur.get(e) + r * (g[i][e] - mg - xh[i][e] * mgx));
-                    dwa[i][e] += dyv[i][e] * xh[i][e];
-                    dba[i][e] += dyv[i][e];
+                    const float xh = (xp[i].get(e) - m) * r;
+                    const float g = dp[i].get(e) * wv[i].get(e);
+                    nv.set(e, cur[i].get(e) + r * (g - mg - xh * mgx));
                 }
                 store_vec(dx + vi * EPV, nv);
             }
@@ -297,45 +301,87 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
     for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) pj[c] = red[c];
 }
 
-// dw[c] += sum_j partial[j][c]; db[c] += sum_j partial[j][C+c]  (j in order)
-__global__ void layernorm_backward_reduce(float* __restrict__ dw, float* __restrict__ db,
-                                          const float* __restrict__ partial, int G, int C) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= 2 * C) return;
-    float s = 0.f;
-    for (int j = 0; j < G; j++) s += partial[(size_t)j * 2 * C + c];
-    if (c < C) dw[c] += s; else db[c - C] += s;
+// Column sums of a (G x W) fp32 partial matrix, in a fixed order: a 256-thread block
+// takes 32 columns; thread (c, g) sums rows g, g+8, g+16, ... of column c, then the
+// eight group sums are added in group order.  Column w < split goes to out0[w], the
+// rest to out1[w - split] (both accumulate).
+#define CR_COLS 32
+#define CR_GROUPS 8
+__global__ void __launch_bounds__(CR_COLS * CR_GROUPS)
+column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
+                     const float* __restrict__ partial, int G, int W) {
+    __shared__ float sm[CR_GROUPS][CR_COLS];
+    const int c = threadIdx.x % CR_COLS, g = threadIdx.x / CR_COLS;
+    const int w = blockIdx.x * CR_COLS + c;
+    float s0 = 0.f, s1 = 0.f;
+    if (w < W) {
+        int j = g;
+        for (; j + CR_GROUPS < G; j += 2 * CR_GROUPS) {
+            s0 += partial[(size_t)j * W + w];
+            s1 += partial[(size_t)(j + CR_GROUPS) * W + w];
+        }
+        if (j < G) s0 += partial[(size_t)j * W + w];
+    }
+    sm[g][c] = s0 + s1;
+    __syncthreads();
+    if (g == 0 && w < W) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < CR_GROUPS; k++) s += sm[k][c];
+        if (w < split) out0[w] += s; else out1[w - split] += s;
+    }
 }
 
 // ============================================================== column sums (bias grads)
-// partial[r][n] = sum of x[m][n] over rows m of chunk r (in order); then
-// out[n] += sum_r partial[r][n] (in order).
+// partial[r][n] = sum of x[m][n] over the rows m of chunk r, in row order (a thread
+// owns one 16-byte packet of columns); column_reduce_kernel then adds the chunks.
 template <typename T>
 __global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x,
                                       int M, int N, int rows_per_chunk) {
-    int n = blockIdx.x * blockDim.x + threadIdx.x;
-    int r = blockIdx.y;
+    constexpr int EPV = Vec<T>::N;
+    const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+    const int r = blockIdx.y;
+    if (cv * EPV >= N) return;
+    const int m0 = r * rows_per_chunk, m1 = min(M, m0 + rows_per_chunk);
+    float s[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; e++) s[e] = 0.f;
+    int m = m0;
+    for (; m + 1 < m1; m += 2) {
+        Vec<T> a = load_vec(x + (size_t)m * N + cv * EPV);
+        Vec<T> b = load_vec(x + (size_t)(m + 1) * N + cv * EPV);
+#pragma unroll
+        for (int e = 0; e < EPV; e++) s[e] += a.get(e) + b.get(e);
+    }
+    if (m < m1) {
+        Vec<T> a = load_vec(x + (size_t)m * N + cv * EPV);
+#pragma unroll
+        for (int e = 0; e < EPV; e++) s[e] += a.get(e);
+    }
+    float* p = partial + (size_t)r * N + cv * EPV;
+#pragma unroll
+    for (int e = 0; e < EPV; e++) p[e] = s[e];
+}
+// one column per thread, for widths that are not a multiple of the packet
+template <typename T>
+__global__ void colsum_partial_scalar_kernel(float* __restrict__ partial, const T* __restrict__ x,
+                                             int M, int N, int rows_per_chunk) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    const int r = blockIdx.y;
     if (n >= N) return;
-    int m0 = r * rows_per_chunk, m1 = min(M, m0 + rows_per_chunk);
+    const int m0 = r * rows_per_chunk, m1 = min(M, m0 + rows_per_chunk);
     float s = 0.f;
     for (int m = m0; m < m1; m++) s += to_f32(x[(size_t)m * N + n]);
     partial[(size_t)r * N + n] = s;
 }
-__global__ void colsum_final_kernel(float* __restrict__ out, const float* __restrict__ partial,
-                                    int R, int N) {
-    int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
-    float s = 0.f;
-    for (int r = 0; r < R; r++) s += partial[(size_t)r * N + n];
-    out[n] += s;
-}
 
 // ============================================================== softmax + cross-entropy
 // One block per row of logits (Vp entries).  Pass 1: online max / sum of exp over the V
-// real columns; lse = max + log(sum); loss = lse - z[target].  Pass 2 overwrites the row
-// with d(mean loss)/dz = (exp(z - lse) - [j == target]) * dloss for j < V and 0 for the
-// padded columns.  Without targets the kernel is not launched.
+// real columns; lse = max + log(sum); loss = lse - z[target].  Pass 2 (the row is still
+// in L2) overwrites it with d(mean loss)/dz = (exp(z - lse) - [j == target]) * dloss for
+// j < V and 0 for the padded columns.  exp(a) is computed as exp2(a * log2 e).
 #define XENT_THREADS 1024
+#define XENT_LOG2E 1.4426950408889634f
 template <typename T>
 __global__ void __launch_bounds__(XENT_THREADS)
 softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
@@ -352,59 +398,62 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
         if (!tgt_ok) raise_error(err, ERRBIT_TOKEN);
         sm_zt = tgt_ok ? to_f32(z[tgt]) : 0.f;
     }
+    const int nfull = V / EPV;              // packets whose columns are all real
     const int nvec = Vp / EPV;
-    float mx = -INFINITY, sum = 0.f;
+    // pass 1, in the log2 domain: mx2 = max(z) log2e, sum = sum 2^(z log2e - mx2)
+    float mx2 = -INFINITY, sum = 0.f;
     for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
         Vec<T> p = load_vec(z + (size_t)vi * EPV);
+        float y[EPV];
         float vmax = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < EPV; e++)
-            if (vi * EPV + e < V) vmax = fmaxf(vmax, p.get(e));
+        for (int e = 0; e < EPV; e++) {
+            y[e] = (vi < nfull || vi * EPV + e < V) ? p.get(e) * XENT_LOG2E : -INFINITY;
+            vmax = fmaxf(vmax, y[e]);
+        }
         if (vmax == -INFINITY) continue;
-        float nm = fmaxf(mx, vmax);
-        float s = sum * expf(mx - nm);
+        const float nm = fmaxf(mx2, vmax);
+        float acc = sum * exp2f(mx2 - nm);
 #pragma unroll
-        for (int e = 0; e < EPV; e++)
-            if (vi * EPV + e < V) s += expf(p.get(e) - nm);
-        mx = nm;
-        sum = s;
+        for (int e = 0; e < EPV; e++) acc += exp2f(y[e] - nm);
+        mx2 = nm;
+        sum = acc;
     }
-    // combine (max, sum) pairs: within the warp, then across warps in order
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        float om = __shfl_xor_sync(0xffffffffu, mx, o), os = __shfl_xor_sync(0xffffffffu, sum, o);
-        float nm = fmaxf(mx, om);
-        float a = (mx == -INFINITY) ? 0.f : sum * expf(mx - nm);
-        float b = (om == -INFINITY) ? 0.f : os * expf(om - nm);
-        mx = nm;
+        const float om = __shfl_xor_sync(0xffffffffu, mx2, o), os = __shfl_xor_sync(0xffffffffu, sum, o);
+        const float nm = fmaxf(mx2, om);
+        const float a = (mx2 == -INFINITY) ? 0.f : sum * exp2f(mx2 - nm);
+        const float b = (om == -INFINITY) ? 0.f : os * exp2f(om - nm);
+        mx2 = nm;
         sum = a + b;
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) { sm_m[warp] = mx; sm_s[warp] = sum; }
+    if (lane == 0) { sm_m[warp] = mx2; sm_s[warp] = sum; }
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = -INFINITY, S = 0.f;
         for (int wi = 0; wi < (int)(blockDim.x >> 5); wi++) {
-            float om = sm_m[wi], os = sm_s[wi];
-            float nm = fmaxf(M, om);
-            float a = (M == -INFINITY) ? 0.f : S * expf(M - nm);
-            float b = (om == -INFINITY) ? 0.f : os * expf(om - nm);
+            const float om = sm_m[wi], os = sm_s[wi];
+            const float nm = fmaxf(M, om);
+            const float a = (M == -INFINITY) ? 0.f : S * exp2f(M - nm);
+            const float b = (om == -INFINITY) ? 0.f : os * exp2f(om - nm);
             M = nm;
             S = a + b;
         }
-        float lse = M + logf(S);
-        sm_lse = lse;
-        losses[row] = tgt_ok ? (lse - sm_zt) : 0.f;
+        const float lse2 = M + log2f(S);            // log2 of sum exp(z)
+        sm_lse = lse2;
+        losses[row] = tgt_ok ? (lse2 / XENT_LOG2E - sm_zt) : 0.f;
     }
     __syncthreads();
-    const float lse = sm_lse;
+    const float lse2 = sm_lse;
     for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
         Vec<T> p = load_vec(z + (size_t)vi * EPV), o;
 #pragma unroll
         for (int e = 0; e < EPV; e++) {
-            int j = vi * EPV + e;
+            const int j = vi * EPV + e;
             float d = 0.f;
-            if (j < V) d = (expf(p.get(e) - lse) - (j == tgt ? 1.f : 0.f)) * dloss;
+            if (j < V) d = (exp2f(fmaf(p.get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
             o.set(e, d);
         }
         store_vec(z + (size_t)vi * EPV, o);
