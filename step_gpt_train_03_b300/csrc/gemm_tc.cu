@@ -14,8 +14,12 @@
 //   warp 0      TMA producer: 128x64 A tile and BNx64 B tile per stage, 4-stage ring
 //   warp 1      TMEM owner and MMA issuer (one thread): 128xBN fp32 accumulator,
 //               two accumulators in TMEM so the epilogue of tile i overlaps tile i+1
-//   warps 2-5   epilogue: tcgen05.ld the accumulator rows, fuse bias / GELU /
-//               residual / GELU-backward / fp32 accumulate, store
+//   warps 2-5   epilogue: tcgen05.ld 32 rows x 64 columns of the accumulator, fuse
+//               bias / GELU / residual / GELU-backward, stage the chunk in a
+//               128B-swizzled shared buffer and write it with one TMA store (fp32
+//               weight gradients: one TMA reduce-add, so each element is added once);
+//               residual and pre-activation inputs arrive by TMA load into the same
+//               buffer
 // Every mbarrier wait is bounded: on expiry the kernel raises the timeout bit in the
 // library's error word, the other roles see the abort flag and stop, in-flight copies
 // and MMAs are waited for (again bounded), TMEM is freed and the kernel returns.
@@ -87,6 +91,33 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"((uint64_t)map), "r"(smem_u32(src)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"((uint64_t)map), "r"(smem_u32(src)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// hardware tanh (relative error ~2^-11, below the bf16 rounding of the stored result)
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_fast(float x) {
+    return 0.5f * x * (1.0f + tanh_fast(GELU_K0 * (x + GELU_K1 * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_fast(float x) {
+    const float th = tanh_fast(GELU_K0 * (x + GELU_K1 * x * x * x));
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GELU_K0 * (1.0f + 3.0f * GELU_K1 * x * x);
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
@@ -147,78 +178,24 @@ struct TcSmem {
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
     static constexpr int B_BYTES = BN * TC_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int BAR_OFF = TC_STAGES * STAGE_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], done, then tmem address + abort flag
-    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 5) * 8 + 16 + 1024;
+    // two 4 KB staging buffers (32 rows x 128 bytes) per epilogue warp
+    static constexpr int STG_OFF = TC_STAGES * STAGE_BYTES;
+    static constexpr int STG_BYTES = 4096;
+    static constexpr int BAR_OFF = STG_OFF + 4 * 2 * STG_BYTES;
+    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[4]; tmem address, abort flag
+    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 9) * 8 + 16 + 1024;
 };
 
-template <int EPI>
-__device__ __forceinline__ void tc_epilogue_store(const TcEpi& ep, int grow, int col, int nvalid,
-                                                  const uint32_t (&r)[32], int M, int N) {
-    // 32 consecutive columns [col, col+32) of row grow; nvalid of them are < N
-    if (grow >= M || nvalid <= 0) return;
-    const size_t o = (size_t)grow * ep.ldo + col;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
-    if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
-        float* out = reinterpret_cast<float*>(ep.out) + o;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            if (q * 4 >= nvalid) break;
-            float4 a = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if constexpr (EPI == EPI_ACC_F32) {
-                float4 b = *reinterpret_cast<const float4*>(out + 4 * q);
-                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            *reinterpret_cast<float4*>(out + 4 * q) = a;
-        }
-        return;
-    } else {
-        if (ep.bias && EPI != EPI_GELU_BWD) {
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                if (q * 8 >= nvalid) break;
-                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
-            }
-        }
-        bf16* out = reinterpret_cast<bf16*>(ep.out) + o;
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            if (q * 8 >= nvalid) break;
-            Vec<bf16> res;
-            if constexpr (EPI == EPI_STORE) {
-#pragma unroll
-                for (int e = 0; e < 8; e++) res.set(e, v[8 * q + e]);
-            } else if constexpr (EPI == EPI_GELU) {
-                Vec<bf16> pre;
-#pragma unroll
-                for (int e = 0; e < 8; e++) pre.set(e, v[8 * q + e]);
-                store_vec(reinterpret_cast<bf16*>(ep.aux) + o + 8 * q, pre);
-#pragma unroll
-                for (int e = 0; e < 8; e++) res.set(e, gelu_f(pre.get(e)));
-            } else if constexpr (EPI == EPI_RESID) {
-                Vec<bf16> rs = load_vec(reinterpret_cast<const bf16*>(ep.aux) + o + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 8; e++) res.set(e, rs.get(e) + v[8 * q + e]);
-            } else if constexpr (EPI == EPI_GELU_BWD) {
-                Vec<bf16> pre = load_vec(reinterpret_cast<const bf16*>(ep.aux) + o + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 8; e++) res.set(e, v[8 * q + e] * gelu_grad_f(pre.get(e)));
-            }
-            store_vec(out + 8 * q, res);
-        }
-    }
-}
+// byte offset of 16-byte chunk j of row r in a 128B-swizzled staging buffer
+__device__ __forceinline__ int stg_off(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
 
 // D (M x N) over units = m_tiles x n_tiles x splits, n fastest.  Split s of a tile
 // covers k-blocks [s*kb_per, min(nkb, (s+1)*kb_per)); partial epilogues write tile
 // (s) of the scratch at out + s*M*ldo.
 template <int BN, int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux, int M, int N,
                int K, int splits, TcEpi ep, unsigned* err) {
     using S = TcSmem<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -228,7 +205,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* acc_full = empty + TC_STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* aux_bar = done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,10 +219,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < TC_STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
         mbar_init(done, 1);
+        for (int i = 0; i < 4; i++) mbar_init(&aux_bar[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmOut);
+        if (EPI == EPI_GELU || EPI == EPI_RESID || EPI == EPI_GELU_BWD) tma_prefetch_desc(&tmAux);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -337,10 +318,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else {
         // ---------------------------------------------------------- epilogue warps 2..5
+        const int ew = warp - 2;                       // epilogue warp 0..3
         const int lane_grp = warp & 3;                 // TMEM lanes 32*lane_grp .. +31
-        const int row = lane_grp * 32 + lane;
+        uint8_t* stg = smem + S::STG_OFF + ew * 2 * S::STG_BYTES;
+        uint64_t* auxb = &aux_bar[ew];
+        uint32_t aux_phase = 0;
+        int nbuf = 0;                                  // staging buffer in use: nbuf & 1
         int local = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, local++) {
+        bool alive = true;
+        for (int u = blockIdx.x; u < units && alive; u += gridDim.x, local++) {
             const int sp = u % splits, tile = u / splits;
             const int nt = tile % n_tiles, mt = tile / n_tiles;
             const int acc = local & 1;
@@ -352,21 +338,115 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!okw) break;
             __syncwarp();
             tc_fence_after();
-            const int grow = mt * TC_BM + row;
-            TcEpi e = ep;
-            if constexpr (EPI == TC_EPI_PARTIAL) e.out = reinterpret_cast<float*>(ep.out) + (size_t)sp * M * ep.ldo;
+            const int row0 = mt * TC_BM + lane_grp * 32;   // first of this warp's 32 rows
+            const int yout = (EPI == TC_EPI_PARTIAL) ? sp * M + row0 : row0;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((uint32_t)(lane_grp * 32) << 16) + acc * BN + c, r);
-                tmem_ld_wait();
+            for (int c = 0; c < BN; c += 64) {
                 const int col = nt * BN + c;
-                tc_epilogue_store<EPI>(e, grow, col, N - col, r, M, N);
+                if (col >= N) break;
+                uint32_t r0[32], r1[32];
+                const uint32_t ta = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + acc * BN + c;
+                tmem_ld32(ta, r0);
+                tmem_ld32(ta + 32, r1);
+                tmem_ld_wait();
+                float v[64];
+#pragma unroll
+                for (int i = 0; i < 32; i++) { v[i] = __uint_as_float(r0[i]); v[32 + i] = __uint_as_float(r1[i]); }
+                if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            *reinterpret_cast<float4*>(sb + stg_off(lane, j)) =
+                                make_float4(v[32 * h + 4 * j], v[32 * h + 4 * j + 1], v[32 * h + 4 * j + 2],
+                                            v[32 * h + 4 * j + 3]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && col + 32 * h < N) {
+                            if constexpr (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmOut, sb, col + 32 * h, yout);
+                            else tma_store_2d(&tmOut, sb, col + 32 * h, yout);
+                            bulk_commit();
+                        }
+                        nbuf++;
+                    }
+                } else {
+                    if (ep.bias && EPI != EPI_GELU_BWD) {
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            if (col + 8 * q < N) {
+                                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
+#pragma unroll
+                                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+                            }
+                        }
+                    }
+                    uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD) {
+                        // the residual / pre-activation tile of these 32 rows x 64 columns
+                        if (lane == 0) {
+                            mbar_expect_tx(auxb, S::STG_BYTES);
+                            tma_load_2d(sb, &tmAux, auxb, col, row0);
+                        }
+                        int oka = 1;
+                        if (lane == 0) oka = mbar_wait(auxb, aux_phase, abort_flag, err) ? 1 : 0;
+                        oka = __shfl_sync(0xffffffffu, oka, 0);
+                        aux_phase ^= 1;
+                        if (!oka) { alive = false; break; }
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            Vec<bf16> a;
+                            a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
+#pragma unroll
+                            for (int e = 0; e < 8; e++) {
+                                if constexpr (EPI == EPI_RESID) v[8 * j + e] += a.get(e);
+                                else v[8 * j + e] *= gelu_grad_fast(a.get(e));
+                            }
+                        }
+                    } else if constexpr (EPI == EPI_GELU) {
+                        // pre-activation out first, then the activation into the other buffer
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            Vec<bf16> o;
+#pragma unroll
+                            for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                            *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+#pragma unroll
+                            for (int e = 0; e < 8; e++) v[8 * j + e] = gelu_fast(o.get(e));
+                        }
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0); bulk_commit(); }
+                        nbuf++;
+                        sb = stg + (nbuf & 1) * S::STG_BYTES;
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        Vec<bf16> o;
+#pragma unroll
+                        for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
+                    nbuf++;
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
+        // every store this warp issued has completed before the CTA retires
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -426,25 +506,27 @@ size_t gemm_tc_scratch_floats(size_t M, size_t N) {
     return (size_t)TC_MAX_SPLITS * TC_SPLIT_SM_BOUND * TC_BM * 256;
 }
 
-// 2-D bf16 tensor map: inner dimension `inner` (contiguous), outer `outer`, row pitch
-// `ld` elements; box {64, box_outer}; 128-byte swizzle; out-of-range reads give zero.
+// 2-D tensor map: inner dimension `inner` (contiguous), outer `outer`, row pitch `ld`
+// elements of `ebytes` bytes; box {box_inner, box_outer} (box_inner * ebytes = 128);
+// 128-byte swizzle; out-of-range reads give zero and out-of-range writes are dropped.
 static bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-                     uint32_t box_outer) {
+                     uint32_t box_outer, int ebytes = 2) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {64, box_outer};
+    cuuint64_t strides[1] = {ld * ebytes};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / ebytes), box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, ebytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 template <int BN, int EPI, bool A_MN, bool B_MN>
-static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                     int splits, const TcEpi& ep, unsigned* err) {
+static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                     const CUtensorMap& tx, int M, int N, int K, int splits, const TcEpi& ep, unsigned* err) {
     using SM = TcSmem<BN>;
     static bool attr_set = false;
     auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN>;
@@ -455,7 +537,7 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
     }
     const int units = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN) * splits;
     const int grid = units < g_num_sms ? units : g_num_sms;
-    kern<<<grid, TC_THREADS, SM::TOTAL, s>>>(ta, tb, M, N, K, splits, ep, err);
+    kern<<<grid, TC_THREADS, SM::TOTAL, s>>>(ta, tb, to, tx, M, N, K, splits, ep, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
@@ -466,13 +548,19 @@ int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, c
     if (N % 8 || K % 8 || M < 1 || !aligned16(out) || !aligned16(inp) || !aligned16(W) ||
         (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
         return GPT2_EUNSUPPORTED;
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, inp, K, M, K, TC_BM) || !make_map(&tb, W, K, N, K, 256)) return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb, to, tx;
+    if (!make_map(&ta, inp, K, M, K, TC_BM) || !make_map(&tb, W, K, N, K, 256) || !make_map(&to, out, N, M, N, 32))
+        return GPT2_EUNSUPPORTED;
+    if (aux) {
+        if (!make_map(&tx, aux, N, M, N, 32)) return GPT2_EUNSUPPORTED;
+    } else {
+        tx = to;
+    }
     TcEpi ep{out, bias, aux, (long)N};
     switch (epi) {
-        case EPI_STORE: return launch_tc<256, EPI_STORE, false, false>(s, ta, tb, M, N, K, 1, ep, err);
-        case EPI_GELU: return launch_tc<256, EPI_GELU, false, false>(s, ta, tb, M, N, K, 1, ep, err);
-        case EPI_RESID: return launch_tc<256, EPI_RESID, false, false>(s, ta, tb, M, N, K, 1, ep, err);
+        case EPI_STORE: return launch_tc<256, EPI_STORE, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_GELU: return launch_tc<256, EPI_GELU, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_RESID: return launch_tc<256, EPI_RESID, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
         default: return GPT2_EUNSUPPORTED;
     }
 }
@@ -485,11 +573,17 @@ int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16
     if (N % 8 || K % 8 || M < 1 || !aligned16(dinp) || !aligned16(dout) || !aligned16(W) ||
         (aux && !aligned16(aux)))
         return GPT2_EUNSUPPORTED;
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, dout, N, M, N, TC_BM) || !make_map(&tb, W, K, N, K, 64)) return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb, to, tx;
+    if (!make_map(&ta, dout, N, M, N, TC_BM) || !make_map(&tb, W, K, N, K, 64) || !make_map(&to, dinp, K, M, K, 32))
+        return GPT2_EUNSUPPORTED;
+    if (aux) {
+        if (!make_map(&tx, aux, K, M, K, 32)) return GPT2_EUNSUPPORTED;
+    } else {
+        tx = to;
+    }
     TcEpi ep{dinp, nullptr, (void*)aux, (long)K};
-    if (epi == EPI_GELU_BWD) return launch_tc<256, EPI_GELU_BWD, false, true>(s, ta, tb, M, K, N, 1, ep, err);
-    if (epi == EPI_STORE) return launch_tc<256, EPI_STORE, false, true>(s, ta, tb, M, K, N, 1, ep, err);
+    if (epi == EPI_GELU_BWD) return launch_tc<256, EPI_GELU_BWD, false, true>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
+    if (epi == EPI_STORE) return launch_tc<256, EPI_STORE, false, true>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
     return GPT2_EUNSUPPORTED;
 }
 
@@ -516,18 +610,23 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
     if (N % 8 || K % 8 || M < 1 || !aligned16(dW) || !aligned16(dout) || !aligned16(inp))
         return GPT2_EUNSUPPORTED;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, to;
     if (!make_map(&ta, dout, N, M, N, 64) || !make_map(&tb, inp, K, M, K, 64)) return GPT2_EUNSUPPORTED;
     const int tiles = ((N + TC_BM - 1) / TC_BM) * ((K + 255) / 256);
     const int nkb = (M + TC_BK - 1) / TC_BK;
     int splits = choose_splits(tiles, nkb);
-    if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch))) splits = 1;
+    // partial tiles of split s are rows [s*N, (s+1)*N) of one map, so a tile must not
+    // straddle two splits: N a multiple of the 128-row tile
+    if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch) || N % TC_BM))
+        splits = 1;
     if (splits == 1) {
+        if (!make_map(&to, dW, K, N, K, 32, 4)) return GPT2_EUNSUPPORTED;
         TcEpi ep{dW, nullptr, nullptr, (long)K};
-        return launch_tc<256, EPI_ACC_F32, true, true>(s, ta, tb, N, K, M, 1, ep, err);
+        return launch_tc<256, EPI_ACC_F32, true, true>(s, ta, tb, to, to, N, K, M, 1, ep, err);
     }
+    if (!make_map(&to, scratch, K, (uint64_t)splits * N, K, 32, 4)) return GPT2_EUNSUPPORTED;
     TcEpi ep{scratch, nullptr, nullptr, (long)K};
-    int rc = launch_tc<256, TC_EPI_PARTIAL, true, true>(s, ta, tb, N, K, M, splits, ep, err);
+    int rc = launch_tc<256, TC_EPI_PARTIAL, true, true>(s, ta, tb, to, to, N, K, M, splits, ep, err);
     if (rc != GPT2_OK) return rc;
     const size_t n4 = (size_t)N * K / 4;
     splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(dW, scratch, n4, splits);
