@@ -215,6 +215,23 @@ int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias, c
                                     const float* inp, const float* weight, const float* mean,
                                     const float* rstd, int N, int C, void* stream);
 
+/* Causal self-attention forward over qkv (B,T,3C) (q, k, v thirds; head h uses columns
+ * [h*hs, (h+1)*hs) of each, hs = C/NH): out (B,T,C) = softmax(q k^T / sqrt(hs) over keys
+ * j <= t) v, heads concatenated.  precision GPT2_BF16: bf16 tensors, lse (B,NH,T) fp32
+ * receives each score row's log-sum-exp (natural log) for the backward; GPT2_FP32: fp32
+ * tensors, and `lse` must hold the probabilities instead: (B,NH,T,T) fp32.
+ * T <= 1024 (fp32: any T); hs <= 128. */
+int gpt2_attention_forward(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
+                           int precision, void* stream);
+
+/* Backward: dqkv (B,T,3C) [overwritten] from dout (B,T,C) and the forward's qkv, out
+ * and lse (fp32 path: probabilities).  scratch (device): bf16 path (B,NH,T) fp32 row
+ * sums; fp32 path (B,NH,T,T) fp32; size from gpt2_attention_backward_scratch_bytes. */
+size_t gpt2_attention_backward_scratch_bytes(int B, int T, int NH, int precision);
+int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
+                            const float* lse, int B, int T, int C, int NH, int precision,
+                            void* scratch, size_t scratch_bytes, void* stream);
+
 /* Matmul forward: out (M,N) = inp (M,K) * weight(N,K)^T + bias (N, nullable).
  * precision GPT2_FP32: all float*; GPT2_BF16: out, inp, weight, bias are bf16 (bias
  * nullable), fp32 accumulation. */

@@ -14,6 +14,7 @@
 #include "../../include/gpt2.h"
 #include "runtime.h"
 #include "attention_mma.cuh"
+#include "attention_tc.h"
 
 #define FA_WARPS 8
 #define FA_MAX_HS 128
@@ -74,19 +75,22 @@ fa_forward_simt(bf16* __restrict__ out, float* __restrict__ lse, const bf16* __r
     if (lane == 0) lse[((size_t)b * NH + h) * Tn + t] = mx + logf(sum);
 }
 
-// D[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]
+// D[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; one thread per (b, t, h), 16-byte loads
+// (hs a multiple of 8)
 __global__ void fa_backward_D(float* __restrict__ D, const bf16* __restrict__ dout,
                               const bf16* __restrict__ out, int B, int Tn, int C, int NH) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gw = blockIdx.x * FA_WARPS + warp;
-    if (gw >= B * NH * Tn) return;
-    const int t = gw % Tn, h = (gw / Tn) % NH, b = gw / (Tn * NH);
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= B * Tn * NH) return;
+    const int h = idx % NH, bt = idx / NH, b = bt / Tn, t = bt % Tn;
     const int hs = C / NH;
-    const size_t o = ((size_t)b * Tn + t) * C + h * hs;
+    const size_t o = (size_t)bt * C + h * hs;
     float s = 0.f;
-    for (int d = lane; d < hs; d += 32) s += __bfloat162float(dout[o + d]) * __bfloat162float(out[o + d]);
-    s = warp_sum(s);
-    if (lane == 0) D[((size_t)b * NH + h) * Tn + t] = s;
+    for (int d = 0; d < hs; d += 8) {
+        Vec<bf16> a = load_vec(dout + o + d), c = load_vec(out + o + d);
+#pragma unroll
+        for (int e = 0; e < 8; e++) s += a.get(e) * c.get(e);
+    }
+    D[((size_t)b * NH + h) * Tn + t] = s;
 }
 
 // dQ, one warp per query row t: dq = scale * sum_{j<=t} P_tj (dP_tj - D_t) k_j
@@ -207,10 +211,12 @@ fa_backward_dkv_simt(bf16* __restrict__ dqkv, const bf16* __restrict__ dout, con
 }
 
 int attention_flash_forward(cudaStream_t s, bf16* out, float* lse, const bf16* qkv, int B, int Tn, int C,
-                            int NH) {
+                            int NH, unsigned* err) {
     const int hs = C / NH;
     if (hs > FA_MAX_HS) return GPT2_EUNSUPPORTED;
     if (hs == AM_HS) {
+        int rc = attention_tc_forward(s, out, lse, qkv, B, Tn, C, NH, err);
+        if (rc != GPT2_EUNSUPPORTED) return rc;
         dim3 grid((Tn + AMF_Q - 1) / AMF_Q, B * NH);
         attention_forward_mma<<<grid, AMF_THREADS, 0, s>>>(out, lse, qkv, B, Tn, C, NH);
         rt_note_launches(1);
@@ -230,14 +236,16 @@ int attention_flash_forward(cudaStream_t s, bf16* out, float* lse, const bf16* q
 }
 
 int attention_flash_backward(cudaStream_t s, bf16* dqkv, const bf16* dout, const bf16* qkv, const bf16* out,
-                             const float* lse, float* scratch, int B, int Tn, int C, int NH) {
+                             const float* lse, float* scratch, int B, int Tn, int C, int NH, unsigned* err) {
     const int hs = C / NH;
     if (hs > FA_MAX_HS) return GPT2_EUNSUPPORTED;
     const int rows = B * NH * Tn;
     const int grid = ceil_div(rows, FA_WARPS);
     rt_note_launches(3);
-    fa_backward_D<<<grid, FA_WARPS * 32, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
+    fa_backward_D<<<ceil_div(rows, 256), 256, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
     if (hs == AM_HS) {
+        int rc = attention_tc_backward(s, dqkv, dout, qkv, lse, scratch, B, Tn, C, NH, err);
+        if (rc != GPT2_EUNSUPPORTED) return rc;
         dim3 g2((Tn + AMB_ROWS - 1) / AMB_ROWS, B * NH);
         attention_backward_dkv_mma<<<g2, AMB_THREADS, 0, s>>>(dqkv, dout, qkv, lse, scratch, B, Tn, C, NH);
         attention_backward_dq_mma<<<g2, AMB_THREADS, 0, s>>>(dqkv, dout, qkv, lse, scratch, B, Tn, C, NH);

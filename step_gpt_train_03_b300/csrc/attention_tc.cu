@@ -1,0 +1,864 @@
+// Causal flash attention for head size 64 on the sm_103a tensor cores (tcgen05, TMEM,
+// TMA).
+//
+// ujoy.net llm.c article, section "用C语言实现LLM": causal self-attention forward and
+// backward.  Per head: S = Q K^T / sqrt(64) over keys j <= t, P = softmax(S), O = P V;
+// the forward keeps O and each row's log-sum-exp only.
+//
+// Forward kernel, persistent, one CTA per SM, 320 threads; work item = (128-query
+// tile, batch*head), heaviest tiles (most keys) first:
+//   warp 0     TMA producer: Q tile (double-buffered across work items), then K and V
+//              tiles of 128 keys through a 4-slot ring
+//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M=128, N=128, K=64) into one of two
+//              TMEM S buffers, then O += P V (M=128, N=64, K=128) into the TMEM O buffer
+//   warps 2-9  softmax, two warps per query row quadrant (each takes half the keys of a
+//              tile): read the S row from TMEM, keep the running max / sum, write P
+//              (bf16) into one of two shared buffers for the P V product; at the end
+//              normalise O and write it with a TMA store, plus the row LSE
+// The softmax reads each S row from TMEM twice, 32 columns at a time (max, then the
+// exponentials), which keeps the code small and the reductions short (trees).
+// The exponent reference of a row (its max so far) is only raised when a new score
+// exceeds it by more than 2^8: then, and only then, the row of O in TMEM is rescaled
+// (after waiting for the P V in flight).  Numerator and denominator always use the same
+// reference, so O / l is exact; p <= 256 stays far inside fp32 and bf16 range.  With P
+// double-buffered, the softmax of tile j+1 never waits for P V of tile j, and S(j+1) is
+// computed while the softmax works on tile j.  Every wait is bounded.
+// The tensor maps are 3-D (columns, T, B) so no tile ever reads or writes past its own
+// sequence.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "attention_tc.h"
+#include "common.cuh"
+#include "runtime.h"
+#include "tc_ptx.cuh"
+#include "../../include/gpt2.h"
+
+#define AT_HS 64
+#define AT_BM 128                  // queries per tile
+#define AT_BN 128                  // keys per tile
+#define AT_RING 4                  // K / V tile slots: K_{j+1} never waits on P V_{j-1}
+#define AT_TILE_BYTES (128 * 64 * 2)
+#define AT_THREADS 320               // producer, MMA issuer, 8 compute warps (2 per TMEM lane quadrant)
+#define AT_LOG2E 1.4426950408889634f
+
+#define AT_RESCALE_LOG2 8.0f        // raise a row's exponent reference only past 2^8
+
+// 2^x with the hardware approximation (2 ulp); 2^-inf = 0.  P is rounded to bf16 and
+// the row sum carries the same values, so the approximation cancels in O / l.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+struct AtSmem {
+    static constexpr int Q_OFF = 0;                                          // 2 x 16 KB
+    static constexpr int RING_OFF = Q_OFF + 2 * AT_TILE_BYTES;
+    static constexpr int P_OFF = RING_OFF + AT_RING * AT_TILE_BYTES;         // 2 x (2 x 16 KB)
+    static constexpr int O_OFF = P_OFF + 4 * AT_TILE_BYTES;                  // output staging
+    static constexpr int X_OFF = O_OFF + AT_TILE_BYTES;                      // row max / sum exchange
+    static constexpr int BAR_OFF = X_OFF + 3 * 1024;
+    // q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], s_free[2],
+    // p_full[2], o_done[2], o_free, done; then tmem address and abort flag
+    static constexpr int NBAR = 4 + 2 * AT_RING + 4 + 4 + 2;
+    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmO,
+                            float* __restrict__ lse, int B, int Tn, int C, int NH, unsigned* err) {
+    using S = AtSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+    uint64_t* q_full = bars;
+    uint64_t* q_empty = bars + 2;
+    uint64_t* ring_full = bars + 4;
+    uint64_t* ring_empty = ring_full + AT_RING;
+    uint64_t* s_full = ring_empty + AT_RING;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* o_done = p_full + 2;
+    uint64_t* o_free = o_done + 2;
+    uint64_t* done = o_free + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = B * NH;
+    const int nqt = (Tn + AT_BM - 1) / AT_BM;
+    const int n_items = nqt * BH;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+        for (int i = 0; i < AT_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 1); }
+        for (int i = 0; i < 2; i++) { mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 8); }
+        for (int i = 0; i < 2; i++) { mbar_init(&p_full[i], 8); mbar_init(&o_done[i], 1); }
+        mbar_init(o_free, 8);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmQKV);
+        tma_prefetch_desc(&tmO);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(512) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t TM_S = tmem_base;          // S buffers at columns 0 and 128
+    const uint32_t TM_O = tmem_base + 256;    // O at columns 256..319
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int rc = 0, local = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
+                const int qt = nqt - 1 - it / BH, bh = it % BH, b = bh / NH, h = bh % NH;
+                const int qb = local & 1;
+                if (!mbar_wait(&q_empty[qb], ((local >> 1) & 1) ^ 1, abort_flag, err)) break;
+                mbar_expect_tx(&q_full[qb], AT_TILE_BYTES);
+                tma_load_3d(smem + S::Q_OFF + qb * AT_TILE_BYTES, &tmQKV, &q_full[qb], h * AT_HS, qt * AT_BM, b);
+                const int nk = qt + 1;
+                for (int j = 0; j < nk && ok; j++) {
+                    for (int kv = 0; kv < 2; kv++, rc++) {
+                        const int s = rc % AT_RING;
+                        if (!mbar_wait(&ring_empty[s], ((rc / AT_RING) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+                        mbar_expect_tx(&ring_full[s], AT_TILE_BYTES);
+                        tma_load_3d(smem + S::RING_OFF + s * AT_TILE_BYTES, &tmQKV, &ring_full[s],
+                                    (kv + 1) * C + h * AT_HS, j * AT_BN, b);
+                    }
+                }
+            }
+            // in-flight copies land before the CTA retires
+            for (int back = 0; back < AT_RING && back < rc; back++) {
+                const int k = rc - 1 - back;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&ring_full[k % AT_RING], (k / AT_RING) & 1))
+                    if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(AT_BM, AT_BN, false, false);
+            constexpr uint32_t IDESC_O = idesc_bf16(AT_BM, AT_HS, false, true);
+            int rc = 0, sc = 0, pc = 0, local = 0;
+            bool ok = true;
+            // S = Q K^T for the K tile at ring index kidx into S buffer sc % 2
+            auto issue_s = [&](uint32_t q_addr, int kidx) -> bool {
+                const int sb = sc & 1, slot = kidx % AT_RING;
+                if (!mbar_wait(&s_free[sb], ((sc >> 1) & 1) ^ 1, abort_flag, err)) return false;
+                if (!mbar_wait(&ring_full[slot], (kidx / AT_RING) & 1, abort_flag, err)) return false;
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(smem + S::RING_OFF + slot * AT_TILE_BYTES);
+#pragma unroll
+                for (int k = 0; k < AT_HS / 16; k++)
+                    tc_mma(TM_S + sb * AT_BN, sdesc(q_addr + k * 32, 16, 1024), sdesc(k_addr + k * 32, 16, 1024),
+                           IDESC_S, k > 0 ? 1u : 0u);
+                tc_commit(&s_full[sb]);
+                tc_commit(&ring_empty[slot]);
+                sc++;
+                return true;
+            };
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
+                const int qt = nqt - 1 - it / BH;
+                const int nk = qt + 1;
+                const int qb = local & 1;
+                if (!mbar_wait(&q_full[qb], (local >> 1) & 1, abort_flag, err)) break;
+                const uint32_t q_addr = smem_u32(smem + S::Q_OFF + qb * AT_TILE_BYTES);
+                // K_j sits at ring index rc + 2j, V_j at rc + 2j + 1
+                if (!issue_s(q_addr, rc)) break;
+                for (int j = 0; j < nk && ok; j++) {
+                    if (j + 1 < nk && !issue_s(q_addr, rc + 2 * (j + 1))) { ok = false; break; }
+                    if (j == nk - 1) tc_commit(&q_empty[qb]);   // Q buffer free once the last S completes
+                    // O += P_j V_j, P_j in buffer pc % 2
+                    const int vidx = rc + 2 * j + 1, vslot = vidx % AT_RING;
+                    const int pb = pc & 1;
+                    if (!mbar_wait(&ring_full[vslot], (vidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
+                    if (!mbar_wait(&p_full[pb], (pc >> 1) & 1, abort_flag, err)) { ok = false; break; }
+                    if (j == 0 && local > 0 && !mbar_wait(o_free, (local - 1) & 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t p_addr = smem_u32(smem + S::P_OFF + pb * 2 * AT_TILE_BYTES);
+                    const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vslot * AT_TILE_BYTES);
+#pragma unroll
+                    for (int k = 0; k < AT_BN / 16; k++)
+                        tc_mma(TM_O, sdesc(p_addr + (k >> 2) * AT_TILE_BYTES + (k & 3) * 32, 16, 1024),
+                               sdesc(v_addr + k * 2048, 8192, 1024), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(&o_done[pb]);
+                    tc_commit(&ring_empty[vslot]);
+                    pc++;
+                }
+                rc += 2 * nk;
+            }
+            tc_commit(done);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(done, 0))
+                if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps 2..9
+        // Two warps per TMEM lane quadrant: `half` picks columns [64*half, 64*half + 64) of
+        // every S tile (and [32*half, 32*half + 32) of O).  The pair swaps its row maxima
+        // through shared memory once per tile; the row sums stay split until the end.
+        const int lane_grp = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = lane_grp * 32 + lane;                 // query row in the tile
+        const uint32_t lrow = (uint32_t)(lane_grp * 32) << 16;
+        uint8_t* obuf = smem + S::O_OFF;
+        float* xmax = reinterpret_cast<float*>(smem + S::X_OFF);   // [tile parity][half][128]
+        float* xsum = xmax + 512;                                   // [half][128]
+        const int pair_bar = 2 + lane_grp;                          // named barrier of the pair
+        const float sl2 = AT_LOG2E * 0.125f;                // log2(e) / sqrt(64)
+        int sc = 0, pc = 0, local = 0;
+        int seen0 = 0, seen1 = 0;                           // o_done phases observed, per P buffer
+        bool alive = true;
+        // wait until P V number `i` has completed (phases of each buffer are observed in order)
+        auto wait_pv = [&](int i) -> bool {
+            const int bb = i & 1, ph = i >> 1;
+            if ((bb ? seen1 : seen0) > ph) return true;
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(&o_done[bb], ph & 1, abort_flag, err) ? 1 : 0;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            if (bb) seen1 = ph + 1; else seen0 = ph + 1;
+            __syncwarp();
+            return okw != 0;
+        };
+        for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x, local++) {
+            const int qt = nqt - 1 - it / BH, bh = it % BH, b = bh / NH, h = bh % NH;
+            const int nk = qt + 1;
+            const int q = qt * AT_BM + r;
+            const int pc0 = pc;                             // index of this item's first P V
+            float m = -INFINITY, l = 0.f;                   // exponent reference, partial running sum
+            for (int j = 0; j < nk; j++) {
+                const int sb = sc & 1;
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(&s_full[sb], (sc >> 1) & 1, abort_flag, err) ? 1 : 0;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (!okw) { alive = false; break; }
+                __syncwarp();
+                tc_fence_after();
+                const uint32_t srow = TM_S + sb * AT_BN + lrow;
+                // keys after the query are masked on the diagonal tile: columns > lim
+                const int lim = (j == nk - 1) ? (q - j * AT_BN) : AT_BN;
+                // pass 1: max over this warp's 64 columns, then over the pair
+                float mx = -INFINITY;
+                const bool masked = lim < AT_BN;            // only the diagonal tile
+#pragma unroll 1
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(srow + c, rr);
+                    tmem_ld_wait();
+                    float v[32];
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = (c + i <= lim) ? __uint_as_float(rr[i]) : -INFINITY;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(rr[i]);
+                    }
+#pragma unroll
+                    for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                        for (int i = 0; i < w; i++) v[i] = fmaxf(v[i], v[i + w]);
+                    mx = fmaxf(mx, v[0]);
+                }
+                mx *= sl2;                                  // scaling by sl2 > 0 keeps the max
+                float* xm = xmax + (sc & 1) * 256;
+                xm[half * 128 + r] = mx;
+                named_bar(pair_bar, 64);
+                mx = fmaxf(mx, xm[(half ^ 1) * 128 + r]);
+                // raise the reference only when needed; then O must be rescaled, after the
+                // P V still in flight for this item has landed
+                const bool raise = mx > m + AT_RESCALE_LOG2;
+                const float m_new = raise ? mx : m;
+                const float corr = ex2_fast(m - m_new);     // 1 when unchanged, 0 on the first tile
+                if (__any_sync(0xffffffffu, raise && j > 0)) {
+                    if (!wait_pv(pc0 + j - 1)) { alive = false; break; }
+                    tc_fence_after();
+                    uint32_t rr[32];
+                    tmem_ld32(TM_O + lrow + half * 32, rr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
+                    tmem_st32(TM_O + lrow + half * 32, rr);
+                    tmem_st_wait();
+                }
+                m = m_new;
+                // the P buffer of this tile was last read by P V two tiles back
+                const int pb = pc & 1;
+                if (pc >= 2 && !wait_pv(pc - 2)) { alive = false; break; }
+                uint8_t* pbuf = smem + S::P_OFF + pb * 2 * AT_TILE_BYTES;
+                // pass 2: p = 2^(s - m), partial row sum, P into the swizzled A operand
+                float rs = 0.f;
+#pragma unroll 1
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(srow + c, rr);
+                    tmem_ld_wait();
+                    float p[32];
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            p[i] = (c + i <= lim) ? ex2_fast(fmaf(__uint_as_float(rr[i]), sl2, -m)) : 0.f;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) p[i] = ex2_fast(fmaf(__uint_as_float(rr[i]), sl2, -m));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int ch = (c >> 3) + k;
+                        Vec<bf16> pv;
+#pragma unroll
+                        for (int e = 0; e < 8; e++) pv.set(e, p[8 * k + e]);
+                        *reinterpret_cast<uint4*>(pbuf + (ch >> 3) * AT_TILE_BYTES + r * 128 +
+                                                  (((ch & 7) ^ (r & 7)) << 4)) = pv.v;
+                    }
+#pragma unroll
+                    for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                        for (int i = 0; i < w; i++) p[i] += p[i + w];
+                    rs += p[0];
+                }
+                l = l * corr + rs;
+                tc_fence_before();
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s_free[sb]);
+                    mbar_arrive(&p_full[pb]);
+                }
+                sc++;
+                pc++;
+            }
+            if (!alive) break;
+            // the last P V of the item, then normalise and write this row of O
+            if (!wait_pv(pc - 1)) break;
+            tc_fence_after();
+            float o[32];
+            {
+                uint32_t rr[32];
+                tmem_ld32(TM_O + lrow + half * 32, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; i++) o[i] = __uint_as_float(rr[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            xsum[half * 128 + r] = l;
+            named_bar(pair_bar, 64);
+            const float lt = l + xsum[(half ^ 1) * 128 + r];
+            const float inv = 1.0f / lt;
+            // the previous item's O store must have finished reading the staging buffer
+            if (threadIdx.x == 64) bulk_wait_read<0>();
+            named_bar(1, 256);
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int ch = half * 4 + k;
+                Vec<bf16> ov;
+#pragma unroll
+                for (int e = 0; e < 8; e++) ov.set(e, o[8 * k + e] * inv);
+                *reinterpret_cast<uint4*>(obuf + r * 128 + ((ch ^ (r & 7)) << 4)) = ov.v;
+            }
+            fence_async_smem();
+            named_bar(1, 256);
+            if (threadIdx.x == 64) {
+                tma_store_3d(&tmO, obuf, h * AT_HS, qt * AT_BM, b);
+                bulk_commit();
+            }
+            if (half == 0 && q < Tn) lse[(size_t)bh * Tn + q] = (m + log2f(lt)) / AT_LOG2E;
+        }
+        if (threadIdx.x == 64) bulk_wait<0>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    __syncwarp();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
+}
+
+// ==================================================================== backward
+// One kernel, two modes (no atomics, deterministic):
+//   DKV  item = (128-key tile t, b*h); for every query tile u >= t:
+//          S^T = K_t Q_u^T, dP^T = V_t dO_u^T                 (TMEM, M=128 N=128 K=64)
+//          P^T = 2^(S^T log2e/8 - LSE_u log2e), dS^T = P^T (dP^T - D_u)   (compute warps)
+//          dV += P^T dO_u, dK += dS^T Q_u                     (TMEM, M=128 N=64 K=128)
+//        then dK / 8 and dV go to dqkv by TMA store.
+//   DQ   item = (128-query tile t, b*h); for every key tile u <= t:
+//          S = Q_t K_u^T, dP = dO_t V_u^T; P = 2^(S log2e/8 - LSE log2e), dS = P (dP - D)
+//          dQ += dS K_u;  then dQ / 8 to dqkv.
+// Warp 0 loads (the item's two row tiles once; the per-u tiles through a 2-stage ring
+// with, in DKV mode, that u's LSE and D vectors); warp 1 issues the MMAs (the next
+// S/dP pair is issued before the dV/dK (dQ) products of the current one); warps 2-9
+// compute, two warps per TMEM lane quadrant, each on half the columns of a tile (a
+// TMEM lane is a key row in DKV mode, a query row in DQ mode).
+#define AB_STAGE_BYTES (2 * AT_TILE_BYTES + 1024)   // two tiles + LSE[128] + D[128]
+#define AB_RING 2
+
+template <bool DKV>
+struct AbSmem {
+    static constexpr int R_OFF = 0;                                        // 2 row tiles
+    static constexpr int RING_OFF = R_OFF + 2 * AT_TILE_BYTES;
+    static constexpr int P_OFF = RING_OFF + AB_RING * AB_STAGE_BYTES;       // P^T (DKV only), 32 KB
+    static constexpr int DS_OFF = P_OFF + 2 * AT_TILE_BYTES;               // dS or dS^T, 32 KB
+    static constexpr int BAR_OFF = DS_OFF + 2 * AT_TILE_BYTES;
+    // rr_full, rr_empty, ring_full[2], ring_empty[2], x_full, x_free, pds_full, pds_free,
+    // acc_free, done; tmem address, abort flag
+    static constexpr int NBAR = 2 + 2 * AB_RING + 6;
+    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
+};
+
+template <bool DKV>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
+                             const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
+                             const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
+                             const float* __restrict__ Dsum, int B, int Tn, int C, int NH, unsigned* err) {
+    using S = AbSmem<DKV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+    uint64_t* rr_full = bars;
+    uint64_t* rr_empty = bars + 1;
+    uint64_t* ring_full = bars + 2;
+    uint64_t* ring_empty = ring_full + AB_RING;
+    uint64_t* x_full = ring_empty + AB_RING;
+    uint64_t* x_free = x_full + 1;
+    uint64_t* pds_full = x_free + 1;
+    uint64_t* pds_free = pds_full + 1;
+    uint64_t* acc_free = pds_free + 1;
+    uint64_t* done = acc_free + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = B * NH;
+    const int nt = (Tn + AT_BM - 1) / AT_BM;
+    const int n_items = nt * BH;
+    // item -> (row tile, bh, range of u), heaviest items first
+    auto item_of = [&](int it, int& t, int& bh, int& u0, int& u1) {
+        bh = it % BH;
+        if (DKV) { t = it / BH; u0 = t; u1 = nt; }
+        else { t = nt - 1 - it / BH; u0 = 0; u1 = t + 1; }
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(rr_full, 1);
+        mbar_init(rr_empty, 1);
+        for (int i = 0; i < AB_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 1); }
+        mbar_init(x_full, 1);
+        mbar_init(x_free, 8);
+        mbar_init(pds_full, 8);
+        mbar_init(pds_free, 1);
+        mbar_init(acc_free, 8);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmQKV);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmDQKV);
+        if (DKV) { tma_prefetch_desc(&tmL); tma_prefetch_desc(&tmD); }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(512) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t TM_X1 = tmem_base, TM_X2 = tmem_base + 128, TM_A1 = tmem_base + 256, TM_A2 = tmem_base + 320;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ loads
+        if (lane == 0) {
+            int rc = 0, local = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
+                int t, bh, u0, u1;
+                item_of(it, t, bh, u0, u1);
+                const int b = bh / NH, h = bh % NH;
+                if (!mbar_wait(rr_empty, (local & 1) ^ 1, abort_flag, err)) break;
+                mbar_expect_tx(rr_full, 2 * AT_TILE_BYTES);
+                if (DKV) {
+                    tma_load_3d(smem + S::R_OFF, &tmQKV, rr_full, C + h * AT_HS, t * AT_BM, b);                  // K_t
+                    tma_load_3d(smem + S::R_OFF + AT_TILE_BYTES, &tmQKV, rr_full, 2 * C + h * AT_HS, t * AT_BM, b);  // V_t
+                } else {
+                    tma_load_3d(smem + S::R_OFF, &tmQKV, rr_full, h * AT_HS, t * AT_BM, b);                      // Q_t
+                    tma_load_3d(smem + S::R_OFF + AT_TILE_BYTES, &tmDO, rr_full, h * AT_HS, t * AT_BM, b);       // dO_t
+                }
+                for (int u = u0; u < u1; u++, rc++) {
+                    const int slot = rc % AB_RING;
+                    if (!mbar_wait(&ring_empty[slot], ((rc / AB_RING) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+                    uint8_t* st = smem + S::RING_OFF + slot * AB_STAGE_BYTES;
+                    if (DKV) {
+                        mbar_expect_tx(&ring_full[slot], 2 * AT_TILE_BYTES + 1024);
+                        tma_load_3d(st, &tmQKV, &ring_full[slot], h * AT_HS, u * AT_BM, b);                       // Q_u
+                        tma_load_3d(st + AT_TILE_BYTES, &tmDO, &ring_full[slot], h * AT_HS, u * AT_BM, b);        // dO_u
+                        tma_load_2d(st + 2 * AT_TILE_BYTES, &tmL, &ring_full[slot], u * AT_BM, bh);               // LSE_u
+                        tma_load_2d(st + 2 * AT_TILE_BYTES + 512, &tmD, &ring_full[slot], u * AT_BM, bh);         // D_u
+                    } else {
+                        mbar_expect_tx(&ring_full[slot], 2 * AT_TILE_BYTES);
+                        tma_load_3d(st, &tmQKV, &ring_full[slot], C + h * AT_HS, u * AT_BM, b);                   // K_u
+                        tma_load_3d(st + AT_TILE_BYTES, &tmQKV, &ring_full[slot], 2 * C + h * AT_HS, u * AT_BM, b);  // V_u
+                    }
+                }
+            }
+            for (int back = 0; back < AB_RING && back < rc; back++) {
+                const int k = rc - 1 - back;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&ring_full[k % AB_RING], (k / AB_RING) & 1))
+                    if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_X = idesc_bf16(AT_BM, AT_BN, false, false);
+            constexpr uint32_t IDESC_A = idesc_bf16(AT_BM, AT_HS, false, true);
+            const uint32_t r0 = smem_u32(smem + S::R_OFF), r1 = r0 + AT_TILE_BYTES;
+            const uint32_t pbuf = smem_u32(smem + S::P_OFF), dsbuf = smem_u32(smem + S::DS_OFF);
+            int rc = 0, xc = 0, gc = 0, local = 0;
+            bool ok = true;
+            // the S / dP pair for the ring stage of index `idx`
+            auto issue_x = [&](int idx) -> bool {
+                const int slot = idx % AB_RING;
+                if (!mbar_wait(&ring_full[slot], (idx / AB_RING) & 1, abort_flag, err)) return false;
+                if (!mbar_wait(x_free, (xc & 1) ^ 1, abort_flag, err)) return false;
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + S::RING_OFF + slot * AB_STAGE_BYTES);
+#pragma unroll
+                for (int k = 0; k < AT_HS / 16; k++)
+                    tc_mma(TM_X1, sdesc(r0 + k * 32, 16, 1024), sdesc(st + k * 32, 16, 1024), IDESC_X, k > 0);
+#pragma unroll
+                for (int k = 0; k < AT_HS / 16; k++)
+                    tc_mma(TM_X2, sdesc(r1 + k * 32, 16, 1024), sdesc(st + AT_TILE_BYTES + k * 32, 16, 1024), IDESC_X,
+                           k > 0);
+                tc_commit(x_full);
+                xc++;
+                return true;
+            };
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
+                int t, bh, u0, u1;
+                item_of(it, t, bh, u0, u1);
+                const int nu = u1 - u0;
+                if (!mbar_wait(rr_full, local & 1, abort_flag, err)) break;
+                if (!issue_x(rc)) break;
+                for (int i = 0; i < nu && ok; i++) {
+                    if (i + 1 < nu && !issue_x(rc + i + 1)) { ok = false; break; }
+                    if (i == nu - 1) tc_commit(rr_empty);          // row tiles free after the last S / dP
+                    const int slot = (rc + i) % AB_RING;
+                    const uint32_t st = smem_u32(smem + S::RING_OFF + slot * AB_STAGE_BYTES);
+                    if (!mbar_wait(pds_full, gc & 1, abort_flag, err)) { ok = false; break; }
+                    if (i == 0 && local > 0 && !mbar_wait(acc_free, (local - 1) & 1, abort_flag, err)) { ok = false; break; }
+                    tc_fence_after();
+                    if (DKV) {
+                        // dV += P^T dO_u ; dK += dS^T Q_u
+#pragma unroll
+                        for (int k = 0; k < AT_BN / 16; k++) {
+                            const uint32_t aoff = (k >> 2) * AT_TILE_BYTES + (k & 3) * 32;
+                            tc_mma(TM_A1, sdesc(pbuf + aoff, 16, 1024), sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024),
+                                   IDESC_A, (i > 0 || k > 0));
+                            tc_mma(TM_A2, sdesc(dsbuf + aoff, 16, 1024), sdesc(st + k * 2048, 8192, 1024), IDESC_A,
+                                   (i > 0 || k > 0));
+                        }
+                    } else {
+                        // dQ += dS K_u
+#pragma unroll
+                        for (int k = 0; k < AT_BN / 16; k++)
+                            tc_mma(TM_A1, sdesc(dsbuf + (k >> 2) * AT_TILE_BYTES + (k & 3) * 32, 16, 1024),
+                                   sdesc(st + k * 2048, 8192, 1024), IDESC_A, (i > 0 || k > 0));
+                    }
+                    tc_commit(pds_free);
+                    tc_commit(&ring_empty[slot]);
+                    gc++;
+                }
+                rc += nu;
+            }
+            tc_commit(done);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(done, 0))
+                if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps 2..9
+        const int lane_grp = warp & 3;
+        const int half = (warp - 2) >> 2;                   // columns [64*half, 64*half + 64) of a tile
+        const int r = lane_grp * 32 + lane;                 // TMEM lane = row of the item's tile
+        const uint32_t lrow = (uint32_t)(lane_grp * 32) << 16;
+        const float sl2 = AT_LOG2E * 0.125f;
+        uint8_t* pbuf = smem + S::P_OFF;
+        uint8_t* dsbuf = smem + S::DS_OFF;
+        int rc = 0, xc = 0, gc = 0, pf_seen = 0, local = 0;
+        bool alive = true;
+        auto wait_one = [&](uint64_t* bar, uint32_t parity) -> bool {
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(bar, parity, abort_flag, err) ? 1 : 0;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            __syncwarp();
+            return okw != 0;
+        };
+        // wait for the dV/dK (dQ) products number n (pds_free phases, observed in order)
+        auto wait_pds_free = [&](int n) -> bool {
+            if (pf_seen > n) return true;
+            pf_seen = n + 1;
+            return wait_one(pds_free, n & 1);
+        };
+        for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x, local++) {
+            int t, bh, u0, u1;
+            item_of(it, t, bh, u0, u1);
+            const int b = bh / NH, h = bh % NH;
+            const int grow = t * AT_BM + r;                 // this thread's key (DKV) or query (DQ)
+            float Lrow = 0.f, Drow = 0.f;
+            if (!DKV && grow < Tn) {
+                Lrow = lse[(size_t)bh * Tn + grow] * AT_LOG2E;
+                Drow = Dsum[(size_t)bh * Tn + grow];
+            }
+            for (int u = u0; u < u1; u++, rc++, xc++, gc++) {
+                if (!wait_one(x_full, xc & 1)) { alive = false; break; }
+                tc_fence_after();
+                const uint8_t* st = smem + S::RING_OFF + (rc % AB_RING) * AB_STAGE_BYTES;
+                const float* Lv = reinterpret_cast<const float*>(st + 2 * AT_TILE_BYTES);
+                const float* Dv = Lv + 128;
+                // the previous products must have finished reading the P / dS buffers
+                if (gc > 0 && !wait_pds_free(gc - 1)) { alive = false; break; }
+#pragma unroll 1
+                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                    uint32_t s1[32], s2[32];
+                    tmem_ld32(TM_X1 + lrow + c, s1);
+                    tmem_ld32(TM_X2 + lrow + c, s2);
+                    tmem_ld_wait();
+                    if (c == half * 64 + 32) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(x_free);      // S / dP TMEM may be overwritten
+                    }
+                    float p[32], ds[32];
+                    float Lc[32], Dc[32];
+                    if (DKV) {
+                        // LSE (to the exp2 domain) and D of these 32 query columns
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            const float4 lv = *reinterpret_cast<const float4*>(Lv + c + 4 * k);
+                            const float4 dv = *reinterpret_cast<const float4*>(Dv + c + 4 * k);
+                            Lc[4 * k] = lv.x * AT_LOG2E; Lc[4 * k + 1] = lv.y * AT_LOG2E;
+                            Lc[4 * k + 2] = lv.z * AT_LOG2E; Lc[4 * k + 3] = lv.w * AT_LOG2E;
+                            Dc[4 * k] = dv.x; Dc[4 * k + 1] = dv.y; Dc[4 * k + 2] = dv.z; Dc[4 * k + 3] = dv.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) { Lc[i] = Lrow; Dc[i] = Drow; }
+                    }
+                    // masking is needed only where the tile meets the diagonal or the end of T
+                    const int col0 = u * AT_BN + c;
+                    const bool masked = DKV ? (col0 < grow + 1 || col0 + 31 >= Tn) : (col0 + 31 > grow);
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            const int col = col0 + i;            // query (DKV) or key (DQ) index
+                            const bool valid = DKV ? ((col >= grow) && (col < Tn)) : (col <= grow);
+                            const float pv = ex2_fast(fmaf(__uint_as_float(s1[i]), sl2, -Lc[i]));
+                            p[i] = valid ? pv : 0.f;
+                            ds[i] = valid ? pv * (__uint_as_float(s2[i]) - Dc[i]) : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            p[i] = ex2_fast(fmaf(__uint_as_float(s1[i]), sl2, -Lc[i]));
+                            ds[i] = p[i] * (__uint_as_float(s2[i]) - Dc[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int ch = (c >> 3) + k;
+                        const int off = (ch >> 3) * AT_TILE_BYTES + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                        Vec<bf16> dv;
+#pragma unroll
+                        for (int e = 0; e < 8; e++) dv.set(e, ds[8 * k + e]);
+                        *reinterpret_cast<uint4*>(dsbuf + off) = dv.v;
+                        if (DKV) {
+                            Vec<bf16> pv;
+#pragma unroll
+                            for (int e = 0; e < 8; e++) pv.set(e, p[8 * k + e]);
+                            *reinterpret_cast<uint4*>(pbuf + off) = pv.v;
+                        }
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pds_full);
+            }
+            if (!alive) break;
+            // accumulators of the item: wait for its last products, read, release, store
+            if (!wait_pds_free(gc - 1)) break;
+            tc_fence_after();
+            float a1[32], a2[32];
+            {
+                uint32_t rr[32];
+                tmem_ld32(TM_A1 + lrow + half * 32, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; i++) a1[i] = __uint_as_float(rr[i]);
+                if (DKV) {
+                    tmem_ld32(TM_A2 + lrow + half * 32, rr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) a2[i] = __uint_as_float(rr[i]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free);
+            // stage in the (now idle) P / dS buffers, 128B-swizzled rows, then TMA-store
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int ch = half * 4 + k;
+                const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+                Vec<bf16> v1;
+                if (DKV) {
+                    Vec<bf16> v2;
+#pragma unroll
+                    for (int e = 0; e < 8; e++) { v1.set(e, a1[8 * k + e]); v2.set(e, a2[8 * k + e] * 0.125f); }
+                    *reinterpret_cast<uint4*>(pbuf + off) = v1.v;      // dV
+                    *reinterpret_cast<uint4*>(dsbuf + off) = v2.v;     // dK / 8
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; e++) v1.set(e, a1[8 * k + e] * 0.125f);
+                    *reinterpret_cast<uint4*>(dsbuf + off) = v1.v;     // dQ / 8
+                }
+            }
+            fence_async_smem();
+            named_bar(1, 256);
+            if (threadIdx.x == 64) {
+                if (DKV) {
+                    tma_store_3d(&tmDQKV, pbuf, 2 * C + h * AT_HS, t * AT_BM, b);
+                    tma_store_3d(&tmDQKV, dsbuf, C + h * AT_HS, t * AT_BM, b);
+                } else {
+                    tma_store_3d(&tmDQKV, dsbuf, h * AT_HS, t * AT_BM, b);
+                }
+                bulk_commit();
+                bulk_wait_read<0>();      // the buffers are reused by the next item
+            }
+            named_bar(1, 256);
+        }
+        if (threadIdx.x == 64) bulk_wait<0>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    __syncwarp();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+static int g_sms = 0;
+static int g_at_ok = -1;
+static std::mutex g_at_mutex;
+
+int attention_tc_available() {
+    std::lock_guard<std::mutex> lock(g_at_mutex);
+    if (g_at_ok >= 0) return g_at_ok;
+    g_at_ok = 0;
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return 0;
+    if (prop.major != 10) return 0;
+    g_sms = prop.multiProcessorCount;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return 0;
+    g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    if (cudaFuncSetAttribute(attention_tc_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AtSmem::TOTAL) != cudaSuccess)
+        return 0;
+    g_at_ok = 1;
+    return 1;
+}
+
+// 3-D bf16 map over (cols, T, B) with row pitch `ld` elements; box {64, 128, 1}.
+static bool make_map3(CUtensorMap* map, const void* base, int cols, int Tn, int B, int ld) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)Tn, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * Tn};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const __nv_bfloat16* qkv, int B, int Tn,
+                         int C, int NH, unsigned* err) {
+    if (!attention_tc_available()) return GPT2_EUNSUPPORTED;
+    if (C / NH != AT_HS || (((uintptr_t)qkv | (uintptr_t)out) & 15)) return GPT2_EUNSUPPORTED;
+    CUtensorMap tq, to;
+    if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&to, out, C, Tn, B, C)) return GPT2_EUNSUPPORTED;
+    const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
+    const int grid = items < g_sms ? items : g_sms;
+    attention_tc_forward_kernel<<<grid, AT_THREADS, AtSmem::TOTAL, s>>>(tq, to, lse, B, Tn, C, NH, err);
+    rt_note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
+}
+
+// 2-D fp32 map over (T, rows) with pitch T; box {128, 1}; no swizzle.
+static bool make_map_vec(CUtensorMap* map, const float* base, int Tn, int rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)Tn, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)Tn * 4};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return g_enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool DKV>
+static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tl,
+                      const CUtensorMap& td, const CUtensorMap& tdq, const float* lse, const float* D, int B, int Tn,
+                      int C, int NH, unsigned* err) {
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(attention_tc_backward_kernel<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AbSmem<DKV>::TOTAL) != cudaSuccess)
+            return GPT2_ECUDA;
+        attr = true;
+    }
+    const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
+    const int grid = items < g_sms ? items : g_sms;
+    attention_tc_backward_kernel<DKV><<<grid, AT_THREADS, AbSmem<DKV>::TOTAL, s>>>(tq, tdo, tl, td, tdq, lse, D, B,
+                                                                                    Tn, C, NH, err);
+    rt_note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
+}
+
+int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
+                          const float* lse, const float* D, int B, int Tn, int C, int NH, unsigned* err) {
+    if (!attention_tc_available()) return GPT2_EUNSUPPORTED;
+    if (C / NH != AT_HS || Tn % 4 || (((uintptr_t)qkv | (uintptr_t)dout | (uintptr_t)dqkv | (uintptr_t)lse |
+                                       (uintptr_t)D) & 15))
+        return GPT2_EUNSUPPORTED;
+    CUtensorMap tq, tdo, tl, td, tdq;
+    if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&tdo, dout, C, Tn, B, C) ||
+        !make_map_vec(&tl, lse, Tn, B * NH) || !make_map_vec(&td, D, Tn, B * NH) ||
+        !make_map3(&tdq, dqkv, 3 * C, Tn, B, 3 * C))
+        return GPT2_EUNSUPPORTED;
+    int rc = launch_bwd<true>(s, tq, tdo, tl, td, tdq, lse, D, B, Tn, C, NH, err);
+    if (rc != GPT2_OK) return rc;
+    return launch_bwd<false>(s, tq, tdo, tl, td, tdq, lse, D, B, Tn, C, NH, err);
+}

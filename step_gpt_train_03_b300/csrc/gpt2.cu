@@ -150,7 +150,7 @@ static int validate_cfg(const GPT2Config* c, int maxB, int maxT, int prec) {
     if (c->num_layers < 1 || c->num_heads < 1 || c->channels < 64) return GPT2_EINVAL;
     if (c->channels % 64 != 0 || c->channels % c->num_heads != 0) return GPT2_EINVAL;
     if (c->channels > 2048) return GPT2_EUNSUPPORTED;
-    if (c->channels / c->num_heads > ATT_MAX_HS) return GPT2_EUNSUPPORTED;
+    if (c->channels / c->num_heads > ATT_MAX_HS || (c->channels / c->num_heads) % 8) return GPT2_EUNSUPPORTED;
     if (c->vocab_size < 1 || c->padded_vocab_size < c->vocab_size) return GPT2_EINVAL;
     if (c->padded_vocab_size % 64 != 0) return GPT2_EINVAL;
     if (c->max_seq_len < 1 || maxB < 1 || maxT < 1 || maxT > c->max_seq_len) return GPT2_EINVAL;
@@ -435,7 +435,7 @@ static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, in
     ProfScope ps(s, PC_ATTENTION_FWD, attn_fwd_flops(B, Tn, C), 0);
     if constexpr (sizeof(T) == 2) {
         float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
-        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH);
+        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, m->err);
     } else {
         float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
         int rows = B * NH * Tn;
@@ -455,7 +455,7 @@ static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const 
     if constexpr (sizeof(T) == 2) {
         const float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
         return attention_flash_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out,
-                                     lse, m->attn_scratch, B, Tn, C, NH);
+                                     lse, m->attn_scratch, B, Tn, C, NH, m->err);
     } else {
         (void)out;
         const float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
@@ -802,6 +802,59 @@ extern "C" int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, co
         RC(mm_backward_dx<bf16>(&shim, s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_STORE, nullptr));
         RC(mm_backward_dw<bf16>(&shim, s, dweight, (const bf16*)dout, (const bf16*)inp, M, N, K));
         if (dbias) RC(colsum<bf16>(s, dbias, (const bf16*)dout, M, N, part, pf));
+        return GPT2_OK;
+    }
+    return GPT2_EINVAL;
+}
+
+// ------------------------------------------------------------------ attention (single layer)
+static int attn_args_ok(int B, int Tn, int C, int NH) {
+    if (B < 1 || Tn < 1 || NH < 1 || C < NH || C % NH || C / NH > ATT_MAX_HS || (C / NH) % 8) return 0;
+    return 1;
+}
+
+extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, int B, int Tn, int C, int NH,
+                                      int precision, void* stream) {
+    if (!out || !lse || !qkv || !attn_args_ok(B, Tn, C, NH)) return GPT2_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (precision == GPT2_BF16)
+        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, nullptr);
+    if (precision == GPT2_FP32) {
+        const int rows = B * NH * Tn;
+        attention_forward_simt<float><<<ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s>>>(
+            (float*)out, lse, (const float*)qkv, B, Tn, C, NH);
+        rt_note_launches(1);
+        CK(cudaGetLastError());
+        return GPT2_OK;
+    }
+    return GPT2_EINVAL;
+}
+
+extern "C" size_t gpt2_attention_backward_scratch_bytes(int B, int Tn, int NH, int precision) {
+    if (B < 1 || Tn < 1 || NH < 1) return 0;
+    const size_t rows = (size_t)B * NH * Tn;
+    return precision == GPT2_FP32 ? rows * Tn * sizeof(float) : rows * sizeof(float);
+}
+
+extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
+                                       const float* lse, int B, int Tn, int C, int NH, int precision,
+                                       void* scratch, size_t scratch_bytes, void* stream) {
+    if (!dqkv || !dout || !qkv || !out || !lse || !scratch || !attn_args_ok(B, Tn, C, NH)) return GPT2_EINVAL;
+    if (scratch_bytes < gpt2_attention_backward_scratch_bytes(B, Tn, NH, precision)) return GPT2_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (precision == GPT2_BF16)
+        return attention_flash_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
+                                        (float*)scratch, B, Tn, C, NH, nullptr);
+    if (precision == GPT2_FP32) {
+        const int rows = B * NH * Tn;
+        const int grid = ceil_div(rows, ATT_WARPS);
+        float* ds = (float*)scratch;
+        rt_note_launches(3);
+        attention_backward_ds<float><<<grid, ATT_WARPS * 32, 0, s>>>(ds, lse, (const float*)dout, (const float*)qkv, B, Tn, C, NH);
+        attention_backward_dq<float><<<grid, ATT_WARPS * 32, 0, s>>>((float*)dqkv, ds, (const float*)qkv, B, Tn, C, NH);
+        attention_backward_dkv<float><<<grid, ATT_WARPS * 32, 0, s>>>((float*)dqkv, ds, lse, (const float*)qkv,
+                                                                   (const float*)dout, B, Tn, C, NH);
+        CK(cudaGetLastError());
         return GPT2_OK;
     }
     return GPT2_EINVAL;

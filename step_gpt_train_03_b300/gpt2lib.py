@@ -67,6 +67,9 @@ SIGNATURES = {
     "gpt2_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
     "gpt2_layernorm_backward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
+    "gpt2_attention_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "gpt2_attention_backward_scratch_bytes": (_sz, [_i, _i, _i, _i]),
+    "gpt2_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_matmul_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_matmul_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_matmul_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
@@ -330,6 +333,24 @@ def layernorm_backward_noalloc(dinp, dweight, dbias, dout, inp, weight, mean, rs
     check(lib.gpt2_layernorm_backward_noalloc(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout),
                                               _ptr(inp), _ptr(weight), _ptr(mean), _ptr(rstd), N, C,
                                               _stream_handle(stream)), "gpt2_layernorm_backward_noalloc")
+
+
+def attention_forward(out, lse, qkv, NH, precision, stream=None):
+    """qkv (B,T,3C) -> out (B,T,C); lse (B,NH,T) fp32 (bf16) or probabilities (B,NH,T,T) (fp32)."""
+    B, T, C3 = qkv.shape
+    check(lib.gpt2_attention_forward(_ptr(out), _ptr(lse), _ptr(qkv), B, T, C3 // 3, NH, PRECISIONS[precision],
+                                     _stream_handle(stream)), "gpt2_attention_forward")
+
+
+def attention_backward_scratch_bytes(B, T, NH, precision) -> int:
+    return int(lib.gpt2_attention_backward_scratch_bytes(B, T, NH, PRECISIONS[precision]))
+
+
+def attention_backward(dqkv, dout, qkv, out, lse, NH, precision, scratch, stream=None):
+    B, T, C3 = qkv.shape
+    check(lib.gpt2_attention_backward(_ptr(dqkv), _ptr(dout), _ptr(qkv), _ptr(out), _ptr(lse), B, T, C3 // 3, NH,
+                                      PRECISIONS[precision], _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                      _stream_handle(stream)), "gpt2_attention_backward")
 
 
 def matmul_forward(out, inp, weight, bias, precision, stream=None):

@@ -130,3 +130,40 @@ def test_matmul_bf16(L, M, N, K):
     e = _mm_case(L, M, N, K, "bf16")
     assert e["y"] < BF16_TOL and e["dx"] < BF16_TOL, e
     assert e["dw"] < 1e-4 and e["db"] < 1e-4, e      # fp32 outputs: only the products' order differs
+
+
+# bf16 attention: inputs are bf16, P is rounded to bf16 before P V and outputs are
+# stored in bf16, so 2e-2 of the tensor's max bounds the rounding; LSE is fp32 math on
+# bf16 scores (abs 2e-2).
+ATT_TOL = 2e-2
+
+
+@pytest.mark.parametrize("B,T,NH,C,precision", [(2, 64, 4, 256, "bf16"), (1, 200, 2, 128, "bf16"),
+                                                (2, 1024, 12, 768, "bf16"), (3, 37, 4, 64, "bf16"),
+                                                (2, 40, 4, 64, "fp32"), (1, 129, 2, 128, "fp32")])
+def test_attention_forward_backward(L, B, T, NH, C, precision):
+    import torch
+    rng = np.random.default_rng(B * 1000 + T)
+    qkv = rng.standard_normal((B, T, 3 * C)).astype(np.float32)
+    dout = rng.standard_normal((B, T, C)).astype(np.float32)
+    tdt = torch.bfloat16 if precision == "bf16" else torch.float32
+    qkv_d = torch.as_tensor(qkv).cuda().to(tdt)
+    dout_d = torch.as_tensor(dout).cuda().to(tdt)
+    q64 = qkv_d.float().cpu().numpy().astype(np.float64)
+    d64 = dout_d.float().cpu().numpy().astype(np.float64)
+    out = torch.empty((B, T, C), device="cuda", dtype=tdt)
+    lse = torch.empty((B, NH, T) if precision == "bf16" else (B, NH, T, T), device="cuda")
+    L.attention_forward(out, lse, qkv_d, NH, precision)
+    dqkv = torch.empty_like(qkv_d)
+    scratch = torch.empty(L.attention_backward_scratch_bytes(B, T, NH, precision), dtype=torch.uint8, device="cuda")
+    L.attention_backward(dqkv, dout_d, qkv_d, out, lse, NH, precision, scratch)
+    torch.cuda.synchronize()
+    ref_out, pre, att = O.attention_forward(q64, NH)
+    ref_dqkv = O.attention_backward(d64, q64, att, NH)
+    tol = ATT_TOL if precision == "bf16" else OUT_TOL
+    assert norm_err(out.float().cpu().numpy(), ref_out) < tol
+    assert norm_err(dqkv.float().cpu().numpy(), ref_dqkv) < (tol if precision == "bf16" else GRAD_TOL)
+    if precision == "bf16":
+        m = pre.max(-1, keepdims=True)
+        ref_lse = (m + np.log(np.exp(pre - m).sum(-1, keepdims=True)))[..., 0]
+        assert np.abs(lse.cpu().numpy() - ref_lse).max() < 2e-2
