@@ -19,7 +19,8 @@
 //               128B-swizzled shared buffer and write it with one TMA store (fp32
 //               weight gradients: one TMA reduce-add, so each element is added once);
 //               residual and pre-activation inputs arrive by TMA load into the same
-//               buffer
+//               buffers, one chunk ahead (the next tile's first chunk is requested
+//               before its accumulator is ready)
 // Every mbarrier wait is bounded: on expiry the kernel raises the timeout bit in the
 // library's error word, the other roles see the abort flag and stop, in-flight copies
 // and MMAs are waited for (again bounded), TMEM is freed and the kernel returns.
@@ -61,8 +62,9 @@ struct TcSmem {
     static constexpr int STG_OFF = TC_STAGES * STAGE_BYTES;
     static constexpr int STG_BYTES = 4096;
     static constexpr int BAR_OFF = STG_OFF + 4 * 2 * STG_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[4]; tmem address, abort flag
-    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 9) * 8 + 16 + 1024;
+    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[4 warps][2 buffers];
+    // tmem address, abort flag
+    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 13) * 8 + 16 + 1024;
 };
 
 // byte offset of 16-byte chunk j of row r in a 128B-swizzled staging buffer
@@ -85,7 +87,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     uint64_t* aux_bar = done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -98,7 +100,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < TC_STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
         mbar_init(done, 1);
-        for (int i = 0; i < 4; i++) mbar_init(&aux_bar[i], 1);
+        for (int i = 0; i < 8; i++) mbar_init(&aux_bar[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
@@ -200,11 +202,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int ew = warp - 2;                       // epilogue warp 0..3
         const int lane_grp = warp & 3;                 // TMEM lanes 32*lane_grp .. +31
         uint8_t* stg = smem + S::STG_OFF + ew * 2 * S::STG_BYTES;
-        uint64_t* auxb = &aux_bar[ew];
-        uint32_t aux_phase = 0;
+        constexpr bool AUX_IN = (EPI == EPI_RESID || EPI == EPI_GELU_BWD);
+        constexpr int NCH = BN / 64;                   // 64-column chunks per tile
+        uint64_t* auxb = &aux_bar[ew * 2];             // one barrier per staging buffer
+        uint32_t aux_ph = 0;                           // bit b: phase of buffer b's barrier
+        uint32_t aux_pend = 0;                         // bit b: a load into buffer b not yet waited for
         int nbuf = 0;                                  // staging buffer in use: nbuf & 1
         int local = 0;
         bool alive = true;
+        // residual / pre-activation inputs: the load of chunk (unit uu, chunk c) goes to
+        // buffer kb once every store still reading a staging buffer has finished
+        auto aux_issue = [&](int uu, int c, int kb) {
+            if (lane == 0) {
+                const int tile = uu / splits;
+                const int col = (tile % n_tiles) * BN + c * 64, row0 = (tile / n_tiles) * TC_BM + lane_grp * 32;
+                bulk_wait_read<0>();
+                aux_pend |= 1u << kb;
+                mbar_expect_tx(&auxb[kb], S::STG_BYTES);
+                tma_load_2d(stg + kb * S::STG_BYTES, &tmAux, &auxb[kb], col, row0);
+            }
+        };
+        if (AUX_IN && blockIdx.x < units) aux_issue(blockIdx.x, 0, 0);
         for (int u = blockIdx.x; u < units && alive; u += gridDim.x, local++) {
             const int sp = u % splits, tile = u / splits;
             const int nt = tile % n_tiles, mt = tile / n_tiles;
@@ -220,9 +238,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int row0 = mt * TC_BM + lane_grp * 32;   // first of this warp's 32 rows
             const int yout = (EPI == TC_EPI_PARTIAL) ? sp * M + row0 : row0;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 64) {
+            for (int ci = 0; ci < NCH; ci++) {
+                const int c = ci * 64;
                 const int col = nt * BN + c;
-                if (col >= N) break;
+                if (!AUX_IN && col >= N) break;
                 uint32_t r0[32], r1[32];
                 const uint32_t ta = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + acc * BN + c;
                 tmem_ld32(ta, r0);
@@ -251,8 +270,47 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         nbuf++;
                     }
+                } else if constexpr (AUX_IN) {
+                    // this chunk's input was loaded into buffer nbuf & 1 ahead of time; start
+                    // the next chunk's (or the next tile's first) load into the other buffer
+                    const int kb = nbuf & 1;
+                    if (ci + 1 < NCH) aux_issue(u, ci + 1, kb ^ 1);
+                    else if (u + gridDim.x < units) aux_issue(u + gridDim.x, 0, kb ^ 1);
+                    int oka = 1;
+                    if (lane == 0) oka = mbar_wait(&auxb[kb], (aux_ph >> kb) & 1, abort_flag, err) ? 1 : 0;
+                    oka = __shfl_sync(0xffffffffu, oka, 0);
+                    aux_ph ^= 1u << kb;
+                    aux_pend &= ~(1u << kb);
+                    if (!oka) { alive = false; break; }
+                    __syncwarp();
+                    uint8_t* sb = stg + kb * S::STG_BYTES;
+                    if (ep.bias && EPI == EPI_RESID) {
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            if (col + 8 * q < N) {
+                                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
+#pragma unroll
+                                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        Vec<bf16> a, o;
+                        a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            if constexpr (EPI == EPI_RESID) o.set(e, v[8 * j + e] + a.get(e));
+                            else o.set(e, v[8 * j + e] * gelu_grad_fast(a.get(e)));
+                        }
+                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && col < N) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
+                    nbuf++;
                 } else {
-                    if (ep.bias && EPI != EPI_GELU_BWD) {
+                    if (ep.bias) {
 #pragma unroll
                         for (int q = 0; q < 8; q++) {
                             if (col + 8 * q < N) {
@@ -265,29 +323,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
-                    if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD) {
-                        // the residual / pre-activation tile of these 32 rows x 64 columns
-                        if (lane == 0) {
-                            mbar_expect_tx(auxb, S::STG_BYTES);
-                            tma_load_2d(sb, &tmAux, auxb, col, row0);
-                        }
-                        int oka = 1;
-                        if (lane == 0) oka = mbar_wait(auxb, aux_phase, abort_flag, err) ? 1 : 0;
-                        oka = __shfl_sync(0xffffffffu, oka, 0);
-                        aux_phase ^= 1;
-                        if (!oka) { alive = false; break; }
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            Vec<bf16> a;
-                            a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
-#pragma unroll
-                            for (int e = 0; e < 8; e++) {
-                                if constexpr (EPI == EPI_RESID) v[8 * j + e] += a.get(e);
-                                else v[8 * j + e] *= gelu_grad_fast(a.get(e));
-                            }
-                        }
-                    } else if constexpr (EPI == EPI_GELU) {
+                    if constexpr (EPI == EPI_GELU) {
                         // pre-activation out first, then the activation into the other buffer
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
@@ -323,8 +359,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
-        // every store this warp issued has completed before the CTA retires
-        if (lane == 0) bulk_wait<0>();
+        // every store this warp issued has completed, and no load is still landing in
+        // its staging buffers (only possible after an abort), before the CTA retires
+        if (lane == 0) {
+            bulk_wait<0>();
+            for (int kb = 0; kb < 2; kb++) {
+                if (!((aux_pend >> kb) & 1)) continue;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&auxb[kb], (aux_ph >> kb) & 1))
+                    if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+            }
+        }
         __syncwarp();
     }
     tc_fence_before();
