@@ -1,0 +1,83 @@
+"""Run one kernel of the training step on its own, at the 124M workload's sizes, a few
+times: the target of per-kernel Nsight Compute captures.
+
+    python -m step_gpt_train_03_b300.kernel_cases <case> [--iters N]
+
+Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
+  matmul_fc_forward       (16384 x 768) @ (3072 x 768)^T
+  matmul_lmhead_forward   (16384 x 768) @ (50304 x 768)^T
+  matmul_lmhead_backward  dX (16384 x 768) and dW (50304 x 768, fp32 +=) of the LM head
+  attention_forward       causal, B=16, T=1024, hs=64
+  attention_backward      same sizes (dK/dV kernel, then dQ kernel)
+  layernorm_backward_fp32 (8192 x 768) fp32, the standalone layernorm workload
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    import torch
+    from step_gpt_train_03_b300 import gpt2lib as G
+    torch.manual_seed(0)
+    BT, C, NH, Vp, B, T = 16384, 768, 12, 50304, 16, 1024
+    dev = "cuda"
+    bf = torch.bfloat16
+    case = args.case
+    if case.startswith("matmul"):
+        N = 3072 if case == "matmul_fc_forward" else Vp
+        x = torch.randn(BT, C, device=dev).to(bf)
+        w = (0.02 * torch.randn(N, C, device=dev)).to(bf)
+        if case.endswith("forward"):
+            out = torch.empty(BT, N, device=dev, dtype=bf)
+            run = lambda: G.matmul_forward(out, x, w, None, "bf16")
+        else:
+            dy = (1e-4 * torch.randn(BT, N, device=dev)).to(bf)
+            dx = torch.empty(BT, C, device=dev, dtype=bf)
+            dW = torch.zeros(N, C, device=dev)
+            sc = torch.empty(G.matmul_backward_scratch_bytes(BT, N), dtype=torch.uint8, device=dev)
+            run = lambda: G.matmul_backward(dx, dW, None, dy, x, w, "bf16", sc)
+    elif case.startswith("attention"):
+        qkv = torch.randn(B, T, 3 * C, device=dev).to(bf)
+        out = torch.empty(B, T, C, device=dev, dtype=bf)
+        lse = torch.empty(B, NH, T, device=dev)
+        G.attention_forward(out, lse, qkv, NH, "bf16")
+        if case == "attention_forward":
+            run = lambda: G.attention_forward(out, lse, qkv, NH, "bf16")
+        else:
+            dout = torch.randn(B, T, C, device=dev).to(bf)
+            dqkv = torch.empty_like(qkv)
+            sc = torch.empty(G.attention_backward_scratch_bytes(B, T, NH, "bf16"), dtype=torch.uint8, device=dev)
+            run = lambda: G.attention_backward(dqkv, dout, qkv, out, lse, NH, "bf16", sc)
+    elif case == "layernorm_backward_fp32":
+        N = 8192
+        x = 3 * torch.randn(N, C, device=dev) + 0.5
+        w = 1 + 0.1 * torch.randn(C, device=dev)
+        b = 0.1 * torch.randn(C, device=dev)
+        dy = torch.randn(N, C, device=dev)
+        y = torch.empty_like(x)
+        mean = torch.empty(N, device=dev)
+        rstd = torch.empty(N, device=dev)
+        G.layernorm_forward(y, mean, rstd, x, w, b)
+        dx = torch.zeros_like(x)
+        dw = torch.zeros(C, device=dev)
+        db = torch.zeros(C, device=dev)
+        sc = torch.empty(G.layernorm_backward_scratch_bytes(N, C), dtype=torch.uint8, device=dev)
+        run = lambda: G.layernorm_backward(dx, dw, db, dy, x, w, mean, rstd, sc)
+    else:
+        print(f"unknown case {case}", file=sys.stderr)
+        return 2
+    for _ in range(args.iters):
+        run()
+    torch.cuda.synchronize()
+    print(f"{case}: {args.iters} runs ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
