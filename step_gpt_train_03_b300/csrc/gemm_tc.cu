@@ -536,6 +536,8 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
         return GPT2_EUNSUPPORTED;
     CUtensorMap ta, tb, to;
     if (!make_map(&ta, dout, N, M, N, 64) || !make_map(&tb, inp, K, M, K, 64)) return GPT2_EUNSUPPORTED;
+    // 256-wide tiles throughout (measured faster than 128-wide tiles for every weight
+    // gradient of the model); split-K fills the GPU when there are fewer tiles than SMs
     const int tiles = ((N + TC_BM - 1) / TC_BM) * ((K + 255) / 256);
     const int nkb = (M + TC_BK - 1) / TC_BK;
     int splits = choose_splits(tiles, nkb);

@@ -130,8 +130,7 @@ static size_t plan(GPT2* m, char* base) {
     m->dfch = take(BT * 4 * C * es);
     // partials: layernorm backward (<= 1024 blocks x 2C) and column sums (<= 256 x 4C);
     // the matmul backward on tensor cores may also use it for split-K partial tiles.
-    size_t pf = 1024 * 2 * C;
-    if (256 * 4 * C > pf) pf = 256 * 4 * C;
+    size_t pf = 1024 * 4 * C;          // >= 296 x 3C (layernorm) and 1024 x 4C (column sums)
     size_t tc_pf = gemm_tc_scratch_floats(BT, C);
     if (tc_pf > pf) pf = tc_pf;
     m->partials_floats = pf;
@@ -310,33 +309,47 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
 // two resident blocks per SM on a 148-SM part; each warp then walks ~7 rows at N = 16384
 static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 2), 296)); }
 
+// dsum (nullable): also add the column sums of the updated dinp (bias gradient of the
+// layer whose output is this residual stream)
 template <typename T>
 static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
                        const T* w, const float* mean, const float* rstd, int N, int C,
-                       float* partial, size_t partial_floats) {
+                       float* partial, size_t partial_floats, float* dsum = nullptr) {
     constexpr int EPV = Vec<T>::N;
     const int nv = ceil_div(C / EPV, 32);
     const int G = ln_backward_grid(N);
-    if ((size_t)G * 2 * C > partial_floats) return GPT2_EINVAL;
-    const size_t smem = 2 * C * sizeof(float);
+    const int W = dsum ? 3 : 2;
+    if ((size_t)G * W * C > partial_floats) return GPT2_EINVAL;
+    const size_t smem = (dsum ? (3 + LN_WARPS) : 2) * C * sizeof(float);
     ProfScope ps(s, PC_LAYERNORM_BWD, 0, 4.0 * N * C * sizeof(T) + 8.0 * N + 3.0 * C * sizeof(T) + 8.0 * C);
     rt_note_launches(2);
-    switch (nv) {
-#define LNB_CASE(k) case k: layernorm_backward_kernel<T, k><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
-        LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
-        LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
+    if (dsum) {
+        switch (nv) {
+#define LNB_CASE(k) case k: if (smem > 48 * 1024) cudaFuncSetAttribute(layernorm_backward_kernel<T, k, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+                            layernorm_backward_kernel<T, k, true><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
+            LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
+            LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
 #undef LNB_CASE
-        default: return GPT2_EUNSUPPORTED;
+            default: return GPT2_EUNSUPPORTED;
+        }
+    } else {
+        switch (nv) {
+#define LNB_CASE(k) case k: layernorm_backward_kernel<T, k, false><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
+            LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
+            LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
+#undef LNB_CASE
+            default: return GPT2_EUNSUPPORTED;
+        }
     }
     CK(cudaGetLastError());
-    column_reduce_kernel<<<ceil_div(2 * C, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(dw, db, C, partial, G, 2 * C);
+    column_reduce_kernel<<<ceil_div(W * C, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(dw, db, C, partial, G, W * C, dsum);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
 
 static void colsum_shape(int M, int N, int* R, int* rows) {
     (void)N;
-    int r = std::max(1, std::min(512, ceil_div(M, 32)));
+    int r = std::max(1, std::min(1024, ceil_div(M, 16)));
     *rows = ceil_div(M, r);
     *R = ceil_div(M, *rows);
 }
@@ -560,7 +573,10 @@ static int backward_impl(GPT2* m) {
     RC(mm_backward_dw<T>(m, s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C));
     RC(launch_zero(s, dresid, (size_t)BT * C * sizeof(T)));
     const T* xlast = (const T*)m->res3 + (L - 1) * BTmax * C;
-    RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf));
+    // the updated residual gradient is d(res3) of the last layer: its column sums are
+    // that layer's MLP-projection bias gradient
+    RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf,
+                      G(P_FCPROJB) + (L - 1) * C));
     for (int l = L - 1; l >= 0; l--) {
         const T* x_in = (l == 0) ? (const T*)m->encoded : (const T*)m->res3 + (l - 1) * BTmax * C;
         const T* ln1 = (const T*)m->ln1 + l * BTmax * C;
@@ -575,17 +591,16 @@ static int backward_impl(GPT2* m) {
         // MLP output projection (dresid = d res3)
         RC(mm_backward_dx<T>(m, s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch));
         RC(mm_backward_dw<T>(m, s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C));
-        RC(colsum<T>(s, G(P_FCPROJB) + l * C, dresid, BT, C, part, pf));
         // MLP input projection
         RC(mm_backward_dx<T>(m, s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C));
         RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
-        RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf));
+        RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
+                          G(P_ATTPROJB) + l * C));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
         RC(mm_backward_dx<T>(m, s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C));
-        RC(colsum<T>(s, G(P_ATTPROJB) + l * C, dresid, BT, C, part, pf));
         // attention
         RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn));
         // qkv projection
@@ -593,7 +608,8 @@ static int backward_impl(GPT2* m) {
         RC(mm_backward_dw<T>(m, s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C));
         RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf));
         // ln1 (dresid becomes d x_l)
-        RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf));
+        RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
+                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr));   // d(res3) of layer l-1
     }
     // encoder: deterministic scatter-add into dwte (ids sorted in the forward), dwpe
     ProfScope ps(s, PC_ENCODER_BWD, 0, (double)BT * C * sizeof(T) + 8.0 * BT * C + 8.0 * Tn * C);

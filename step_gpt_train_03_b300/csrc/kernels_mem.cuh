@@ -212,16 +212,22 @@ layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* _
 // warp order through shared memory and the block writes partial[j][0:2C].  The row's
 // x and dy stay packed (16-byte packets) in registers and xhat is recomputed in the
 // second pass, which keeps two blocks resident per SM.
-template <typename T, int NV>
+// With SUM the block also sums the updated dinp rows (partial[j][2C:3C]): in the model
+// that is the bias gradient of the linear layer whose output is the residual stream.
+// Each warp keeps that sum in its own shared-memory row (its lanes own distinct
+// columns), which leaves the register budget of two blocks per SM untouched.
+template <typename T, int NV, bool SUM>
 __global__ void __launch_bounds__(LN_WARPS * 32, (NV * Vec<T>::N <= 24) ? 2 : 1)
 layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
                           const T* __restrict__ dout, const T* __restrict__ inp,
                           const T* __restrict__ w, const float* __restrict__ mean,
                           const float* __restrict__ rstd, int N, int C) {
     constexpr int EPV = Vec<T>::N;
-    extern __shared__ float red[];   // 2C floats
+    extern __shared__ float red[];   // 2C floats (SUM: 3C, then LN_WARPS rows of C)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvec = C / EPV;
+    constexpr int W = SUM ? 3 : 2;
+    float* wsum = red + 3 * C + warp * C;           // this warp's running column sums (SUM)
     Vec<T> wv[NV];
     float dwa[NV][EPV], dba[NV][EPV];
 #pragma unroll
@@ -230,6 +236,9 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
         if (vi < nvec) wv[i] = load_vec(w + vi * EPV);
 #pragma unroll
         for (int e = 0; e < EPV; e++) { dwa[i][e] = 0.f; dba[i][e] = 0.f; }
+        if (SUM && vi < nvec)
+#pragma unroll
+            for (int e = 0; e < EPV; e++) wsum[vi * EPV + e] = 0.f;
     }
     for (int row = blockIdx.x * LN_WARPS + warp; row < N; row += gridDim.x * LN_WARPS) {
         const T* x = inp + (size_t)row * C;
@@ -276,6 +285,10 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
                     nv.set(e, cur[i].get(e) + r * (g - mg - xh * mgx));
                 }
                 store_vec(dx + vi * EPV, nv);
+                if (SUM) {
+#pragma unroll
+                    for (int e = 0; e < EPV; e++) wsum[vi * EPV + e] += nv.get(e);   // the stored (rounded) value
+                }
             }
         }
     }
@@ -289,27 +302,28 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
 #pragma unroll
                     for (int e = 0; e < EPV; e++) {
                         int c = vi * EPV + e;
-                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; }
-                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; }
+                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum[c]; }
+                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum[c]; }
                     }
                 }
             }
         }
         __syncthreads();
     }
-    float* pj = partial + (size_t)blockIdx.x * 2 * C;
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) pj[c] = red[c];
+    float* pj = partial + (size_t)blockIdx.x * W * C;
+    for (int c = threadIdx.x; c < W * C; c += blockDim.x) pj[c] = red[c];
 }
 
 // Column sums of a (G x W) fp32 partial matrix, in a fixed order: a 256-thread block
 // takes 32 columns; thread (c, g) sums rows g, g+8, g+16, ... of column c, then the
 // eight group sums are added in group order.  Column w < split goes to out0[w], the
-// rest to out1[w - split] (both accumulate).
+// rest to out1[w - split], or with out2, columns [2*split, 3*split) to out2 (all
+// accumulate).
 #define CR_COLS 32
 #define CR_GROUPS 8
 __global__ void __launch_bounds__(CR_COLS * CR_GROUPS)
 column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
-                     const float* __restrict__ partial, int G, int W) {
+                     const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
     __shared__ float sm[CR_GROUPS][CR_COLS];
     const int c = threadIdx.x % CR_COLS, g = threadIdx.x / CR_COLS;
     const int w = blockIdx.x * CR_COLS + c;
@@ -328,7 +342,9 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int spl
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < CR_GROUPS; k++) s += sm[k][c];
-        if (w < split) out0[w] += s; else out1[w - split] += s;
+        if (w < split) out0[w] += s;
+        else if (!out2 || w < 2 * split) out1[w - split] += s;
+        else out2[w - 2 * split] += s;
     }
 }
 
@@ -339,6 +355,7 @@ template <typename T>
 __global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x,
                                       int M, int N, int rows_per_chunk) {
     constexpr int EPV = Vec<T>::N;
+    constexpr int U = 8;                       // rows in flight per thread
     const int cv = blockIdx.x * blockDim.x + threadIdx.x;
     const int r = blockIdx.y;
     if (cv * EPV >= N) return;
@@ -347,13 +364,16 @@ __global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __re
 #pragma unroll
     for (int e = 0; e < EPV; e++) s[e] = 0.f;
     int m = m0;
-    for (; m + 1 < m1; m += 2) {
-        Vec<T> a = load_vec(x + (size_t)m * N + cv * EPV);
-        Vec<T> b = load_vec(x + (size_t)(m + 1) * N + cv * EPV);
+    for (; m + U <= m1; m += U) {
+        Vec<T> a[U];
 #pragma unroll
-        for (int e = 0; e < EPV; e++) s[e] += a.get(e) + b.get(e);
+        for (int k = 0; k < U; k++) a[k] = load_vec(x + (size_t)(m + k) * N + cv * EPV);
+#pragma unroll
+        for (int k = 0; k < U; k++)
+#pragma unroll
+            for (int e = 0; e < EPV; e++) s[e] += a[k].get(e);
     }
-    if (m < m1) {
+    for (; m < m1; m++) {
         Vec<T> a = load_vec(x + (size_t)m * N + cv * EPV);
 #pragma unroll
         for (int e = 0; e < EPV; e++) s[e] += a.get(e);
@@ -382,6 +402,12 @@ __global__ void colsum_partial_scalar_kernel(float* __restrict__ partial, const 
 // j < V and 0 for the padded columns.  exp(a) is computed as exp2(a * log2 e).
 #define XENT_THREADS 1024
 #define XENT_LOG2E 1.4426950408889634f
+// 2^x by the hardware approximation (relative error ~2^-22); 2^-inf = 0
+__device__ __forceinline__ float xent_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 template <typename T>
 __global__ void __launch_bounds__(XENT_THREADS)
 softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
@@ -413,9 +439,9 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
         }
         if (vmax == -INFINITY) continue;
         const float nm = fmaxf(mx2, vmax);
-        float acc = sum * exp2f(mx2 - nm);
+        float acc = sum * xent_ex2(mx2 - nm);
 #pragma unroll
-        for (int e = 0; e < EPV; e++) acc += exp2f(y[e] - nm);
+        for (int e = 0; e < EPV; e++) acc += xent_ex2(y[e] - nm);
         mx2 = nm;
         sum = acc;
     }
@@ -453,7 +479,7 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
         for (int e = 0; e < EPV; e++) {
             const int j = vi * EPV + e;
             float d = 0.f;
-            if (j < V) d = (exp2f(fmaf(p.get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
+            if (j < V) d = (xent_ex2(fmaf(p.get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
             o.set(e, d);
         }
         store_vec(z + (size_t)vi * EPV, o);
