@@ -93,6 +93,35 @@ __global__ void fa_backward_D(float* __restrict__ D, const bf16* __restrict__ do
     D[((size_t)b * NH + h) * Tn + t] = s;
 }
 
+// The same row sums for hs == 64: eight lanes per (b, t, h) row, one 16-byte packet of
+// dO and of O each, added across the eight lanes by shuffles (a warp reads four
+// consecutive rows: 512 contiguous bytes per load).
+__global__ void fa_backward_D64(float* __restrict__ D, const bf16* __restrict__ dout,
+                                const bf16* __restrict__ out, int B, int Tn, int C, int NH) {
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = gid >> 3;
+    const int sub = threadIdx.x & 7;
+    const bool valid = row < (long long)B * Tn * NH;
+    float s = 0.f;
+    if (valid) {
+        const int h = (int)(row % NH);
+        const long long bt = row / NH;
+        const size_t o = (size_t)bt * C + h * 64 + sub * 8;
+        Vec<bf16> a = load_vec(dout + o), c = load_vec(out + o);
+#pragma unroll
+        for (int e = 0; e < 8; e++) s += a.get(e) * c.get(e);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (valid && sub == 0) {
+        const int h = (int)(row % NH);
+        const long long bt = row / NH;
+        const int b = (int)(bt / Tn), t = (int)(bt % Tn);
+        D[((size_t)b * NH + h) * Tn + t] = s;
+    }
+}
+
 // dQ, one warp per query row t: dq = scale * sum_{j<=t} P_tj (dP_tj - D_t) k_j
 template <int NDV>
 __global__ void __launch_bounds__(FA_WARPS * 32)
@@ -242,7 +271,8 @@ int attention_flash_backward(cudaStream_t s, bf16* dqkv, const bf16* dout, const
     const int rows = B * NH * Tn;
     const int grid = ceil_div(rows, FA_WARPS);
     rt_note_launches(3);
-    fa_backward_D<<<ceil_div(rows, 256), 256, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
+    if (hs == 64) fa_backward_D64<<<(int)(((long long)rows * 8 + 255) / 256), 256, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
+    else fa_backward_D<<<ceil_div(rows, 256), 256, 0, s>>>(scratch, dout, out, B, Tn, C, NH);
     if (hs == AM_HS) {
         int rc = attention_tc_backward(s, dqkv, dout, qkv, lse, scratch, B, Tn, C, NH, err);
         if (rc != GPT2_EUNSUPPORTED) return rc;

@@ -307,49 +307,80 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
 }
 
 // two resident blocks per SM on a 148-SM part; each warp then walks ~7 rows at N = 16384
+// column sums of a (G x W) fp32 partial matrix into out0/out1/out2 (see column_reduce_kernel)
+static void column_reduce_any(cudaStream_t s, float* out0, float* out1, int split, const float* partial, int G,
+                              int W, float* out2) {
+    if (W % 4 == 0 && ((uintptr_t)partial & 15) == 0)
+        column_reduce4_kernel<<<ceil_div(W, 32), 256, 0, s>>>(out0, out1, split, partial, G, W, out2);
+    else
+        column_reduce_kernel<<<ceil_div(W, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(out0, out1, split, partial, G, W, out2);
+}
+
 static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 2), 296)); }
 
 // dsum (nullable): also add the column sums of the updated dinp (bias gradient of the
-// layer whose output is this residual stream)
+// layer whose output is this residual stream).  The shared-memory pipelined kernel runs
+// whenever its stages fit and the rows are 16-byte aligned; otherwise the register one.
+template <typename T, int NV, bool SUM>
+static int ln_backward_launch(cudaStream_t s, int& G, T* dinp, float* partial, const T* dout, const T* inp, const T* w,
+                              const float* mean, const float* rstd, int N, int C, unsigned* err) {
+    constexpr int W = SUM ? 3 : 2;
+    const size_t pipe_smem = (size_t)(W * C + (SUM ? LN_WARPS * C : 0)) * sizeof(float) +
+                             (size_t)LN_WARPS * 2 * 3 * C * sizeof(T) + 2 * LN_WARPS * sizeof(uint64_t);
+    const bool aligned = ((((uintptr_t)dinp | (uintptr_t)dout | (uintptr_t)inp) & 15) == 0) &&
+                         ((size_t)C * sizeof(T)) % 16 == 0;
+    if (aligned && pipe_smem <= 227 * 1024) {
+        if (pipe_smem > 48 * 1024 &&
+            cudaFuncSetAttribute(layernorm_backward_pipe_kernel<T, NV, SUM>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe_smem) != cudaSuccess)
+            return GPT2_ECUDA;
+        if (pipe_smem > 113 * 1024) G = std::min(G, 148);     // one block per SM: a single wave
+        layernorm_backward_pipe_kernel<T, NV, SUM><<<G, LN_WARPS * 32, pipe_smem, s>>>(dinp, partial, dout, inp, w,
+                                                                                     mean, rstd, N, C, err);
+    } else {
+        const size_t smem = (SUM ? (3 + LN_WARPS) : 2) * C * sizeof(float);
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(layernorm_backward_kernel<T, NV, SUM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        layernorm_backward_kernel<T, NV, SUM><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd,
+                                                                            N, C);
+    }
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
 template <typename T>
 static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
                        const T* w, const float* mean, const float* rstd, int N, int C,
-                       float* partial, size_t partial_floats, float* dsum = nullptr) {
+                       float* partial, size_t partial_floats, float* dsum = nullptr, unsigned* err = nullptr) {
     constexpr int EPV = Vec<T>::N;
     const int nv = ceil_div(C / EPV, 32);
-    const int G = ln_backward_grid(N);
+    int G = ln_backward_grid(N);
     const int W = dsum ? 3 : 2;
     if ((size_t)G * W * C > partial_floats) return GPT2_EINVAL;
-    const size_t smem = (dsum ? (3 + LN_WARPS) : 2) * C * sizeof(float);
     ProfScope ps(s, PC_LAYERNORM_BWD, 0, 4.0 * N * C * sizeof(T) + 8.0 * N + 3.0 * C * sizeof(T) + 8.0 * C);
     rt_note_launches(2);
-    if (dsum) {
-        switch (nv) {
-#define LNB_CASE(k) case k: if (smem > 48 * 1024) cudaFuncSetAttribute(layernorm_backward_kernel<T, k, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-                            layernorm_backward_kernel<T, k, true><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
-            LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
-            LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
+    int rc = GPT2_EUNSUPPORTED;
+    switch (nv) {
+#define LNB_CASE(k)                                                                                            \
+    case k:                                                                                                    \
+        rc = dsum ? ln_backward_launch<T, k, true>(s, G, dinp, partial, dout, inp, w, mean, rstd, N, C, err)   \
+                  : ln_backward_launch<T, k, false>(s, G, dinp, partial, dout, inp, w, mean, rstd, N, C, err); \
+        break;
+        LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
+        LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
 #undef LNB_CASE
-            default: return GPT2_EUNSUPPORTED;
-        }
-    } else {
-        switch (nv) {
-#define LNB_CASE(k) case k: layernorm_backward_kernel<T, k, false><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd, N, C); break;
-            LNB_CASE(1) LNB_CASE(2) LNB_CASE(3) LNB_CASE(4) LNB_CASE(5) LNB_CASE(6) LNB_CASE(7) LNB_CASE(8)
-            LNB_CASE(9) LNB_CASE(10) LNB_CASE(11) LNB_CASE(12) LNB_CASE(13) LNB_CASE(14) LNB_CASE(15) LNB_CASE(16)
-#undef LNB_CASE
-            default: return GPT2_EUNSUPPORTED;
-        }
+        default: break;
     }
-    CK(cudaGetLastError());
-    column_reduce_kernel<<<ceil_div(W * C, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(dw, db, C, partial, G, W * C, dsum);
+    if (rc != GPT2_OK) return rc;
+    column_reduce_any(s, dw, db, C, partial, G, W * C, dsum);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
 
 static void colsum_shape(int M, int N, int* R, int* rows) {
     (void)N;
-    int r = std::max(1, std::min(1024, ceil_div(M, 16)));
+    int r = std::max(1, std::min(1024, ceil_div(M, 128)));
     *rows = ceil_div(M, r);
     *R = ceil_div(M, *rows);
 }
@@ -364,9 +395,9 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
     rt_note_launches(2);
     constexpr int EPV = Vec<T>::N;
     if (N % EPV) colsum_partial_scalar_kernel<T><<<dim3(ceil_div(N, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
-    else colsum_partial_kernel<T><<<dim3(ceil_div(N / EPV, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
+    else colsum_partial_kernel<T><<<dim3(ceil_div(N / EPV, 32), R), CS_WARPS * 32, 0, s>>>(partial, x, M, N, rows);
     CK(cudaGetLastError());
-    column_reduce_kernel<<<ceil_div(N, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(out, out, N, partial, R, N);
+    column_reduce_any(s, out, out, N, partial, R, N, nullptr);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
@@ -576,7 +607,7 @@ static int backward_impl(GPT2* m) {
     // the updated residual gradient is d(res3) of the last layer: its column sums are
     // that layer's MLP-projection bias gradient
     RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf,
-                      G(P_FCPROJB) + (L - 1) * C));
+                      G(P_FCPROJB) + (L - 1) * C, m->err));
     for (int l = L - 1; l >= 0; l--) {
         const T* x_in = (l == 0) ? (const T*)m->encoded : (const T*)m->res3 + (l - 1) * BTmax * C;
         const T* ln1 = (const T*)m->ln1 + l * BTmax * C;
@@ -597,7 +628,7 @@ static int backward_impl(GPT2* m) {
         RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
-                          G(P_ATTPROJB) + l * C));      // d(res2) column sums: attention-projection bias
+                          G(P_ATTPROJB) + l * C, m->err));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
         RC(mm_backward_dx<T>(m, s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C));
@@ -609,14 +640,15 @@ static int backward_impl(GPT2* m) {
         RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf));
         // ln1 (dresid becomes d x_l)
         RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
-                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr));   // d(res3) of layer l-1
+                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err));   // d(res3) of layer l-1
     }
     // encoder: deterministic scatter-add into dwte (ids sorted in the forward), dwpe
     ProfScope ps(s, PC_ENCODER_BWD, 0, (double)BT * C * sizeof(T) + 8.0 * BT * C + 8.0 * Tn * C);
     rt_note_launches(3);
-    encoder_backward_wte_partial<T><<<ceil_div(BT, ENC_CHUNK), 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, dresid, BT, C, m->V);
+    const int enc_threads = std::min(256, ceil_div(C / Vec<T>::N, 32) * 32);
+    encoder_backward_wte_partial<T><<<ceil_div(BT, ENC_CHUNK), enc_threads, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, dresid, BT, C, m->V);
     CK(cudaGetLastError());
-    encoder_backward_wte_final<<<BT, 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
+    encoder_backward_wte_final<<<ceil_div(BT, ENC_CHUNK), 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
     CK(cudaGetLastError());
     encoder_backward_wpe<T><<<ceil_div(Tn * C, 256), 256, 0, s>>>(G(P_WPE), dresid, B, Tn, C);
     CK(cudaGetLastError());

@@ -7,6 +7,7 @@
 // results are bitwise reproducible run to run (no floating-point atomics).
 #pragma once
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 // ============================================================== encoder
 // out[bt, :] = wte[tok[bt], :] + wpe[bt % T, :].  One thread per 16-byte packet.
@@ -74,11 +75,14 @@ __global__ void encoder_sort_kernel(unsigned* __restrict__ sorted, const int* __
 // of ENC_CHUNK sorted positions walks its runs of equal id; a run whose id occurs
 // only inside this chunk is added straight into dwte (no other chunk touches that
 // row), a run of an id that spans chunks leaves its partial sum at the run's first
-// sorted index.
+// sorted index.  A thread owns one 16-byte packet of columns and has eight rows in
+// flight.  C must be a multiple of the packet.
 template <typename T>
 __global__ void encoder_backward_wte_partial(float* __restrict__ dwte, float* __restrict__ partial,
                                              const unsigned* __restrict__ sorted,
                                              const T* __restrict__ dout, int BT, int C, int V) {
+    constexpr int EPV = Vec<T>::N;
+    constexpr int U = 8;
     __shared__ unsigned sk[ENC_CHUNK + 2];
     const int c0 = blockIdx.x * ENC_CHUNK;
     const int n = min(ENC_CHUNK, BT - c0);
@@ -88,51 +92,82 @@ __global__ void encoder_backward_wte_partial(float* __restrict__ dwte, float* __
     }
     __syncthreads();
     const unsigned ubt = (unsigned)BT;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        float acc = 0.f;
+    const int nvec = C / EPV;
+    for (int cv = threadIdx.x; cv < nvec; cv += blockDim.x) {
+        float acc[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; e++) acc[e] = 0.f;
         int run_start = 0;
-        for (int i = 0; i < n; i++) {
-            unsigned key = sk[i + 1];
-            unsigned id = key / ubt, pos = key % ubt;
-            acc += to_f32(dout[(size_t)pos * C + c]);
-            unsigned nxt = sk[i + 2];
-            bool last = (i == n - 1) || (nxt / ubt != id);
-            if (last) {
-                bool from_prev = (run_start == 0) && (c0 > 0) && (sk[0] / ubt == id);
-                bool into_next = (i == n - 1) && (c0 + n < BT) && (nxt / ubt == id);
-                if ((int)id < V) {
-                    if (!from_prev && !into_next) dwte[(size_t)id * C + c] += acc;
-                    else partial[(size_t)(c0 + run_start) * C + c] = acc;
+        for (int i0 = 0; i0 < n; i0 += U) {
+            Vec<T> a[U];
+#pragma unroll
+            for (int k = 0; k < U; k++)
+                if (i0 + k < n) a[k] = load_vec(dout + (size_t)(sk[i0 + k + 1] % ubt) * C + cv * EPV);
+#pragma unroll
+            for (int k = 0; k < U; k++) {
+                const int i = i0 + k;
+                if (i >= n) break;
+                const unsigned id = sk[i + 1] / ubt;
+#pragma unroll
+                for (int e = 0; e < EPV; e++) acc[e] += a[k].get(e);
+                const unsigned nxt = sk[i + 2];
+                const bool last = (i == n - 1) || (nxt / ubt != id);
+                if (last) {
+                    const bool from_prev = (run_start == 0) && (c0 > 0) && (sk[0] / ubt == id);
+                    const bool into_next = (i == n - 1) && (c0 + n < BT) && (nxt / ubt == id);
+                    if ((int)id < V) {
+                        float* dst = (!from_prev && !into_next) ? dwte + (size_t)id * C + cv * EPV
+                                                                 : partial + (size_t)(c0 + run_start) * C + cv * EPV;
+                        const bool add = !from_prev && !into_next;
+#pragma unroll
+                        for (int q = 0; q < EPV / 4; q++) {
+                            float4* d4 = reinterpret_cast<float4*>(dst) + q;
+                            float4 o = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                            if (add) { const float4 c = *d4; o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w; }
+                            *d4 = o;
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < EPV; e++) acc[e] = 0.f;
+                    run_start = i + 1;
                 }
-                acc = 0.f;
-                run_start = i + 1;
             }
         }
     }
 }
 
-// Pass 2: for each id whose run spans chunks, add its partials (at the run start and at
-// every chunk boundary inside the run) in order.  One block per sorted index.
+// Pass 2: a run that spans chunks is the last run of the chunk it starts in; that
+// chunk's block adds the run's partials (at the run start and at every later chunk
+// start inside the run) in order.
 __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float* __restrict__ partial,
                                            const unsigned* __restrict__ sorted, int BT, int C, int V) {
-    const int i = blockIdx.x;
+    const int c0 = blockIdx.x * ENC_CHUNK;
+    const int last = min(BT, c0 + ENC_CHUNK) - 1;
+    if (last + 1 >= BT) return;                            // no later chunk
     const unsigned ubt = (unsigned)BT;
-    unsigned id = sorted[i] / ubt;
+    const unsigned id = sorted[last] / ubt;
     if ((int)id >= V) return;
-    if (i > 0 && sorted[i - 1] / ubt == id) return;        // not the start of a run
+    if (sorted[last + 1] / ubt != id) return;              // the chunk's last run ends inside it
+    // first index of the run: first key >= id * BT
+    const unsigned lo_key = id * ubt;
+    int lo = 0, hi = last;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (sorted[mid] < lo_key) lo = mid + 1; else hi = mid;
+    }
+    const int i = lo;
+    if (i < c0) return;                                     // started in an earlier chunk
     // end of the run: first index whose key reaches (id+1)*BT
-    unsigned lim = (id + 1) * ubt;
-    int lo = i, hi = BT;
+    const unsigned lim = (id + 1) * ubt;
+    lo = last + 1; hi = BT;
     while (lo < hi) {
         int mid = (lo + hi) >> 1;
         if (sorted[mid] < lim) lo = mid + 1; else hi = mid;
     }
     const int e = lo;
-    if (i / ENC_CHUNK == (e - 1) / ENC_CHUNK) return;     // handled in pass 1
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
         float s = partial[(size_t)i * C + c];
-        for (int b = (i / ENC_CHUNK + 1) * ENC_CHUNK; b < e; b += ENC_CHUNK)
-            s += partial[(size_t)b * C + c];
+        for (int b = c0 + ENC_CHUNK; b < e; b += ENC_CHUNK) s += partial[(size_t)b * C + c];
         dwte[(size_t)id * C + c] += s;
     }
 }
@@ -216,6 +251,29 @@ layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* _
 // that is the bias gradient of the linear layer whose output is the residual stream.
 // Each warp keeps that sum in its own shared-memory row (its lanes own distinct
 // columns), which leaves the register budget of two blocks per SM untouched.
+// Per-warp running column sums of the layernorm backward, laid out as EPV/4 planes of
+// float4 (plane p holds elements 4p..4p+3 of every vector), so that the 32 lanes of a warp
+// touch 32 consecutive 16-byte words: no shared-memory bank conflicts.
+template <int EPV>
+__device__ __forceinline__ void wsum_zero(float* ws, int nvec, int vi) {
+#pragma unroll
+    for (int p = 0; p < EPV / 4; p++)
+        *reinterpret_cast<float4*>(ws + (size_t)p * nvec * 4 + vi * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+template <int EPV, typename V>
+__device__ __forceinline__ void wsum_add(float* ws, int nvec, int vi, const V& v) {
+#pragma unroll
+    for (int p = 0; p < EPV / 4; p++) {
+        float4* q = reinterpret_cast<float4*>(ws + (size_t)p * nvec * 4 + vi * 4);
+        float4 a = *q;
+        a.x += v.get(4 * p); a.y += v.get(4 * p + 1); a.z += v.get(4 * p + 2); a.w += v.get(4 * p + 3);
+        *q = a;
+    }
+}
+__device__ __forceinline__ float wsum_get(const float* ws, int nvec, int vi, int e) {
+    return ws[(size_t)(e >> 2) * nvec * 4 + vi * 4 + (e & 3)];
+}
+
 template <typename T, int NV, bool SUM>
 __global__ void __launch_bounds__(LN_WARPS * 32, (NV * Vec<T>::N <= 24) ? 2 : 1)
 layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
@@ -236,9 +294,7 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
         if (vi < nvec) wv[i] = load_vec(w + vi * EPV);
 #pragma unroll
         for (int e = 0; e < EPV; e++) { dwa[i][e] = 0.f; dba[i][e] = 0.f; }
-        if (SUM && vi < nvec)
-#pragma unroll
-            for (int e = 0; e < EPV; e++) wsum[vi * EPV + e] = 0.f;
+        if (SUM && vi < nvec) wsum_zero<EPV>(wsum, nvec, vi);
     }
     for (int row = blockIdx.x * LN_WARPS + warp; row < N; row += gridDim.x * LN_WARPS) {
         const T* x = inp + (size_t)row * C;
@@ -285,10 +341,7 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
                     nv.set(e, cur[i].get(e) + r * (g - mg - xh * mgx));
                 }
                 store_vec(dx + vi * EPV, nv);
-                if (SUM) {
-#pragma unroll
-                    for (int e = 0; e < EPV; e++) wsum[vi * EPV + e] += nv.get(e);   // the stored (rounded) value
-                }
+                if (SUM) wsum_add<EPV>(wsum, nvec, vi, nv);          // the stored (rounded) value
             }
         }
     }
@@ -302,8 +355,142 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
 #pragma unroll
                     for (int e = 0; e < EPV; e++) {
                         int c = vi * EPV + e;
-                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum[c]; }
-                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum[c]; }
+                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum_get(wsum, nvec, vi, e); }
+                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum_get(wsum, nvec, vi, e); }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float* pj = partial + (size_t)blockIdx.x * W * C;
+    for (int c = threadIdx.x; c < W * C; c += blockDim.x) pj[c] = red[c];
+}
+
+// Same computation, with each warp's rows streamed through shared memory: lane 0 of the
+// warp fetches row k+1's x, dy and dinp with 1-D bulk copies (two stages, one mbarrier
+// each) while the warp works on row k from shared memory, so loads stay in flight the
+// whole time and the row no longer occupies registers.  Shared memory: partial sums
+// (W*C floats), the SUM rows (LN_WARPS*C floats), then LN_WARPS x 2 stages x 3 rows of C
+// elements, then 2*LN_WARPS mbarriers.  Bounded waits: on a timeout the warp stops,
+// sets the error bit, and lets its copies land before the block finishes.
+template <typename T, int NV, bool SUM>
+__global__ void __launch_bounds__(LN_WARPS * 32, (NV * Vec<T>::N <= 24) ? 2 : 1)
+layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial,
+                               const T* __restrict__ dout, const T* __restrict__ inp,
+                               const T* __restrict__ w, const float* __restrict__ mean,
+                               const float* __restrict__ rstd, int N, int C, unsigned* err) {
+    constexpr int EPV = Vec<T>::N;
+    constexpr int W = SUM ? 3 : 2;
+    extern __shared__ __align__(16) float red[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvec = C / EPV;
+    const size_t row_bytes = (size_t)C * sizeof(T);
+    float* wsum = red + W * C + warp * C;
+    T* stage_base = reinterpret_cast<T*>(red + W * C + (SUM ? LN_WARPS * C : 0));
+    T* st = stage_base + (size_t)warp * 2 * 3 * C;          // this warp's two stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base + (size_t)LN_WARPS * 2 * 3 * C) + 2 * warp;
+    if (lane == 0) { mbar_init(&bars[0], 1); mbar_init(&bars[1], 1); }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    Vec<T> wv[NV];
+    float dwa[NV][EPV], dba[NV][EPV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int vi = lane + 32 * i;
+        if (vi < nvec) wv[i] = load_vec(w + vi * EPV);
+#pragma unroll
+        for (int e = 0; e < EPV; e++) { dwa[i][e] = 0.f; dba[i][e] = 0.f; }
+        if (SUM && vi < nvec) wsum_zero<EPV>(wsum, nvec, vi);
+    }
+    const int step = gridDim.x * LN_WARPS;
+    const int row0 = blockIdx.x * LN_WARPS + warp;
+    const int nrows = row0 < N ? (N - row0 + step - 1) / step : 0;
+    auto fetch = [&](int k) {
+        const int row = row0 + k * step;
+        T* d = st + (size_t)(k & 1) * 3 * C;
+        fence_async_smem();
+        mbar_expect_tx(&bars[k & 1], (uint32_t)(3 * row_bytes));
+        bulk_load(d, inp + (size_t)row * C, (uint32_t)row_bytes, &bars[k & 1]);
+        bulk_load(d + C, dout + (size_t)row * C, (uint32_t)row_bytes, &bars[k & 1]);
+        bulk_load(d + 2 * C, dinp + (size_t)row * C, (uint32_t)row_bytes, &bars[k & 1]);
+    };
+    if (lane == 0 && nrows > 0) fetch(0);
+    int issued = nrows > 0 ? 1 : 0, waited = 0;
+    for (int k = 0; k < nrows; k++) {
+        const int row = row0 + k * step;
+        const float m = mean[row], r = rstd[row];
+        __syncwarp();                                  // every lane is done with row k-1's stage
+        if (lane == 0 && k + 1 < nrows) { fetch(k + 1); issued++; }
+        // wait for row k (bounded)
+        bool ok = mbar_try_wait(&bars[k & 1], (k >> 1) & 1);
+        if (!ok) {
+            const long long t0 = clock64();
+            while (!(ok = mbar_try_wait(&bars[k & 1], (k >> 1) & 1)))
+                if (clock64() - t0 > TC_WAIT_LIMIT) break;
+        }
+        if (!__all_sync(0xffffffffu, ok)) { if (lane == 0) raise_error(err, ERRBIT_TIMEOUT); break; }
+        waited++;
+        const T* xs = st + (size_t)(k & 1) * 3 * C;
+        const T* dys = xs + C;
+        const T* cs = xs + 2 * C;
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                Vec<T> xp = load_vec(xs + vi * EPV), dp = load_vec(dys + vi * EPV);
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    const float xh = (xp.get(e) - m) * r;
+                    const float d = dp.get(e);
+                    const float g = d * wv[i].get(e);
+                    sg += g;
+                    sgx += g * xh;
+                    dwa[i][e] += d * xh;
+                    dba[i][e] += d;
+                }
+            }
+        }
+        const float mg = warp_sum(sg) / (float)C;
+        const float mgx = warp_sum(sgx) / (float)C;
+        T* dx = dinp + (size_t)row * C;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int vi = lane + 32 * i;
+            if (vi < nvec) {
+                Vec<T> xp = load_vec(xs + vi * EPV), dp = load_vec(dys + vi * EPV), cur = load_vec(cs + vi * EPV), nv;
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    const float xh = (xp.get(e) - m) * r;
+                    const float g = dp.get(e) * wv[i].get(e);
+                    nv.set(e, cur.get(e) + r * (g - mg - xh * mgx));
+                }
+                store_vec(dx + vi * EPV, nv);
+                if (SUM) wsum_add<EPV>(wsum, nvec, vi, nv);
+            }
+        }
+    }
+    // copies issued but not waited for (only after a timeout) land before the block ends
+    if (lane == 0) {
+        for (int k = waited; k < issued; k++) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[k & 1], (k >> 1) & 1))
+                if (clock64() - t0 > TC_WAIT_LIMIT) break;
+        }
+    }
+    __syncwarp();
+    for (int wi = 0; wi < LN_WARPS; wi++) {
+        if (warp == wi) {
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                int vi = lane + 32 * i;
+                if (vi < nvec) {
+#pragma unroll
+                    for (int e = 0; e < EPV; e++) {
+                        int c = vi * EPV + e;
+                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum_get(wsum, nvec, vi, e); }
+                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum_get(wsum, nvec, vi, e); }
                     }
                 }
             }
@@ -348,39 +535,93 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int spl
     }
 }
 
+// The same sums for W a multiple of 4 (16-byte aligned rows): a 256-thread block takes
+// 32 columns as 8 float4 packets; thread (p, g) adds rows g, g+32, g+64, ... of packet p
+// (four loads in flight), then the 32 group sums of each column are added in group order.
+__global__ void __launch_bounds__(256)
+column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
+                      const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
+    __shared__ float sm[32][33];
+    const int p = threadIdx.x & 7, g = threadIdx.x >> 3;
+    const int w = blockIdx.x * 32 + p * 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (w < W) {
+        const float* col = partial + w;
+        int j = g;
+        for (; j + 96 < G; j += 128) {
+            float4 a[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) a[k] = *reinterpret_cast<const float4*>(col + (size_t)(j + 32 * k) * W);
+#pragma unroll
+            for (int k = 0; k < 4; k++) { s.x += a[k].x; s.y += a[k].y; s.z += a[k].z; s.w += a[k].w; }
+        }
+        for (; j < G; j += 32) {
+            const float4 a = *reinterpret_cast<const float4*>(col + (size_t)j * W);
+            s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
+        }
+    }
+    sm[g][p * 4 + 0] = s.x; sm[g][p * 4 + 1] = s.y; sm[g][p * 4 + 2] = s.z; sm[g][p * 4 + 3] = s.w;
+    __syncthreads();
+    const int t = threadIdx.x, wc = blockIdx.x * 32 + t;
+    if (t < 32 && wc < W) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 32; k++) acc += sm[k][t];
+        if (wc < split) out0[wc] += acc;
+        else if (!out2 || wc < 2 * split) out1[wc - split] += acc;
+        else out2[wc - 2 * split] += acc;
+    }
+}
+
 // ============================================================== column sums (bias grads)
-// partial[r][n] = sum of x[m][n] over the rows m of chunk r, in row order (a thread
-// owns one 16-byte packet of columns); column_reduce_kernel then adds the chunks.
+// partial[r][n] = sum of x[m][n] over the rows m of chunk r.  A 256-thread block takes
+// 32 16-byte packets of columns of one chunk; warp w adds rows w, w+8, w+16, ... (four
+// loads in flight per lane), then the eight warp sums are added in warp order.
+#define CS_WARPS 8
 template <typename T>
-__global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x,
-                                      int M, int N, int rows_per_chunk) {
+__global__ void __launch_bounds__(CS_WARPS * 32)
+colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x, int M, int N, int rows_per_chunk) {
     constexpr int EPV = Vec<T>::N;
-    constexpr int U = 8;                       // rows in flight per thread
-    const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int U = 4;
+    __shared__ float sm[CS_WARPS][EPV * 32];          // [warp][element][lane]: conflict-free
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cv = blockIdx.x * 32 + lane;
     const int r = blockIdx.y;
-    if (cv * EPV >= N) return;
     const int m0 = r * rows_per_chunk, m1 = min(M, m0 + rows_per_chunk);
     float s[EPV];
 #pragma unroll
     for (int e = 0; e < EPV; e++) s[e] = 0.f;
-    int m = m0;
-    for (; m + U <= m1; m += U) {
-        Vec<T> a[U];
+    if (cv * EPV < N) {
+        const T* xc = x + cv * EPV;
+        int m = m0 + warp;
+        for (; m + (U - 1) * CS_WARPS < m1; m += U * CS_WARPS) {
+            Vec<T> a[U];
 #pragma unroll
-        for (int k = 0; k < U; k++) a[k] = load_vec(x + (size_t)(m + k) * N + cv * EPV);
+            for (int k = 0; k < U; k++) a[k] = load_vec(xc + (size_t)(m + k * CS_WARPS) * N);
 #pragma unroll
-        for (int k = 0; k < U; k++)
+            for (int k = 0; k < U; k++)
 #pragma unroll
-            for (int e = 0; e < EPV; e++) s[e] += a[k].get(e);
+                for (int e = 0; e < EPV; e++) s[e] += a[k].get(e);
+        }
+        for (; m < m1; m += CS_WARPS) {
+            Vec<T> a = load_vec(xc + (size_t)m * N);
+#pragma unroll
+            for (int e = 0; e < EPV; e++) s[e] += a.get(e);
+        }
     }
-    for (; m < m1; m++) {
-        Vec<T> a = load_vec(x + (size_t)m * N + cv * EPV);
 #pragma unroll
-        for (int e = 0; e < EPV; e++) s[e] += a.get(e);
+    for (int e = 0; e < EPV; e++) sm[warp][e * 32 + lane] = s[e];
+    __syncthreads();
+    for (int t = threadIdx.x; t < 32 * EPV; t += blockDim.x) {
+        const int l = t / EPV, e = t % EPV;
+        const int n = (blockIdx.x * 32 + l) * EPV + e;
+        if (n < N) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < CS_WARPS; w++) acc += sm[w][e * 32 + l];
+            partial[(size_t)r * N + n] = acc;
+        }
     }
-    float* p = partial + (size_t)r * N + cv * EPV;
-#pragma unroll
-    for (int e = 0; e < EPV; e++) p[e] = s[e];
 }
 // one column per thread, for widths that are not a multiple of the packet
 template <typename T>
