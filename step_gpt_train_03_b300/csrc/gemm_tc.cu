@@ -10,17 +10,21 @@
 // contiguous); the MMA reads both forms directly (instruction-descriptor major bits),
 // so no transposed copies are made.
 //
-// Kernel: persistent, one CTA per SM, 192 threads.
+// Kernel: persistent, one CTA per SM, 320 threads; large products run on CTA pairs
+// (2-CTA clusters, 256 x 256 tiles, tcgen05 cta_group::2: each CTA stages half of B and
+// reads half the operand bytes per MMA).
 //   warp 0      TMA producer: 128x64 A tile and BNx64 B tile per stage, 4-stage ring
 //   warp 1      TMEM owner and MMA issuer (one thread): 128xBN fp32 accumulator,
 //               two accumulators in TMEM so the epilogue of tile i overlaps tile i+1
-//   warps 2-5   epilogue: tcgen05.ld 32 rows x 64 columns of the accumulator, fuse
-//               bias / GELU / residual / GELU-backward, stage the chunk in a
-//               128B-swizzled shared buffer and write it with one TMA store (fp32
-//               weight gradients: one TMA reduce-add, so each element is added once);
-//               residual and pre-activation inputs arrive by TMA load into the same
-//               buffers, one chunk ahead (the next tile's first chunk is requested
-//               before its accumulator is ready)
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant (warp w reads lanes
+//               32*(w%4)..+31), each taking half of the tile's columns: tcgen05.ld
+//               32 rows x 64 columns of the accumulator, fuse bias / GELU / residual /
+//               GELU-backward, stage 32-column pieces in 64B-swizzled 2 KB shared
+//               buffers and write each with one TMA store (fp32 weight gradients: one
+//               TMA reduce-add, so each element is added once); residual and
+//               pre-activation inputs arrive by TMA load into the same buffers, one
+//               piece ahead (the next tile's first piece is requested before its
+//               accumulator is ready)
 // Every mbarrier wait is bounded: on expiry the kernel raises the timeout bit in the
 // library's error word, the other roles see the abort flag and stop, in-flight copies
 // and MMAs are waited for (again bounded), TMEM is freed and the kernel returns.
@@ -40,8 +44,12 @@
 #define TC_BM 128
 #define TC_BK 64
 #define TC_STAGES 4
-#define TC_THREADS 192
+#define TC_EPI_WARPS 8
+#define TC_THREADS (64 + 32 * TC_EPI_WARPS)
 #define TC_EPI_PARTIAL 5          // fp32 split-K partial tile into scratch
+#ifndef TC_PAIR_NACC
+#define TC_PAIR_NACC 2            // TMEM accumulators of a CTA pair
+#endif
 
 #include "tc_ptx.cuh"
 
@@ -53,54 +61,83 @@ struct TcEpi {
     long ldo;           // row stride of out and aux (elements)
 };
 
-template <int BN>
+// CL = 1: one CTA holds a 128 x 64 A and a BN x 64 B block per stage, 4 stages.
+// CL = 2 (CTA pair): each CTA holds its 128 x 64 A block and half of the B block, so a
+// stage is 2/3 the size and 6 stages fit.
+template <int BN, int CL = 1>
 struct TcSmem {
+    static constexpr int STAGES = CL == 2 ? 6 : TC_STAGES;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
-    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int B_BYTES = BN / CL * TC_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // two 4 KB staging buffers (32 rows x 128 bytes) per epilogue warp
-    static constexpr int STG_OFF = TC_STAGES * STAGE_BYTES;
-    static constexpr int STG_BYTES = 4096;
-    static constexpr int BAR_OFF = STG_OFF + 4 * 2 * STG_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[4 warps][2 buffers];
+    // two 2 KB staging buffers (32 rows x 64 bytes) per epilogue warp
+    static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+    static constexpr int STG_BYTES = 2048;
+    static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * 2 * STG_BYTES;
+    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[epilogue warps][2 buffers];
     // tmem address, abort flag
-    static constexpr int TOTAL = BAR_OFF + (2 * TC_STAGES + 13) * 8 + 16 + 1024;
+    static constexpr int NBAR = 2 * STAGES + 5 + 2 * TC_EPI_WARPS;
+    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
 };
 
-// byte offset of 16-byte chunk j of row r in a 128B-swizzled staging buffer
-__device__ __forceinline__ int stg_off(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
+// byte offset of 16-byte unit j (0..3) of row r in a 64B-swizzled staging buffer of
+// 64-byte rows: the unit index is XORed with bits 1-2 of the row, so the 32 rows of a
+// warp's 16-byte store fall on distinct bank groups in each quarter-warp phase
+__device__ __forceinline__ int stg_off(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
 
-// D (M x N) over units = m_tiles x n_tiles x splits, n fastest.  Split s of a tile
-// covers k-blocks [s*kb_per, min(nkb, (s+1)*kb_per)); partial epilogues write tile
-// (s) of the scratch at out + s*M*ldo.
-template <int BN, int EPI, bool A_MN, bool B_MN>
+// D (M x N) over units = m_groups x n_tiles x splits, where a group is CL consecutive
+// 128-row tiles; units run n fastest, or m fastest when B is the larger operand (each B
+// tile is then read once while all of A stays in L2).  Split s of a tile covers k-blocks [s*kb_per, min(nkb,
+// (s+1)*kb_per)); partial epilogues write tile (s) of the scratch at out + s*M*ldo.
+// CL = 2: the two CTAs of a cluster are a CTA pair computing one 256 x BN tile with
+// 256-row MMAs issued by the leader (rank 0) on both CTAs' tensor cores.  Each CTA
+// loads its own 128 A rows and its half of the B columns; all loads count on the
+// leader's full barrier; the leader's commits release the stage and announce the
+// accumulator in both CTAs; each CTA's epilogue drains its own 128 rows of TMEM and
+// frees the accumulator on the leader's barrier.  Per CTA this halves the B operand
+// reads and shared-memory traffic of each MMA.  NACC accumulators of BN columns.
+template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux, int M, int N,
-               int K, int splits, TcEpi ep, unsigned* err) {
-    using S = TcSmem<BN>;
+               int K, int splits, int m_fast, TcEpi ep, unsigned* err) {
+    using S = TcSmem<BN, CL>;
+    constexpr int STAGES = S::STAGES;
+    constexpr int NACC = CL == 2 ? TC_PAIR_NACC : 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
-    uint64_t* empty = full + TC_STAGES;
-    uint64_t* acc_full = empty + TC_STAGES;
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     uint64_t* aux_bar = done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * TC_EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (M + TC_BM - 1) / TC_BM, n_tiles = (N + BN - 1) / BN;
     const int nkb = (K + TC_BK - 1) / TC_BK;
     const int kb_per = (nkb + splits - 1) / splits;
-    const int units = m_tiles * n_tiles * splits;
+    const int m_groups = (m_tiles + CL - 1) / CL;
+    const int units = m_groups * n_tiles * splits;
+    const int crank = CL > 1 ? (int)cluster_rank() : 0;
+    const bool leader = crank == 0;
+    const int ustart = blockIdx.x / CL, ustep = gridDim.x / CL;    // this cluster's units
+    constexpr uint16_t CMASK = (1u << CL) - 1;
+    auto decode = [&](int u, int& sp, int& mt, int& nt) {
+        sp = u % splits;
+        const int tile = u / splits;
+        const int mg = m_fast ? tile % m_groups : tile / n_tiles;
+        nt = m_fast ? tile / m_groups : tile % n_tiles;
+        mt = mg * CL + crank;
+    };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < TC_STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-        for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+        for (int i = 0; i < STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], CL * TC_EPI_WARPS); }
         mbar_init(done, 1);
-        for (int i = 0; i < 8; i++) mbar_init(&aux_bar[i], 1);
+        for (int i = 0; i < 2 * TC_EPI_WARPS; i++) mbar_init(&aux_bar[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
@@ -109,72 +146,125 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (EPI == EPI_GELU || EPI == EPI_RESID || EPI == EPI_GELU_BWD) tma_prefetch_desc(&tmAux);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(tmem_slot)), "r"(2 * BN) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (CL == 1) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(smem_u32(tmem_slot)), "r"(NACC * BN) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        } else {
+            // one warp of each CTA of the pair: the same columns in both CTAs' TMEM
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(smem_u32(tmem_slot)), "r"(NACC * BN) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync();        // the peer's barriers and TMEM address exist from here on
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the pair's MMAs write one TMEM address in both CTAs: if the two allocations
+    // differ, no work is done (both CTAs see the same two values and agree)
+    bool pair_ok = true;
+    if (CL > 1) {
+        pair_ok = ld_shared_cluster_u32(mapa_shared(tmem_slot, (uint32_t)(crank ^ 1))) == tmem_base;
+        if (!pair_ok && threadIdx.x == 0) raise_error(err, ERRBIT_TIMEOUT);
+    }
+    const int ufirst = pair_ok ? ustart : units;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const int sp = u % splits, tile = u / splits;
-                const int nt = tile % n_tiles, mt = tile / n_tiles;
+            const uint32_t full_lead = CL > 1 ? mapa_shared(full, 0) : 0;   // the leader's full[0]
+            constexpr int BH = BN / CL;                                      // B rows (or columns) per CTA
+            for (int u = ufirst; u < units && ok; u += ustep) {
+                int sp, mt, nt;
+                decode(u, sp, mt, nt);
                 const int kb0 = sp * kb_per, kb1 = min(nkb, kb0 + kb_per);
+                const int nb0 = nt * BN + crank * BH;                        // first B row of this CTA's share
                 for (int kb = kb0; kb < kb1; kb++, it++) {
-                    const int s = it % TC_STAGES;
-                    const uint32_t ph = (it / TC_STAGES) & 1;
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, err)) { ok = false; break; }
                     uint8_t* a = smem + s * S::STAGE_BYTES;
                     uint8_t* b = a + S::A_BYTES;
-                    mbar_expect_tx(&full[s], S::STAGE_BYTES);
-                    if (!A_MN) {
-                        tma_load_2d(a, &tmA, &full[s], kb * TC_BK, mt * TC_BM);
-                    } else {
+                    if constexpr (CL == 1) {
+                        mbar_expect_tx(&full[s], S::STAGE_BYTES);
+                        if (!A_MN) {
+                            tma_load_2d(a, &tmA, &full[s], kb * TC_BK, mt * TC_BM);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < TC_BM / 64; j++)
-                            tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * TC_BK);
-                    }
-                    if (!B_MN) {
-                        tma_load_2d(b, &tmB, &full[s], kb * TC_BK, nt * BN);
-                    } else {
+                            for (int j = 0; j < TC_BM / 64; j++)
+                                tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * TC_BK);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d(b, &tmB, &full[s], kb * TC_BK, nb0);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; j++)
-                            tma_load_2d(b + j * 8192, &tmB, &full[s], nt * BN + j * 64, kb * TC_BK);
+                            for (int j = 0; j < BN / 64; j++)
+                                tma_load_2d(b + j * 8192, &tmB, &full[s], nb0 + j * 64, kb * TC_BK);
+                        }
+                    } else {
+                        // both CTAs' bytes are counted on the leader's barrier
+                        const uint32_t fb = full_lead + s * 8;
+                        if (leader) mbar_expect_tx(&full[s], CL * S::STAGE_BYTES);
+                        if (!A_MN) {
+                            tma_load_2d_pair(a, &tmA, fb, kb * TC_BK, mt * TC_BM);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < TC_BM / 64; j++)
+                                tma_load_2d_pair(a + j * 8192, &tmA, fb, mt * TC_BM + j * 64, kb * TC_BK);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d_pair(b, &tmB, fb, kb * TC_BK, nb0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BH / 64; j++)
+                                tma_load_2d_pair(b + j * 8192, &tmB, fb, nb0 + j * 64, kb * TC_BK);
+                        }
                     }
                 }
             }
-            // before leaving, every copy this thread started must have landed
-            for (int back = 0; back < TC_STAGES && back < it; back++) {
-                const int j = it - 1 - back;
-                const long long t0 = clock64();
-                while (!mbar_try_wait(&full[j % TC_STAGES], (j / TC_STAGES) & 1))
-                    if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+            // before leaving, every copy this CTA's barriers count must have landed (in a
+            // pair the leader's barriers count both CTAs' copies)
+            if (CL == 1 || leader) {
+                for (int back = 0; back < STAGES && back < it; back++) {
+                    const int j = it - 1 - back;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&full[j % STAGES], (j / STAGES) & 1))
+                        if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+                }
+            }
+            // and, in a pair, every release of the last stages (the leader's commits) must
+            // have arrived on this CTA's barriers
+            if (CL > 1) {
+                for (int back = 0; back < STAGES && back < it; back++) {
+                    const int j = it - 1 - back;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&empty[j % STAGES], (j / STAGES) & 1))
+                        if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
+                }
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16(TC_BM, BN, A_MN, B_MN);
+        // (in a pair only the leader's thread issues; its MMAs drive both tensor cores)
+        if (lane == 0 && (CL == 1 || leader)) {
+            constexpr uint32_t IDESC = idesc_bf16(TC_BM * CL, BN, A_MN, B_MN);
             int it = 0, local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, local++) {
+            for (int u = ufirst; u < units && ok; u += ustep, local++) {
                 const int sp = u % splits;
                 const int kb0 = sp * kb_per, kb1 = min(nkb, kb0 + kb_per);
-                const int acc = local & 1;
-                const uint32_t aph = (local >> 1) & 1;
+                const int acc = local % NACC;
+                const uint32_t aph = (local / NACC) & 1;
                 if (!mbar_wait(&acc_empty[acc], aph ^ 1, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = kb0; kb < kb1; kb++, it++) {
-                    const int s = it % TC_STAGES;
-                    const uint32_t ph = (it / TC_STAGES) & 1;
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(&full[s], ph, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a = smem_u32(smem + s * S::STAGE_BYTES);
@@ -185,49 +275,74 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         // MN-major: 16 k-rows are two 1024-byte swizzle atoms
                         const uint64_t ad = A_MN ? sdesc(a + k * 2048, 8192, 1024) : sdesc(a + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? sdesc(b + k * 2048, 8192, 1024) : sdesc(b + k * 32, 16, 1024);
-                        tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if constexpr (CL == 1) tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        else tc_mma_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(&empty[s]);     // the stage is free once these MMAs have read it
+                    // the stage is free (in both CTAs of a pair) once these MMAs have read it
+                    if constexpr (CL == 1) tc_commit(&empty[s]);
+                    else tc_commit_pair_mc(&empty[s], CMASK);
                 }
-                if (ok) tc_commit(&acc_full[acc]);
+                if (ok) {
+                    if constexpr (CL == 1) tc_commit(&acc_full[acc]);
+                    else tc_commit_pair_mc(&acc_full[acc], CMASK);
+                }
             }
             // all MMAs issued by this thread complete before the teardown
-            tc_commit(done);
+            if constexpr (CL == 1) tc_commit(done);
+            else tc_commit_pair(done);
             const long long t0 = clock64();
             while (!mbar_try_wait(done, 0))
                 if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
         }
     } else {
-        // ---------------------------------------------------------- epilogue warps 2..5
-        const int ew = warp - 2;                       // epilogue warp 0..3
+        // ---------------------------------------------------------- epilogue warps 2..9
+        const int ew = warp - 2;                       // epilogue warp 0..7
         const int lane_grp = warp & 3;                 // TMEM lanes 32*lane_grp .. +31
+        const int cbase = (ew >> 2) * (BN / 2);        // this warp's half of the tile's columns
         uint8_t* stg = smem + S::STG_OFF + ew * 2 * S::STG_BYTES;
         constexpr bool AUX_IN = (EPI == EPI_RESID || EPI == EPI_GELU_BWD);
-        constexpr int NCH = BN / 64;                   // 64-column chunks per tile
+        constexpr int NPAIR = BN / 128;                // 64-column accumulator loads per warp per tile
+        constexpr int NPC = 2 * NPAIR;                 // 32-column pieces per warp per tile
         uint64_t* auxb = &aux_bar[ew * 2];             // one barrier per staging buffer
         uint32_t aux_ph = 0;                           // bit b: phase of buffer b's barrier
         uint32_t aux_pend = 0;                         // bit b: a load into buffer b not yet waited for
         int nbuf = 0;                                  // staging buffer in use: nbuf & 1
         int local = 0;
         bool alive = true;
-        // residual / pre-activation inputs: the load of chunk (unit uu, chunk c) goes to
-        // buffer kb once every store still reading a staging buffer has finished
-        auto aux_issue = [&](int uu, int c, int kb) {
+        // residual / pre-activation inputs: the load of piece pc of unit uu goes to buffer
+        // kb once every store still reading a staging buffer has finished
+        auto aux_issue = [&](int uu, int pc, int kb) {
             if (lane == 0) {
-                const int tile = uu / splits;
-                const int col = (tile % n_tiles) * BN + c * 64, row0 = (tile / n_tiles) * TC_BM + lane_grp * 32;
+                int usp, umt, unt;
+                decode(uu, usp, umt, unt);
+                const int col = unt * BN + cbase + pc * 32;
+                const int row0 = umt * TC_BM + lane_grp * 32;
                 bulk_wait_read<0>();
                 aux_pend |= 1u << kb;
                 mbar_expect_tx(&auxb[kb], S::STG_BYTES);
                 tma_load_2d(stg + kb * S::STG_BYTES, &tmAux, &auxb[kb], col, row0);
             }
         };
-        if (AUX_IN && blockIdx.x < units) aux_issue(blockIdx.x, 0, 0);
-        for (int u = blockIdx.x; u < units && alive; u += gridDim.x, local++) {
-            const int sp = u % splits, tile = u / splits;
-            const int nt = tile % n_tiles, mt = tile / n_tiles;
-            const int acc = local & 1;
-            const uint32_t aph = (local >> 1) & 1;
+        // bias (nullable) added to 32 columns starting at global column col
+        auto add_bias = [&](float* v, int col) {
+            if (ep.bias) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    if (col + 8 * q < N) {
+                        Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+                    }
+                }
+            }
+        };
+        const uint32_t acc_empty_lead = CL > 1 ? mapa_shared(acc_empty, 0) : 0;
+        if (AUX_IN && ufirst < units) aux_issue(ufirst, 0, 0);
+        for (int u = ufirst; u < units && alive; u += ustep, local++) {
+            int sp, mt, nt;
+            decode(u, sp, mt, nt);
+            const int acc = local % NACC;
+            const uint32_t aph = (local / NACC) & 1;
             // one lane waits; the warp then proceeds converged (tcgen05.ld is warp-wide)
             int okw = 1;
             if (lane == 0) okw = mbar_wait(&acc_full[acc], aph, abort_flag, err) ? 1 : 0;
@@ -238,126 +353,120 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int row0 = mt * TC_BM + lane_grp * 32;   // first of this warp's 32 rows
             const int yout = (EPI == TC_EPI_PARTIAL) ? sp * M + row0 : row0;
 #pragma unroll 1
-            for (int ci = 0; ci < NCH; ci++) {
-                const int c = ci * 64;
-                const int col = nt * BN + c;
-                if (!AUX_IN && col >= N) break;
+            for (int pi = 0; pi < NPAIR && alive; pi++) {
+                const int c = cbase + pi * 64;
+                if (!AUX_IN && nt * BN + c >= N) break;
                 uint32_t r0[32], r1[32];
                 const uint32_t ta = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + acc * BN + c;
                 tmem_ld32(ta, r0);
                 tmem_ld32(ta + 32, r1);
                 tmem_ld_wait();
-                float v[64];
+                float v2[64];
 #pragma unroll
-                for (int i = 0; i < 32; i++) { v[i] = __uint_as_float(r0[i]); v[32 + i] = __uint_as_float(r1[i]); }
-                if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
+                for (int i = 0; i < 32; i++) { v2[i] = __uint_as_float(r0[i]); v2[32 + i] = __uint_as_float(r1[i]); }
 #pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
-                        if (lane == 0) bulk_wait_read<1>();
-                        __syncwarp();
+                for (int h = 0; h < 2; h++) {
+                    float* v = v2 + 32 * h;
+                    const int pc = 2 * pi + h;                 // piece index within this warp's half
+                    const int col = nt * BN + c + 32 * h;      // first global column of the piece
+                    if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
+                        if (col < N) {
 #pragma unroll
-                        for (int j = 0; j < 8; j++)
-                            *reinterpret_cast<float4*>(sb + stg_off(lane, j)) =
-                                make_float4(v[32 * h + 4 * j], v[32 * h + 4 * j + 1], v[32 * h + 4 * j + 2],
-                                            v[32 * h + 4 * j + 3]);
-                        fence_async_smem();
-                        __syncwarp();
-                        if (lane == 0 && col + 32 * h < N) {
-                            if constexpr (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmOut, sb, col + 32 * h, yout);
-                            else tma_store_2d(&tmOut, sb, col + 32 * h, yout);
-                            bulk_commit();
-                        }
-                        nbuf++;
-                    }
-                } else if constexpr (AUX_IN) {
-                    // this chunk's input was loaded into buffer nbuf & 1 ahead of time; start
-                    // the next chunk's (or the next tile's first) load into the other buffer
-                    const int kb = nbuf & 1;
-                    if (ci + 1 < NCH) aux_issue(u, ci + 1, kb ^ 1);
-                    else if (u + gridDim.x < units) aux_issue(u + gridDim.x, 0, kb ^ 1);
-                    int oka = 1;
-                    if (lane == 0) oka = mbar_wait(&auxb[kb], (aux_ph >> kb) & 1, abort_flag, err) ? 1 : 0;
-                    oka = __shfl_sync(0xffffffffu, oka, 0);
-                    aux_ph ^= 1u << kb;
-                    aux_pend &= ~(1u << kb);
-                    if (!oka) { alive = false; break; }
-                    __syncwarp();
-                    uint8_t* sb = stg + kb * S::STG_BYTES;
-                    if (ep.bias && EPI == EPI_RESID) {
+                            for (int q = 0; q < 2; q++) {          // 16 fp32 columns per 64-byte row
+                                uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
+                                if (lane == 0) bulk_wait_read<1>();
+                                __syncwarp();
 #pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            if (col + 8 * q < N) {
-                                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
-#pragma unroll
-                                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+                                for (int j = 0; j < 4; j++)
+                                    *reinterpret_cast<float4*>(sb + stg_off(lane, j)) =
+                                        make_float4(v[16 * q + 4 * j], v[16 * q + 4 * j + 1], v[16 * q + 4 * j + 2],
+                                                    v[16 * q + 4 * j + 3]);
+                                fence_async_smem();
+                                __syncwarp();
+                                if (lane == 0 && col + 16 * q < N) {
+                                    if constexpr (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmOut, sb, col + 16 * q, yout);
+                                    else tma_store_2d(&tmOut, sb, col + 16 * q, yout);
+                                    bulk_commit();
+                                }
+                                nbuf++;
                             }
                         }
-                    }
+                    } else if constexpr (AUX_IN) {
+                        // this piece's input was loaded into buffer nbuf & 1 ahead of time; start
+                        // the next piece's (or the next tile's first) load into the other buffer
+                        const int kb = nbuf & 1;
+                        if (pc + 1 < NPC) aux_issue(u, pc + 1, kb ^ 1);
+                        else if (u + ustep < units) aux_issue(u + ustep, 0, kb ^ 1);
+                        int oka = 1;
+                        if (lane == 0) oka = mbar_wait(&auxb[kb], (aux_ph >> kb) & 1, abort_flag, err) ? 1 : 0;
+                        oka = __shfl_sync(0xffffffffu, oka, 0);
+                        aux_ph ^= 1u << kb;
+                        aux_pend &= ~(1u << kb);
+                        if (!oka) { alive = false; break; }
+                        __syncwarp();
+                        uint8_t* sb = stg + kb * S::STG_BYTES;
+                        if (EPI == EPI_RESID) add_bias(v, col);
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        Vec<bf16> a, o;
-                        a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
+                        for (int j = 0; j < 4; j++) {
+                            Vec<bf16> a, o;
+                            a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
 #pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            if constexpr (EPI == EPI_RESID) o.set(e, v[8 * j + e] + a.get(e));
-                            else o.set(e, v[8 * j + e] * gelu_grad_fast(a.get(e)));
-                        }
-                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
-                    }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && col < N) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
-                    nbuf++;
-                } else {
-                    if (ep.bias) {
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            if (col + 8 * q < N) {
-                                Vec<bf16> b = load_vec(ep.bias + col + 8 * q);
-#pragma unroll
-                                for (int e = 0; e < 8; e++) v[8 * q + e] += b.get(e);
+                            for (int e = 0; e < 8; e++) {
+                                if constexpr (EPI == EPI_RESID) o.set(e, v[8 * j + e] + a.get(e));
+                                else o.set(e, v[8 * j + e] * gelu_grad_fast(a.get(e)));
                             }
-                        }
-                    }
-                    uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    if constexpr (EPI == EPI_GELU) {
-                        // pre-activation out first, then the activation into the other buffer
-#pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            Vec<bf16> o;
-#pragma unroll
-                            for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
                             *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
-#pragma unroll
-                            for (int e = 0; e < 8; e++) v[8 * j + e] = gelu_fast(o.get(e));
                         }
                         fence_async_smem();
                         __syncwarp();
-                        if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0); bulk_commit(); }
+                        if (lane == 0 && col < N) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
                         nbuf++;
-                        sb = stg + (nbuf & 1) * S::STG_BYTES;
-                        if (lane == 0) bulk_wait_read<1>();
-                        __syncwarp();
-                    }
+                    } else {
+                        if (col < N) {
+                            add_bias(v, col);
+                            uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
+                            if (lane == 0) bulk_wait_read<1>();
+                            __syncwarp();
+                            if constexpr (EPI == EPI_GELU) {
+                                // pre-activation out first, then the activation into the other buffer
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        Vec<bf16> o;
+                                for (int j = 0; j < 4; j++) {
+                                    Vec<bf16> o;
 #pragma unroll
-                        for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
-                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+                                    for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                                    *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+#pragma unroll
+                                    for (int e = 0; e < 8; e++) v[8 * j + e] = gelu_fast(o.get(e));
+                                }
+                                fence_async_smem();
+                                __syncwarp();
+                                if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0); bulk_commit(); }
+                                nbuf++;
+                                sb = stg + (nbuf & 1) * S::STG_BYTES;
+                                if (lane == 0) bulk_wait_read<1>();
+                                __syncwarp();
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                Vec<bf16> o;
+#pragma unroll
+                                for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                                *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+                            }
+                            fence_async_smem();
+                            __syncwarp();
+                            if (lane == 0) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
+                            nbuf++;
+                        }
                     }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
-                    nbuf++;
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) {
+                if (CL == 1 || leader) mbar_arrive(&acc_empty[acc]);
+                else mbar_arrive_cluster(acc_empty_lead + acc * 8);     // the pair's accumulator lives on
+            }
         }
         // every store this warp issued has completed, and no load is still landing in
         // its staging buffers (only possible after an abort), before the CTA retires
@@ -374,11 +483,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    // the peer's multicast commits to this CTA's barriers have all landed (its MMA thread
+    // waited for its own MMAs) before either CTA of the cluster exits
+    if (CL > 1) cluster_sync();
     tc_fence_after();
     __syncwarp();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * BN)
-                     : "memory");
+    if (warp == 1) {
+        if constexpr (CL == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(NACC * BN)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(NACC * BN)
+                         : "memory");
+    }
 }
 
 // out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic)
@@ -446,22 +563,55 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS;
 }
 
+// epilogue map: box of 64-byte rows x 32 rows (32 bf16 or 16 fp32 columns), 64-byte
+// swizzle, matching the epilogue's 2 KB staging buffers
+static bool make_epi_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                         int ebytes = 2) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * ebytes};
+    cuuint32_t box[2] = {(cuuint32_t)(64 / ebytes), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, ebytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-template <int BN, int EPI, bool A_MN, bool B_MN>
+template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1>
 static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                      const CUtensorMap& tx, int M, int N, int K, int splits, const TcEpi& ep, unsigned* err) {
-    using SM = TcSmem<BN>;
-    static bool attr_set = false;
-    auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN>;
-    if (!attr_set) {
+    using SM = TcSmem<BN, CL>;
+    static int max_clusters = 0;            // co-resident clusters of CL CTAs (0: not yet queried)
+    auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN, CL>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = SM::TOTAL;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::TOTAL) != cudaSuccess)
             return GPT2_ECUDA;
-        attr_set = true;
+        cfg.gridDim = dim3(g_num_sms / CL * CL);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return GPT2_ECUDA;
+        max_clusters = n;
     }
-    const int units = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN) * splits;
-    const int grid = units < g_num_sms ? units : g_num_sms;
-    kern<<<grid, TC_THREADS, SM::TOTAL, s>>>(ta, tb, to, tx, M, N, K, splits, ep, err);
+    const int units = ((M + TC_BM - 1) / TC_BM + CL - 1) / CL * ((N + BN - 1) / BN) * splits;
+    const int clusters = units < max_clusters ? units : max_clusters;
+    cfg.gridDim = dim3(clusters * CL);
+    // stream the larger operand once: m fastest when B (N x K) is larger than A (M x K)
+    const int m_fast = N > M ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, to, tx, M, N, K, splits, m_fast, ep, err) != cudaSuccess)
+        return GPT2_ECUDA;
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
@@ -473,18 +623,28 @@ int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, c
         (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
         return GPT2_EUNSUPPORTED;
     CUtensorMap ta, tb, to, tx;
-    if (!make_map(&ta, inp, K, M, K, TC_BM) || !make_map(&tb, W, K, N, K, 256) || !make_map(&to, out, N, M, N, 32))
+    // CTA pairs (256 x 256 tiles, half of B per CTA) except for the smallest products,
+    // where the halved unit count costs more than the pair saves
+    const int cl = (N <= 768 && K <= 768) ? 1 : 2;
+    if (!make_map(&ta, inp, K, M, K, TC_BM) || !make_map(&tb, W, K, N, K, 256 / cl) ||
+        !make_epi_map(&to, out, N, M, N))
         return GPT2_EUNSUPPORTED;
     if (aux) {
-        if (!make_map(&tx, aux, N, M, N, 32)) return GPT2_EUNSUPPORTED;
+        if (!make_epi_map(&tx, aux, N, M, N)) return GPT2_EUNSUPPORTED;
     } else {
         tx = to;
     }
     TcEpi ep{out, bias, aux, (long)N};
     switch (epi) {
-        case EPI_STORE: return launch_tc<256, EPI_STORE, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
-        case EPI_GELU: return launch_tc<256, EPI_GELU, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
-        case EPI_RESID: return launch_tc<256, EPI_RESID, false, false>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_STORE:
+            return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_STORE, false, false, 1>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_GELU:
+            return cl == 2 ? launch_tc<256, EPI_GELU, false, false, 2>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_GELU, false, false, 1>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_RESID:
+            return cl == 2 ? launch_tc<256, EPI_RESID, false, false, 2>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_RESID, false, false, 1>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
         default: return GPT2_EUNSUPPORTED;
     }
 }
@@ -498,16 +658,21 @@ int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16
         (aux && !aligned16(aux)))
         return GPT2_EUNSUPPORTED;
     CUtensorMap ta, tb, to, tx;
-    if (!make_map(&ta, dout, N, M, N, TC_BM) || !make_map(&tb, W, K, N, K, 64) || !make_map(&to, dinp, K, M, K, 32))
+    if (!make_map(&ta, dout, N, M, N, TC_BM) || !make_map(&tb, W, K, N, K, 64) || !make_epi_map(&to, dinp, K, M, K))
         return GPT2_EUNSUPPORTED;
     if (aux) {
-        if (!make_map(&tx, aux, K, M, K, 32)) return GPT2_EUNSUPPORTED;
+        if (!make_epi_map(&tx, aux, K, M, K)) return GPT2_EUNSUPPORTED;
     } else {
         tx = to;
     }
     TcEpi ep{dinp, nullptr, (void*)aux, (long)K};
-    if (epi == EPI_GELU_BWD) return launch_tc<256, EPI_GELU_BWD, false, true>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
-    if (epi == EPI_STORE) return launch_tc<256, EPI_STORE, false, true>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
+    const int cl = (N <= 768 && K <= 768) ? 1 : 2;      // as in the forward
+    if (epi == EPI_GELU_BWD)
+        return cl == 2 ? launch_tc<256, EPI_GELU_BWD, false, true, 2>(s, ta, tb, to, tx, M, K, N, 1, ep, err)
+                       : launch_tc<256, EPI_GELU_BWD, false, true, 1>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
+    if (epi == EPI_STORE)
+        return cl == 2 ? launch_tc<256, EPI_STORE, false, true, 2>(s, ta, tb, to, tx, M, K, N, 1, ep, err)
+                       : launch_tc<256, EPI_STORE, false, true, 1>(s, ta, tb, to, tx, M, K, N, 1, ep, err);
     return GPT2_EUNSUPPORTED;
 }
 
@@ -546,11 +711,11 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
     if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch) || N % TC_BM))
         splits = 1;
     if (splits == 1) {
-        if (!make_map(&to, dW, K, N, K, 32, 4)) return GPT2_EUNSUPPORTED;
+        if (!make_epi_map(&to, dW, K, N, K, 4)) return GPT2_EUNSUPPORTED;
         TcEpi ep{dW, nullptr, nullptr, (long)K};
         return launch_tc<256, EPI_ACC_F32, true, true>(s, ta, tb, to, to, N, K, M, 1, ep, err);
     }
-    if (!make_map(&to, scratch, K, (uint64_t)splits * N, K, 32, 4)) return GPT2_EUNSUPPORTED;
+    if (!make_epi_map(&to, scratch, K, (uint64_t)splits * N, K, 4)) return GPT2_EUNSUPPORTED;
     TcEpi ep{scratch, nullptr, nullptr, (long)K};
     int rc = launch_tc<256, TC_EPI_PARTIAL, true, true>(s, ta, tb, to, to, N, K, M, splits, ep, err);
     if (rc != GPT2_OK) return rc;
