@@ -37,7 +37,7 @@ UNIT = "tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -62,60 +62,100 @@ def mfu_flops_per_token(shape, T):
 
 # ------------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """SM clock, power and clock-event reasons of this process's GPU, sampled every 20 ms
+    through NVML from a background thread while the timed region runs (the GPU is found
+    by its PCI bus id, so the NVML index need not match the CUDA one); nvidia-smi at
+    200 ms when NVML is unavailable."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NV_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
+    def __init__(self, cuda_index):
+        self.cuda_index = cuda_index
+        self.samples = []          # (sm_mhz, max_mhz, power_w, set of reasons)
+        self.stop_ev = threading.Event()
+        self.t = None
         self.proc = None
-        self.lines = []
+        self.nv = None
+        self.handle = None
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            pr = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+            self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            self.nv = pynvml
+        except Exception:
+            self.nv = None
+
+    def _poll_nvml(self):
+        nv, h = self.nv, self.handle
+        max_mhz = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        while not self.stop_ev.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                rs = {name for name, const in self.REASONS if mask & getattr(nv, const, 0)}
+                self.samples.append((float(sm), float(max_mhz), pw, rs))
+            except Exception:
+                pass
+            self.stop_ev.wait(0.02)
+
+    def _read_smi(self):
+        names = [r[0] for r in self.REASONS[:4]]
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rs = {n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")}
+                self.samples.append((float(f[1]), float(f[2]), float(f[3]), rs))
+            except ValueError:
+                continue
 
     def start(self):
+        if self.nv is not None:
+            self.t = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.NV_FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t = threading.Thread(target=self._read_smi, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.t.join(timeout=2)
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
+        self.stop_ev.set()
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=5)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0}
+        sm = [x[0] for x in self.samples]
+        reasons = set().union(*[x[3] for x in self.samples])
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": max(x[1] for x in self.samples),
+                "power_w_median": statistics.median(x[2] for x in self.samples),
+                "power_w_max": max(x[2] for x in self.samples),
+                "samples": len(sm), "source": "nvml" if self.nv is not None else "nvidia-smi",
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------------ CPU oracle leg
@@ -228,15 +268,14 @@ def ours(args):
             fam_ms[c] = v
     dominant = max(fam_ms, key=fam_ms.get)
     dom_classes = families.get(dominant, [dominant])
-    G.profile_enable(dom_classes)     # live tracing of the dominant kernel only
-
+    # the timed region: K untraced steps
+    G.profile_enable([])
     clocks = ClockSampler(local_rank)
     launches0 = G.kernel_launches()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
     start.record(stream)
     with torch.cuda.stream(stream):
         for i in range(args.steps):
@@ -248,6 +287,21 @@ def ours(args):
     clk = clocks.stop()
     launches = G.kernel_launches() - launches0
     ms = start.elapsed_time(end)
+    m.check()
+    # the roofline pass: the same K steps again, CUDA events around every launch of the
+    # dominant kernel family on the step's stream (events between launches add gaps, so
+    # this pass is kept out of the headline)
+    G.profile_enable(dom_classes)
+    G.profile_reset()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(args.warmup + i, args.warmup + args.steps + i + 1)
+    t_end.record(stream)
+    t_end.synchronize()
+    ms_traced = t_start.elapsed_time(t_end)
     m.check()
     live = G.profile_read()
     G.profile_enable([])
@@ -268,7 +322,7 @@ def ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
-            m.step_host(th[args.warmup + i], gh[args.warmup + i], *hp, n_batches + i + 1)
+            m.step_host(th[args.warmup + i], gh[args.warmup + i], *hp, n_batches + args.steps + i + 1)
         e2e_s = time.perf_counter() - t0
         if world > 1:
             import torch.distributed as dist
@@ -301,14 +355,18 @@ def ours(args):
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                 "peak_source": f"{src} bf16 sustained (kernel timed inside a long step)",
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
-                "share_of_traced_step": fam_ms[dominant] / total_ms}
+                "share_of_traced_step": fam_ms[dominant] / total_ms,
+                "timing": f"CUDA events around each launch on the step's stream, over a second timed pass "
+                          f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)"}
     else:
         achieved = d_by / (d_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy bandwidth",
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
-                "share_of_traced_step": fam_ms[dominant] / total_ms}
+                "share_of_traced_step": fam_ms[dominant] / total_ms,
+                "timing": f"CUDA events around each launch on the step's stream, over a second timed pass "
+                          f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)"}
     fpt, nparams = mfu_flops_per_token(w.shape, T)
     step_s = ms / 1000.0 / args.steps
     mfu = fpt * BT / step_s / 1e12

@@ -676,17 +676,17 @@ int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16
     return GPT2_EUNSUPPORTED;
 }
 
-static int choose_splits(int tiles, int nkb) {
-    // with fewer tiles than SMs, fill the SMs: the split count with the best SM
-    // occupancy over whole waves, each split keeping at least 8 k-blocks
-    if (tiles >= g_num_sms || g_num_sms > TC_SPLIT_SM_BOUND) return 1;
+static int choose_splits(int tiles, int nkb, int slots) {
+    // with fewer tiles than slots (SMs, or CTA pairs), fill them: the split count with
+    // the best occupancy over whole waves, each split keeping at least 8 k-blocks
+    if (tiles >= slots || g_num_sms > TC_SPLIT_SM_BOUND) return 1;
     int best = 1;
     double best_eff = 0;
     for (int sp = 1; sp <= TC_MAX_SPLITS; sp++) {
         if (sp > 1 && nkb / sp < 8) break;
         const int units = tiles * sp;
-        const int waves = (units + g_num_sms - 1) / g_num_sms;
-        const double eff = (double)units / (waves * g_num_sms);
+        const int waves = (units + slots - 1) / slots;
+        const double eff = (double)units / (waves * slots);
         if (eff > best_eff + 1e-9) { best_eff = eff; best = sp; }
     }
     return best;
@@ -702,22 +702,27 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
     CUtensorMap ta, tb, to;
     if (!make_map(&ta, dout, N, M, N, 64) || !make_map(&tb, inp, K, M, K, 64)) return GPT2_EUNSUPPORTED;
     // 256-wide tiles throughout (measured faster than 128-wide tiles for every weight
-    // gradient of the model); split-K fills the GPU when there are fewer tiles than SMs
-    const int tiles = ((N + TC_BM - 1) / TC_BM) * ((K + 255) / 256);
+    // gradient of the model), on CTA pairs (256 x 256 tiles) when the 256-row groups tile
+    // N exactly; split-K fills the GPU when there are fewer tiles than SMs (pairs)
+    const bool okpair = N % (2 * TC_BM) == 0;
+    const int cl = okpair ? 2 : 1;
+    const int tiles = ((N + cl * TC_BM - 1) / (cl * TC_BM)) * ((K + 255) / 256);
     const int nkb = (M + TC_BK - 1) / TC_BK;
-    int splits = choose_splits(tiles, nkb);
-    // partial tiles of split s are rows [s*N, (s+1)*N) of one map, so a tile must not
-    // straddle two splits: N a multiple of the 128-row tile
-    if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch) || N % TC_BM))
+    int splits = choose_splits(tiles, nkb, g_num_sms / cl);
+    // partial tiles of split s are rows [s*N, (s+1)*N) of one map, so a tile (pair) must
+    // not straddle two splits: N a multiple of the tile (pair) height
+    if (splits > 1 && (!scratch || (size_t)splits * N * K > scratch_floats || !aligned16(scratch) || N % (cl * TC_BM)))
         splits = 1;
     if (splits == 1) {
         if (!make_epi_map(&to, dW, K, N, K, 4)) return GPT2_EUNSUPPORTED;
         TcEpi ep{dW, nullptr, nullptr, (long)K};
-        return launch_tc<256, EPI_ACC_F32, true, true>(s, ta, tb, to, to, N, K, M, 1, ep, err);
+        return cl == 2 ? launch_tc<256, EPI_ACC_F32, true, true, 2>(s, ta, tb, to, to, N, K, M, 1, ep, err)
+                       : launch_tc<256, EPI_ACC_F32, true, true, 1>(s, ta, tb, to, to, N, K, M, 1, ep, err);
     }
     if (!make_epi_map(&to, scratch, K, (uint64_t)splits * N, K, 4)) return GPT2_EUNSUPPORTED;
     TcEpi ep{scratch, nullptr, nullptr, (long)K};
-    int rc = launch_tc<256, TC_EPI_PARTIAL, true, true>(s, ta, tb, to, to, N, K, M, splits, ep, err);
+    int rc = cl == 2 ? launch_tc<256, TC_EPI_PARTIAL, true, true, 2>(s, ta, tb, to, to, N, K, M, splits, ep, err)
+                     : launch_tc<256, TC_EPI_PARTIAL, true, true, 1>(s, ta, tb, to, to, N, K, M, splits, ep, err);
     if (rc != GPT2_OK) return rc;
     const size_t n4 = (size_t)N * K / 4;
     splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(dW, scratch, n4, splits);
