@@ -61,20 +61,56 @@ def mfu_flops_per_token(shape, T):
 
 
 # ------------------------------------------------------------------------ clocks
+class _Nvml:
+    """The few NVML calls the clock sampler needs, through ctypes on the driver's
+    libnvidia-ml (present wherever the GPU driver is)."""
+    CLOCK_SM = 1
+    REASONS = (("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40),
+               ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, cuda_index):
+        import ctypes
+        import torch
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        pr = torch.cuda.get_device_properties(cuda_index)
+        bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+        self.h = ctypes.c_void_p()
+        rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h))
+        if rc != 0:
+            n = ctypes.c_uint(0)
+            self.lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+            if n.value != 1 or self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+                raise RuntimeError(f"no NVML handle for {bus.decode()} (rc {rc})")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def max_sm(self):
+        v = self.c.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.c.byref(v))
+        return float(v.value)
+
+    def sample(self):
+        c = self.c
+        sm, pw, rs = c.c_uint(0), c.c_uint(0), c.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, c.byref(sm)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return float(sm.value), pw.value / 1000.0, {n for n, b in self.REASONS if rs.value & b}
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of this process's GPU, sampled every 20 ms
-    through NVML from a background thread while the timed region runs (the GPU is found
-    by its PCI bus id, so the NVML index need not match the CUDA one); nvidia-smi at
-    200 ms when NVML is unavailable."""
+    through NVML (ctypes on libnvidia-ml; the GPU is found by its PCI bus id, so the NVML
+    index need not match the CUDA one) from a background thread while the timed region
+    runs; nvidia-smi at 200 ms when NVML cannot be opened."""
 
     NV_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
     def __init__(self, cuda_index):
         self.cuda_index = cuda_index
@@ -83,34 +119,26 @@ class ClockSampler:
         self.t = None
         self.proc = None
         self.nv = None
-        self.handle = None
+        self.note = None
         try:
-            import pynvml
-            import torch
-            pynvml.nvmlInit()
-            pr = torch.cuda.get_device_properties(cuda_index)
-            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
-            self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            self.nv = pynvml
-        except Exception:
+            self.nv = _Nvml(cuda_index)
+        except Exception as e:
             self.nv = None
+            self.note = f"NVML unavailable ({e!r:.160}); nvidia-smi at 200 ms"
 
     def _poll_nvml(self):
-        nv, h = self.nv, self.handle
-        max_mhz = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        mx = self.nv.max_sm()
         while not self.stop_ev.is_set():
             try:
-                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
-                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-                rs = {name for name, const in self.REASONS if mask & getattr(nv, const, 0)}
-                self.samples.append((float(sm), float(max_mhz), pw, rs))
+                r = self.nv.sample()
+                if r is not None:
+                    self.samples.append((r[0], mx, r[1], r[2]))
             except Exception:
                 pass
             self.stop_ev.wait(0.02)
 
     def _read_smi(self):
-        names = [r[0] for r in self.REASONS[:4]]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.proc.stdout:
             f = [x.strip() for x in line.strip().split(",")]
             if len(f) < 9:
@@ -147,14 +175,15 @@ class ClockSampler:
         if self.t is not None:
             self.t.join(timeout=5)
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0,
+                    "source": self.note or "nvml"}
         sm = [x[0] for x in self.samples]
         reasons = set().union(*[x[3] for x in self.samples])
         return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
                 "sm_max_mhz": max(x[1] for x in self.samples),
                 "power_w_median": statistics.median(x[2] for x in self.samples),
                 "power_w_max": max(x[2] for x in self.samples),
-                "samples": len(sm), "source": "nvml" if self.nv is not None else "nvidia-smi",
+                "samples": len(sm), "source": "nvml, 20 ms" if self.nv is not None else self.note,
                 "reasons": sorted(reasons)}
 
 
@@ -243,21 +272,28 @@ def ours(args):
     torch.cuda.synchronize()
 
     def step(i, t):
-        m.forward(toks[i], tgts[i], want_loss=False)
-        m.zero_grad()
-        m.backward()
-        m.update(*hp, t)
+        # the library's whole-step call: one CUDA graph launch once the shape is captured
+        m.step_device(toks[i], tgts[i], *hp, t, want_loss=False)
 
-    # warm-up, traced in full to get every kernel class's share of the step
+    # warm-up: the first W-2 steps traced in full (every kernel class's share of the
+    # step, launched kernel by kernel), the last two untraced (the second captures the
+    # step graph that the timed region replays)
+    n_traced = max(1, args.warmup - 2)
     G.profile_enable(None)
     G.profile_reset()
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
+        for i in range(n_traced):
             step(i, i + 1)
     stream.synchronize()
     m.check()
     warm_prof = G.profile_read()
     G.profile_reset()
+    G.profile_enable([])
+    with torch.cuda.stream(stream):
+        for i in range(n_traced, args.warmup):
+            step(i, i + 1)
+    stream.synchronize()
+    m.check()
     shares = {k: v["ms"] for k, v in warm_prof.items()}
     total_ms = sum(shares.values()) or 1.0
     # the dominant kernel: the class family with the largest traced time
@@ -370,7 +406,7 @@ def ours(args):
     fpt, nparams = mfu_flops_per_token(w.shape, T)
     step_s = ms / 1000.0 / args.steps
     mfu = fpt * BT / step_s / 1e12
-    kernels = {k: {"ms_per_step": v["ms"] / max(args.warmup, 1),
+    kernels = {k: {"ms_per_step": v["ms"] / n_traced,
                    "share": v["ms"] / total_ms,
                    "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
                    "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["bytes"] and v["ms"] else None}

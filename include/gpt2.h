@@ -151,11 +151,26 @@ int gpt2_update(GPT2* model, float lr, float beta1, float beta2, float eps,
                 float weight_decay, int t);
 
 /* One whole training step from HOST token buffers: copies tokens/targets (pinned host
- * memory recommended) to the device, runs forward, zero_grad, backward and update, and
- * copies the mean loss back into *loss_out (host).  Synchronises the stream. */
+ * memory recommended) to the device, runs forward, zero_grad, backward and update (as
+ * one CUDA graph once the shape has been seen, see gpt2_step), and copies the mean loss
+ * back into *loss_out (host).  Synchronises the stream. */
 int gpt2_step_host(GPT2* model, const int32_t* tokens_host, const int32_t* targets_host,
                    int B, int T, float lr, float beta1, float beta2, float eps,
                    float weight_decay, int t, float* loss_out);
+
+/* The same step from DEVICE token buffers (B*T int32 each, read before the call
+ * returns control of the stream).  loss_out (host) may be NULL: the call then does not
+ * synchronise.  With graphs enabled (the default) and the tracer off, the first step of
+ * a (B, T) shape runs kernel by kernel, the second is captured into one CUDA graph, and
+ * later steps of that shape replay it with the step's AdamW scalars (same kernels, same
+ * results bit for bit).  Other steps of the model (gpt2_forward, ...) are unaffected. */
+int gpt2_step(GPT2* model, const int32_t* tokens, const int32_t* targets, int B, int T,
+              float lr, float beta1, float beta2, float eps, float weight_decay, int t,
+              float* loss_out);
+
+/* Enable (1, the default) or disable (0) the step graph of gpt2_step / gpt2_step_host;
+ * disabling frees a captured graph.  GPT2_EINVAL for a NULL model. */
+int gpt2_set_graphs(GPT2* model, int enable);
 
 /* Device pointers into the last forward's outputs: the mean loss (1 float), the
  * per-position losses (B*T floats) and the logits (B*T rows of Vp entries, fp32 or bf16

@@ -8,6 +8,7 @@
 // runs AdamW over the flat buffer (same article, section "训练过程": forward, backward
 // and update chained into one loop).
 #include <cuda_runtime.h>
+#include <vector>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -68,6 +69,15 @@ struct GPT2 {
     int have_fwd, have_targets;
     // tensor-core plan (bf16 mode)
     int use_tc;
+    // the whole step as one CUDA graph, captured for (gB, gT) on the second step of that
+    // shape; the AdamW node's scalars are set before each launch
+    int use_graph, g_seen;
+    int gB, gT;
+    cudaStream_t cap_stream;           // private stream the step is captured on
+    cudaGraph_t graph;
+    cudaGraphExec_t gexec;
+    cudaGraphNode_t g_adam;
+    long long g_kernels;
 };
 
 static const size_t kAlign = 1024;
@@ -231,6 +241,14 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     m->ws_bytes = workspace_bytes;
     m->stream = (cudaStream_t)stream;
     m->use_tc = (precision == GPT2_BF16) ? gemm_tc_available() : 0;
+    m->use_graph = 1;
+    m->g_seen = 0;
+    m->gB = m->gT = 0;
+    m->cap_stream = nullptr;
+    m->graph = nullptr;
+    m->gexec = nullptr;
+    m->g_adam = nullptr;
+    m->g_kernels = 0;
     if (cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              32768 * (int)sizeof(unsigned)) != cudaSuccess) {
         free(m);
@@ -245,7 +263,21 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     return GPT2_OK;
 }
 
-extern "C" void gpt2_free(GPT2* m) { free(m); }
+static void drop_graph(GPT2* m) {
+    if (m->gexec) cudaGraphExecDestroy(m->gexec);
+    if (m->graph) cudaGraphDestroy(m->graph);
+    m->gexec = nullptr;
+    m->graph = nullptr;
+    m->g_adam = nullptr;
+    m->g_seen = 0;
+}
+
+extern "C" void gpt2_free(GPT2* m) {
+    if (!m) return;
+    drop_graph(m);
+    if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+    free(m);
+}
 
 extern "C" int gpt2_set_stream(GPT2* m, void* stream) {
     if (!m) return GPT2_EINVAL;
@@ -719,18 +751,155 @@ extern "C" int gpt2_backward(GPT2* m) {
     return rc;
 }
 
+// AdamW's launch shape and arguments for step t (bias corrections computed in double)
+struct AdamArgs {
+    float* p; const float* g; float* mm; float* vv; bf16* shadow; size_t n4;
+    float lr, b1, b2, eps, wd, bc1, bc2;
+    int grid;
+    void* kp[13];
+};
+static void adam_args(GPT2* m, AdamArgs& a, float lr, float beta1, float beta2, float eps, float wd, int t) {
+    a.p = m->params; a.g = m->grads; a.mm = m->m; a.vv = m->v; a.shadow = m->wbf;
+    a.n4 = m->n_flat / 4;
+    a.lr = lr; a.b1 = beta1; a.b2 = beta2; a.eps = eps; a.wd = wd;
+    a.bc1 = (float)(1.0 - pow((double)beta1, (double)t));
+    a.bc2 = (float)(1.0 - pow((double)beta2, (double)t));
+    a.grid = (int)std::min<size_t>(ceil_div_sz(a.n4, 256), 148 * 16);
+    void* kp[13] = {&a.p, &a.g, &a.mm, &a.vv, &a.shadow, &a.n4, &a.lr, &a.b1, &a.b2, &a.eps, &a.wd, &a.bc1, &a.bc2};
+    for (int i = 0; i < 13; i++) a.kp[i] = kp[i];
+}
+
 extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float eps, float wd, int t) {
     if (!m || t < 1) return GPT2_EINVAL;
-    double bc1 = 1.0 - pow((double)beta1, (double)t);
-    double bc2 = 1.0 - pow((double)beta2, (double)t);
-    size_t n4 = m->n_flat / 4;
-    int grid = (int)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 16);
+    AdamArgs a;
+    adam_args(m, a, lr, beta1, beta2, eps, wd, t);
     ProfScope ps(m->stream, PC_ADAMW, 0, (double)m->n_flat * (m->wbf ? 30.0 : 28.0));
     rt_note_launches(1);
-    adamw_kernel<<<grid, 256, 0, m->stream>>>(m->params, m->grads, m->m, m->v, m->wbf, n4, lr, beta1,
-                                              beta2, eps, wd, (float)bc1, (float)bc2);
+    adamw_kernel<<<a.grid, 256, 0, m->stream>>>(a.p, a.g, a.mm, a.vv, a.shadow, a.n4, a.lr, a.b1, a.b2, a.eps,
+                                                a.wd, a.bc1, a.bc2);
     CK(cudaGetLastError());
     return GPT2_OK;
+}
+
+// forward (with targets), zero_grad, backward and AdamW on the model's stream, as
+// launched one by one
+static int step_eager(GPT2* m, int B, int Tn, float lr, float b1, float b2, float eps, float wd, int t) {
+    RC(forward_dispatch(m, B, Tn, true));
+    RC(gpt2_zero_grad(m));
+    RC(gpt2_backward(m));
+    return gpt2_update(m, lr, b1, b2, eps, wd, t);
+}
+
+// Capture the step for (B, Tn) into a graph and find its AdamW node.  Lazy set-up
+// (function attributes, occupancy queries) has already run in an earlier eager step.
+// The capture runs on a private stream (the caller's may be the legacy default stream,
+// which cannot be captured); the graph is then launched into the caller's stream.
+static int capture_step(GPT2* m, int B, int Tn) {
+    drop_graph(m);
+    if (!m->cap_stream) CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    const long long n0 = rt_launches();
+    cudaStream_t user = m->stream;
+    m->stream = m->cap_stream;
+    cudaError_t cb = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed);
+    if (cb != cudaSuccess) {
+        m->stream = user;
+        g_last_cuda_error = cb;
+        return GPT2_ECUDA;
+    }
+    int rc = step_eager(m, B, Tn, 0.f, 0.9f, 0.999f, 1e-8f, 0.f, 1);
+    cudaGraph_t g = nullptr;
+    cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &g);
+    m->stream = user;
+    const long long captured = rt_launches() - n0;
+    rt_note_launches(-captured);                // recorded, not run
+    if (rc != GPT2_OK || ce != cudaSuccess || !g) {
+        if (g) cudaGraphDestroy(g);
+        return rc != GPT2_OK ? rc : GPT2_ECUDA;
+    }
+    size_t nn = 0;
+    cudaGraphGetNodes(g, nullptr, &nn);
+    std::vector<cudaGraphNode_t> nodes(nn);
+    cudaGraphGetNodes(g, nodes.data(), &nn);
+    cudaGraphNode_t adam = nullptr;
+    for (cudaGraphNode_t nd : nodes) {
+        cudaGraphNodeType ty;
+        if (cudaGraphNodeGetType(nd, &ty) != cudaSuccess || ty != cudaGraphNodeTypeKernel) continue;
+        cudaKernelNodeParams kp;
+        if (cudaGraphKernelNodeGetParams(nd, &kp) == cudaSuccess && kp.func == (void*)adamw_kernel) adam = nd;
+    }
+    cudaGraphExec_t ex = nullptr;
+    if (!adam || cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return GPT2_ECUDA;
+    }
+    m->graph = g;
+    m->gexec = ex;
+    m->g_adam = adam;
+    m->g_kernels = captured;
+    m->gB = B;
+    m->gT = Tn;
+    return GPT2_OK;
+}
+
+// One training step on the batch already in m->tokens / m->targets.  With graphs on and
+// the tracer off: the first step of a shape runs eagerly, the second captures the step,
+// and from then on each step is one graph launch with this step's AdamW scalars.
+static int run_step(GPT2* m, int B, int Tn, float lr, float b1, float b2, float eps, float wd, int t) {
+    if (!m->use_graph || rt_tracing_on()) return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
+    if (m->gexec && (m->gB != B || m->gT != Tn)) drop_graph(m);
+    if (!m->gexec) {
+        if (!m->g_seen || m->gB != B || m->gT != Tn) {
+            m->g_seen = 1;
+            m->gB = B;
+            m->gT = Tn;
+            return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
+        }
+        int rc = capture_step(m, B, Tn);
+        if (rc != GPT2_OK) {                    // no graph for this model: stay eager
+            m->use_graph = 0;
+            return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
+        }
+    }
+    AdamArgs a;
+    adam_args(m, a, lr, b1, b2, eps, wd, t);
+    cudaKernelNodeParams kp = {};
+    kp.func = (void*)adamw_kernel;
+    kp.gridDim = dim3(a.grid);
+    kp.blockDim = dim3(256);
+    kp.sharedMemBytes = 0;
+    kp.kernelParams = a.kp;
+    kp.extra = nullptr;
+    CK(cudaGraphExecKernelNodeSetParams(m->gexec, m->g_adam, &kp));
+    CK(cudaGraphLaunch(m->gexec, m->stream));
+    rt_note_launches(m->g_kernels);
+    m->B = B;
+    m->T = Tn;
+    m->have_fwd = 0;                            // the logits now hold d loss / d logits
+    m->have_targets = 1;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_set_graphs(GPT2* m, int enable) {
+    if (!m) return GPT2_EINVAL;
+    m->use_graph = enable ? 1 : 0;
+    if (!enable) drop_graph(m);
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_step(GPT2* m, const int32_t* tokens, const int32_t* targets, int B, int Tn, float lr,
+                         float beta1, float beta2, float eps, float wd, int t, float* loss_out) {
+    if (!m || !tokens || !targets || t < 1) return GPT2_EINVAL;
+    RC(check_bt(m, B, Tn));
+    const size_t BT = (size_t)B * Tn;
+    CK(cudaMemcpyAsync(m->tokens, tokens, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    CK(cudaMemcpyAsync(m->targets, targets, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    RC(run_step(m, B, Tn, lr, beta1, beta2, eps, wd, t));
+    if (!loss_out) return GPT2_OK;
+    float l = -1.f;
+    CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+    int rc = read_error(m);
+    *loss_out = l;
+    return rc;
 }
 
 extern "C" int gpt2_step_host(GPT2* m, const int32_t* tokens_host, const int32_t* targets_host, int B,
@@ -741,10 +910,7 @@ extern "C" int gpt2_step_host(GPT2* m, const int32_t* tokens_host, const int32_t
     const size_t BT = (size_t)B * Tn;
     CK(cudaMemcpyAsync(m->tokens, tokens_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
     CK(cudaMemcpyAsync(m->targets, targets_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
-    RC(forward_dispatch(m, B, Tn, true));
-    RC(gpt2_zero_grad(m));
-    RC(gpt2_backward(m));
-    RC(gpt2_update(m, lr, beta1, beta2, eps, wd, t));
+    RC(run_step(m, B, Tn, lr, beta1, beta2, eps, wd, t));
     float l = -1.f;
     CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
     int rc = read_error(m);

@@ -54,6 +54,8 @@ ProfScope::~ProfScope() {
 }
 
 extern "C" long long gpt2_kernel_launches(void) { return g_launches.load(); }
+long long rt_launches() { return g_launches.load(); }
+bool rt_tracing_on() { return T.on; }
 
 extern "C" int gpt2_profile_enable(unsigned class_mask) {
     const bool on = class_mask != 0;

@@ -11,6 +11,10 @@ enum ProfClass {
 
 // Count `n` kernel launches made by this library (process-wide).
 void rt_note_launches(long long n);
+// The launch count so far, and whether the tracer is recording (the step graph is then
+// not used: its launches carry no events).
+long long rt_launches();
+bool rt_tracing_on();
 
 // RAII scope: when tracing is on, records a CUDA event on `s` at construction and at
 // destruction, attributing the interval and the given algorithmic work to `cls`.

@@ -48,6 +48,8 @@ SIGNATURES = {
     "gpt2_backward": (_i, [_vp]),
     "gpt2_update": (_i, [_vp, _f, _f, _f, _f, _f, _i]),
     "gpt2_step_host": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
+    "gpt2_step": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
+    "gpt2_set_graphs": (_i, [_vp, _i]),
     "gpt2_loss": (_vp, [_vp]),
     "gpt2_losses": (_vp, [_vp]),
     "gpt2_logits": (_vp, [_vp]),
@@ -249,6 +251,18 @@ class GPT2:
                                  lr, beta1, beta2, eps, weight_decay, t, ctypes.byref(loss)),
               "gpt2_step_host")
         return loss.value
+
+    def step_device(self, tokens, targets, lr, beta1, beta2, eps, weight_decay, t, want_loss=False):
+        """Whole step from int32 CUDA tensors (B, T) through gpt2_step (a CUDA graph once
+        the shape has been seen).  Returns the mean loss (synchronises) when want_loss."""
+        B, T = tokens.shape
+        loss = ctypes.c_float(0.0)
+        check(lib.gpt2_step(self.handle, _ptr(tokens), _ptr(targets), B, T, lr, beta1, beta2, eps,
+                            weight_decay, t, ctypes.byref(loss) if want_loss else None), "gpt2_step")
+        return loss.value if want_loss else None
+
+    def set_graphs(self, enable: bool):
+        check(lib.gpt2_set_graphs(self.handle, 1 if enable else 0), "gpt2_set_graphs")
 
     def losses(self, n):
         import torch

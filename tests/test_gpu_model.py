@@ -265,3 +265,24 @@ def test_step_from_host_buffers_matches_device_path():
     lb = b.step_host(th, gh, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], 1)
     assert la == lb
     assert torch.equal(a.flat_params(), b.flat_params())
+
+
+@pytest.mark.parametrize("precision", ["bf16", "fp32"])
+def test_graph_steps_match_eager_steps_bitwise(precision):
+    """gpt2_step replays one captured CUDA graph per (B, T) from its third step of that
+    shape; every step (learning rate changing each time, a batch-size change in the
+    middle forcing a new capture) equals the kernel-by-kernel step bit for bit."""
+    import torch
+    shape = synth.ModelShape(64, 512, 512, 2, 4, 64)
+    batches = synth.zipf_batches(512, 4, 64, 9, 11)
+    g = gpu_model(shape, 4, 64, precision, 3)
+    e = gpu_model(shape, 4, 64, precision, 3)
+    e.set_graphs(False)
+    for i, (tok, tgt) in enumerate(batches):
+        Bi = 4 if i < 5 else 2                          # shape change at step 5
+        tk, tg = dev_tokens(tok[:Bi]), dev_tokens(tgt[:Bi])
+        lr = 1e-3 * (1 + 0.1 * i)
+        lg = g.step_device(tk, tg, lr, 0.9, 0.95, 1e-8, 0.1, i + 1, want_loss=True)
+        le = e.step_device(tk, tg, lr, 0.9, 0.95, 1e-8, 0.1, i + 1, want_loss=True)
+        assert lg == le, (i, lg, le)
+        assert torch.equal(g.flat_params(), e.flat_params()), i
