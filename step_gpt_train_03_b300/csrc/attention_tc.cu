@@ -399,24 +399,27 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
 //   DQ   item = (128-query tile t, b*h); for every key tile u <= t:
 //          S = Q_t K_u^T, dP = dO_t V_u^T; P = 2^(S log2e/8 - LSE log2e), dS = P (dP - D)
 //          dQ += dS K_u;  then dQ / 8 to dqkv.
-// Warp 0 loads (the item's two row tiles once; the per-u tiles through a 2-stage ring
-// with, in DKV mode, that u's LSE and D vectors); warp 1 issues the MMAs (the next
-// S/dP pair is issued before the dV/dK (dQ) products of the current one); warps 2-9
-// compute, two warps per TMEM lane quadrant, each on half the columns of a tile (a
-// TMEM lane is a key row in DKV mode, a query row in DQ mode).
+// Warp 0 loads (the item's two row tiles once; the per-u tiles through a ring of 2
+// (DKV) or 3 (DQ) stages with, in DKV mode, that u's LSE and D vectors); warp 1 issues
+// the MMAs (the next S/dP pair is issued before the dV/dK (dQ) products of the current
+// one); warps 2-9 compute, two warps per TMEM lane quadrant, each on half the columns of
+// a tile (a TMEM lane is a key row in DKV mode, a query row in DQ mode).  The operands
+// the compute warps produce for the products are double-buffered, so tile u+1 is
+// computed while the products of tile u run: dS (dS^T) in shared memory and, in DKV
+// mode, P^T (bf16, two per 32-bit column) in TMEM, read there as the A operand of
+// dV += P^T dO_u.
 #define AB_STAGE_BYTES (2 * AT_TILE_BYTES + 1024)   // two tiles + LSE[128] + D[128]
-#define AB_RING 2
 
 template <bool DKV>
 struct AbSmem {
+    static constexpr int RING = DKV ? 2 : 3;
     static constexpr int R_OFF = 0;                                        // 2 row tiles
     static constexpr int RING_OFF = R_OFF + 2 * AT_TILE_BYTES;
-    static constexpr int P_OFF = RING_OFF + AB_RING * AB_STAGE_BYTES;       // P^T (DKV only), 32 KB
-    static constexpr int DS_OFF = P_OFF + 2 * AT_TILE_BYTES;               // dS or dS^T, 32 KB
-    static constexpr int BAR_OFF = DS_OFF + 2 * AT_TILE_BYTES;
-    // rr_full, rr_empty, ring_full[2], ring_empty[2], x_full, x_free, pds_full, pds_free,
-    // acc_free, done; tmem address, abort flag
-    static constexpr int NBAR = 2 + 2 * AB_RING + 6;
+    static constexpr int DS_OFF = RING_OFF + RING * AB_STAGE_BYTES;        // 2 x dS or dS^T, 32 KB each
+    static constexpr int BAR_OFF = DS_OFF + 4 * AT_TILE_BYTES;
+    // rr_full, rr_empty, ring_full[RING], ring_empty[RING], x_full, x_free, pds_full[2],
+    // pds_free[2], acc_free, done; tmem address, abort flag
+    static constexpr int NBAR = 2 + 2 * RING + 8;
     static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
 };
 
@@ -427,6 +430,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                              const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
                              const float* __restrict__ Dsum, int B, int Tn, int C, int NH, unsigned* err) {
     using S = AbSmem<DKV>;
+    constexpr int AB_RING = S::RING;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
@@ -436,9 +440,9 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
     uint64_t* ring_empty = ring_full + AB_RING;
     uint64_t* x_full = ring_empty + AB_RING;
     uint64_t* x_free = x_full + 1;
-    uint64_t* pds_full = x_free + 1;
-    uint64_t* pds_free = pds_full + 1;
-    uint64_t* acc_free = pds_free + 1;
+    uint64_t* pds_full = x_free + 1;       // [2]
+    uint64_t* pds_free = pds_full + 2;     // [2]
+    uint64_t* acc_free = pds_free + 2;
     uint64_t* done = acc_free + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -460,8 +464,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
         for (int i = 0; i < AB_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 1); }
         mbar_init(x_full, 1);
         mbar_init(x_free, 8);
-        mbar_init(pds_full, 8);
-        mbar_init(pds_free, 1);
+        for (int i = 0; i < 2; i++) { mbar_init(&pds_full[i], 8); mbar_init(&pds_free[i], 1); }
         mbar_init(acc_free, 8);
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -480,7 +483,9 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // S (S^T), dP (dP^T), dV or dQ, dK, then (DKV) two P^T buffers of 64 columns
     const uint32_t TM_X1 = tmem_base, TM_X2 = tmem_base + 128, TM_A1 = tmem_base + 256, TM_A2 = tmem_base + 320;
+    const uint32_t TM_P = tmem_base + 384;
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
@@ -530,7 +535,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             constexpr uint32_t IDESC_X = idesc_bf16(AT_BM, AT_BN, false, false);
             constexpr uint32_t IDESC_A = idesc_bf16(AT_BM, AT_HS, false, true);
             const uint32_t r0 = smem_u32(smem + S::R_OFF), r1 = r0 + AT_TILE_BYTES;
-            const uint32_t pbuf = smem_u32(smem + S::P_OFF), dsbuf = smem_u32(smem + S::DS_OFF);
+            const uint32_t dsbase = smem_u32(smem + S::DS_OFF);
             int rc = 0, xc = 0, gc = 0, local = 0;
             bool ok = true;
             // the S / dP pair for the ring stage of index `idx`
@@ -562,16 +567,19 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                     if (i == nu - 1) tc_commit(rr_empty);          // row tiles free after the last S / dP
                     const int slot = (rc + i) % AB_RING;
                     const uint32_t st = smem_u32(smem + S::RING_OFF + slot * AB_STAGE_BYTES);
-                    if (!mbar_wait(pds_full, gc & 1, abort_flag, err)) { ok = false; break; }
+                    const int pb = gc & 1;                           // P / dS buffer of this tile
+                    const uint32_t dsbuf = dsbase + pb * 2 * AT_TILE_BYTES;
+                    if (!mbar_wait(&pds_full[pb], (gc >> 1) & 1, abort_flag, err)) { ok = false; break; }
                     if (i == 0 && local > 0 && !mbar_wait(acc_free, (local - 1) & 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     if (DKV) {
-                        // dV += P^T dO_u ; dK += dS^T Q_u
+                        // dV += P^T dO_u (P^T from TMEM, 8 columns per 16 queries) ; dK += dS^T Q_u
+                        const uint32_t pt = TM_P + pb * 64;
 #pragma unroll
                         for (int k = 0; k < AT_BN / 16; k++) {
                             const uint32_t aoff = (k >> 2) * AT_TILE_BYTES + (k & 3) * 32;
-                            tc_mma(TM_A1, sdesc(pbuf + aoff, 16, 1024), sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024),
-                                   IDESC_A, (i > 0 || k > 0));
+                            tc_mma_ts(TM_A1, pt + k * 8, sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024), IDESC_A,
+                                      (i > 0 || k > 0));
                             tc_mma(TM_A2, sdesc(dsbuf + aoff, 16, 1024), sdesc(st + k * 2048, 8192, 1024), IDESC_A,
                                    (i > 0 || k > 0));
                         }
@@ -582,7 +590,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                             tc_mma(TM_A1, sdesc(dsbuf + (k >> 2) * AT_TILE_BYTES + (k & 3) * 32, 16, 1024),
                                    sdesc(st + k * 2048, 8192, 1024), IDESC_A, (i > 0 || k > 0));
                     }
-                    tc_commit(pds_free);
+                    tc_commit(&pds_free[pb]);
                     tc_commit(&ring_empty[slot]);
                     gc++;
                 }
@@ -600,9 +608,9 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
         const int r = lane_grp * 32 + lane;                 // TMEM lane = row of the item's tile
         const uint32_t lrow = (uint32_t)(lane_grp * 32) << 16;
         const float sl2 = AT_LOG2E * 0.125f;
-        uint8_t* pbuf = smem + S::P_OFF;
-        uint8_t* dsbuf = smem + S::DS_OFF;
-        int rc = 0, xc = 0, gc = 0, pf_seen = 0, local = 0;
+        uint8_t* dsbase = smem + S::DS_OFF;
+        int rc = 0, xc = 0, gc = 0, local = 0;
+        int pf_seen0 = 0, pf_seen1 = 0;                     // pds_free completions observed per buffer
         bool alive = true;
         auto wait_one = [&](uint64_t* bar, uint32_t parity) -> bool {
             int okw = 1;
@@ -611,11 +619,18 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             __syncwarp();
             return okw != 0;
         };
-        // wait for the dV/dK (dQ) products number n (pds_free phases, observed in order)
+        // wait for the dV/dK (dQ) products of tile n: completion n >> 1 of buffer n & 1's
+        // barrier (each buffer's completions are observed in order)
         auto wait_pds_free = [&](int n) -> bool {
-            if (pf_seen > n) return true;
-            pf_seen = n + 1;
-            return wait_one(pds_free, n & 1);
+            const int b = n & 1, need = (n >> 1) + 1;
+            if (b == 0) {
+                if (pf_seen0 >= need) return true;
+                pf_seen0 = need;
+            } else {
+                if (pf_seen1 >= need) return true;
+                pf_seen1 = need;
+            }
+            return wait_one(&pds_free[b], (n >> 1) & 1);
         };
         for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x, local++) {
             int t, bh, u0, u1;
@@ -633,8 +648,8 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 const uint8_t* st = smem + S::RING_OFF + (rc % AB_RING) * AB_STAGE_BYTES;
                 const float* Lv = reinterpret_cast<const float*>(st + 2 * AT_TILE_BYTES);
                 const float* Dv = Lv + 128;
-                // the previous products must have finished reading the P / dS buffers
-                if (gc > 0 && !wait_pds_free(gc - 1)) { alive = false; break; }
+                const int pb = gc & 1;
+                uint8_t* dsbuf = dsbase + pb * 2 * AT_TILE_BYTES;
 #pragma unroll 1
                 for (int c = half * 64; c < half * 64 + 64; c += 32) {
                     uint32_t s1[32], s2[32];
@@ -681,6 +696,8 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                             ds[i] = p[i] * (__uint_as_float(s2[i]) - Dc[i]);
                         }
                     }
+                    // the products of tile gc-2 must have finished reading this buffer
+                    if (c == half * 64 && gc >= 2 && !wait_pds_free(gc - 2)) { alive = false; break; }
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int ch = (c >> 3) + k;
@@ -689,22 +706,31 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
 #pragma unroll
                         for (int e = 0; e < 8; e++) dv.set(e, ds[8 * k + e]);
                         *reinterpret_cast<uint4*>(dsbuf + off) = dv.v;
-                        if (DKV) {
-                            Vec<bf16> pv;
+                    }
+                    if (DKV) {
+                        // P^T row r, queries c..c+31: 16 columns of bf16 pairs
+                        uint32_t pk[16];
 #pragma unroll
-                            for (int e = 0; e < 8; e++) pv.set(e, p[8 * k + e]);
-                            *reinterpret_cast<uint4*>(pbuf + off) = pv.v;
+                        for (int k = 0; k < 16; k++) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(p[2 * k], p[2 * k + 1]);
+                            pk[k] = *reinterpret_cast<uint32_t*>(&h2);
                         }
+                        tmem_st16(TM_P + pb * 64 + lrow + (c >> 1), pk);
                     }
                 }
+                if (!alive) break;
+                if (DKV) tmem_st_wait();
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(pds_full);
+                if (lane == 0) mbar_arrive(&pds_full[pb]);
             }
             if (!alive) break;
             // accumulators of the item: wait for its last products, read, release, store
             if (!wait_pds_free(gc - 1)) break;
+            // staging: the last tile's dS buffer (its products are done; the next item's
+            // first tile uses the other buffer)
+            uint8_t* stg = dsbase + ((gc - 1) & 1) * 2 * AT_TILE_BYTES;
             tc_fence_after();
             float a1[32], a2[32];
             {
@@ -733,22 +759,22 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                     Vec<bf16> v2;
 #pragma unroll
                     for (int e = 0; e < 8; e++) { v1.set(e, a1[8 * k + e]); v2.set(e, a2[8 * k + e] * 0.125f); }
-                    *reinterpret_cast<uint4*>(pbuf + off) = v1.v;      // dV
-                    *reinterpret_cast<uint4*>(dsbuf + off) = v2.v;     // dK / 8
+                    *reinterpret_cast<uint4*>(stg + off) = v1.v;                   // dV
+                    *reinterpret_cast<uint4*>(stg + AT_TILE_BYTES + off) = v2.v;   // dK / 8
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; e++) v1.set(e, a1[8 * k + e] * 0.125f);
-                    *reinterpret_cast<uint4*>(dsbuf + off) = v1.v;     // dQ / 8
+                    *reinterpret_cast<uint4*>(stg + off) = v1.v;                   // dQ / 8
                 }
             }
             fence_async_smem();
             named_bar(1, 256);
             if (threadIdx.x == 64) {
                 if (DKV) {
-                    tma_store_3d(&tmDQKV, pbuf, 2 * C + h * AT_HS, t * AT_BM, b);
-                    tma_store_3d(&tmDQKV, dsbuf, C + h * AT_HS, t * AT_BM, b);
+                    tma_store_3d(&tmDQKV, stg, 2 * C + h * AT_HS, t * AT_BM, b);
+                    tma_store_3d(&tmDQKV, stg + AT_TILE_BYTES, C + h * AT_HS, t * AT_BM, b);
                 } else {
-                    tma_store_3d(&tmDQKV, dsbuf, h * AT_HS, t * AT_BM, b);
+                    tma_store_3d(&tmDQKV, stg, h * AT_HS, t * AT_BM, b);
                 }
                 bulk_commit();
                 bulk_wait_read<0>();      // the buffers are reused by the next item

@@ -637,11 +637,14 @@ __global__ void colsum_partial_scalar_kernel(float* __restrict__ partial, const 
 }
 
 // ============================================================== softmax + cross-entropy
-// One block per row of logits (Vp entries).  Pass 1: online max / sum of exp over the V
-// real columns; lse = max + log(sum); loss = lse - z[target].  Pass 2 (the row is still
-// in L2) overwrites it with d(mean loss)/dz = (exp(z - lse) - [j == target]) * dloss for
-// j < V and 0 for the padded columns.  exp(a) is computed as exp2(a * log2 e).
-#define XENT_THREADS 1024
+// One 256-thread block per row of logits (Vp entries); eight rows in flight per SM.
+// Pass 1: online max / sum of exp over the V real columns, four 16-byte packets per
+// step (one rescale per step); lse = max + log(sum); loss = lse - z[target].  Pass 2
+// (the row is still in L2) overwrites it with d(mean loss)/dz = (exp(z - lse) -
+// [j == target]) * dloss for j < V and 0 for the padded columns.  exp(a) is computed as
+// exp2(a * log2 e).
+#define XENT_THREADS 256
+#define XENT_U 4
 #define XENT_LOG2E 1.4426950408889634f
 // 2^x by the hardware approximation (relative error ~2^-22); 2^-inf = 0
 __device__ __forceinline__ float xent_ex2(float x) {
@@ -649,81 +652,100 @@ __device__ __forceinline__ float xent_ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// (m, s) pairs in the log2 domain: the combined pair of two partial sums
+__device__ __forceinline__ void xent_merge(float& m, float& s, float om, float os) {
+    const float nm = fmaxf(m, om);
+    const float a = (m == -INFINITY) ? 0.f : s * exp2f(m - nm);
+    const float b = (om == -INFINITY) ? 0.f : os * exp2f(om - nm);
+    m = nm;
+    s = a + b;
+}
 template <typename T>
 __global__ void __launch_bounds__(XENT_THREADS)
 softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
                     const int* __restrict__ targets, int V, int Vp, float dloss, unsigned* err) {
     constexpr int EPV = Vec<T>::N;
-    __shared__ float sm_m[32], sm_s[32];
-    __shared__ float sm_lse, sm_zt;
+    constexpr int NW = XENT_THREADS / 32;
+    __shared__ float sm_m[NW], sm_s[NW];
+    __shared__ float sm_lse;
     const int row = blockIdx.x;
     T* z = logits + (size_t)row * Vp;
     const int tgt_raw = targets[row];
     const bool tgt_ok = tgt_raw >= 0 && tgt_raw < V;
     const int tgt = tgt_ok ? tgt_raw : -1;
-    if (threadIdx.x == 0) {
-        if (!tgt_ok) raise_error(err, ERRBIT_TOKEN);
-        sm_zt = tgt_ok ? to_f32(z[tgt]) : 0.f;
-    }
     const int nfull = V / EPV;              // packets whose columns are all real
     const int nvec = Vp / EPV;
     // pass 1, in the log2 domain: mx2 = max(z) log2e, sum = sum 2^(z log2e - mx2)
     float mx2 = -INFINITY, sum = 0.f;
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-        Vec<T> p = load_vec(z + (size_t)vi * EPV);
-        float y[EPV];
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += XENT_U * XENT_THREADS) {
+        Vec<T> p[XENT_U];
+#pragma unroll
+        for (int u = 0; u < XENT_U; u++) {
+            const int vi = v0 + u * XENT_THREADS;
+            if (vi < nvec) p[u] = load_vec(z + (size_t)vi * EPV);
+        }
+        float y[XENT_U][EPV];
         float vmax = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < EPV; e++) {
-            y[e] = (vi < nfull || vi * EPV + e < V) ? p.get(e) * XENT_LOG2E : -INFINITY;
-            vmax = fmaxf(vmax, y[e]);
+        for (int u = 0; u < XENT_U; u++) {
+            const int vi = v0 + u * XENT_THREADS;
+#pragma unroll
+            for (int e = 0; e < EPV; e++) {
+                y[u][e] = (vi < nfull || (vi < nvec && vi * EPV + e < V)) ? p[u].get(e) * XENT_LOG2E : -INFINITY;
+                vmax = fmaxf(vmax, y[u][e]);
+            }
         }
         if (vmax == -INFINITY) continue;
         const float nm = fmaxf(mx2, vmax);
         float acc = sum * xent_ex2(mx2 - nm);
 #pragma unroll
-        for (int e = 0; e < EPV; e++) acc += xent_ex2(y[e] - nm);
+        for (int u = 0; u < XENT_U; u++)
+#pragma unroll
+            for (int e = 0; e < EPV; e++) acc += xent_ex2(y[u][e] - nm);
         mx2 = nm;
         sum = acc;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, mx2, o), os = __shfl_xor_sync(0xffffffffu, sum, o);
-        const float nm = fmaxf(mx2, om);
-        const float a = (mx2 == -INFINITY) ? 0.f : sum * exp2f(mx2 - nm);
-        const float b = (om == -INFINITY) ? 0.f : os * exp2f(om - nm);
-        mx2 = nm;
-        sum = a + b;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+        xent_merge(mx2, sum, __shfl_xor_sync(0xffffffffu, mx2, o), __shfl_xor_sync(0xffffffffu, sum, o));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) { sm_m[warp] = mx2; sm_s[warp] = sum; }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = -INFINITY, S = 0.f;
-        for (int wi = 0; wi < (int)(blockDim.x >> 5); wi++) {
-            const float om = sm_m[wi], os = sm_s[wi];
-            const float nm = fmaxf(M, om);
-            const float a = (M == -INFINITY) ? 0.f : S * exp2f(M - nm);
-            const float b = (om == -INFINITY) ? 0.f : os * exp2f(om - nm);
-            M = nm;
-            S = a + b;
+    if (warp == 0) {
+        float M = lane < NW ? sm_m[lane] : -INFINITY, S = lane < NW ? sm_s[lane] : 0.f;
+#pragma unroll
+        for (int o = NW / 2; o > 0; o >>= 1)
+            xent_merge(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
+        if (lane == 0) {
+            const float lse2 = M + log2f(S);            // log2 of sum exp(z)
+            sm_lse = lse2;
+            if (!tgt_ok) raise_error(err, ERRBIT_TOKEN);
+            losses[row] = tgt_ok ? (lse2 / XENT_LOG2E - to_f32(z[tgt])) : 0.f;
         }
-        const float lse2 = M + log2f(S);            // log2 of sum exp(z)
-        sm_lse = lse2;
-        losses[row] = tgt_ok ? (lse2 / XENT_LOG2E - sm_zt) : 0.f;
     }
     __syncthreads();
     const float lse2 = sm_lse;
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-        Vec<T> p = load_vec(z + (size_t)vi * EPV), o;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += XENT_U * XENT_THREADS) {
+        Vec<T> p[XENT_U];
 #pragma unroll
-        for (int e = 0; e < EPV; e++) {
-            const int j = vi * EPV + e;
-            float d = 0.f;
-            if (j < V) d = (xent_ex2(fmaf(p.get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
-            o.set(e, d);
+        for (int u = 0; u < XENT_U; u++) {
+            const int vi = v0 + u * XENT_THREADS;
+            if (vi < nvec) p[u] = load_vec(z + (size_t)vi * EPV);
         }
-        store_vec(z + (size_t)vi * EPV, o);
+#pragma unroll
+        for (int u = 0; u < XENT_U; u++) {
+            const int vi = v0 + u * XENT_THREADS;
+            if (vi >= nvec) break;
+            Vec<T> o;
+#pragma unroll
+            for (int e = 0; e < EPV; e++) {
+                const int j = vi * EPV + e;
+                float d = 0.f;
+                if (j < V) d = (xent_ex2(fmaf(p[u].get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
+                o.set(e, d);
+            }
+            store_vec(z + (size_t)vi * EPV, o);
+        }
     }
 }
 
