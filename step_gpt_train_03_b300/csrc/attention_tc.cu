@@ -399,8 +399,8 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
 //   DQ   item = (128-query tile t, b*h); for every key tile u <= t:
 //          S = Q_t K_u^T, dP = dO_t V_u^T; P = 2^(S log2e/8 - LSE log2e), dS = P (dP - D)
 //          dQ += dS K_u;  then dQ / 8 to dqkv.
-// Warp 0 loads (the item's two row tiles once; the per-u tiles through a ring of 2
-// (DKV) or 3 (DQ) stages with, in DKV mode, that u's LSE and D vectors); warp 1 issues
+// Warp 0 loads (the item's two row tiles once; the per-u tiles through a 3-stage ring
+// with, in DKV mode, that u's LSE and D vectors); warp 1 issues
 // the MMAs (the next S/dP pair is issued before the dV/dK (dQ) products of the current
 // one); warps 2-9 compute, two warps per TMEM lane quadrant, each on half the columns of
 // a tile (a TMEM lane is a key row in DKV mode, a query row in DQ mode).  The operands
@@ -412,7 +412,7 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
 
 template <bool DKV>
 struct AbSmem {
-    static constexpr int RING = DKV ? 2 : 3;
+    static constexpr int RING = 3;
     static constexpr int R_OFF = 0;                                        // 2 row tiles
     static constexpr int RING_OFF = R_OFF + 2 * AT_TILE_BYTES;
     static constexpr int DS_OFF = RING_OFF + RING * AB_STAGE_BYTES;        // 2 x dS or dS^T, 32 KB each
@@ -611,6 +611,14 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
         uint8_t* dsbase = smem + S::DS_OFF;
         int rc = 0, xc = 0, gc = 0, local = 0;
         int pf_seen0 = 0, pf_seen1 = 0;                     // pds_free completions observed per buffer
+        int stg_pending = -1;                               // dS buffer an item's store may still be reading
+        // before this buffer is written again, the store issued from it has read it
+        auto stg_release = [&](int buf) {
+            if (stg_pending != buf) return;
+            if (threadIdx.x == 64) bulk_wait_read<0>();
+            named_bar(1, 256);
+            stg_pending = -1;
+        };
         bool alive = true;
         auto wait_one = [&](uint64_t* bar, uint32_t parity) -> bool {
             int okw = 1;
@@ -696,8 +704,10 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                             ds[i] = p[i] * (__uint_as_float(s2[i]) - Dc[i]);
                         }
                     }
-                    // the products of tile gc-2 must have finished reading this buffer
+                    // the products of tile gc-2, and an item's output store, must have
+                    // finished reading this buffer
                     if (c == half * 64 && gc >= 2 && !wait_pds_free(gc - 2)) { alive = false; break; }
+                    if (c == half * 64) stg_release(pb);
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int ch = (c >> 3) + k;
@@ -731,6 +741,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             // staging: the last tile's dS buffer (its products are done; the next item's
             // first tile uses the other buffer)
             uint8_t* stg = dsbase + ((gc - 1) & 1) * 2 * AT_TILE_BYTES;
+            stg_release((gc - 1) & 1);
             tc_fence_after();
             float a1[32], a2[32];
             {
@@ -777,9 +788,8 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                     tma_store_3d(&tmDQKV, stg, h * AT_HS, t * AT_BM, b);
                 }
                 bulk_commit();
-                bulk_wait_read<0>();      // the buffers are reused by the next item
             }
-            named_bar(1, 256);
+            stg_pending = (gc - 1) & 1;   // read before that buffer is next written
         }
         if (threadIdx.x == 64) bulk_wait<0>();
     }
