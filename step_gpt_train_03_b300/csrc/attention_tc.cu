@@ -15,8 +15,9 @@
 //              tile): read the S row from TMEM, keep the running max / sum, write P
 //              (bf16) into one of two shared buffers for the P V product; at the end
 //              normalise O and write it with a TMA store, plus the row LSE
-// The softmax reads each S row from TMEM twice, 32 columns at a time (max, then the
-// exponentials), which keeps the code small and the reductions short (trees).
+// The softmax reads its 64 scores of an S row from TMEM once (the S buffer is released
+// right away, so S(j+2) can be computed while the softmax works on tile j), takes the
+// row max over the warp pair, then the exponentials from registers.
 // The exponent reference of a row (its max so far) is only raised when a new score
 // exceeds it by more than 2^8: then, and only then, the row of O in TMEM is rescaled
 // (after waiting for the P V in flight).  Numerator and denominator always use the same
@@ -251,27 +252,35 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 const uint32_t srow = TM_S + sb * AT_BN + lrow;
                 // keys after the query are masked on the diagonal tile: columns > lim
                 const int lim = (j == nk - 1) ? (q - j * AT_BN) : AT_BN;
-                // pass 1: max over this warp's 64 columns, then over the pair
-                float mx = -INFINITY;
                 const bool masked = lim < AT_BN;            // only the diagonal tile
-#pragma unroll 1
-                for (int c = half * 64; c < half * 64 + 64; c += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32(srow + c, rr);
+                // this warp's 64 scores of the row, read once; the S buffer is then free
+                uint32_t sr[64];
+                {
+                    uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+                    uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+                    tmem_ld32(srow + half * 64, s0);
+                    tmem_ld32(srow + half * 64 + 32, s1);
                     tmem_ld_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[sb]);
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 64; i++)
+                        if (half * 64 + i > lim) sr[i] = __float_as_uint(-INFINITY);
+                }
+                // max over this warp's 64 columns, then over the pair
+                float mx;
+                {
                     float v[32];
-                    if (masked) {
 #pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = (c + i <= lim) ? __uint_as_float(rr[i]) : -INFINITY;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(rr[i]);
-                    }
+                    for (int i = 0; i < 32; i++) v[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[32 + i]));
 #pragma unroll
                     for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
                         for (int i = 0; i < w; i++) v[i] = fmaxf(v[i], v[i + w]);
-                    mx = fmaxf(mx, v[0]);
+                    mx = v[0];
                 }
                 mx *= sl2;                                  // scaling by sl2 > 0 keeps the max
                 float* xm = xmax + (sc & 1) * 256;
@@ -299,22 +308,15 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 const int pb = pc & 1;
                 if (pc >= 2 && !wait_pv(pc - 2)) { alive = false; break; }
                 uint8_t* pbuf = smem + S::P_OFF + pb * 2 * AT_TILE_BYTES;
-                // pass 2: p = 2^(s - m), partial row sum, P into the swizzled A operand
+                // p = 2^(s - m) (masked scores are -inf: p = 0), partial row sum, P into the
+                // swizzled A operand
                 float rs = 0.f;
-#pragma unroll 1
-                for (int c = half * 64; c < half * 64 + 64; c += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32(srow + c, rr);
-                    tmem_ld_wait();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int c = half * 64 + h2 * 32;
                     float p[32];
-                    if (masked) {
 #pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            p[i] = (c + i <= lim) ? ex2_fast(fmaf(__uint_as_float(rr[i]), sl2, -m)) : 0.f;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) p[i] = ex2_fast(fmaf(__uint_as_float(rr[i]), sl2, -m));
-                    }
+                    for (int i = 0; i < 32; i++) p[i] = ex2_fast(fmaf(__uint_as_float(sr[h2 * 32 + i]), sl2, -m));
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int ch = (c >> 3) + k;
@@ -331,13 +333,9 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                     rs += p[0];
                 }
                 l = l * corr + rs;
-                tc_fence_before();
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&s_free[sb]);
-                    mbar_arrive(&p_full[pb]);
-                }
+                if (lane == 0) mbar_arrive(&p_full[pb]);
                 sc++;
                 pc++;
             }
