@@ -274,6 +274,59 @@ __device__ __forceinline__ float wsum_get(const float* ws, int nvec, int vi, int
     return ws[(size_t)(e >> 2) * nvec * 4 + vi * 4 + (e & 3)];
 }
 
+// The block's column sums: every warp's dw, db (and column sums of the new dinp) are
+// added into `red`, warps in order, in the float4 plane layout of the per-warp sums (32
+// consecutive 16-byte words per warp access: no bank conflicts); the block's partial
+// row is then written in column order.
+template <int EPV, int NV, bool SUM>
+__device__ __forceinline__ void ln_combine(float* red, const float* wsum, const float (&dwa)[NV][EPV],
+                                           const float (&dba)[NV][EPV], int warp, int lane, int nvec, int C,
+                                           float* __restrict__ pj) {
+    constexpr int W = SUM ? 3 : 2;
+    for (int wi = 0; wi < LN_WARPS; wi++) {
+        if (warp == wi) {
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                const int vi = lane + 32 * i;
+                if (vi < nvec) {
+#pragma unroll
+                    for (int p = 0; p < EPV / 4; p++) {
+                        const int o = p * nvec * 4 + vi * 4;
+                        const float4 a = make_float4(dwa[i][4 * p], dwa[i][4 * p + 1], dwa[i][4 * p + 2], dwa[i][4 * p + 3]);
+                        const float4 b = make_float4(dba[i][4 * p], dba[i][4 * p + 1], dba[i][4 * p + 2], dba[i][4 * p + 3]);
+                        float4* r0 = reinterpret_cast<float4*>(red + o);
+                        float4* r1 = reinterpret_cast<float4*>(red + C + o);
+                        if (wi == 0) {
+                            *r0 = a;
+                            *r1 = b;
+                            if (SUM) *reinterpret_cast<float4*>(red + 2 * C + o) = *reinterpret_cast<const float4*>(wsum + o);
+                        } else {
+                            float4 x = *r0, y = *r1;
+                            x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+                            y.x += b.x; y.y += b.y; y.z += b.z; y.w += b.w;
+                            *r0 = x;
+                            *r1 = y;
+                            if (SUM) {
+                                float4* r2 = reinterpret_cast<float4*>(red + 2 * C + o);
+                                const float4 z = *reinterpret_cast<const float4*>(wsum + o);
+                                float4 t = *r2;
+                                t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
+                                *r2 = t;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    for (int c = threadIdx.x; c < W * C; c += blockDim.x) {
+        const int arr = c / C, cc = c - arr * C, vi = cc / EPV, e = cc - vi * EPV;
+        pj[c] = red[arr * C + (e >> 2) * nvec * 4 + vi * 4 + (e & 3)];
+    }
+}
+
+
 template <typename T, int NV, bool SUM>
 __global__ void __launch_bounds__(LN_WARPS * 32, (NV * Vec<T>::N <= 24) ? 2 : 1)
 layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
@@ -346,25 +399,7 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
         }
     }
     // combine the warps in order 0..LN_WARPS-1
-    for (int wi = 0; wi < LN_WARPS; wi++) {
-        if (warp == wi) {
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                int vi = lane + 32 * i;
-                if (vi < nvec) {
-#pragma unroll
-                    for (int e = 0; e < EPV; e++) {
-                        int c = vi * EPV + e;
-                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum_get(wsum, nvec, vi, e); }
-                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum_get(wsum, nvec, vi, e); }
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-    float* pj = partial + (size_t)blockIdx.x * W * C;
-    for (int c = threadIdx.x; c < W * C; c += blockDim.x) pj[c] = red[c];
+    ln_combine<EPV, NV, SUM>(red, wsum, dwa, dba, warp, lane, nvec, C, partial + (size_t)blockIdx.x * W * C);
 }
 
 // Same computation, with each warp's rows streamed through shared memory: lane 0 of the
@@ -416,10 +451,15 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
         bulk_load(d + 2 * C, dinp + (size_t)row * C, (uint32_t)row_bytes, &bars[k & 1]);
     };
     if (lane == 0 && nrows > 0) fetch(0);
+    // the statistics of this warp's rows, fetched together up front: lane k holds row k's
+    // (rows past the 32nd load their own when reached)
+    float mk = 0.f, rk = 0.f;
+    if (lane < nrows) { mk = mean[row0 + lane * step]; rk = rstd[row0 + lane * step]; }
     int issued = nrows > 0 ? 1 : 0, waited = 0;
     for (int k = 0; k < nrows; k++) {
         const int row = row0 + k * step;
-        const float m = mean[row], r = rstd[row];
+        float m = __shfl_sync(0xffffffffu, mk, k & 31), r = __shfl_sync(0xffffffffu, rk, k & 31);
+        if (k >= 32) { m = mean[row]; r = rstd[row]; }
         __syncwarp();                                  // every lane is done with row k-1's stage
         if (lane == 0 && k + 1 < nrows) { fetch(k + 1); issued++; }
         // wait for row k (bounded)
@@ -480,25 +520,7 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
         }
     }
     __syncwarp();
-    for (int wi = 0; wi < LN_WARPS; wi++) {
-        if (warp == wi) {
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                int vi = lane + 32 * i;
-                if (vi < nvec) {
-#pragma unroll
-                    for (int e = 0; e < EPV; e++) {
-                        int c = vi * EPV + e;
-                        if (wi == 0) { red[c] = dwa[i][e]; red[C + c] = dba[i][e]; if (SUM) red[2 * C + c] = wsum_get(wsum, nvec, vi, e); }
-                        else { red[c] += dwa[i][e]; red[C + c] += dba[i][e]; if (SUM) red[2 * C + c] += wsum_get(wsum, nvec, vi, e); }
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-    float* pj = partial + (size_t)blockIdx.x * W * C;
-    for (int c = threadIdx.x; c < W * C; c += blockDim.x) pj[c] = red[c];
+    ln_combine<EPV, NV, SUM>(red, wsum, dwa, dba, warp, lane, nvec, C, partial + (size_t)blockIdx.x * W * C);
 }
 
 // Column sums of a (G x W) fp32 partial matrix, in a fixed order: a 256-thread block
