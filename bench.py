@@ -187,6 +187,31 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------------------------------ ncu traffic
+TRAFFIC_PROFILE = os.path.join("profiles", "matmul_dram_traffic_gpt2_124m_bf16_b16_t1024.md")
+
+
+def matmul_traffic(workload):
+    """DRAM bytes per matmul launch from the committed ncu summary of this workload, or
+    (None, why) when there is none or the kernel's sources changed since the capture."""
+    import hashlib
+    if workload != WORKLOAD:
+        return None, "no capture for this workload"
+    try:
+        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as f:
+            kv = dict(l.split(":", 1) for l in f.read().splitlines() if l.startswith(
+                ("traffic_bytes_per_launch:", "kernel_sources:", "sources_sha256:")))
+        h = hashlib.sha256()
+        for src in kv["kernel_sources"].split():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+    except (OSError, KeyError, ValueError) as e:
+        return None, f"no traffic capture ({e!r:.80})"
+    if h.hexdigest() != kv["sources_sha256"].strip():
+        return None, "the matmul kernel changed since the DRAM counters were taken"
+    return float(kv["traffic_bytes_per_launch"]), f"{TRAFFIC_PROFILE} (ncu dram__bytes_read.sum + dram__bytes_write.sum, mean per launch of the family in one step)"
+
+
 # ------------------------------------------------------------------------ CPU oracle leg
 def oracle_tokens_per_s(w, sample_B, sample_T, steps, warmup=0, seed_offset=0):
     """Time the CPU oracle (float32, as the pages' program) on a bounded sample of the
@@ -387,8 +412,9 @@ def ours(args):
     if d_fl > 0:
         achieved = d_fl / (d_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
+        traffic, traffic_src = matmul_traffic(args.workload) if dominant == "matmul" else (None, "no capture")
         roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                 "peak_source": f"{src} bf16 sustained (kernel timed inside a long step)",
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
                 "share_of_traced_step": fam_ms[dominant] / total_ms,
