@@ -245,7 +245,10 @@ def reference_arm(args):
         return 0
     from step_gpt_train_03_b300 import synth
     w = synth.WORKLOADS[args.workload]
-    sB, sT = 1, 512
+    # each step a bounded sample (one sequence), shorter as the step count grows, so the
+    # whole run stays within a few minutes of host time
+    n = args.steps + args.warmup
+    sB, sT = 1, min(512 if n <= 13 else 256 if n <= 26 else 128, w.shape.max_seq_len)
     tps, cores, total, per = oracle_tokens_per_s(w, sB, sT, args.steps, args.warmup)
     sample = (f"{args.steps} timed whole steps (after {args.warmup} warm-up) of the fp32 CPU oracle "
               f"on the {w.name} model at B={sB}, T={sT} ({sB * sT} tokens each)")
@@ -287,7 +290,8 @@ def ours(args):
     B, T = w.B, w.T
     BT = B * T
     stream = torch.cuda.Stream()
-    m = G.GPT2(w.shape, B, T, "bf16", stream=stream)
+    prec = w.precision                      # "bf16" (fp32 master weights) or "fp32"
+    m = G.GPT2(w.shape, B, T, prec, stream=stream)
     m.load_params(synth.init_params(w.shape, w.seed))
     n_batches = args.warmup + args.steps
     host = synth.zipf_batches(w.shape.vocab_size, B, T, n_batches, w.seed + 7919 * rank)
@@ -411,11 +415,18 @@ def ours(args):
     d_by = sum(live[c]["bytes"] for c in dom_classes)
     if d_fl > 0:
         achieved = d_fl / (d_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        if prec == "bf16":
+            bound, peak = "tensor", peaks["bf16_tflops_sustained"]
+            peak_src = f"{src} bf16 sustained (kernel timed inside a long step)"
+        else:
+            # the fp32 path's matmuls run on the FP32 FMA units: 148 SMs x 128 lanes x 2 flops
+            # at the 2032 MHz maximum SM clock
+            bound, peak = "alu", 148 * 128 * 2 * 2.032e9 / 1e12
+            peak_src = "derived: 148 SMs x 128 FP32 lanes x 2 flop/FMA x 2.032 GHz"
         traffic, traffic_src = matmul_traffic(args.workload) if dominant == "matmul" else (None, "no capture")
-        roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+        roof = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
-                "peak_source": f"{src} bf16 sustained (kernel timed inside a long step)",
+                "peak_source": peak_src,
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
                 "share_of_traced_step": fam_ms[dominant] / total_ms,
                 "timing": f"CUDA events around each launch on the step's stream, over a second timed pass "
@@ -439,7 +450,7 @@ def ours(args):
                for k, v in warm_prof.items() if v["launches"]}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        sB, sT = 1, 1024
+        sB, sT = 1, min(1024, w.shape.max_seq_len)
         tps, cores, total, per = oracle_tokens_per_s(w, sB, sT, 1)
         cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"one whole step (fwd+bwd+AdamW) of the fp32 CPU oracle on the {w.name} model "
@@ -447,12 +458,15 @@ def ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prec == "bf16" else "f32",
         "data": "synthetic (seeded Zipf s=1.1 int32 token stream, fresh batch per step; random-init weights)",
-        "config": {"workload": w.name, "model": "GPT-2 124M (L=12, C=768, NH=12, V=50257 padded to 50304)",
+        "config": {"workload": w.name,
+                   "shape": (f"L={w.shape.num_layers}, C={w.shape.channels}, NH={w.shape.num_heads}, "
+                             f"V={w.shape.vocab_size} padded to {w.shape.padded_vocab_size}"),
                    "global_batch": B * world, "seq_len": T,
                    "parallelism": "replicas only" if world > 1 else "single GPU",
-                   "precision": "bf16 weights/activations, fp32 master weights and AdamW state",
+                   "precision": ("bf16 weights/activations, fp32 master weights and AdamW state" if prec == "bf16"
+                                 else "fp32 throughout"),
                    "l2": "no flush: the step's working set (GBs of activations) is far larger than the 126 MB L2"},
         "clocks": clk,
         "gpu_launches": launches,

@@ -1,7 +1,10 @@
 """Run one kernel of the training step on its own, at the 124M workload's sizes, a few
 times: the target of per-kernel Nsight Compute captures.
 
-    python -m step_gpt_train_03_b300.kernel_cases <case> [--iters N]
+    python -m step_gpt_train_03_b300.kernel_cases <case> [--iters N] [--time]
+
+With --time, the runs are timed with CUDA events (after the untimed ones) and the
+case's algorithmic work rate is printed (TFLOP/s for products, GB/s for layernorm).
 
 Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
   matmul_fc_forward       (16384 x 768) @ (3072 x 768)^T
@@ -9,7 +12,8 @@ Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
   matmul_lmhead_backward  dX (16384 x 768) and dW (50304 x 768, fp32 +=) of the LM head
   attention_forward       causal, B=16, T=1024, hs=64
   attention_backward      same sizes (dK/dV kernel, then dQ kernel)
-  layernorm_backward_fp32 (8192 x 768) fp32, the standalone layernorm workload
+  layernorm_forward_fp32  (8192 x 768) fp32, the standalone layernorm workload
+  layernorm_backward_fp32 the same workload's backward
 """
 from __future__ import annotations
 
@@ -21,6 +25,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("case")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--time", action="store_true")
     args = ap.parse_args(argv)
     import torch
     from step_gpt_train_03_b300 import gpt2lib as G
@@ -33,6 +38,7 @@ def main(argv=None):
         N = 3072 if case == "matmul_fc_forward" else Vp
         x = torch.randn(BT, C, device=dev).to(bf)
         w = (0.02 * torch.randn(N, C, device=dev)).to(bf)
+        work, unit = 2.0 * BT * N * C, "flop"
         if case.endswith("forward"):
             out = torch.empty(BT, N, device=dev, dtype=bf)
             run = lambda: G.matmul_forward(out, x, w, None, "bf16")
@@ -42,11 +48,13 @@ def main(argv=None):
             dW = torch.zeros(N, C, device=dev)
             sc = torch.empty(G.matmul_backward_scratch_bytes(BT, N), dtype=torch.uint8, device=dev)
             run = lambda: G.matmul_backward(dx, dW, None, dy, x, w, "bf16", sc)
+            work = 2 * work                                # dX and dW
     elif case.startswith("attention"):
         qkv = torch.randn(B, T, 3 * C, device=dev).to(bf)
         out = torch.empty(B, T, C, device=dev, dtype=bf)
         lse = torch.empty(B, NH, T, device=dev)
         G.attention_forward(out, lse, qkv, NH, "bf16")
+        work, unit = 4.0 * B * C * T * (T + 1) / 2, "flop"       # Q K^T and P V over the causal half
         if case == "attention_forward":
             run = lambda: G.attention_forward(out, lse, qkv, NH, "bf16")
         else:
@@ -54,7 +62,8 @@ def main(argv=None):
             dqkv = torch.empty_like(qkv)
             sc = torch.empty(G.attention_backward_scratch_bytes(B, T, NH, "bf16"), dtype=torch.uint8, device=dev)
             run = lambda: G.attention_backward(dqkv, dout, qkv, out, lse, NH, "bf16", sc)
-    elif case == "layernorm_backward_fp32":
+            work = 2 * work                                # dP, dV, dK, dQ (recomputed S not counted)
+    elif case in ("layernorm_backward_fp32", "layernorm_forward_fp32"):
         N = 8192
         x = 3 * torch.randn(N, C, device=dev) + 0.5
         w = 1 + 0.1 * torch.randn(C, device=dev)
@@ -68,7 +77,12 @@ def main(argv=None):
         dw = torch.zeros(C, device=dev)
         db = torch.zeros(C, device=dev)
         sc = torch.empty(G.layernorm_backward_scratch_bytes(N, C), dtype=torch.uint8, device=dev)
-        run = lambda: G.layernorm_backward(dx, dw, db, dy, x, w, mean, rstd, sc)
+        if case == "layernorm_backward_fp32":
+            run = lambda: G.layernorm_backward(dx, dw, db, dy, x, w, mean, rstd, sc)
+            work, unit = 4.0 * N * C * 4 + 8.0 * N, "byte"     # dy, x, dinp read; dinp written; stats
+        else:
+            run = lambda: G.layernorm_forward(y, mean, rstd, x, w, b)
+            work, unit = 2.0 * N * C * 4 + 8.0 * N, "byte"     # x read, y written; stats
     else:
         print(f"unknown case {case}", file=sys.stderr)
         return 2
@@ -76,6 +90,16 @@ def main(argv=None):
         run()
     torch.cuda.synchronize()
     print(f"{case}: {args.iters} runs ok")
+    if args.time:
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.iters):
+            run()
+        e.record()
+        e.synchronize()
+        sec = s.elapsed_time(e) / 1e3 / args.iters
+        rate = f"{work / sec / 1e12:.1f} TFLOP/s" if unit == "flop" else f"{work / sec / 1e9:.0f} GB/s"
+        print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic)")
     return 0
 
 
