@@ -286,3 +286,20 @@ def test_graph_steps_match_eager_steps_bitwise(precision):
         le = e.step_device(tk, tg, lr, 0.9, 0.95, 1e-8, 0.1, i + 1, want_loss=True)
         assert lg == le, (i, lg, le)
         assert torch.equal(g.flat_params(), e.flat_params()), i
+
+
+def test_split_weight_gradients_are_bitwise_deterministic():
+    """At the 124M shape with B*T = 1024 rows, the weight-gradient products of the fc and
+    attention layers split their 1024-row contraction; the splits add into the gradient
+    in a fixed order, so two runs from the same state agree bit for bit."""
+    import torch
+    shape = synth.GPT2_124M
+    tok, tgt = synth.zipf_batches(shape.vocab_size, 2, 512, 1, 5)[0]
+    out = []
+    for _ in range(2):
+        m = gpu_model(shape, 2, 512, "bf16", 1)
+        m.forward(dev_tokens(tok), dev_tokens(tgt))
+        m.zero_grad()
+        m.backward()
+        out.append(m.flat_grads().clone())
+    assert torch.equal(out[0], out[1])
