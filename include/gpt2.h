@@ -72,7 +72,9 @@ enum {
     GPT2_ENONFINITE = 5,   /* the mean loss was NaN or Inf */
     GPT2_ETIMEOUT = 6,     /* a bounded device-side wait ran out; the kernel gave up */
     GPT2_ENOMEM = 7,       /* the workspace passed to gpt2_build is too small */
-    GPT2_EUNSUPPORTED = 8  /* shape or precision this build does not implement */
+    GPT2_EUNSUPPORTED = 8, /* shape or precision this build does not implement */
+    GPT2_EIO = 9           /* a parameter file could not be read or written, or its header
+                              does not describe this model */
 };
 
 /* Names of the 16 parameter tensors, in the order of the flat buffer:
@@ -171,6 +173,33 @@ int gpt2_step(GPT2* model, const int32_t* tokens, const int32_t* targets, int B,
 /* Enable (1, the default) or disable (0) the step graph of gpt2_step / gpt2_step_host;
  * disabling frees a captured graph.  GPT2_EINVAL for a NULL model. */
 int gpt2_set_graphs(GPT2* model, int enable);
+
+/* Next-token sampling (the llm.c article's training run: after training, the program
+ * generates samples from the model).  Needs a preceding gpt2_forward WITHOUT targets
+ * (the logits are kept; GPT2_ESTATE otherwise).  For each sequence b of that forward,
+ * draws a token from p_j = softmax(z[b, pos, j] / temperature) over the V real columns
+ * by inverse CDF: u_b = (top 53 bits of output b+1 of SplitMix64 started at `seed`) /
+ * 2^53, and the token is the first j whose running sum of exp((z_j - max) / temperature)
+ * exceeds u_b times the total (sums in a fixed order, so a seed always gives the same
+ * tokens).  out_tokens: B int32, device, caller-owned; written on the model's stream
+ * (no synchronisation).  GPT2_EINVAL for pos outside [0, T) of that forward, a
+ * temperature that is not > 0, or a NULL pointer. */
+int gpt2_sample(GPT2* model, int pos, float temperature, unsigned long long seed, int32_t* out_tokens);
+
+/* Parameter files.  The llm.c article ("用C语言实现LLM" / the training run) saves the
+ * model's weights to a checkpoint that the C program loads into its one parameter
+ * buffer before training.  Layout (little-endian): 256 int32 header words -- [0] magic
+ * 20240326, [1] version 3, [2] max_seq_len, [3] vocab_size, [4] num_layers, [5] num_heads,
+ * [6] channels, [7] padded_vocab_size, the rest 0 -- then every parameter tensor in the
+ * order of gpt2_param_tensor (wte with all padded_vocab_size rows, wpe, ln1w, ..., lnfb),
+ * fp32, back to back.  gpt2_save_params synchronises the model's stream and writes the
+ * fp32 master weights.  gpt2_load_params requires the header to match the model's
+ * configuration exactly (else GPT2_EIO, parameters untouched), copies the tensors into
+ * the master weights, refreshes the bf16 shadow and zeroes the AdamW moments (a fresh
+ * optimiser state for the loaded weights), and synchronises.  GPT2_EIO also for a file
+ * that cannot be opened or is shorter than the header says. */
+int gpt2_save_params(GPT2* model, const char* path);
+int gpt2_load_params(GPT2* model, const char* path);
 
 /* Device pointers into the last forward's outputs: the mean loss (1 float), the
  * per-position losses (B*T floats) and the logits (B*T rows of Vp entries, fp32 or bf16

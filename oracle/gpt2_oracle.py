@@ -278,6 +278,67 @@ def adamw_update(params, grads, m, v, lr, beta1, beta2, eps, weight_decay, t):
 # --------------------------------------------------------------------------------------
 # the model: layers chained into forward / zero_grad / backward / update
 # --------------------------------------------------------------------------------------
+# ----------------------------------------------------------------- sampling and files
+# The llm.c article, section "训练过程" (training run): after the fine-tuning loop the
+# program generates samples from the model, and it starts from a checkpoint file of
+# the weights written for the C program to load.  The pages give neither the sampler
+# nor the file layout; the readings (inverse-CDF sampling driven by SplitMix64, and a
+# 256-word int32 header followed by the fp32 tensors in parameter order) are in the
+# design notes.
+
+_M64 = (1 << 64) - 1
+
+
+def splitmix64(seed, i):
+    """Output i (i >= 1) of the SplitMix64 generator started at `seed`, from its published
+    definition (Steele, Lea, Flood, "Fast splittable pseudorandom number generators",
+    OOPSLA 2014): the state advances by the golden-ratio increment 0x9E3779B97F4A7C15 and
+    the output is the state mixed by (z ^ z>>30) * 0xBF58476D1CE4E5B9,
+    (z ^ z>>27) * 0x94D049BB133111EB, z ^ z>>31, all modulo 2^64."""
+    z = (seed + i * 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def sample_token(z, V, temperature, seed, b):
+    """Inverse-CDF draw from softmax(z[:V] / temperature) for sequence b: u = top 53 bits
+    of SplitMix64 output b+1 over 2^53; the token is the first j whose running sum of
+    exp((z_j - max) / temperature) exceeds u times the total.  Returns (token, lo, hi,
+    threshold, total): [lo, hi) is the token's interval of the running sum."""
+    x = np.asarray(z[:V], dtype=np.float64)
+    e = np.exp((x - x.max()) / temperature)
+    c = np.cumsum(e)
+    u = (splitmix64(seed, b + 1) >> 11) / float(1 << 53)
+    thr = u * c[-1]
+    k = int(np.searchsorted(c, thr, side="right"))
+    k = min(k, V - 1)
+    lo = 0.0 if k == 0 else float(c[k - 1])
+    return k, lo, float(c[k]), thr, float(c[-1])
+
+
+PARAM_FILE_MAGIC = 20240326
+PARAM_FILE_VERSION = 3
+
+
+def read_param_file(path):
+    """(header ints, {name: fp32 array} in parameter order) of a parameter file: 256
+    little-endian int32 header words, then the tensors back to back.  The tensor
+    shapes follow from the header's max_seq_len, padded vocab, layers and channels."""
+    with open(path, "rb") as f:
+        h = np.frombuffer(f.read(1024), dtype="<i4")
+        rest = np.frombuffer(f.read(), dtype="<f4")
+    max_seq_len, L, C, Vp = int(h[2]), int(h[4]), int(h[6]), int(h[7])
+    out, off = {}, 0
+    for name, shp in param_shapes(max_seq_len, Vp, L, C).items():
+        n = int(np.prod(shp))
+        out[name] = rest[off:off + n].reshape(shp)
+        off += n
+    if off != rest.size:
+        raise ValueError(f"{rest.size - off} trailing values in {path}")
+    return h, out
+
+
 class GPT2Oracle:
     """GPT-2 over one flat parameter buffer (views carve it into tensors).
 

@@ -318,6 +318,83 @@ extern "C" int gpt2_sync_params(GPT2* m) {
     return rc;
 }
 
+// ------------------------------------------------------------------ sampling
+extern "C" int gpt2_sample(GPT2* m, int pos, float temperature, unsigned long long seed, int32_t* out) {
+    if (!m || !out || !(temperature > 0.f)) return GPT2_EINVAL;
+    if (!m->have_fwd || m->have_targets) return GPT2_ESTATE;
+    if (pos < 0 || pos >= m->T) return GPT2_EINVAL;
+    const float inv = 1.0f / temperature;
+    if (m->prec == GPT2_BF16)
+        sample_kernel<bf16><<<m->B, SAMPLE_THREADS, 0, m->stream>>>(out, (const bf16*)m->logits, m->T, pos, m->V,
+                                                                   m->Vp, inv, seed);
+    else
+        sample_kernel<float><<<m->B, SAMPLE_THREADS, 0, m->stream>>>(out, (const float*)m->logits, m->T, pos, m->V,
+                                                                    m->Vp, inv, seed);
+    rt_note_launches(1);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ parameter files
+#define GPT2_FILE_MAGIC 20240326
+#define GPT2_FILE_VERSION 3
+
+static void file_header(const GPT2* m, int32_t (&h)[256]) {
+    memset(h, 0, sizeof(h));
+    h[0] = GPT2_FILE_MAGIC;
+    h[1] = GPT2_FILE_VERSION;
+    h[2] = m->cfg.max_seq_len;
+    h[3] = m->cfg.vocab_size;
+    h[4] = m->cfg.num_layers;
+    h[5] = m->cfg.num_heads;
+    h[6] = m->cfg.channels;
+    h[7] = m->cfg.padded_vocab_size;
+}
+
+extern "C" int gpt2_save_params(GPT2* m, const char* path) {
+    if (!m || !path) return GPT2_EINVAL;
+    CK(cudaStreamSynchronize(m->stream));
+    int32_t h[256];
+    file_header(m, h);
+    FILE* f = fopen(path, "wb");
+    if (!f) return GPT2_EIO;
+    bool ok = fwrite(h, sizeof(h), 1, f) == 1;
+    std::vector<float> buf;
+    for (int i = 0; i < GPT2_NUM_PARAM_TENSORS && ok; i++) {
+        buf.resize(m->pnum[i]);
+        if (cudaMemcpy(buf.data(), m->params + m->poff[i], m->pnum[i] * 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            fclose(f);
+            return GPT2_ECUDA;
+        }
+        ok = fwrite(buf.data(), 4, m->pnum[i], f) == m->pnum[i];
+    }
+    if (fclose(f) != 0) ok = false;
+    return ok ? GPT2_OK : GPT2_EIO;
+}
+
+extern "C" int gpt2_load_params(GPT2* m, const char* path) {
+    if (!m || !path) return GPT2_EINVAL;
+    int32_t want[256], h[256];
+    file_header(m, want);
+    FILE* f = fopen(path, "rb");
+    if (!f) return GPT2_EIO;
+    if (fread(h, sizeof(h), 1, f) != 1 || memcmp(h, want, sizeof(h)) != 0) { fclose(f); return GPT2_EIO; }
+    // read everything first, so a short file leaves the parameters untouched
+    std::vector<std::vector<float>> t(GPT2_NUM_PARAM_TENSORS);
+    for (int i = 0; i < GPT2_NUM_PARAM_TENSORS; i++) {
+        t[i].resize(m->pnum[i]);
+        if (fread(t[i].data(), 4, m->pnum[i], f) != m->pnum[i]) { fclose(f); return GPT2_EIO; }
+    }
+    fclose(f);
+    CK(cudaStreamSynchronize(m->stream));
+    for (int i = 0; i < GPT2_NUM_PARAM_TENSORS; i++)
+        CK(cudaMemcpy(m->params + m->poff[i], t[i].data(), m->pnum[i] * 4, cudaMemcpyHostToDevice));
+    const int rc = gpt2_sync_params(m);
+    if (rc != GPT2_OK) return rc;
+    CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
 // ------------------------------------------------------------------ layer launchers
 template <typename T>
 static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T* inp, const T* w,
@@ -936,6 +1013,7 @@ extern "C" const char* gpt2_strerror(int st) {
         case GPT2_ETIMEOUT: return "bounded device wait ran out";
         case GPT2_ENOMEM: return "workspace too small";
         case GPT2_EUNSUPPORTED: return "unsupported shape or precision";
+        case GPT2_EIO: return "parameter file unreadable, unwritable or for another model";
         default: return "unknown status";
     }
 }

@@ -791,6 +791,84 @@ mean_loss_kernel(float* __restrict__ loss, const float* __restrict__ losses, int
     }
 }
 
+// ============================================================== next-token sampling
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+// OOPSLA 2014): output i of the generator started at `seed` mixes seed + i * gamma
+// (gamma = the 64-bit golden-ratio constant) with two multiply-xorshift rounds.
+__device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed, unsigned long long i) {
+    unsigned long long z = seed + i * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// One 1024-thread block per sequence b: e_j = exp((z_j - max) / temperature) over the V
+// real columns of row (b, pos); thread t sums its contiguous chunk of e in order, the
+// chunk sums are scanned in a fixed order (warp shuffles, then warp totals), u_b = the
+// top 53 bits of SplitMix64 output b+1 scaled to [0, 1), and the token is the first
+// index whose running sum exceeds u_b * total: the last chunk whose prefix is <= that
+// threshold is scanned by its thread.
+#define SAMPLE_THREADS 1024
+template <typename T>
+__global__ void __launch_bounds__(SAMPLE_THREADS)
+sample_kernel(int* __restrict__ out, const T* __restrict__ logits, int Tn, int pos, int V, int Vp,
+              float inv_temp, unsigned long long seed) {
+    __shared__ float s_red[32];
+    __shared__ float s_pre[SAMPLE_THREADS];
+    __shared__ int s_pick;
+    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const T* z = logits + ((size_t)b * Tn + pos) * Vp;
+    float mx = -INFINITY;
+    for (int j = t; j < V; j += SAMPLE_THREADS) mx = fmaxf(mx, to_f32(z[j]));
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[warp] = mx;
+    __syncthreads();
+    mx = s_red[0];
+    for (int w = 1; w < SAMPLE_THREADS / 32; w++) mx = fmaxf(mx, s_red[w]);
+    __syncthreads();
+    const int chunk = (V + SAMPLE_THREADS - 1) / SAMPLE_THREADS;
+    const int j0 = min(V, t * chunk), j1 = min(V, j0 + chunk);
+    float cs = 0.f;
+    for (int j = j0; j < j1; j++) cs += expf((to_f32(z[j]) - mx) * inv_temp);
+    // exclusive prefix of the chunk sums, in a fixed order
+    float inc = cs;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) s_red[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        float w = s_red[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
+        }
+        s_red[lane] = w;                                   // inclusive warp totals
+    }
+    __syncthreads();
+    const float pre = (warp > 0 ? s_red[warp - 1] : 0.f) + (inc - cs);
+    const float total = s_red[SAMPLE_THREADS / 32 - 1];
+    s_pre[t] = pre;
+    if (t == 0) s_pick = 0;
+    __syncthreads();
+    const unsigned long long r = splitmix64_at(seed, (unsigned long long)b + 1ull);
+    const float thr = (float)((double)(r >> 11) * (1.0 / 9007199254740992.0)) * total;
+    // the last chunk (highest t with a non-empty chunk) whose prefix is <= thr
+    if (j0 < j1 && pre <= thr) atomicMax(&s_pick, t);
+    __syncthreads();
+    if (t == s_pick) {
+        int k = j1 - 1;
+        float acc = pre;
+        for (int j = j0; j < j1; j++) {
+            const float e = expf((to_f32(z[j]) - mx) * inv_temp);
+            acc += e;
+            if (acc > thr && e > 0.f) { k = j; break; }
+        }
+        out[b] = k;
+    }
+}
+
 // ============================================================== AdamW
 // One pass over the flat buffer (n a multiple of 4).  bc1 = 1 - b1^t, bc2 = 1 - b2^t.
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,

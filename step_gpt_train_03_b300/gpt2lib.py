@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(HERE, "libgpt2_b300.so")
 FP32, BF16 = 0, 1
 PRECISIONS = {"fp32": FP32, "bf16": BF16}
 STATUS = {0: "GPT2_OK", 1: "GPT2_EINVAL", 2: "GPT2_ESTATE", 3: "GPT2_ECUDA", 4: "GPT2_ETOKEN",
-          5: "GPT2_ENONFINITE", 6: "GPT2_ETIMEOUT", 7: "GPT2_ENOMEM", 8: "GPT2_EUNSUPPORTED"}
+          5: "GPT2_ENONFINITE", 6: "GPT2_ETIMEOUT", 7: "GPT2_ENOMEM", 8: "GPT2_EUNSUPPORTED",
+          9: "GPT2_EIO"}
 PARAM_ORDER = ("wte", "wpe", "ln1w", "ln1b", "qkvw", "qkvb", "attprojw", "attprojb",
                "ln2w", "ln2b", "fcw", "fcb", "fcprojw", "fcprojb", "lnfw", "lnfb")
 
@@ -50,6 +51,9 @@ SIGNATURES = {
     "gpt2_step_host": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
     "gpt2_step": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
     "gpt2_set_graphs": (_i, [_vp, _i]),
+    "gpt2_sample": (_i, [_vp, _i, _f, ctypes.c_ulonglong, _vp]),
+    "gpt2_save_params": (_i, [_vp, ctypes.c_char_p]),
+    "gpt2_load_params": (_i, [_vp, ctypes.c_char_p]),
     "gpt2_loss": (_vp, [_vp]),
     "gpt2_losses": (_vp, [_vp]),
     "gpt2_logits": (_vp, [_vp]),
@@ -221,6 +225,7 @@ class GPT2:
         """tokens/targets: int32 CUDA tensors (B, T).  Returns the mean loss (synchronises)
         when want_loss, else None (no synchronisation)."""
         B, T = tokens.shape
+        self.last_B = B
         loss = ctypes.c_float(0.0)
         st = lib.gpt2_forward(self.handle, _ptr(tokens), _ptr(targets), B, T,
                               ctypes.byref(loss) if want_loss else None)
@@ -260,6 +265,36 @@ class GPT2:
         check(lib.gpt2_step(self.handle, _ptr(tokens), _ptr(targets), B, T, lr, beta1, beta2, eps,
                             weight_decay, t, ctypes.byref(loss) if want_loss else None), "gpt2_step")
         return loss.value if want_loss else None
+
+    def sample(self, pos: int, temperature: float, seed: int, out=None):
+        """Next token of every sequence of the last forward (run without targets), from the
+        logits at position `pos` (see gpt2_sample).  Returns an int32 CUDA tensor (B,)."""
+        import torch
+        B = self.last_B
+        if out is None:
+            out = torch.empty(B, dtype=torch.int32, device="cuda")
+        check(lib.gpt2_sample(self.handle, pos, temperature, seed, _ptr(out)), "gpt2_sample")
+        return out
+
+    def generate(self, prompt, n_new: int, temperature: float, seed: int):
+        """Extend int32 CUDA token sequences (B, T0) by n_new sampled tokens: one full
+        forward of the sequence so far per new token, sampled at its last position (the
+        sampler's seed advances by B per token).  Returns (B, T0 + n_new)."""
+        import torch
+        toks = prompt.clone()
+        for i in range(n_new):
+            self.forward(toks, None, want_loss=False)
+            nxt = self.sample(toks.shape[1] - 1, temperature, seed + i * toks.shape[0])
+            toks = torch.cat([toks, nxt.view(-1, 1)], dim=1).contiguous()
+        return toks
+
+    def save(self, path: str):
+        """Write the fp32 master weights to a parameter file (see gpt2_save_params)."""
+        check(lib.gpt2_save_params(self.handle, str(path).encode()), "gpt2_save_params")
+
+    def load(self, path: str):
+        """Load a parameter file written for this configuration (see gpt2_load_params)."""
+        check(lib.gpt2_load_params(self.handle, str(path).encode()), "gpt2_load_params")
 
     def set_graphs(self, enable: bool):
         check(lib.gpt2_set_graphs(self.handle, 1 if enable else 0), "gpt2_set_graphs")

@@ -14,6 +14,8 @@ Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
   attention_backward      same sizes (dK/dV kernel, then dQ kernel)
   layernorm_forward_fp32  (8192 x 768) fp32, the standalone layernorm workload
   layernorm_backward_fp32 the same workload's backward
+  eval_124m               forward-only evaluation of GPT-2 124M (bf16, B=16, T=1024, loss)
+  sample_124m             next-token sampling over the 16 rows of that forward's logits
 """
 from __future__ import annotations
 
@@ -83,6 +85,22 @@ def main(argv=None):
         else:
             run = lambda: G.layernorm_forward(y, mean, rstd, x, w, b)
             work, unit = 2.0 * N * C * 4 + 8.0 * N, "byte"     # x read, y written; stats
+    elif case in ("eval_124m", "sample_124m"):
+        from step_gpt_train_03_b300 import synth
+        w = synth.WORKLOADS["gpt2_124m_bf16_b16_t1024"]
+        m = G.GPT2(w.shape, B, T, "bf16")
+        m.load_params(synth.init_params(w.shape, w.seed))
+        tok, tgt = synth.zipf_batches(w.shape.vocab_size, B, T, 1, w.seed)[0]
+        tok = torch.as_tensor(tok).to(dev)
+        tgt = torch.as_tensor(tgt).to(dev)
+        if case == "eval_124m":
+            run = lambda: m.forward(tok, tgt, want_loss=False)
+            work, unit = float(B * T), "token"
+        else:
+            m.forward(tok, None, want_loss=False)
+            outk = torch.empty(B, dtype=torch.int32, device=dev)
+            run = lambda: m.sample(T - 1, 1.0, 7, outk)
+            work, unit = float(B), "token"
     else:
         print(f"unknown case {case}", file=sys.stderr)
         return 2
@@ -98,7 +116,8 @@ def main(argv=None):
         e.record()
         e.synchronize()
         sec = s.elapsed_time(e) / 1e3 / args.iters
-        rate = f"{work / sec / 1e12:.1f} TFLOP/s" if unit == "flop" else f"{work / sec / 1e9:.0f} GB/s"
+        rate = (f"{work / sec / 1e12:.1f} TFLOP/s" if unit == "flop" else
+                f"{work / sec / 1e9:.0f} GB/s" if unit == "byte" else f"{work / sec:.0f} tokens/s")
         print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic)")
     return 0
 

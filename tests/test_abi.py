@@ -56,5 +56,5 @@ def test_workspace_size_and_validation(lib):
 
 
 def test_strerror_names_every_status(lib):
-    for st in range(9):
+    for st in range(len(lib.STATUS)):
         assert lib.lib.gpt2_strerror(st).decode() != "unknown status"

@@ -310,3 +310,39 @@ def test_matches_pytorch_layers_gpt2_124m_shape_short_sequence():
     assert abs(loss - tl.item()) < 1e-12 * loss
     for k in O.PARAM_ORDER:
         assert rel_max_err(o.g[k], P[k].grad.numpy()) < 1e-9, k
+
+
+# ---------------------------------------------------------------- sampling (next rows)
+def test_splitmix64_published_first_output():
+    """SplitMix64 started at 0: its first output is 0xE220A8397B1DCDAF (the value the
+    generator's reference implementation produces)."""
+    assert O.splitmix64(0, 1) == 0xE220A8397B1DCDAF
+
+
+def test_sampler_low_temperature_is_argmax():
+    rng = np.random.default_rng(3)
+    for trial in range(20):
+        z = rng.standard_normal(50)
+        k, lo, hi, thr, tot = O.sample_token(z, 50, 1e-4, 1234 + trial, trial)
+        assert k == int(np.argmax(z))
+
+
+def test_sampler_frequencies_match_softmax():
+    """Over 20000 draws (sequence index b varying) the frequencies of a 5-way softmax
+    match its probabilities (chi-square, 4 degrees of freedom, far below the 0.1%
+    critical value 18.5)."""
+    z = np.array([0.3, -1.0, 2.0, 0.0, 1.1])
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    n = 20000
+    counts = np.zeros(5)
+    for b in range(n):
+        counts[O.sample_token(z, 5, 1.0, 77, b)[0]] += 1
+    chi2 = float((((counts - n * p) ** 2) / (n * p)).sum())
+    assert chi2 < 18.5, (chi2, counts / n, p)
+
+
+def test_sampler_ignores_padded_columns():
+    z = np.array([0.0, 0.0, 50.0, 50.0])          # columns 2, 3 are padding (V = 2)
+    for b in range(100):
+        assert O.sample_token(z, 2, 1.0, 5, b)[0] in (0, 1)
