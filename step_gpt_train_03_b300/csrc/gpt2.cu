@@ -62,6 +62,8 @@ struct GPT2 {
     size_t partials_floats;
     float *enc_partial;                // (BT, C) encoder-backward partial sums
     unsigned* sorted_keys;             // (BT)
+    float* red_arena;                  // per-reduction partials of one backward pass (deferred sums)
+    size_t red_arena_floats;
     int *tokens, *targets;             // staging copies of the last batch
     unsigned* err;
     // state
@@ -145,6 +147,13 @@ static size_t plan(GPT2* m, char* base) {
     if (tc_pf > pf) pf = tc_pf;
     m->partials_floats = pf;
     m->partials = (float*)take(pf * 4);
+    // deferred column sums: (2L+1) layernorm backwards of up to 3C-wide partials over at
+    // most 296 blocks, 2L bias gradients of up to 4C-wide partials over 128-row chunks
+    {
+        const size_t R = std::max<size_t>(1, std::min<size_t>(1024, (BT + 127) / 128));
+        m->red_arena_floats = (2 * L + 1) * 296 * 3 * C + 2 * L * R * 4 * C;
+        m->red_arena = (float*)take(m->red_arena_floats * 4);
+    }
     m->enc_partial = (float*)take(BT * C * 4);
     m->sorted_keys = (unsigned*)take(BT * 4);
     m->tokens = (int*)take(BT * 4);
@@ -416,6 +425,40 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
 }
 
 // two resident blocks per SM on a 148-SM part; each warp then walks ~7 rows at N = 16384
+// Column sums deferred to the end of a backward pass: each reduction gets its own
+// partial region from the arena and a segment in the batch; flush() reduces them all in
+// one launch (the per-segment arithmetic is column_reduce4's, so the sums are the same).
+struct RedQueue {
+    float* arena;
+    size_t cap, used;
+    RedBatch batch;
+    int n;
+    int max_w;
+    // a partial region of `floats` (16-byte aligned), or nullptr when the arena is full
+    float* take(size_t floats) {
+        const size_t need = (floats + 3) & ~(size_t)3;
+        if (!arena || used + need > cap || n >= RED_MAX_SEGS) return nullptr;
+        float* p = arena + used;
+        used += need;
+        return p;
+    }
+    void push(const float* partial, float* out0, float* out1, float* out2, int split, int G, int W) {
+        batch.seg[n++] = RedSeg{partial, out0, out1, out2, split, G, W, 0};
+        max_w = std::max(max_w, W);
+    }
+};
+static int red_flush(cudaStream_t s, RedQueue& q) {
+    if (q.n == 0) return GPT2_OK;
+    ProfScope ps(s, PC_MISC, 0, 0);
+    rt_note_launches(1);
+    column_reduce_batch_kernel<<<dim3(ceil_div(q.max_w, 32), q.n), 256, 0, s>>>(q.batch);
+    CK(cudaGetLastError());
+    q.n = 0;
+    q.used = 0;
+    q.max_w = 0;
+    return GPT2_OK;
+}
+
 // column sums of a (G x W) fp32 partial matrix into out0/out1/out2 (see column_reduce_kernel)
 static void column_reduce_any(cudaStream_t s, float* out0, float* out1, int split, const float* partial, int G,
                               int W, float* out2) {
@@ -461,14 +504,18 @@ static int ln_backward_launch(cudaStream_t s, int& G, T* dinp, float* partial, c
 template <typename T>
 static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
                        const T* w, const float* mean, const float* rstd, int N, int C,
-                       float* partial, size_t partial_floats, float* dsum = nullptr, unsigned* err = nullptr) {
+                       float* partial, size_t partial_floats, float* dsum = nullptr, unsigned* err = nullptr,
+                       RedQueue* q = nullptr) {
     constexpr int EPV = Vec<T>::N;
     const int nv = ceil_div(C / EPV, 32);
     int G = ln_backward_grid(N);
     const int W = dsum ? 3 : 2;
-    if ((size_t)G * W * C > partial_floats) return GPT2_EINVAL;
+    // with a queue the partials get their own region and the sums are deferred
+    float* qpart = (q && (W * C) % 4 == 0) ? q->take((size_t)G * W * C) : nullptr;
+    if (qpart) partial = qpart;
+    else if ((size_t)G * W * C > partial_floats) return GPT2_EINVAL;
     ProfScope ps(s, PC_LAYERNORM_BWD, 0, 4.0 * N * C * sizeof(T) + 8.0 * N + 3.0 * C * sizeof(T) + 8.0 * C);
-    rt_note_launches(2);
+    rt_note_launches(qpart ? 1 : 2);
     int rc = GPT2_EUNSUPPORTED;
     switch (nv) {
 #define LNB_CASE(k)                                                                                            \
@@ -482,6 +529,10 @@ static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* d
         default: break;
     }
     if (rc != GPT2_OK) return rc;
+    if (qpart) {
+        q->push(partial, dw, db, dsum, C, G, W * C);         // G may have shrunk in the launcher
+        return GPT2_OK;
+    }
     column_reduce_any(s, dw, db, C, partial, G, W * C, dsum);
     CK(cudaGetLastError());
     return GPT2_OK;
@@ -496,16 +547,22 @@ static void colsum_shape(int M, int N, int* R, int* rows) {
 
 template <typename T>
 static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* partial,
-                  size_t partial_floats) {
+                  size_t partial_floats, RedQueue* q = nullptr) {
     int R, rows;
     colsum_shape(M, N, &R, &rows);
-    if ((size_t)R * N > partial_floats) return GPT2_EINVAL;
+    float* qpart = (q && N % 4 == 0) ? q->take((size_t)R * N) : nullptr;
+    if (qpart) partial = qpart;
+    else if ((size_t)R * N > partial_floats) return GPT2_EINVAL;
     ProfScope ps(s, PC_BIAS_GRAD, 0, (double)M * N * sizeof(T) + 8.0 * N);
-    rt_note_launches(2);
+    rt_note_launches(qpart ? 1 : 2);
     constexpr int EPV = Vec<T>::N;
     if (N % EPV) colsum_partial_scalar_kernel<T><<<dim3(ceil_div(N, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
     else colsum_partial_kernel<T><<<dim3(ceil_div(N / EPV, 32), R), CS_WARPS * 32, 0, s>>>(partial, x, M, N, rows);
     CK(cudaGetLastError());
+    if (qpart) {
+        q->push(partial, out, out, nullptr, N, R, N);
+        return GPT2_OK;
+    }
     column_reduce_any(s, out, out, N, partial, R, N, nullptr);
     CK(cudaGetLastError());
     return GPT2_OK;
@@ -708,6 +765,12 @@ static int backward_impl(GPT2* m) {
     const T* dlogits = (const T*)m->logits;
     float* part = m->partials;
     const size_t pf = m->partials_floats;
+    RedQueue rq;
+    rq.arena = m->red_arena;
+    rq.cap = m->red_arena_floats;
+    rq.used = 0;
+    rq.n = 0;
+    rq.max_w = 0;
     // LM head (tied): dlnf = dlogits wte; dwte += dlogits^T lnf
     RC(mm_backward_dx<T>(m, s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr));
     RC(mm_backward_dw<T>(m, s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C));
@@ -716,7 +779,7 @@ static int backward_impl(GPT2* m) {
     // the updated residual gradient is d(res3) of the last layer: its column sums are
     // that layer's MLP-projection bias gradient
     RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf,
-                      G(P_FCPROJB) + (L - 1) * C, m->err));
+                      G(P_FCPROJB) + (L - 1) * C, m->err, &rq));
     for (int l = L - 1; l >= 0; l--) {
         const T* x_in = (l == 0) ? (const T*)m->encoded : (const T*)m->res3 + (l - 1) * BTmax * C;
         const T* ln1 = (const T*)m->ln1 + l * BTmax * C;
@@ -734,10 +797,10 @@ static int backward_impl(GPT2* m) {
         // MLP input projection
         RC(mm_backward_dx<T>(m, s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C));
-        RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf));
+        RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
-                          G(P_ATTPROJB) + l * C, m->err));      // d(res2) column sums: attention-projection bias
+                          G(P_ATTPROJB) + l * C, m->err, &rq));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
         RC(mm_backward_dx<T>(m, s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C));
@@ -746,11 +809,14 @@ static int backward_impl(GPT2* m) {
         // qkv projection
         RC(mm_backward_dx<T>(m, s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr));
         RC(mm_backward_dw<T>(m, s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C));
-        RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf));
+        RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq));
         // ln1 (dresid becomes d x_l)
         RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
-                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err));   // d(res3) of layer l-1
+                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err, &rq));   // d(res3) of layer l-1
+        if (rq.n + 4 > RED_MAX_SEGS) RC(red_flush(s, rq));
     }
+    // the deferred column sums (layernorm weight and bias gradients, linear biases)
+    RC(red_flush(s, rq));
     // encoder: deterministic scatter-add into dwte (ids sorted in the forward), dwpe
     ProfScope ps(s, PC_ENCODER_BWD, 0, (double)BT * C * sizeof(T) + 8.0 * BT * C + 8.0 * Tn * C);
     rt_note_launches(3);

@@ -560,12 +560,12 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int spl
 // The same sums for W a multiple of 4 (16-byte aligned rows): a 256-thread block takes
 // 32 columns as 8 float4 packets; thread (p, g) adds rows g, g+32, g+64, ... of packet p
 // (four loads in flight), then the 32 group sums of each column are added in group order.
-__global__ void __launch_bounds__(256)
-column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
-                      const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
+__device__ __forceinline__ void column_reduce4_block(float* __restrict__ out0, float* __restrict__ out1, int split,
+                                                     const float* __restrict__ partial, int G, int W,
+                                                     float* __restrict__ out2, int bx) {
     __shared__ float sm[32][33];
     const int p = threadIdx.x & 7, g = threadIdx.x >> 3;
-    const int w = blockIdx.x * 32 + p * 4;
+    const int w = bx * 32 + p * 4;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (w < W) {
         const float* col = partial + w;
@@ -584,7 +584,7 @@ column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int sp
     }
     sm[g][p * 4 + 0] = s.x; sm[g][p * 4 + 1] = s.y; sm[g][p * 4 + 2] = s.z; sm[g][p * 4 + 3] = s.w;
     __syncthreads();
-    const int t = threadIdx.x, wc = blockIdx.x * 32 + t;
+    const int t = threadIdx.x, wc = bx * 32 + t;
     if (t < 32 && wc < W) {
         float acc = 0.f;
 #pragma unroll 8
@@ -593,6 +593,29 @@ column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int sp
         else if (!out2 || wc < 2 * split) out1[wc - split] += acc;
         else out2[wc - 2 * split] += acc;
     }
+}
+__global__ void __launch_bounds__(256)
+column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
+                      const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
+    column_reduce4_block(out0, out1, split, partial, G, W, out2, blockIdx.x);
+}
+
+// The same reduction for many (G x W) partial matrices in one launch: blockIdx.y picks
+// the segment (the step's layernorm and bias-gradient reductions, all deferred to the
+// end of the backward pass, since only the optimiser reads those gradients).
+struct RedSeg {
+    const float* partial;
+    float *out0, *out1, *out2;
+    int split, G, W, pad;
+};
+#define RED_MAX_SEGS 128
+struct RedBatch {
+    RedSeg seg[RED_MAX_SEGS];
+};
+__global__ void __launch_bounds__(256) column_reduce_batch_kernel(const __grid_constant__ RedBatch b) {
+    const RedSeg& sg = b.seg[blockIdx.y];
+    if ((int)blockIdx.x * 32 >= sg.W) return;
+    column_reduce4_block(sg.out0, sg.out1, sg.split, sg.partial, sg.G, sg.W, sg.out2, blockIdx.x);
 }
 
 // ============================================================== column sums (bias grads)
