@@ -62,6 +62,8 @@ struct GPT2 {
     size_t partials_floats;
     float *enc_partial;                // (BT, C) encoder-backward partial sums
     unsigned* sorted_keys;             // (BT)
+    unsigned* sort_tmp;                // (BT) keys between radix passes
+    unsigned* sort_hist;               // (256 x ceil(BT / 1024)) digit counts, then offsets
     float* red_arena;                  // per-reduction partials of one backward pass (deferred sums)
     size_t red_arena_floats;
     int *tokens, *targets;             // staging copies of the last batch
@@ -156,6 +158,8 @@ static size_t plan(GPT2* m, char* base) {
     }
     m->enc_partial = (float*)take(BT * C * 4);
     m->sorted_keys = (unsigned*)take(BT * 4);
+    m->sort_tmp = (unsigned*)take(BT * 4);
+    m->sort_hist = (unsigned*)take(256 * ((BT + RADIX_BLOCK - 1) / RADIX_BLOCK) * 4);
     m->tokens = (int*)take(BT * 4);
     m->targets = (int*)take(BT * 4);
     m->err = (unsigned*)take(16);
@@ -173,7 +177,7 @@ static int validate_cfg(const GPT2Config* c, int maxB, int maxT, int prec) {
     if (c->padded_vocab_size % 64 != 0) return GPT2_EINVAL;
     if (c->max_seq_len < 1 || maxB < 1 || maxT < 1 || maxT > c->max_seq_len) return GPT2_EINVAL;
     const long long BT = (long long)maxB * maxT;
-    if (BT > 32768) return GPT2_EUNSUPPORTED;                       // encoder-backward sort
+    if (BT > 32768) return GPT2_EUNSUPPORTED;                       // index arithmetic checked up to here
     if ((long long)(c->padded_vocab_size + 1) * BT > 0xffffffffLL) return GPT2_EUNSUPPORTED;
     return GPT2_OK;
 }
@@ -258,11 +262,6 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     m->gexec = nullptr;
     m->g_adam = nullptr;
     m->g_kernels = 0;
-    if (cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             32768 * (int)sizeof(unsigned)) != cudaSuccess) {
-        free(m);
-        return GPT2_ECUDA;
-    }
     int rc = launch_zero(m->stream, m->params, (size_t)m->n_flat * 4 * 4);   // params, grads, m, v
     if (rc == GPT2_OK) rc = launch_zero(m->stream, m->err, 16);
     if (rc == GPT2_OK && m->wbf) rc = launch_zero(m->stream, m->wbf, m->n_flat * 2);
@@ -738,13 +737,25 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
             mean_loss_kernel<<<1, 1024, 0, s>>>(m->loss, m->losses, BT, m->err);
             CK(cudaGetLastError());
         }
-        // order the token positions by id now; the encoder backward consumes it
-        int NP = 1;
-        while (NP < BT) NP <<= 1;
-        ProfScope ps2(s, PC_ENCODER_BWD, 0, 8.0 * BT);
-        rt_note_launches(1);
-        encoder_sort_kernel<<<1, 1024, NP * sizeof(unsigned), s>>>(m->sorted_keys, m->tokens, BT, m->V, NP);
-        CK(cudaGetLastError());
+        // order the token positions by id now; the encoder backward consumes it.  One
+        // 8-bit radix pass per byte of the largest id (V stands for invalid ids); the
+        // passes alternate buffers so that the last one writes sorted_keys.
+        int npass = 0;
+        while (npass < 4 && (m->V >> (8 * npass)) > 0) npass++;
+        const int nblk = ceil_div(BT, RADIX_BLOCK);
+        ProfScope ps2(s, PC_ENCODER_BWD, 0, 8.0 * BT * npass);
+        const unsigned* src = nullptr;
+        for (int p = 0; p < npass; p++) {
+            unsigned* dst = ((npass - 1 - p) & 1) ? m->sort_tmp : m->sorted_keys;
+            rt_note_launches(3);
+            radix_hist_kernel<<<nblk, RADIX_BLOCK, 0, s>>>(m->sort_hist, src, m->tokens, BT, m->V, 8 * p, nblk);
+            CK(cudaGetLastError());
+            radix_scan_kernel<<<1, RADIX_BLOCK, 0, s>>>(m->sort_hist, 256 * nblk);
+            CK(cudaGetLastError());
+            radix_scatter_kernel<<<nblk, RADIX_BLOCK, 0, s>>>(dst, src, m->tokens, m->sort_hist, BT, m->V, 8 * p, nblk);
+            CK(cudaGetLastError());
+            src = dst;
+        }
     }
     return GPT2_OK;
 }

@@ -37,37 +37,91 @@ __global__ void encoder_forward_kernel(T* __restrict__ out, const int* __restric
     store_vec(out + (size_t)bt * C + cv * EPV, o);
 }
 
-// Sort keys (id * BT + position) ascending in one CTA (bitonic network in shared
-// memory).  Invalid ids get key V*BT + position so they sort after every valid one.
-// Equal ids thus become contiguous runs ordered by position, which fixes the order of
-// the scatter-add sums below.  NP = next power of two >= BT, NP <= 32768.
-__global__ void encoder_sort_kernel(unsigned* __restrict__ sorted, const int* __restrict__ tok,
-                                    int BT, int V, int NP) {
-    extern __shared__ unsigned keys[];
-    for (int i = threadIdx.x; i < NP; i += blockDim.x) {
-        unsigned k = 0xffffffffu;
-        if (i < BT) {
-            int id = tok[i];
-            if (id < 0 || id >= V) id = V;
-            k = (unsigned)id * (unsigned)BT + (unsigned)i;
+// Sort keys (id * BT + position) ascending; invalid ids count as V, so they sort after
+// every valid one.  Equal ids thus become contiguous runs ordered by position, which
+// fixes the order of the scatter-add sums below.  The sort is a stable LSD radix sort
+// on the id alone (the input is already in position order), 8 bits per pass, 1024 keys
+// per block:
+// per-block digit counts (digit-major), one exclusive scan, then a stable scatter --
+// a key's rank among equal digits is its rank in its warp (matching lanes) plus the
+// counts of that digit in the block's earlier warps plus the scanned offset.  Pass 0
+// reads the tokens (key = id * BT + position, invalid ids as V); later passes read
+// the previous pass's keys.
+#define RADIX_BLOCK 1024
+__device__ __forceinline__ unsigned radix_key(const unsigned* keys_in, const int* tok, int e, int BT, int V) {
+    if (keys_in) return keys_in[e];
+    int id = tok[e];
+    if (id < 0 || id >= V) id = V;
+    return (unsigned)id * (unsigned)BT + (unsigned)e;
+}
+__global__ void __launch_bounds__(RADIX_BLOCK)
+radix_hist_kernel(unsigned* __restrict__ hist, const unsigned* __restrict__ keys_in, const int* __restrict__ tok,
+                  int BT, int V, int shift, int nblk) {
+    __shared__ unsigned cnt[256];
+    if (threadIdx.x < 256) cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const int e = blockIdx.x * RADIX_BLOCK + threadIdx.x;
+    if (e < BT) atomicAdd(&cnt[((radix_key(keys_in, tok, e, BT, V) / (unsigned)BT) >> shift) & 255u], 1u);
+    __syncthreads();
+    if (threadIdx.x < 256) hist[threadIdx.x * nblk + blockIdx.x] = cnt[threadIdx.x];
+}
+// exclusive scan of n counts, in place (one block, fixed order)
+__global__ void __launch_bounds__(RADIX_BLOCK) radix_scan_kernel(unsigned* __restrict__ hist, int n) {
+    __shared__ unsigned wsum[32];
+    const int per = (n + RADIX_BLOCK - 1) / RADIX_BLOCK;
+    const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
+    unsigned local = 0;
+    for (int i = b0; i < b1; i++) local += hist[i];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned inc = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned w = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
         }
-        keys[i] = k;
+        wsum[lane] = w;
     }
     __syncthreads();
-    for (int k = 2; k <= NP; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < NP; i += blockDim.x) {
-                int p = i ^ j;
-                if (p > i) {
-                    unsigned a = keys[i], b = keys[p];
-                    bool up = (i & k) == 0;
-                    if ((a > b) == up) { keys[i] = b; keys[p] = a; }
-                }
-            }
-            __syncthreads();
+    unsigned run = (warp > 0 ? wsum[warp - 1] : 0u) + inc - local;
+    for (int i = b0; i < b1; i++) {
+        const unsigned c = hist[i];
+        hist[i] = run;
+        run += c;
+    }
+}
+__global__ void __launch_bounds__(RADIX_BLOCK)
+radix_scatter_kernel(unsigned* __restrict__ keys_out, const unsigned* __restrict__ keys_in, const int* __restrict__ tok,
+                     const unsigned* __restrict__ hist, int BT, int V, int shift, int nblk) {
+    __shared__ unsigned wcnt[RADIX_BLOCK / 32][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < (RADIX_BLOCK / 32) * 256; i += RADIX_BLOCK) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int e = blockIdx.x * RADIX_BLOCK + threadIdx.x;
+    const bool valid = e < BT;
+    const unsigned key = valid ? radix_key(keys_in, tok, e, BT, V) : 0u;
+    const unsigned d = valid ? (((key / (unsigned)BT) >> shift) & 255u) : 256u + lane;   // unique for padding lanes
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const unsigned rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) wcnt[warp][d] = __popc(peers);
+    __syncthreads();
+    // counts of each digit in the earlier warps of the block (thread t: digit t)
+    if (threadIdx.x < 256) {
+        unsigned run = 0;
+        for (int w = 0; w < RADIX_BLOCK / 32; w++) {
+            const unsigned c = wcnt[w][threadIdx.x];
+            wcnt[w][threadIdx.x] = run;
+            run += c;
         }
     }
-    for (int i = threadIdx.x; i < BT; i += blockDim.x) sorted[i] = keys[i];
+    __syncthreads();
+    if (valid) keys_out[hist[d * nblk + blockIdx.x] + wcnt[warp][d] + rank] = key;
 }
 
 #define ENC_CHUNK 32
@@ -167,7 +221,16 @@ __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float
     const int e = lo;
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
         float s = partial[(size_t)i * C + c];
-        for (int b = c0 + ENC_CHUNK; b < e; b += ENC_CHUNK) s += partial[(size_t)b * C + c];
+        int b = c0 + ENC_CHUNK;
+        // eight partials in flight, added in chunk order
+        for (; b + 7 * ENC_CHUNK < e; b += 8 * ENC_CHUNK) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) v[k] = partial[(size_t)(b + k * ENC_CHUNK) * C + c];
+#pragma unroll
+            for (int k = 0; k < 8; k++) s += v[k];
+        }
+        for (; b < e; b += ENC_CHUNK) s += partial[(size_t)b * C + c];
         dwte[(size_t)id * C + c] += s;
     }
 }
