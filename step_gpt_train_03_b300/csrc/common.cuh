@@ -43,6 +43,13 @@ template <> struct Vec<bf16> {
         bf16* p = reinterpret_cast<bf16*>(&v);
         p[i] = __float2bfloat16_rn(x);
     }
+    // elements i, i+1 (i even): one packed conversion each way
+    __device__ __forceinline__ float2 get2(int i) const {
+        return __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&v)[i >> 1]);
+    }
+    __device__ __forceinline__ void set2(int i, float x, float y) {
+        reinterpret_cast<__nv_bfloat162*>(&v)[i >> 1] = __floats2bfloat162_rn(x, y);
+    }
 };
 
 template <typename T> __device__ __forceinline__ Vec<T> load_vec(const T* p) {

@@ -61,23 +61,33 @@ struct TcEpi {
     long ldo;           // row stride of out and aux (elements)
 };
 
+// Staging buffers per epilogue warp: four for the GELU epilogues of a CTA pair (two
+// stores per piece forward, a load ahead of each store backward, so two buffers leave
+// the warp waiting on its own stores), else two.
+template <int EPI, int CL>
+struct TcBufs {
+    static constexpr int value = (CL == 2 && (EPI == EPI_GELU || EPI == EPI_GELU_BWD)) ? 4 : 2;
+};
+
 // CL = 1: one CTA holds a 128 x 64 A and a BN x 64 B block per stage, 4 stages.
 // CL = 2 (CTA pair): each CTA holds its 128 x 64 A block and half of the B block, so a
-// stage is 2/3 the size and 6 stages fit.
-template <int BN, int CL = 1>
+// stage is 2/3 the size and 6 stages fit (5 with four staging buffers per warp).
+template <int BN, int CL = 1, int NB = 2>
 struct TcSmem {
-    static constexpr int STAGES = CL == 2 ? 6 : TC_STAGES;
+    static constexpr int STAGES = CL == 2 ? (NB > 2 ? 5 : 6) : TC_STAGES;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
     static constexpr int B_BYTES = BN / CL * TC_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // two 2 KB staging buffers (32 rows x 64 bytes) per epilogue warp
+    // NB 2 KB staging buffers (32 rows x 64 bytes) per epilogue warp
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int STG_BYTES = 2048;
-    static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * 2 * STG_BYTES;
-    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[epilogue warps][2 buffers];
+    static constexpr int BAR_OFF = STG_OFF + TC_EPI_WARPS * NB * STG_BYTES;
+    // full[S], empty[S], acc_full[2], acc_empty[2], done, aux[epilogue warps][NB buffers];
     // tmem address, abort flag
-    static constexpr int NBAR = 2 * STAGES + 5 + 2 * TC_EPI_WARPS;
+    static constexpr int NBAR = 2 * STAGES + 5 + NB * TC_EPI_WARPS;
     static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
+    static_assert(TOTAL <= 232448, "shared memory of one CTA");
+    static_assert(NB == 2 || NB == 4, "staging ring");
 };
 
 // byte offset of 16-byte unit j (0..3) of row r in a 64B-swizzled staging buffer of
@@ -101,7 +111,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux, int M, int N,
                int K, int splits, int m_fast, TcEpi ep, unsigned* err) {
-    using S = TcSmem<BN, CL>;
+    constexpr int NB = TcBufs<EPI, CL>::value;
+    using S = TcSmem<BN, CL, NB>;
     constexpr int STAGES = S::STAGES;
     constexpr int NACC = CL == 2 ? TC_PAIR_NACC : 2;
     extern __shared__ uint8_t smem_raw[];
@@ -112,7 +123,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     uint64_t* aux_bar = done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * TC_EPI_WARPS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + NB * TC_EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,7 +148,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < STAGES; i++) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; i++) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], CL * TC_EPI_WARPS); }
         mbar_init(done, 1);
-        for (int i = 0; i < 2 * TC_EPI_WARPS; i++) mbar_init(&aux_bar[i], 1);
+        for (int i = 0; i < NB * TC_EPI_WARPS; i++) mbar_init(&aux_bar[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
@@ -299,25 +310,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int ew = warp - 2;                       // epilogue warp 0..7
         const int lane_grp = warp & 3;                 // TMEM lanes 32*lane_grp .. +31
         const int cbase = (ew >> 2) * (BN / 2);        // this warp's half of the tile's columns
-        uint8_t* stg = smem + S::STG_OFF + ew * 2 * S::STG_BYTES;
+        uint8_t* stg = smem + S::STG_OFF + ew * NB * S::STG_BYTES;
         constexpr bool AUX_IN = (EPI == EPI_RESID || EPI == EPI_GELU_BWD);
         constexpr int NPAIR = BN / 128;                // 64-column accumulator loads per warp per tile
         constexpr int NPC = 2 * NPAIR;                 // 32-column pieces per warp per tile
-        uint64_t* auxb = &aux_bar[ew * 2];             // one barrier per staging buffer
+        constexpr int AHEAD = NB / 2;                  // input pieces loaded ahead of the one in use
+        uint64_t* auxb = &aux_bar[ew * NB];            // one barrier per staging buffer
         uint32_t aux_ph = 0;                           // bit b: phase of buffer b's barrier
         uint32_t aux_pend = 0;                         // bit b: a load into buffer b not yet waited for
-        int nbuf = 0;                                  // staging buffer in use: nbuf & 1
+        int nbuf = 0;                                  // staging buffer in use: nbuf % NB
         int local = 0;
         bool alive = true;
-        // residual / pre-activation inputs: the load of piece pc of unit uu goes to buffer
-        // kb once every store still reading a staging buffer has finished
-        auto aux_issue = [&](int uu, int pc, int kb) {
-            if (lane == 0) {
+        // residual / pre-activation inputs: with inputs, every tile of this warp is NPC
+        // pieces and piece g uses buffer g % NB.  The load of piece g goes out once the
+        // store of piece g - NB (the buffer's last user) has read it; the stores of the
+        // pieces after that one may still be in flight.
+        auto aux_issue = [&](int g) {
+            const int uu = ufirst + (g / NPC) * ustep, pc = g % NPC, kb = g % NB;
+            if (lane == 0 && uu < units) {
                 int usp, umt, unt;
                 decode(uu, usp, umt, unt);
                 const int col = unt * BN + cbase + pc * 32;
                 const int row0 = umt * TC_BM + lane_grp * 32;
-                bulk_wait_read<0>();
+                bulk_wait_read<NB - AHEAD - 1>();
                 aux_pend |= 1u << kb;
                 mbar_expect_tx(&auxb[kb], S::STG_BYTES);
                 tma_load_2d(stg + kb * S::STG_BYTES, &tmAux, &auxb[kb], col, row0);
@@ -337,7 +352,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         };
         const uint32_t acc_empty_lead = CL > 1 ? mapa_shared(acc_empty, 0) : 0;
-        if (AUX_IN && ufirst < units) aux_issue(ufirst, 0, 0);
+        if constexpr (AUX_IN)
+            for (int g = 0; g < AHEAD; g++) aux_issue(g);
         for (int u = ufirst; u < units && alive; u += ustep, local++) {
             int sp, mt, nt;
             decode(u, sp, mt, nt);
@@ -367,14 +383,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     float* v = v2 + 32 * h;
-                    const int pc = 2 * pi + h;                 // piece index within this warp's half
                     const int col = nt * BN + c + 32 * h;      // first global column of the piece
                     if constexpr (EPI == EPI_ACC_F32 || EPI == TC_EPI_PARTIAL) {
                         if (col < N) {
 #pragma unroll
                             for (int q = 0; q < 2; q++) {          // 16 fp32 columns per 64-byte row
-                                uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
-                                if (lane == 0) bulk_wait_read<1>();
+                                uint8_t* sb = stg + (nbuf % NB) * S::STG_BYTES;
+                                if (lane == 0) bulk_wait_read<NB - 1>();
                                 __syncwarp();
 #pragma unroll
                                 for (int j = 0; j < 4; j++)
@@ -392,11 +407,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             }
                         }
                     } else if constexpr (AUX_IN) {
-                        // this piece's input was loaded into buffer nbuf & 1 ahead of time; start
-                        // the next piece's (or the next tile's first) load into the other buffer
-                        const int kb = nbuf & 1;
-                        if (pc + 1 < NPC) aux_issue(u, pc + 1, kb ^ 1);
-                        else if (u + ustep < units) aux_issue(u + ustep, 0, kb ^ 1);
+                        // this piece's input was loaded into buffer nbuf % NB ahead of time
+                        // (nbuf counts this warp's pieces); start the load AHEAD pieces on
+                        const int kb = nbuf % NB;
+                        aux_issue(nbuf + AHEAD);
                         int oka = 1;
                         if (lane == 0) oka = mbar_wait(&auxb[kb], (aux_ph >> kb) & 1, abort_flag, err) ? 1 : 0;
                         oka = __shfl_sync(0xffffffffu, oka, 0);
@@ -411,9 +425,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             Vec<bf16> a, o;
                             a.v = *reinterpret_cast<const uint4*>(sb + stg_off(lane, j));
 #pragma unroll
-                            for (int e = 0; e < 8; e++) {
-                                if constexpr (EPI == EPI_RESID) o.set(e, v[8 * j + e] + a.get(e));
-                                else o.set(e, v[8 * j + e] * gelu_grad_fast(a.get(e)));
+                            for (int e = 0; e < 8; e += 2) {
+                                const float2 x = a.get2(e), acc2 = make_float2(v[8 * j + e], v[8 * j + e + 1]);
+                                const float2 r = (EPI == EPI_RESID) ? __fadd2_rn(acc2, x) : __fmul2_rn(acc2, gelu_grad2_fast(x));
+                                o.set2(e, r.x, r.y);
                             }
                             *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
                         }
@@ -424,8 +439,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     } else {
                         if (col < N) {
                             add_bias(v, col);
-                            uint8_t* sb = stg + (nbuf & 1) * S::STG_BYTES;
-                            if (lane == 0) bulk_wait_read<1>();
+                            uint8_t* sb = stg + (nbuf % NB) * S::STG_BYTES;
+                            if (lane == 0) bulk_wait_read<NB - 1>();
                             __syncwarp();
                             if constexpr (EPI == EPI_GELU) {
                                 // pre-activation out first, then the activation into the other buffer
@@ -433,24 +448,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 for (int j = 0; j < 4; j++) {
                                     Vec<bf16> o;
 #pragma unroll
-                                    for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                                    for (int e = 0; e < 8; e += 2) o.set2(e, v[8 * j + e], v[8 * j + e + 1]);
                                     *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
 #pragma unroll
-                                    for (int e = 0; e < 8; e++) v[8 * j + e] = gelu_fast(o.get(e));
+                                    for (int e = 0; e < 8; e += 2) {
+                                        const float2 g = gelu2_fast(o.get2(e));      // of the stored pre-activation
+                                        v[8 * j + e] = g.x;
+                                        v[8 * j + e + 1] = g.y;
+                                    }
                                 }
                                 fence_async_smem();
                                 __syncwarp();
                                 if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0); bulk_commit(); }
                                 nbuf++;
-                                sb = stg + (nbuf & 1) * S::STG_BYTES;
-                                if (lane == 0) bulk_wait_read<1>();
+                                sb = stg + (nbuf % NB) * S::STG_BYTES;
+                                if (lane == 0) bulk_wait_read<NB - 1>();
                                 __syncwarp();
                             }
 #pragma unroll
                             for (int j = 0; j < 4; j++) {
                                 Vec<bf16> o;
 #pragma unroll
-                                for (int e = 0; e < 8; e++) o.set(e, v[8 * j + e]);
+                                for (int e = 0; e < 8; e += 2) o.set2(e, v[8 * j + e], v[8 * j + e + 1]);
                                 *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
                             }
                             fence_async_smem();
@@ -472,7 +491,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // its staging buffers (only possible after an abort), before the CTA retires
         if (lane == 0) {
             bulk_wait<0>();
-            for (int kb = 0; kb < 2; kb++) {
+            for (int kb = 0; kb < NB; kb++) {
                 if (!((aux_pend >> kb) & 1)) continue;
                 const long long t0 = clock64();
                 while (!mbar_try_wait(&auxb[kb], (aux_ph >> kb) & 1))
@@ -583,7 +602,7 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1>
 static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                      const CUtensorMap& tx, int M, int N, int K, int splits, const TcEpi& ep, unsigned* err) {
-    using SM = TcSmem<BN, CL>;
+    using SM = TcSmem<BN, CL, TcBufs<EPI, CL>::value>;
     static int max_clusters = 0;            // co-resident clusters of CL CTAs (0: not yet queried)
     auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN, CL>;
     cudaLaunchConfig_t cfg = {};

@@ -110,12 +110,30 @@ __device__ __forceinline__ float tanh_fast(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float gelu_fast(float x) {
-    return 0.5f * x * (1.0f + tanh_fast(GELU_K0 * (x + GELU_K1 * x * x * x)));
+// GELU, tanh form, and its derivative for two values at once in packed f32x2
+// arithmetic, constants folded.  With u = x^2 and g = K0 (x + K1 x^3) = x (K0 + K0 K1 u),
+// th = tanh(g):
+//   gelu(x)  = 0.5 x (1 + th)                 = hx + hx th,               hx = 0.5 x
+//   gelu'(x) = 0.5 (1 + th) + 0.5 x (1 - th^2) K0 (1 + 3 K1 u)
+//            = (0.5 + 0.5 th) + x (1 - th^2) (0.5 K0 + 1.5 K0 K1 u)
+#define GELU_C1 (GELU_K0 * GELU_K1)
+__device__ __forceinline__ float2 gelu_arg2(float2 x, float2 u) {
+    return __fmul2_rn(x, __ffma2_rn(make_float2(GELU_C1, GELU_C1), u, make_float2(GELU_K0, GELU_K0)));
 }
-__device__ __forceinline__ float gelu_grad_fast(float x) {
-    const float th = tanh_fast(GELU_K0 * (x + GELU_K1 * x * x * x));
-    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GELU_K0 * (1.0f + 3.0f * GELU_K1 * x * x);
+__device__ __forceinline__ float2 gelu2_fast(float2 x) {
+    const float2 g = gelu_arg2(x, __fmul2_rn(x, x));
+    const float2 th = make_float2(tanh_fast(g.x), tanh_fast(g.y));
+    const float2 hx = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(hx, th, hx);
+}
+__device__ __forceinline__ float2 gelu_grad2_fast(float2 x) {
+    const float2 u = __fmul2_rn(x, x);
+    const float2 g = gelu_arg2(x, u);
+    const float2 th = make_float2(tanh_fast(g.x), tanh_fast(g.y));
+    const float2 one = make_float2(1.0f, 1.0f), half = make_float2(0.5f, 0.5f);
+    const float2 sech2 = __ffma2_rn(make_float2(-th.x, -th.y), th, one);
+    const float2 dg = __ffma2_rn(make_float2(1.5f * GELU_C1, 1.5f * GELU_C1), u, make_float2(0.5f * GELU_K0, 0.5f * GELU_K0));
+    return __ffma2_rn(__fmul2_rn(x, sech2), dg, __ffma2_rn(half, th, half));
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
