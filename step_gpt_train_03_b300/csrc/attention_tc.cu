@@ -273,14 +273,16 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 // max over this warp's 64 columns, then over the pair
                 float mx;
                 {
-                    float v[32];
+                    // 64 -> 22 -> 8 -> 3 -> 1 with three-input maxima
+                    float a[22], b[8];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[32 + i]));
+                    for (int i = 0; i < 21; i++)
+                        a[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]), __uint_as_float(sr[3 * i + 2]));
+                    a[21] = __uint_as_float(sr[63]);
 #pragma unroll
-                    for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-                        for (int i = 0; i < w; i++) v[i] = fmaxf(v[i], v[i + w]);
-                    mx = v[0];
+                    for (int i = 0; i < 7; i++) b[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+                    b[7] = a[21];
+                    mx = fmax3(fmax3(b[0], b[1], b[2]), fmax3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
                 }
                 mx *= sl2;                                  // scaling by sl2 > 0 keeps the max
                 float* xm = xmax + (sc & 1) * 256;
@@ -316,21 +318,31 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                     const int c = half * 64 + h2 * 32;
                     float p[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) p[i] = ex2_fast(fmaf(__uint_as_float(sr[h2 * 32 + i]), sl2, -m));
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[h2 * 32 + i]), __uint_as_float(sr[h2 * 32 + i + 1])),
+                                                    make_float2(sl2, sl2), make_float2(-m, -m));
+                        p[i] = ex2_fast(a.x);
+                        p[i + 1] = ex2_fast(a.y);
+                    }
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int ch = (c >> 3) + k;
                         Vec<bf16> pv;
 #pragma unroll
-                        for (int e = 0; e < 8; e++) pv.set(e, p[8 * k + e]);
+                        for (int e = 0; e < 8; e += 2) pv.set2(e, p[8 * k + e], p[8 * k + e + 1]);
                         *reinterpret_cast<uint4*>(pbuf + (ch >> 3) * AT_TILE_BYTES + r * 128 +
                                                   (((ch & 7) ^ (r & 7)) << 4)) = pv.v;
                     }
+                    // pairwise tree sum; the levels with w >= 2 in packed pairs
 #pragma unroll
-                    for (int w = 16; w > 0; w >>= 1)
+                    for (int w = 16; w > 1; w >>= 1)
 #pragma unroll
-                        for (int i = 0; i < w; i++) p[i] += p[i + w];
-                    rs += p[0];
+                        for (int i = 0; i < w; i += 2) {
+                            const float2 x = __fadd2_rn(make_float2(p[i], p[i + 1]), make_float2(p[i + w], p[i + w + 1]));
+                            p[i] = x.x;
+                            p[i + 1] = x.y;
+                        }
+                    rs += p[0] + p[1];
                 }
                 l = l * corr + rs;
                 fence_async_smem();
@@ -366,7 +378,7 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 const int ch = half * 4 + k;
                 Vec<bf16> ov;
 #pragma unroll
-                for (int e = 0; e < 8; e++) ov.set(e, o[8 * k + e] * inv);
+                for (int e = 0; e < 8; e += 2) ov.set2(e, o[8 * k + e] * inv, o[8 * k + e + 1] * inv);
                 *reinterpret_cast<uint4*>(obuf + r * 128 + ((ch ^ (r & 7)) << 4)) = ov.v;
             }
             fence_async_smem();
@@ -697,9 +709,16 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            p[i] = ex2_fast(fmaf(__uint_as_float(s1[i]), sl2, -Lc[i]));
-                            ds[i] = p[i] * (__uint_as_float(s2[i]) - Dc[i]);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])),
+                                                        make_float2(sl2, sl2), make_float2(-Lc[i], -Lc[i + 1]));
+                            p[i] = ex2_fast(a.x);
+                            p[i + 1] = ex2_fast(a.y);
+                            const float2 d = __fadd2_rn(make_float2(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])),
+                                                        make_float2(-Dc[i], -Dc[i + 1]));
+                            const float2 g = __fmul2_rn(make_float2(p[i], p[i + 1]), d);
+                            ds[i] = g.x;
+                            ds[i + 1] = g.y;
                         }
                     }
                     // the products of tile gc-2, and an item's output store, must have
@@ -712,7 +731,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                         const int off = (ch >> 3) * AT_TILE_BYTES + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
                         Vec<bf16> dv;
 #pragma unroll
-                        for (int e = 0; e < 8; e++) dv.set(e, ds[8 * k + e]);
+                        for (int e = 0; e < 8; e += 2) dv.set2(e, ds[8 * k + e], ds[8 * k + e + 1]);
                         *reinterpret_cast<uint4*>(dsbuf + off) = dv.v;
                     }
                     if (DKV) {
@@ -767,12 +786,15 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 if (DKV) {
                     Vec<bf16> v2;
 #pragma unroll
-                    for (int e = 0; e < 8; e++) { v1.set(e, a1[8 * k + e]); v2.set(e, a2[8 * k + e] * 0.125f); }
+                    for (int e = 0; e < 8; e += 2) {
+                        v1.set2(e, a1[8 * k + e], a1[8 * k + e + 1]);
+                        v2.set2(e, a2[8 * k + e] * 0.125f, a2[8 * k + e + 1] * 0.125f);
+                    }
                     *reinterpret_cast<uint4*>(stg + off) = v1.v;                   // dV
                     *reinterpret_cast<uint4*>(stg + AT_TILE_BYTES + off) = v2.v;   // dK / 8
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; e++) v1.set(e, a1[8 * k + e] * 0.125f);
+                    for (int e = 0; e < 8; e += 2) v1.set2(e, a1[8 * k + e] * 0.125f, a1[8 * k + e + 1] * 0.125f);
                     *reinterpret_cast<uint4*>(stg + off) = v1.v;                   // dQ / 8
                 }
             }
