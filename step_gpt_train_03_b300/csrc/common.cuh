@@ -30,6 +30,10 @@ template <> struct Vec<float> {
     float4 v;
     __device__ __forceinline__ float get(int i) const { return (&v.x)[i]; }
     __device__ __forceinline__ void set(int i, float x) { (&v.x)[i] = x; }
+    __device__ __forceinline__ float2 get2(int i) const { return i == 0 ? make_float2(v.x, v.y) : make_float2(v.z, v.w); }
+    __device__ __forceinline__ void set2(int i, float x, float y) {
+        if (i == 0) { v.x = x; v.y = y; } else { v.z = x; v.w = y; }
+    }
 };
 template <> struct Vec<bf16> {
     static constexpr int N = 8;

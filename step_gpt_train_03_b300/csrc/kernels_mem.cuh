@@ -797,10 +797,21 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
 #pragma unroll
         for (int u = 0; u < XENT_U; u++) {
             const int vi = v0 + u * XENT_THREADS;
+            if (vi < nfull) {
+                // all columns real: packed pairs, three-input maxima
 #pragma unroll
-            for (int e = 0; e < EPV; e++) {
-                y[u][e] = (vi < nfull || (vi < nvec && vi * EPV + e < V)) ? p[u].get(e) * XENT_LOG2E : -INFINITY;
-                vmax = fmaxf(vmax, y[u][e]);
+                for (int e = 0; e < EPV; e += 2) {
+                    const float2 f = __fmul2_rn(p[u].get2(e), make_float2(XENT_LOG2E, XENT_LOG2E));
+                    y[u][e] = f.x;
+                    y[u][e + 1] = f.y;
+                    vmax = fmax3(vmax, f.x, f.y);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    y[u][e] = (vi < nvec && vi * EPV + e < V) ? p[u].get(e) * XENT_LOG2E : -INFINITY;
+                    vmax = fmaxf(vmax, y[u][e]);
+                }
             }
         }
         if (vmax == -INFINITY) continue;
@@ -809,7 +820,11 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
 #pragma unroll
         for (int u = 0; u < XENT_U; u++)
 #pragma unroll
-            for (int e = 0; e < EPV; e++) acc += xent_ex2(y[u][e] - nm);
+            for (int e = 0; e < EPV; e += 2) {
+                const float2 a = __fadd2_rn(make_float2(y[u][e], y[u][e + 1]), make_float2(-nm, -nm));
+                acc += xent_ex2(a.x);
+                acc += xent_ex2(a.y);
+            }
         mx2 = nm;
         sum = acc;
     }
@@ -845,12 +860,28 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
             const int vi = v0 + u * XENT_THREADS;
             if (vi >= nvec) break;
             Vec<T> o;
+            if (vi < nfull) {
+                // all columns real: (2^(z log2e - lse2) - [j == target]) * dloss in packed
+                // pairs, the target column (at most one packet of the row) redone apart
 #pragma unroll
-            for (int e = 0; e < EPV; e++) {
-                const int j = vi * EPV + e;
-                float d = 0.f;
-                if (j < V) d = (xent_ex2(fmaf(p[u].get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
-                o.set(e, d);
+                for (int e = 0; e < EPV; e += 2) {
+                    const float2 a = __ffma2_rn(p[u].get2(e), make_float2(XENT_LOG2E, XENT_LOG2E), make_float2(-lse2, -lse2));
+                    const float2 d = __fmul2_rn(make_float2(xent_ex2(a.x), xent_ex2(a.y)), make_float2(dloss, dloss));
+                    o.set2(e, d.x, d.y);
+                }
+                if ((unsigned)(tgt - vi * EPV) < (unsigned)EPV) {
+#pragma unroll
+                    for (int e = 0; e < EPV; e++)
+                        if (vi * EPV + e == tgt) o.set(e, (xent_ex2(fmaf(p[u].get(e), XENT_LOG2E, -lse2)) - 1.f) * dloss);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; e++) {
+                    const int j = vi * EPV + e;
+                    float d = 0.f;
+                    if (j < V) d = (xent_ex2(fmaf(p[u].get(e), XENT_LOG2E, -lse2)) - (j == tgt ? 1.f : 0.f)) * dloss;
+                    o.set(e, d);
+                }
             }
             store_vec(z + (size_t)vi * EPV, o);
         }
