@@ -491,14 +491,15 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
     if (lane == 0) { mbar_init(&bars[0], 1); mbar_init(&bars[1], 1); }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncwarp();
-    Vec<T> wv[NV];
+    float wf[NV][EPV];                                  // the weight, converted once
     float dwa[NV][EPV], dba[NV][EPV];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int vi = lane + 32 * i;
-        if (vi < nvec) wv[i] = load_vec(w + vi * EPV);
+        Vec<T> wv;
+        if (vi < nvec) wv = load_vec(w + vi * EPV);
 #pragma unroll
-        for (int e = 0; e < EPV; e++) { dwa[i][e] = 0.f; dba[i][e] = 0.f; }
+        for (int e = 0; e < EPV; e++) { wf[i][e] = vi < nvec ? wv.get(e) : 0.f; dwa[i][e] = 0.f; dba[i][e] = 0.f; }
         if (SUM && vi < nvec) wsum_zero<EPV>(wsum, nvec, vi);
     }
     const int step = gridDim.x * LN_WARPS;
@@ -538,20 +539,26 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
         const T* dys = xs + C;
         const T* cs = xs + 2 * C;
         float sg = 0.f, sgx = 0.f;
+        const float2 m2 = make_float2(-m, -m), r2 = make_float2(r, r);
 #pragma unroll
         for (int i = 0; i < NV; i++) {
             const int vi = lane + 32 * i;
             if (vi < nvec) {
                 Vec<T> xp = load_vec(xs + vi * EPV), dp = load_vec(dys + vi * EPV);
+                // element pairs in packed f32x2 arithmetic; the row sums keep their order
 #pragma unroll
-                for (int e = 0; e < EPV; e++) {
-                    const float xh = (xp.get(e) - m) * r;
-                    const float d = dp.get(e);
-                    const float g = d * wv[i].get(e);
-                    sg += g;
-                    sgx += g * xh;
-                    dwa[i][e] += d * xh;
-                    dba[i][e] += d;
+                for (int e = 0; e < EPV; e += 2) {
+                    const float2 xh = __fmul2_rn(__fadd2_rn(xp.get2(e), m2), r2);
+                    const float2 d = dp.get2(e);
+                    const float2 g = __fmul2_rn(d, make_float2(wf[i][e], wf[i][e + 1]));
+                    sg += g.x;
+                    sg += g.y;
+                    sgx = fmaf(g.x, xh.x, sgx);
+                    sgx = fmaf(g.y, xh.y, sgx);
+                    const float2 dw = __ffma2_rn(d, xh, make_float2(dwa[i][e], dwa[i][e + 1]));
+                    const float2 db = __fadd2_rn(make_float2(dba[i][e], dba[i][e + 1]), d);
+                    dwa[i][e] = dw.x; dwa[i][e + 1] = dw.y;
+                    dba[i][e] = db.x; dba[i][e + 1] = db.y;
                 }
             }
         }
@@ -564,10 +571,13 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
             if (vi < nvec) {
                 Vec<T> xp = load_vec(xs + vi * EPV), dp = load_vec(dys + vi * EPV), cur = load_vec(cs + vi * EPV), nv;
 #pragma unroll
-                for (int e = 0; e < EPV; e++) {
-                    const float xh = (xp.get(e) - m) * r;
-                    const float g = dp.get(e) * wv[i].get(e);
-                    nv.set(e, cur.get(e) + r * (g - mg - xh * mgx));
+                for (int e = 0; e < EPV; e += 2) {
+                    const float2 xh = __fmul2_rn(__fadd2_rn(xp.get2(e), m2), r2);
+                    const float2 g = __fmul2_rn(dp.get2(e), make_float2(wf[i][e], wf[i][e + 1]));
+                    // cur + r (g - mg - xh mgx)
+                    const float2 t = __ffma2_rn(make_float2(-xh.x, -xh.y), make_float2(mgx, mgx), __fadd2_rn(g, make_float2(-mg, -mg)));
+                    const float2 o = __ffma2_rn(r2, t, cur.get2(e));
+                    nv.set2(e, o.x, o.y);
                 }
                 store_vec(dx + vi * EPV, nv);
                 if (SUM) wsum_add<EPV>(wsum, nvec, vi, nv);
