@@ -93,20 +93,21 @@ __global__ void fa_backward_D(float* __restrict__ D, const bf16* __restrict__ do
     D[((size_t)b * NH + h) * Tn + t] = s;
 }
 
-// The same row sums for hs == 64: eight lanes per (b, t, h) row, one 16-byte packet of
-// dO and of O each, added across the eight lanes by shuffles (a warp reads four
-// consecutive rows: 512 contiguous bytes per load).
+// The same row sums for hs == 64: eight lanes per (b, h, t) row, one 16-byte packet of
+// dO and of O each, added across the eight lanes by shuffles (a warp reads four rows of
+// one head at consecutive t: four whole 128-byte segments per load).
 __global__ void fa_backward_D64(float* __restrict__ D, const bf16* __restrict__ dout,
                                 const bf16* __restrict__ out, int B, int Tn, int C, int NH) {
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row = gid >> 3;
+    // rows in D's own order, so a warp's four results are consecutive floats
+    // (B*NH*T < 2^31: 32-bit indices)
+    const int row = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3);
     const int sub = threadIdx.x & 7;
-    const bool valid = row < (long long)B * Tn * NH;
+    const bool valid = row < B * NH * Tn;
     float s = 0.f;
     if (valid) {
-        const int h = (int)(row % NH);
-        const long long bt = row / NH;
-        const size_t o = (size_t)bt * C + h * 64 + sub * 8;
+        const int t = row % Tn, bh = row / Tn;
+        const int b = bh / NH, h = bh % NH;
+        const size_t o = ((size_t)b * Tn + t) * C + h * 64 + sub * 8;
         Vec<bf16> a = load_vec(dout + o), c = load_vec(out + o);
 #pragma unroll
         for (int e = 0; e < 8; e++) s += a.get(e) * c.get(e);
@@ -114,12 +115,7 @@ __global__ void fa_backward_D64(float* __restrict__ D, const bf16* __restrict__ 
     s += __shfl_xor_sync(0xffffffffu, s, 4);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
     s += __shfl_xor_sync(0xffffffffu, s, 1);
-    if (valid && sub == 0) {
-        const int h = (int)(row % NH);
-        const long long bt = row / NH;
-        const int b = (int)(bt / Tn), t = (int)(bt % Tn);
-        D[((size_t)b * NH + h) * Tn + t] = s;
-    }
+    if (valid && sub == 0) D[row] = s;
 }
 
 // dQ, one warp per query row t: dq = scale * sum_{j<=t} P_tj (dP_tj - D_t) k_j
