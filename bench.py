@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--windows", type=int, default=5,
+                    help="timed windows of K steps (the first is the headline; all give the spread)")
     return ap.parse_args()
 
 
@@ -114,7 +116,7 @@ class ClockSampler:
 
     def __init__(self, cuda_index):
         self.cuda_index = cuda_index
-        self.samples = []          # (sm_mhz, max_mhz, power_w, set of reasons)
+        self.samples = []          # (sm_mhz, max_mhz, power_w, set of reasons, host time)
         self.stop_ev = threading.Event()
         self.t = None
         self.proc = None
@@ -132,7 +134,7 @@ class ClockSampler:
             try:
                 r = self.nv.sample()
                 if r is not None:
-                    self.samples.append((r[0], mx, r[1], r[2]))
+                    self.samples.append((r[0], mx, r[1], r[2], time.perf_counter()))
             except Exception:
                 pass
             self.stop_ev.wait(0.02)
@@ -145,7 +147,7 @@ class ClockSampler:
                 continue
             try:
                 rs = {n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")}
-                self.samples.append((float(f[1]), float(f[2]), float(f[3]), rs))
+                self.samples.append((float(f[1]), float(f[2]), float(f[3]), rs, time.perf_counter()))
             except ValueError:
                 continue
 
@@ -163,6 +165,14 @@ class ClockSampler:
             self.t.start()
         except OSError:
             self.proc = None
+
+    def window(self, t0, t1):
+        """Median SM clock and the reasons seen between host times t0 and t1."""
+        w = [x for x in self.samples if t0 <= x[4] <= t1]
+        if not w:
+            return {"sm_mhz": None, "samples": 0, "reasons": []}
+        return {"sm_mhz": statistics.median(x[0] for x in w), "samples": len(w),
+                "reasons": sorted(set().union(*[x[3] for x in w]))}
 
     def stop(self):
         self.stop_ev.set()
@@ -333,25 +343,39 @@ def ours(args):
             fam_ms[c] = v
     dominant = max(fam_ms, key=fam_ms.get)
     dom_classes = families.get(dominant, [dominant])
-    # the timed region: K untraced steps
+    # the timed region: K untraced steps (the headline), then more windows of K steps
+    # each, timed the same way, for the run-to-run spread
     G.profile_enable([])
     clocks = ClockSampler(local_rank)
     launches0 = G.kernel_launches()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    start.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            step(args.warmup + i, args.warmup + i + 1)
-    end.record(stream)
-    end.synchronize()
-    torch.cuda.synchronize()
-    barrier()
+    win_ms, win_clk = [], []
+    t_next = args.warmup
+    for wi in range(max(1, args.windows)):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if wi > 0:
+            barrier()
+            torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        start.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step((args.warmup + i) % n_batches, t_next + 1)
+                t_next += 1
+        end.record(stream)
+        end.synchronize()
+        torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        win_ms.append(start.elapsed_time(end))
+        win_clk.append(clocks.window(h0, h1))
+        if wi == 0:
+            barrier()
+            launches = G.kernel_launches() - launches0
     clk = clocks.stop()
-    launches = G.kernel_launches() - launches0
-    ms = start.elapsed_time(end)
+    clk["headline_window"] = win_clk[0]
+    ms = win_ms[0]
     m.check()
     # the roofline pass: the same K steps again, CUDA events around every launch of the
     # dominant kernel family on the step's stream (events between launches add gaps, so
@@ -363,7 +387,8 @@ def ours(args):
     t_start.record(stream)
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            step(args.warmup + i, args.warmup + args.steps + i + 1)
+            step(args.warmup + i, t_next + 1)
+            t_next += 1
     t_end.record(stream)
     t_end.synchronize()
     ms_traced = t_start.elapsed_time(t_end)
@@ -387,7 +412,8 @@ def ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
-            m.step_host(th[args.warmup + i], gh[args.warmup + i], *hp, n_batches + args.steps + i + 1)
+            m.step_host(th[args.warmup + i], gh[args.warmup + i], *hp, t_next + 1)
+            t_next += 1
         e2e_s = time.perf_counter() - t0
         if world > 1:
             import torch.distributed as dist
@@ -413,33 +439,43 @@ def ours(args):
     d_n = sum(live[c]["launches"] for c in dom_classes)
     d_fl = sum(live[c]["flops"] for c in dom_classes)
     d_by = sum(live[c]["bytes"] for c in dom_classes)
+    sm_med = clk.get("sm_mhz")
+    sm_max = clk.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2032.0)
+    timing = (f"CUDA events around each launch on the step's stream, over a second timed pass "
+              f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)")
     if d_fl > 0:
         achieved = d_fl / (d_ms / 1e3) / 1e12
         if prec == "bf16":
-            bound, peak = "tensor", peaks["bf16_tflops_sustained"]
-            peak_src = f"{src} bf16 sustained (kernel timed inside a long step)"
+            # primary: the burst peak (measured at ~full clock, as these kernels run);
+            # beside it the sustained peak (measured at a lower, power-capped clock) and
+            # the burst peak scaled to the SM clock seen during the headline window
+            bound, peak = "tensor", peaks["bf16_tflops"]
+            extra = {"frac_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "peak_sustained": peaks["bf16_tflops_sustained"],
+                     "frac_clock_normalised": (achieved / (peak * sm_med / sm_max)) if sm_med else None,
+                     "clock_normalisation": f"peak x {sm_med} / {sm_max} MHz (median SM clock of the headline window)"}
+            peak_src = f"{src} bf16 burst (cuBLAS 8192^3, best of 10)"
         else:
             # the fp32 path's matmuls run on the FP32 FMA units: 148 SMs x 128 lanes x 2 flops
             # at the 2032 MHz maximum SM clock
             bound, peak = "alu", 148 * 128 * 2 * 2.032e9 / 1e12
+            extra = {}
             peak_src = "derived: 148 SMs x 128 FP32 lanes x 2 flop/FMA x 2.032 GHz"
         traffic, traffic_src = matmul_traffic(args.workload) if dominant == "matmul" else (None, "no capture")
         roof = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
+                "unit": "TFLOP/s", "frac": achieved / peak, **extra, "traffic": traffic,
+                "traffic_measured": False, "traffic_source": traffic_src,
                 "peak_source": peak_src,
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
-                "share_of_traced_step": fam_ms[dominant] / total_ms,
-                "timing": f"CUDA events around each launch on the step's stream, over a second timed pass "
-                          f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)"}
+                "share_of_traced_step": fam_ms[dominant] / total_ms, "timing": timing}
     else:
         achieved = d_by / (d_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy bandwidth",
+                "frac": achieved / peak, "traffic": None, "traffic_measured": False,
+                "peak_source": f"{src} copy bandwidth",
                 "launches": d_n, "avg_launch_ms": d_ms / max(d_n, 1),
-                "share_of_traced_step": fam_ms[dominant] / total_ms,
-                "timing": f"CUDA events around each launch on the step's stream, over a second timed pass "
-                          f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)"}
+                "share_of_traced_step": fam_ms[dominant] / total_ms, "timing": timing}
     fpt, nparams = mfu_flops_per_token(w.shape, T)
     step_s = ms / 1000.0 / args.steps
     mfu = fpt * BT / step_s / 1e12
@@ -469,6 +505,13 @@ def ours(args):
                                  else "fp32 throughout"),
                    "l2": "no flush: the step's working set (GBs of activations) is far larger than the 126 MB L2"},
         "clocks": clk,
+        "windows": {"n": len(win_ms), "steps_each": args.steps,
+                    "ms_per_step": [x / args.steps for x in win_ms],
+                    "tokens_per_s_median": statistics.median(BT * args.steps * world / (x / 1e3) for x in win_ms),
+                    "tokens_per_s_min": min(BT * args.steps * world / (x / 1e3) for x in win_ms),
+                    "tokens_per_s_max": max(BT * args.steps * world / (x / 1e3) for x in win_ms),
+                    "sm_mhz_median": [c["sm_mhz"] for c in win_clk],
+                    "note": "the headline value is the first window; the others repeat it for the spread"},
         "gpu_launches": launches,
         "e2e": e2e,
         "mfu": {"model_flops_per_step": fpt * BT, "num_parameters": nparams,

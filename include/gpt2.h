@@ -104,12 +104,18 @@ int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int precision,
 
 /* Release the host-side handle (the workspace stays the caller's). */
 void gpt2_free(GPT2* model);
+/* The same, under the name of the boundary sketch (allocate once, then forward,
+ * zero_grad, backward, update, destroy). */
+void gpt2_destroy(GPT2* model);
 
 int gpt2_set_stream(GPT2* model, void* stream);
 
 /* Parameter counts: n_real counts the tensors with V token rows (the pages' count);
  * n_flat is the length of the flat buffers (padded vocabulary and alignment gaps). */
 int gpt2_num_parameters(const GPT2* model, size_t* n_real, size_t* n_flat);
+
+/* Real parameter count (the pages' num_parameters) into *n; GPT2_EINVAL for NULL. */
+int gpt2_num_params(const GPT2* model, size_t* n);
 
 /* Element offset of tensor `index` (0..15, order above) in the flat buffers, and its
  * element count. */
@@ -120,12 +126,18 @@ float* gpt2_params(GPT2* model);     /* master weights; write the initial values
 float* gpt2_grads(GPT2* model);      /* parameter gradients */
 float* gpt2_adam_m(GPT2* model);
 float* gpt2_adam_v(GPT2* model);
+/* The master-weight and gradient pointers with a status (GPT2_EINVAL for NULL arguments). */
+int gpt2_param_ptr(GPT2* model, float** master);
+int gpt2_grad_ptr(GPT2* model, float** grads);
 
 /* After writing gpt2_params(): refresh the bf16 shadow weights (bf16 mode; a no-op in
  * fp32 mode) and clear the AdamW moments. */
 int gpt2_sync_params(GPT2* model);
 
-/* Forward pass of every layer over tokens (device int32, (B,T) row-major, ids in
+/* Forward pass of every layer (ujoy.net llm.c article, section "用C语言实现LLM": encoder,
+ * then per block layernorm, matmul, self-attention, matmul + residual, layernorm, matmul,
+ * GELU, matmul + residual; final layernorm, tied LM head, softmax, cross-entropy) over
+ * tokens (device int32, (B,T) row-major, ids in
  * [0,V)).  With targets (device int32, (B,T)) it also computes the per-position
  * cross-entropy, the mean loss, and -- fused with the softmax -- the gradient of the
  * mean loss with respect to the logits, which backward consumes.  With
@@ -138,14 +150,17 @@ int gpt2_sync_params(GPT2* model);
 int gpt2_forward(GPT2* model, const int32_t* tokens, const int32_t* targets, int B, int T,
                  float* loss_out);
 
-/* Set every parameter gradient to zero. */
+/* Set every parameter gradient to zero (same article, section "训练过程": the training
+ * loop zeroes the gradients before each backward pass). */
 int gpt2_zero_grad(GPT2* model);
 
-/* Backward pass of every layer in reverse order; adds d(mean loss)/d(param) into the
+/* Backward pass of every layer in reverse order (same article, section "用C语言实现LLM":
+ * each layer's hand-written backward, chained from the loss back to the encoder); adds d(mean loss)/d(param) into the
  * gradient buffer.  Needs a preceding gpt2_forward with targets (else GPT2_ESTATE). */
 int gpt2_backward(GPT2* model);
 
-/* One AdamW step over the whole flat buffer:
+/* One AdamW step over the whole flat buffer (same article, section "训练过程": the Adam
+ * update after each backward pass, here with decoupled weight decay):
  *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;  mhat = m/(1-b1^t);  vhat = v/(1-b2^t)
  *   p -= lr (mhat / (sqrt(vhat) + eps) + weight_decay p)
  * then (bf16 mode) refresh the bf16 shadow.  t >= 1 is the 1-based step count. */
@@ -219,8 +234,15 @@ int gpt2_last_cuda_error(void);
 /* ---------------------------------------------------------------------------------
  * Single-layer entry points (same kernels as the model; used for per-layer tests and
  * by callers that chain layers themselves).  All pointers are device pointers;
- * `stream` is a cudaStream_t.
+ * `stream` is a cudaStream_t.  The calls are asynchronous.  A bounded device-side wait
+ * that runs out in one of their kernels (the kernel then gives up and returns) is
+ * latched in a per-device error word of the library, which gpt2_layer_check reads.
  * ------------------------------------------------------------------------------- */
+
+/* Synchronise `stream` and return (then clear) the error latched by the single-layer
+ * entry points on the current device: GPT2_ETIMEOUT if a bounded wait ran out since the
+ * last check (that call's outputs are then incomplete), else GPT2_OK. */
+int gpt2_layer_check(void* stream);
 
 /* Layernorm forward over N rows of C (C % 8 == 0, C <= 2048), fp32; N == 0 is a no-op:
  *   mean = sum(x)/C; rstd = 1/sqrt(sum((x-mean)^2)/C + 1e-5); out = (x-mean) rstd w + b.
@@ -248,29 +270,35 @@ int gpt2_layernorm_backward(float* dinp, float* dweight, float* dbias, const flo
  * kernels it runs, with the scratch taken from an array of GPT2_NOALLOC_SCRATCH_BYTES
  * compiled into the library (held on every GPU that loads it, until the process
  * exits).  Returns GPT2_EINVAL when gpt2_layernorm_backward_scratch_bytes(N, C) exceeds
- * that size (for example C = 768 allows N <= 21824 rows, C = 2048 allows N <= 8192).
- * The first call on each device looks up the array's device address (with that device
- * current) and caches it; make that first call before any stream capture.  All calls
- * share the one array, so calls that overlap on the GPU race: serialise them.  Nothing
- * is carried over between calls (every partial sum read is rewritten first).  Calls no
- * cudaMalloc, cudaFree or allocating routine. */
+ * that size: any N for C <= 1768, N <= 4096 rows for C = 2048 (the partial sums take
+ * min(ceil(N/16), 296) blocks x 2C floats).  Every call looks up the array's address on
+ * the current device, so `stream` must belong to the current device.  With lazy module
+ * loading the first call on a device also loads the module that holds the array: make it
+ * at start-up, before any stream capture.  All calls share the one array, so calls that
+ * overlap on the GPU race: serialise them.  Nothing is carried over between calls (every
+ * partial sum read is rewritten first).  Timeouts are reported by gpt2_layer_check.
+ * Calls no cudaMalloc, cudaFree or allocating routine. */
 #define GPT2_NOALLOC_SCRATCH_BYTES (4u << 20)
 int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias, const float* dout,
                                     const float* inp, const float* weight, const float* mean,
                                     const float* rstd, int N, int C, void* stream);
 
-/* Causal self-attention forward over qkv (B,T,3C) (q, k, v thirds; head h uses columns
+/* Causal self-attention forward (ujoy.net llm.c article, section "用C语言实现LLM": the
+ * self-attention layer) over qkv (B,T,3C) (q, k, v thirds; head h uses columns
  * [h*hs, (h+1)*hs) of each, hs = C/NH): out (B,T,C) = softmax(q k^T / sqrt(hs) over keys
  * j <= t) v, heads concatenated.  precision GPT2_BF16: bf16 tensors, lse (B,NH,T) fp32
  * receives each score row's log-sum-exp (natural log) for the backward; GPT2_FP32: fp32
  * tensors, and `lse` must hold the probabilities instead: (B,NH,T,T) fp32.
- * T <= 1024 (fp32: any T); hs <= 128. */
+ * bf16: head size C/NH = 64 (the tensor-core kernels; other sizes GPT2_EUNSUPPORTED);
+ * fp32: head size <= 128, a multiple of 8. */
 int gpt2_attention_forward(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
                            int precision, void* stream);
 
 /* Backward: dqkv (B,T,3C) [overwritten] from dout (B,T,C) and the forward's qkv, out
- * and lse (fp32 path: probabilities).  scratch (device): bf16 path (B,NH,T) fp32 row
- * sums; fp32 path (B,NH,T,T) fp32; size from gpt2_attention_backward_scratch_bytes. */
+ * and lse (fp32 path: probabilities).  scratch (device, 16-byte aligned): bf16 path the
+ * fp32 row sums D = rowsum(dout * out) and, for T not a multiple of 4, a copy of the
+ * LSE, each (B,NH,T rounded up to a multiple of 4); fp32 path (B,NH,T,T) fp32; size from
+ * gpt2_attention_backward_scratch_bytes. */
 size_t gpt2_attention_backward_scratch_bytes(int B, int T, int NH, int precision);
 int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
                             const float* lse, int B, int T, int C, int NH, int precision,
@@ -278,14 +306,35 @@ int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const
 
 /* Matmul forward: out (M,N) = inp (M,K) * weight(N,K)^T + bias (N, nullable).
  * precision GPT2_FP32: all float*; GPT2_BF16: out, inp, weight, bias are bf16 (bias
- * nullable), fp32 accumulation. */
+ * nullable), fp32 accumulation, on the tensor cores only: N and K multiples of 8 and
+ * 16-byte aligned pointers, else GPT2_EUNSUPPORTED. */
 int gpt2_matmul_forward(void* out, const void* inp, const void* weight, const void* bias,
                         int M, int N, int K, int precision, void* stream);
+
+/* The matmul forward with the epilogue the model fuses into it (ujoy.net llm.c article,
+ * section "用C语言实现LLM": the matmul, GELU and residual layers), with h = inp weight^T
+ * + bias (bias nullable):
+ *   GPT2_EPI_BIAS      out = h                                  (aux unused)
+ *   GPT2_EPI_GELU      aux = h (written); out = gelu(aux as stored), tanh form
+ *   GPT2_EPI_RESIDUAL  out = aux + h (aux (M,N) read: the residual stream)
+ * Same types and limits as gpt2_matmul_forward; aux has out's type and shape. */
+enum { GPT2_EPI_BIAS = 0, GPT2_EPI_GELU = 1, GPT2_EPI_RESIDUAL = 2 };
+int gpt2_matmul_forward_fused(void* out, void* aux, const void* inp, const void* weight,
+                              const void* bias, int M, int N, int K, int epilogue, int precision,
+                              void* stream);
+
+/* Input gradient of a matmul whose input was a GELU output, with the GELU backward fused:
+ * dinp (M,K) = (dout (M,N) weight (N,K)) * gelu'(pre), pre (M,K) the GELU's stored input
+ * (the model's MLP projection backward).  Types and limits as gpt2_matmul_forward. */
+int gpt2_matmul_backward_input_gelu(void* dinp, const void* dout, const void* weight, const void* pre,
+                                    int M, int N, int K, int precision, void* stream);
 
 /* Matmul backward: dinp (M,K) = dout (M,N) * weight (N,K)  [overwrites];
  * dweight (N,K, fp32) += dout^T * inp;  dbias (N, fp32, nullable) += column sums of
  * dout.  dout/inp/weight/dinp are float or bf16 by precision.  `scratch` (device,
- * >= gpt2_matmul_backward_scratch_bytes) holds the deterministic column-sum partials. */
+ * >= gpt2_matmul_backward_scratch_bytes) holds the deterministic column-sum partials and,
+ * in bf16, the partial tiles of a weight gradient whose contraction is split (added in a
+ * fixed order). */
 size_t gpt2_matmul_backward_scratch_bytes(int M, int N);
 int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, const void* dout,
                          const void* inp, const void* weight, int M, int N, int K,

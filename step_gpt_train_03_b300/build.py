@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpt2_b300.so")
-SOURCES = ["gpt2.cu", "gemm_tc.cu", "attention_flash.cu", "attention_tc.cu", "runtime.cu", "noalloc.cu"]
+SOURCES = ["gpt2.cu", "gemm_tc.cu", "attention_tc.cu", "runtime.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

@@ -39,6 +39,7 @@
 #include "tc_ptx.cuh"
 #include "../../include/gpt2.h"
 
+
 #define AT_HS 64
 #define AT_BM 128                  // queries per tile
 #define AT_BN 128                  // keys per tile
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                              const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
                              const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
-                             const float* __restrict__ Dsum, int B, int Tn, int C, int NH, unsigned* err) {
+                             const float* __restrict__ Dsum, int B, int Tn, int Tp, int C, int NH, unsigned* err) {
     using S = AbSmem<DKV>;
     constexpr int AB_RING = S::RING;
     extern __shared__ uint8_t smem_raw[];
@@ -657,8 +658,8 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             const int grow = t * AT_BM + r;                 // this thread's key (DKV) or query (DQ)
             float Lrow = 0.f, Drow = 0.f;
             if (!DKV && grow < Tn) {
-                Lrow = lse[(size_t)bh * Tn + grow] * AT_LOG2E;
-                Drow = Dsum[(size_t)bh * Tn + grow];
+                Lrow = lse[(size_t)bh * Tp + grow] * AT_LOG2E;
+                Drow = Dsum[(size_t)bh * Tp + grow];
             }
             for (int u = u0; u < u1; u++, rc++, xc++, gc++) {
                 if (!wait_one(x_full, xc & 1)) { alive = false; break; }
@@ -873,10 +874,11 @@ int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const _
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
 
-// 2-D fp32 map over (T, rows) with pitch T; box {128, 1}; no swizzle.
-static bool make_map_vec(CUtensorMap* map, const float* base, int Tn, int rows) {
+// 2-D fp32 map over (T, rows) with row pitch Tp (a multiple of 4, so the pitch is a
+// multiple of 16 bytes); columns >= T read as zero.  Box {128, 1}; no swizzle.
+static bool make_map_vec(CUtensorMap* map, const float* base, int Tn, int Tp, int rows) {
     cuuint64_t dims[2] = {(cuuint64_t)Tn, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)Tn * 4};
+    cuuint64_t strides[1] = {(cuuint64_t)Tp * 4};
     cuuint32_t box[2] = {128, 1};
     cuuint32_t estr[2] = {1, 1};
     return g_enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
@@ -884,10 +886,42 @@ static bool make_map_vec(CUtensorMap* map, const float* base, int Tn, int rows) 
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// D[b,h,t] = sum_d dO[b,t,h,d] O[b,t,h,d] (head size 64), the row sums of the softmax
+// backward, written at row pitch Tp.  Eight lanes per (b, h, t) row, one 16-byte packet
+// of dO and of O each, added across the eight lanes by shuffles; rows in D's own order,
+// so a warp's four results are consecutive floats (B*NH*T < 2^31: 32-bit indices).
+// lse_pad (nullable): also copy the forward's LSE row (pitch T) to pitch Tp, for the
+// tensor maps of the backward when T is not a multiple of 4.
+__global__ void attention_rowdot_kernel(float* __restrict__ D, float* __restrict__ lse_pad,
+                                        const float* __restrict__ lse, const bf16* __restrict__ dout,
+                                        const bf16* __restrict__ out, int B, int Tn, int Tp, int C, int NH) {
+    const int row = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3);
+    const int sub = threadIdx.x & 7;
+    const bool valid = row < B * NH * Tn;
+    float s = 0.f;
+    int t = 0, bh = 0;
+    if (valid) {
+        t = row % Tn;
+        bh = row / Tn;
+        const int b = bh / NH, h = bh % NH;
+        const size_t o = ((size_t)b * Tn + t) * C + h * AT_HS + sub * 8;
+        Vec<bf16> a = load_vec(dout + o), c = load_vec(out + o);
+#pragma unroll
+        for (int e = 0; e < 8; e++) s += a.get(e) * c.get(e);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (valid && sub == 0) {
+        D[(size_t)bh * Tp + t] = s;
+        if (lse_pad) lse_pad[(size_t)bh * Tp + t] = lse[row];
+    }
+}
+
 template <bool DKV>
 static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tl,
                       const CUtensorMap& td, const CUtensorMap& tdq, const float* lse, const float* D, int B, int Tn,
-                      int C, int NH, unsigned* err) {
+                      int Tp, int C, int NH, unsigned* err) {
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(attention_tc_backward_kernel<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -898,23 +932,40 @@ static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& 
     const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
     const int grid = items < g_sms ? items : g_sms;
     attention_tc_backward_kernel<DKV><<<grid, AT_THREADS, AbSmem<DKV>::TOTAL, s>>>(tq, tdo, tl, td, tdq, lse, D, B,
-                                                                                    Tn, C, NH, err);
+                                                                                    Tn, Tp, C, NH, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
 
+size_t attention_tc_backward_scratch_floats(int B, int Tn, int NH) {
+    const size_t Tp = (size_t)(Tn + 3) / 4 * 4;
+    return 2 * (size_t)B * NH * Tp;
+}
+
 int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
-                          const float* lse, const float* D, int B, int Tn, int C, int NH, unsigned* err) {
+                          const __nv_bfloat16* out, const float* lse, float* scratch, int B, int Tn, int C, int NH,
+                          unsigned* err) {
     if (!attention_tc_available()) return GPT2_EUNSUPPORTED;
-    if (C / NH != AT_HS || Tn % 4 || (((uintptr_t)qkv | (uintptr_t)dout | (uintptr_t)dqkv | (uintptr_t)lse |
-                                       (uintptr_t)D) & 15))
+    if (C / NH != AT_HS || C % NH ||
+        (((uintptr_t)qkv | (uintptr_t)dout | (uintptr_t)dqkv | (uintptr_t)out | (uintptr_t)scratch) & 15))
         return GPT2_EUNSUPPORTED;
+    // D (and, when T is not a multiple of 4, a copy of the LSE) at a row pitch of Tp
+    const int Tp = (Tn + 3) / 4 * 4;
+    float* D = scratch;
+    float* lse_pad = (Tp != Tn) ? scratch + (size_t)B * NH * Tp : nullptr;
+    const float* lse_k = lse_pad ? lse_pad : lse;
+    if (!lse_pad && ((uintptr_t)lse & 15)) return GPT2_EUNSUPPORTED;
+    const long long rows = (long long)B * NH * Tn;
+    attention_rowdot_kernel<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, s>>>(D, lse_pad, lse, dout, out, B, Tn, Tp,
+                                                                              C, NH);
+    rt_note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return GPT2_ECUDA;
     CUtensorMap tq, tdo, tl, td, tdq;
     if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&tdo, dout, C, Tn, B, C) ||
-        !make_map_vec(&tl, lse, Tn, B * NH) || !make_map_vec(&td, D, Tn, B * NH) ||
+        !make_map_vec(&tl, lse_k, Tn, Tp, B * NH) || !make_map_vec(&td, D, Tn, Tp, B * NH) ||
         !make_map3(&tdq, dqkv, 3 * C, Tn, B, 3 * C))
         return GPT2_EUNSUPPORTED;
-    int rc = launch_bwd<true>(s, tq, tdo, tl, td, tdq, lse, D, B, Tn, C, NH, err);
+    int rc = launch_bwd<true>(s, tq, tdo, tl, td, tdq, lse_k, D, B, Tn, Tp, C, NH, err);
     if (rc != GPT2_OK) return rc;
-    return launch_bwd<false>(s, tq, tdo, tl, td, tdq, lse, D, B, Tn, C, NH, err);
+    return launch_bwd<false>(s, tq, tdo, tl, td, tdq, lse_k, D, B, Tn, Tp, C, NH, err);
 }

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 
 // 1 when the kernels can run on the current device.
 int attention_tc_available();
@@ -11,7 +12,13 @@ int attention_tc_available();
 int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const __nv_bfloat16* qkv, int B, int T,
                          int C, int NH, unsigned* err);
 
-// dqkv (B,T,3C) [overwritten] from dout (B,T,C), qkv, lse (B,NH,T) and D = rowsum(dout*out)
-// (B,NH,T); C / NH must be 64 and T a multiple of 4, else GPT2_EUNSUPPORTED.
+// fp32 scratch elements the backward needs: the row sums D and, for T not a multiple of
+// 4, a copy of the LSE, each (B, NH, T rounded up to a multiple of 4).
+size_t attention_tc_backward_scratch_floats(int B, int T, int NH);
+
+// dqkv (B,T,3C) [overwritten] from dout (B,T,C), the forward's qkv, out and lse
+// (B,NH,T); `scratch` (device, 16-byte aligned, attention_tc_backward_scratch_floats).
+// C / NH must be 64, else GPT2_EUNSUPPORTED.
 int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
-                          const float* lse, const float* D, int B, int T, int C, int NH, unsigned* err);
+                          const __nv_bfloat16* out, const float* lse, float* scratch, int B, int T, int C, int NH,
+                          unsigned* err);

@@ -1,7 +1,8 @@
 // bf16 matmuls of the linear layers on the tcgen05 tensor cores (TMA-fed, TMEM
-// accumulators).  Each call returns GPT2_EUNSUPPORTED for a shape it does not take, and
-// the caller then falls back to the FMA kernel.  `err` (device, nullable) is the error
-// word a kernel sets if one of its bounded waits runs out.
+// accumulators).  Each call returns GPT2_EUNSUPPORTED for a shape it does not take (N or
+// K not a multiple of 8, an operand not 16-byte aligned, no tcgen05 device); there is no
+// other bf16 path.  `err` (device, nullable) is the error word a kernel sets if one of
+// its bounded waits runs out.
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>

@@ -21,7 +21,7 @@
 #include "gemm_simt.cuh"
 #include "attention_simt.cuh"
 #include "gemm_tc.h"
-#include "attention_flash.h"
+#include "attention_tc.h"
 #include "runtime.h"
 
 #define CK(x)                                                   \
@@ -71,8 +71,6 @@ struct GPT2 {
     // state
     int B, T;
     int have_fwd, have_targets;
-    // tensor-core plan (bf16 mode)
-    int use_tc;
     // the whole step as one CUDA graph, captured for (gB, gT) on the second step of that
     // shape; the AdamW node's scalars are set before each launch
     int use_graph, g_seen;
@@ -134,7 +132,7 @@ static size_t plan(GPT2* m, char* base) {
         m->att = nullptr;
         m->lse = (float*)take(L * attT * 4);
         m->datt = nullptr;
-        m->attn_scratch = (float*)take(attT * 4);
+        m->attn_scratch = (float*)take(attention_tc_backward_scratch_floats(m->maxB, m->maxT, m->NH) * 4);
     }
     m->losses = (float*)take(BT * 4);
     m->loss = (float*)take(4);
@@ -173,6 +171,8 @@ static int validate_cfg(const GPT2Config* c, int maxB, int maxT, int prec) {
     if (c->channels % 64 != 0 || c->channels % c->num_heads != 0) return GPT2_EINVAL;
     if (c->channels > 2048) return GPT2_EUNSUPPORTED;
     if (c->channels / c->num_heads > ATT_MAX_HS || (c->channels / c->num_heads) % 8) return GPT2_EUNSUPPORTED;
+    // bf16 runs every product on the tensor cores: attention there takes head size 64
+    if (prec == GPT2_BF16 && c->channels / c->num_heads != 64) return GPT2_EUNSUPPORTED;
     if (c->vocab_size < 1 || c->padded_vocab_size < c->vocab_size) return GPT2_EINVAL;
     if (c->padded_vocab_size % 64 != 0) return GPT2_EINVAL;
     if (c->max_seq_len < 1 || maxB < 1 || maxT < 1 || maxT > c->max_seq_len) return GPT2_EINVAL;
@@ -253,7 +253,11 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     m->ws = (char*)workspace;
     m->ws_bytes = workspace_bytes;
     m->stream = (cudaStream_t)stream;
-    m->use_tc = (precision == GPT2_BF16) ? gemm_tc_available() : 0;
+    // bf16 runs only on the tensor-core kernels; no other path is built for it
+    if (precision == GPT2_BF16 && (!gemm_tc_available() || !attention_tc_available())) {
+        free(m);
+        return GPT2_EUNSUPPORTED;
+    }
     m->use_graph = 1;
     m->g_seen = 0;
     m->gB = m->gT = 0;
@@ -287,6 +291,8 @@ extern "C" void gpt2_free(GPT2* m) {
     free(m);
 }
 
+extern "C" void gpt2_destroy(GPT2* m) { gpt2_free(m); }
+
 extern "C" int gpt2_set_stream(GPT2* m, void* stream) {
     if (!m) return GPT2_EINVAL;
     m->stream = (cudaStream_t)stream;
@@ -297,6 +303,12 @@ extern "C" int gpt2_num_parameters(const GPT2* m, size_t* n_real, size_t* n_flat
     if (!m) return GPT2_EINVAL;
     if (n_real) *n_real = m->n_real;
     if (n_flat) *n_flat = m->n_flat;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_num_params(const GPT2* m, size_t* n) {
+    if (!m || !n) return GPT2_EINVAL;
+    *n = m->n_real;
     return GPT2_OK;
 }
 
@@ -311,6 +323,16 @@ extern "C" float* gpt2_params(GPT2* m) { return m ? m->params : nullptr; }
 extern "C" float* gpt2_grads(GPT2* m) { return m ? m->grads : nullptr; }
 extern "C" float* gpt2_adam_m(GPT2* m) { return m ? m->m : nullptr; }
 extern "C" float* gpt2_adam_v(GPT2* m) { return m ? m->v : nullptr; }
+extern "C" int gpt2_param_ptr(GPT2* m, float** master) {
+    if (!m || !master) return GPT2_EINVAL;
+    *master = m->params;
+    return GPT2_OK;
+}
+extern "C" int gpt2_grad_ptr(GPT2* m, float** grads) {
+    if (!m || !grads) return GPT2_EINVAL;
+    *grads = m->grads;
+    return GPT2_OK;
+}
 extern "C" float* gpt2_loss(GPT2* m) { return m ? m->loss : nullptr; }
 extern "C" float* gpt2_losses(GPT2* m) { return m ? m->losses : nullptr; }
 extern "C" void* gpt2_logits(GPT2* m) { return m ? m->logits : nullptr; }
@@ -567,70 +589,73 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
     return GPT2_OK;
 }
 
-// Linear-layer products.  W is (N, K) row-major for the forward (y = x W^T).
+// Linear-layer products.  W is (N, K) row-major for the forward (y = x W^T).  bf16 runs
+// on the tcgen05 kernels only (a shape they do not take is GPT2_EUNSUPPORTED); fp32 on
+// the FMA kernel.  `err` (device, nullable) is the error word of bounded waits.
 template <typename T>
-static int mm_forward(GPT2* m, cudaStream_t s, T* out, const T* inp, const T* W, const T* bias,
-                      int M, int N, int K, int epi, void* aux) {
-    EpiArgs ep{out, bias, aux, (long)N};
+static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T* bias, int M, int N, int K,
+                      int epi, void* aux, unsigned* err) {
     ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
-        if (m && m->use_tc) {
-            int rc = gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias,
-                                     M, N, K, epi, (bf16*)aux, m->err);
-            if (rc != GPT2_EUNSUPPORTED) return rc;
+        return gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias, M, N, K, epi,
+                               (bf16*)aux, err);
+    } else {
+        (void)err;
+        EpiArgs ep{out, bias, aux, (long)N};
+        cudaError_t e;
+        rt_note_launches(1);
+        switch (epi) {
+            case EPI_STORE: e = launch_gemm_simt<T, true, true, EPI_STORE>(s, inp, K, W, K, M, N, K, ep); break;
+            case EPI_GELU: e = launch_gemm_simt<T, true, true, EPI_GELU>(s, inp, K, W, K, M, N, K, ep); break;
+            case EPI_RESID: e = launch_gemm_simt<T, true, true, EPI_RESID>(s, inp, K, W, K, M, N, K, ep); break;
+            default: return GPT2_EINVAL;
         }
+        CK(e);
+        return GPT2_OK;
     }
-    cudaError_t e;
-    rt_note_launches(1);
-    switch (epi) {
-        case EPI_STORE: e = launch_gemm_simt<T, true, true, EPI_STORE>(s, inp, K, W, K, M, N, K, ep); break;
-        case EPI_GELU: e = launch_gemm_simt<T, true, true, EPI_GELU>(s, inp, K, W, K, M, N, K, ep); break;
-        case EPI_RESID: e = launch_gemm_simt<T, true, true, EPI_RESID>(s, inp, K, W, K, M, N, K, ep); break;
-        default: return GPT2_EINVAL;
-    }
-    CK(e);
-    return GPT2_OK;
 }
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation of dinp's layer)
 template <typename T>
-static int mm_backward_dx(GPT2* m, cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N,
-                          int K, int epi, const T* aux) {
-    EpiArgs ep{dinp, nullptr, (void*)aux, (long)K};
+static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N, int K, int epi,
+                          const T* aux, unsigned* err) {
     ProfScope ps(s, PC_MATMUL_BWD_DX, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
-        if (m && m->use_tc) {
-            int rc = gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
-                                         (const bf16*)aux, m->err);
-            if (rc != GPT2_EUNSUPPORTED) return rc;
-        }
+        return gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
+                                   (const bf16*)aux, err);
+    } else {
+        (void)err;
+        EpiArgs ep{dinp, nullptr, (void*)aux, (long)K};
+        cudaError_t e;
+        rt_note_launches(1);
+        // C(m, k) = sum_n dout[m][n] W[n][k]: A K-contig over n (lda = N), B(k, n) = W[n*K + k]
+        if (epi == EPI_GELU_BWD) e = launch_gemm_simt<T, true, false, EPI_GELU_BWD>(s, dout, N, W, K, M, K, N, ep);
+        else if (epi == EPI_STORE) e = launch_gemm_simt<T, true, false, EPI_STORE>(s, dout, N, W, K, M, K, N, ep);
+        else return GPT2_EINVAL;
+        CK(e);
+        return GPT2_OK;
     }
-    cudaError_t e;
-    rt_note_launches(1);
-    // C(m, k) = sum_n dout[m][n] W[n][k]: A K-contig over n (lda = N), B(k, n) = W[n*K + k]
-    if (epi == EPI_GELU_BWD) e = launch_gemm_simt<T, true, false, EPI_GELU_BWD>(s, dout, N, W, K, M, K, N, ep);
-    else e = launch_gemm_simt<T, true, false, EPI_STORE>(s, dout, N, W, K, M, K, N, ep);
-    CK(e);
-    return GPT2_OK;
 }
 
-// dW (N,K) += dout^T (N,M) inp (M,K)
+// dW (N,K) += dout^T (N,M) inp (M,K); `partials` (device fp32, nullable) lets the
+// tensor-core product split its contraction when the weight has few tiles
 template <typename T>
-static int mm_backward_dw(GPT2* m, cudaStream_t s, float* dW, const T* dout, const T* inp, int M, int N,
-                          int K) {
-    EpiArgs ep{dW, nullptr, nullptr, (long)K};
+static int mm_backward_dw(cudaStream_t s, float* dW, const T* dout, const T* inp, int M, int N, int K,
+                          float* partials, size_t partials_floats, unsigned* err) {
     ProfScope ps(s, PC_MATMUL_BWD_DW, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
-        if (m && m->use_tc) {
-            int rc = gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, m->partials,
-                                         m->partials_floats, m->err);
-            if (rc != GPT2_EUNSUPPORTED) return rc;
-        }
+        return gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, partials, partials_floats,
+                                   err);
+    } else {
+        (void)partials;
+        (void)partials_floats;
+        (void)err;
+        EpiArgs ep{dW, nullptr, nullptr, (long)K};
+        // C(n, k) = sum_m dout[m][n] inp[m][k]: A(n, m) = dout[m*N + n], B(k, m) = inp[m*K + k]
+        rt_note_launches(1);
+        CK((launch_gemm_simt<T, false, false, EPI_ACC_F32>(s, dout, N, inp, K, N, K, M, ep)));
+        return GPT2_OK;
     }
-    // C(n, k) = sum_m dout[m][n] inp[m][k]: A(n, m) = dout[m*N + n], B(k, m) = inp[m*K + k]
-    rt_note_launches(1);
-    CK((launch_gemm_simt<T, false, false, EPI_ACC_F32>(s, dout, N, inp, K, N, K, M, ep)));
-    return GPT2_OK;
 }
 
 static double attn_fwd_flops(int B, int Tn, int C) {
@@ -644,7 +669,7 @@ static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, in
     ProfScope ps(s, PC_ATTENTION_FWD, attn_fwd_flops(B, Tn, C), 0);
     if constexpr (sizeof(T) == 2) {
         float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
-        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, m->err);
+        return attention_tc_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, m->err);
     } else {
         float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
         int rows = B * NH * Tn;
@@ -663,8 +688,8 @@ static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const 
     ProfScope ps(s, PC_ATTENTION_BWD, 2.0 * attn_fwd_flops(B, Tn, C), 0);
     if constexpr (sizeof(T) == 2) {
         const float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
-        return attention_flash_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out,
-                                     lse, m->attn_scratch, B, Tn, C, NH, m->err);
+        return attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
+                                     m->attn_scratch, B, Tn, C, NH, m->err);
     } else {
         (void)out;
         const float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
@@ -717,16 +742,16 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         float* m1 = m->ln1_mean + l * BTmax; float* r1 = m->ln1_rstd + l * BTmax;
         float* m2 = m->ln2_mean + l * BTmax; float* r2 = m->ln2_rstd + l * BTmax;
         RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
-        RC(mm_forward<T>(m, s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr));
+        RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
         RC(attn_forward<T>(m, s, atty, qkv, l, B, Tn));
-        RC(mm_forward<T>(m, s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x));
+        RC(mm_forward<T>(s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x, m->err));
         RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
-        RC(mm_forward<T>(m, s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch));
-        RC(mm_forward<T>(m, s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2));
+        RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err));
+        RC(mm_forward<T>(s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2, m->err));
         x = res3;
     }
     RC(ln_forward<T>(s, (T*)m->lnf, m->lnf_mean, m->lnf_rstd, x, P(P_LNFW), P(P_LNFB), BT, C));
-    RC(mm_forward<T>(m, s, (T*)m->logits, (const T*)m->lnf, P(P_WTE), (const T*)nullptr, BT, m->Vp, C, EPI_STORE, nullptr));
+    RC(mm_forward<T>(s, (T*)m->logits, (const T*)m->lnf, P(P_WTE), (const T*)nullptr, BT, m->Vp, C, EPI_STORE, nullptr, m->err));
     if (with_targets) {
         {
             ProfScope ps(s, PC_SOFTMAX_XENT, 0, 2.0 * BT * m->Vp * sizeof(T) + 12.0 * BT);
@@ -783,8 +808,8 @@ static int backward_impl(GPT2* m) {
     rq.n = 0;
     rq.max_w = 0;
     // LM head (tied): dlnf = dlogits wte; dwte += dlogits^T lnf
-    RC(mm_backward_dx<T>(m, s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr));
-    RC(mm_backward_dw<T>(m, s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C));
+    RC(mm_backward_dx<T>(s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr, m->err));
+    RC(mm_backward_dw<T>(s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C, m->partials, m->partials_floats, m->err));
     RC(launch_zero(s, dresid, (size_t)BT * C * sizeof(T)));
     const T* xlast = (const T*)m->res3 + (L - 1) * BTmax * C;
     // the updated residual gradient is d(res3) of the last layer: its column sums are
@@ -803,23 +828,23 @@ static int backward_impl(GPT2* m) {
         const float* m1 = m->ln1_mean + l * BTmax; const float* r1 = m->ln1_rstd + l * BTmax;
         const float* m2 = m->ln2_mean + l * BTmax; const float* r2 = m->ln2_rstd + l * BTmax;
         // MLP output projection (dresid = d res3)
-        RC(mm_backward_dx<T>(m, s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch));
-        RC(mm_backward_dw<T>(m, s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C));
+        RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err));
+        RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err));
         // MLP input projection
-        RC(mm_backward_dx<T>(m, s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr));
-        RC(mm_backward_dw<T>(m, s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C));
+        RC(mm_backward_dx<T>(s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dw<T>(s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C, m->partials, m->partials_floats, m->err));
         RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
                           G(P_ATTPROJB) + l * C, m->err, &rq));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
-        RC(mm_backward_dx<T>(m, s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr));
-        RC(mm_backward_dw<T>(m, s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C));
+        RC(mm_backward_dx<T>(s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dw<T>(s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C, m->partials, m->partials_floats, m->err));
         // attention
         RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn));
         // qkv projection
-        RC(mm_backward_dx<T>(m, s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr));
-        RC(mm_backward_dw<T>(m, s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C));
+        RC(mm_backward_dx<T>(s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dw<T>(s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C, m->partials, m->partials_floats, m->err));
         RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq));
         // ln1 (dresid becomes d x_l)
         RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
@@ -1096,6 +1121,35 @@ extern "C" const char* gpt2_strerror(int st) {
 }
 
 // ------------------------------------------------------------------ single-layer API
+// The single-layer entry points have no model, so no workspace error word: their kernels'
+// bounded waits report into this word of the library's own device memory (one per
+// device), read and cleared by gpt2_layer_check.  Its address is looked up on every call,
+// with the caller's device current (a lookup, not an allocation).
+static __device__ unsigned g_layer_err;
+
+static int layer_err_word(unsigned** out) {
+    void* p = nullptr;
+    CK(cudaGetSymbolAddress(&p, g_layer_err));
+    *out = (unsigned*)p;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_layer_check(void* stream) {
+    unsigned* err = nullptr;
+    RC(layer_err_word(&err));
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned e = 0;
+    CK(cudaMemcpyAsync(&e, err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (!e) return GPT2_OK;
+    CK(cudaMemsetAsync(err, 0, sizeof(unsigned), s));
+    CK(cudaStreamSynchronize(s));
+    if (e & ERRBIT_TIMEOUT) return GPT2_ETIMEOUT;
+    if (e & ERRBIT_TOKEN) return GPT2_ETOKEN;
+    if (e & ERRBIT_NONFINITE) return GPT2_ENONFINITE;
+    return GPT2_ECUDA;
+}
+
 extern "C" int gpt2_layernorm_forward(float* out, float* mean, float* rstd, const float* inp,
                                       const float* weight, const float* bias, int N, int C, void* stream) {
     if (N < 0 || C < 8 || C % 8 || C > 2048) return GPT2_EINVAL;
@@ -1117,24 +1171,59 @@ extern "C" int gpt2_layernorm_backward(float* dinp, float* dweight, float* dbias
     if (N == 0) return GPT2_OK;
     if (!dinp || !dweight || !dbias || !dout || !inp || !weight || !mean || !rstd) return GPT2_EINVAL;
     if (!scratch || scratch_bytes < gpt2_layernorm_backward_scratch_bytes(N, C)) return GPT2_EINVAL;
+    unsigned* err = nullptr;
+    RC(layer_err_word(&err));
     return ln_backward<float>((cudaStream_t)stream, dinp, dweight, dbias, dout, inp, weight, mean, rstd,
-                              N, C, (float*)scratch, scratch_bytes / sizeof(float));
+                              N, C, (float*)scratch, scratch_bytes / sizeof(float), nullptr, err);
+}
+
+static int epi_of(int epilogue) {
+    switch (epilogue) {
+        case GPT2_EPI_BIAS: return EPI_STORE;
+        case GPT2_EPI_GELU: return EPI_GELU;
+        case GPT2_EPI_RESIDUAL: return EPI_RESID;
+        default: return -1;
+    }
+}
+
+extern "C" int gpt2_matmul_forward_fused(void* out, void* aux, const void* inp, const void* weight,
+                                         const void* bias, int M, int N, int K, int epilogue, int precision,
+                                         void* stream) {
+    const int epi = epi_of(epilogue);
+    if (!out || !inp || !weight || M < 0 || N <= 0 || K <= 0 || epi < 0) return GPT2_EINVAL;
+    if (epi != EPI_STORE && !aux) return GPT2_EINVAL;
+    if (M == 0) return GPT2_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (precision == GPT2_FP32)
+        return mm_forward<float>(s, (float*)out, (const float*)inp, (const float*)weight, (const float*)bias, M, N,
+                                 K, epi, aux, nullptr);
+    if (precision == GPT2_BF16) {
+        unsigned* err = nullptr;
+        RC(layer_err_word(&err));
+        return mm_forward<bf16>(s, (bf16*)out, (const bf16*)inp, (const bf16*)weight, (const bf16*)bias, M, N, K,
+                                epi, aux, err);
+    }
+    return GPT2_EINVAL;
 }
 
 extern "C" int gpt2_matmul_forward(void* out, const void* inp, const void* weight, const void* bias,
                                    int M, int N, int K, int precision, void* stream) {
-    if (!out || !inp || !weight || M < 0 || N <= 0 || K <= 0) return GPT2_EINVAL;
+    return gpt2_matmul_forward_fused(out, nullptr, inp, weight, bias, M, N, K, GPT2_EPI_BIAS, precision, stream);
+}
+
+extern "C" int gpt2_matmul_backward_input_gelu(void* dinp, const void* dout, const void* weight, const void* pre,
+                                               int M, int N, int K, int precision, void* stream) {
+    if (!dinp || !dout || !weight || !pre || M < 0 || N <= 0 || K <= 0) return GPT2_EINVAL;
     if (M == 0) return GPT2_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (precision == GPT2_FP32)
-        return mm_forward<float>(nullptr, s, (float*)out, (const float*)inp, (const float*)weight,
-                                 (const float*)bias, M, N, K, EPI_STORE, nullptr);
+        return mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K,
+                                     EPI_GELU_BWD, (const float*)pre, nullptr);
     if (precision == GPT2_BF16) {
-        GPT2 shim;
-        memset(&shim, 0, sizeof(shim));
-        shim.use_tc = gemm_tc_available();
-        return mm_forward<bf16>(&shim, s, (bf16*)out, (const bf16*)inp, (const bf16*)weight,
-                                (const bf16*)bias, M, N, K, EPI_STORE, nullptr);
+        unsigned* err = nullptr;
+        RC(layer_err_word(&err));
+        return mm_backward_dx<bf16>(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_GELU_BWD,
+                                    (const bf16*)pre, err);
     }
     return GPT2_EINVAL;
 }
@@ -1157,19 +1246,18 @@ extern "C" int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, co
     float* part = (float*)scratch;
     size_t pf = scratch_bytes / sizeof(float);
     if (precision == GPT2_FP32) {
-        RC(mm_backward_dx<float>(nullptr, s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_STORE, nullptr));
-        RC(mm_backward_dw<float>(nullptr, s, dweight, (const float*)dout, (const float*)inp, M, N, K));
+        RC(mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_STORE,
+                                 nullptr, nullptr));
+        RC(mm_backward_dw<float>(s, dweight, (const float*)dout, (const float*)inp, M, N, K, nullptr, 0, nullptr));
         if (dbias) RC(colsum<float>(s, dbias, (const float*)dout, M, N, part, pf));
         return GPT2_OK;
     }
     if (precision == GPT2_BF16) {
-        GPT2 shim;
-        memset(&shim, 0, sizeof(shim));
-        shim.use_tc = gemm_tc_available();
-        shim.partials = part;
-        shim.partials_floats = pf;
-        RC(mm_backward_dx<bf16>(&shim, s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_STORE, nullptr));
-        RC(mm_backward_dw<bf16>(&shim, s, dweight, (const bf16*)dout, (const bf16*)inp, M, N, K));
+        unsigned* err = nullptr;
+        RC(layer_err_word(&err));
+        RC(mm_backward_dx<bf16>(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_STORE, nullptr,
+                                err));
+        RC(mm_backward_dw<bf16>(s, dweight, (const bf16*)dout, (const bf16*)inp, M, N, K, part, pf, err));
         if (dbias) RC(colsum<bf16>(s, dbias, (const bf16*)dout, M, N, part, pf));
         return GPT2_OK;
     }
@@ -1177,17 +1265,23 @@ extern "C" int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, co
 }
 
 // ------------------------------------------------------------------ attention (single layer)
-static int attn_args_ok(int B, int Tn, int C, int NH) {
+static int attn_args_ok(int B, int Tn, int C, int NH, int precision) {
     if (B < 1 || Tn < 1 || NH < 1 || C < NH || C % NH || C / NH > ATT_MAX_HS || (C / NH) % 8) return 0;
+    if (precision == GPT2_BF16 && C / NH != 64) return 0;      // the tensor-core kernels' head size
     return 1;
 }
 
 extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, int B, int Tn, int C, int NH,
                                       int precision, void* stream) {
-    if (!out || !lse || !qkv || !attn_args_ok(B, Tn, C, NH)) return GPT2_EINVAL;
+    if (!out || !lse || !qkv) return GPT2_EINVAL;
+    if (!attn_args_ok(B, Tn, C, NH, GPT2_FP32)) return GPT2_EINVAL;
+    if (!attn_args_ok(B, Tn, C, NH, precision)) return GPT2_EUNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
-    if (precision == GPT2_BF16)
-        return attention_flash_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, nullptr);
+    if (precision == GPT2_BF16) {
+        unsigned* err = nullptr;
+        RC(layer_err_word(&err));
+        return attention_tc_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, err);
+    }
     if (precision == GPT2_FP32) {
         const int rows = B * NH * Tn;
         attention_forward_simt<float><<<ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s>>>(
@@ -1202,18 +1296,24 @@ extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, in
 extern "C" size_t gpt2_attention_backward_scratch_bytes(int B, int Tn, int NH, int precision) {
     if (B < 1 || Tn < 1 || NH < 1) return 0;
     const size_t rows = (size_t)B * NH * Tn;
-    return precision == GPT2_FP32 ? rows * Tn * sizeof(float) : rows * sizeof(float);
+    return precision == GPT2_FP32 ? rows * Tn * sizeof(float)
+                                  : attention_tc_backward_scratch_floats(B, Tn, NH) * sizeof(float);
 }
 
 extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
                                        const float* lse, int B, int Tn, int C, int NH, int precision,
                                        void* scratch, size_t scratch_bytes, void* stream) {
-    if (!dqkv || !dout || !qkv || !out || !lse || !scratch || !attn_args_ok(B, Tn, C, NH)) return GPT2_EINVAL;
+    if (!dqkv || !dout || !qkv || !out || !lse || !scratch) return GPT2_EINVAL;
+    if (!attn_args_ok(B, Tn, C, NH, GPT2_FP32)) return GPT2_EINVAL;
+    if (!attn_args_ok(B, Tn, C, NH, precision)) return GPT2_EUNSUPPORTED;
     if (scratch_bytes < gpt2_attention_backward_scratch_bytes(B, Tn, NH, precision)) return GPT2_EINVAL;
     cudaStream_t s = (cudaStream_t)stream;
-    if (precision == GPT2_BF16)
-        return attention_flash_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
-                                        (float*)scratch, B, Tn, C, NH, nullptr);
+    if (precision == GPT2_BF16) {
+        unsigned* err = nullptr;
+        RC(layer_err_word(&err));
+        return attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
+                                     (float*)scratch, B, Tn, C, NH, err);
+    }
     if (precision == GPT2_FP32) {
         const int rows = B * NH * Tn;
         const int grid = ceil_div(rows, ATT_WARPS);

@@ -16,31 +16,21 @@
 // reads, so nothing is carried over from the previous call and nothing needs clearing.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/gpt2.h"
-
-#define NOALLOC_MAX_DEVICES 256
 
 static __device__ __align__(256) float g_layernorm_scratch[GPT2_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
 // Host code cannot pass the array's name to a kernel: on the host that name is a
-// stand-in object, not a device address.  The device address is looked up once per
-// device, with that device current, and cached.
-static std::mutex g_scratch_mutex;
-static void* g_scratch_addr[NOALLOC_MAX_DEVICES];
-
+// stand-in object, not a device address.  The device address is looked up on every
+// call, with the caller's device current, so it always belongs to the current device
+// and its current context (a cached address would go stale after cudaDeviceReset).  The
+// lookup is cheap and allocates nothing; with lazy module loading the first lookup on a
+// device is what loads the module holding the array, which is why the first call belongs
+// in the caller's start-up.
 static int scratch_address(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GPT2_ECUDA;
-    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GPT2_EUNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_layernorm_scratch) != cudaSuccess || !p) return GPT2_ECUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_layernorm_scratch) != cudaSuccess || !p) return GPT2_ECUDA;
+    *out = p;
     return GPT2_OK;
 }
 

@@ -36,6 +36,13 @@ SIGNATURES = {
     "gpt2_workspace_bytes": (_i, [ctypes.POINTER(GPT2Config), _i, _i, _i, _psz]),
     "gpt2_build": (_i, [ctypes.POINTER(GPT2Config), _i, _i, _i, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "gpt2_free": (None, [_vp]),
+    "gpt2_destroy": (None, [_vp]),
+    "gpt2_num_params": (_i, [_vp, _psz]),
+    "gpt2_param_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
+    "gpt2_grad_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
+    "gpt2_layer_check": (_i, [_vp]),
+    "gpt2_matmul_forward_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "gpt2_matmul_backward_input_gelu": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_set_stream": (_i, [_vp, _vp]),
     "gpt2_num_parameters": (_i, [_vp, _psz, _psz]),
     "gpt2_param_tensor": (_i, [_vp, _i, _psz, _psz]),
@@ -407,6 +414,33 @@ def matmul_forward(out, inp, weight, bias, precision, stream=None):
     N = weight.shape[0]
     check(lib.gpt2_matmul_forward(_ptr(out), _ptr(inp), _ptr(weight), _ptr(bias), M, N, K,
                                   PRECISIONS[precision], _stream_handle(stream)), "gpt2_matmul_forward")
+
+
+EPILOGUES = {"bias": 0, "gelu": 1, "residual": 2}
+
+
+def matmul_forward_fused(out, aux, inp, weight, bias, epilogue, precision, stream=None):
+    """gpt2_matmul_forward_fused: out = epilogue(inp weight^T + bias); aux is the GELU
+    pre-activation (written) or the residual input (read)."""
+    M, K = inp.shape
+    N = weight.shape[0]
+    check(lib.gpt2_matmul_forward_fused(_ptr(out), _ptr(aux), _ptr(inp), _ptr(weight), _ptr(bias), M, N, K,
+                                        EPILOGUES[epilogue], PRECISIONS[precision], _stream_handle(stream)),
+          "gpt2_matmul_forward_fused")
+
+
+def matmul_backward_input_gelu(dinp, dout, weight, pre, precision, stream=None):
+    """gpt2_matmul_backward_input_gelu: dinp = (dout weight) * gelu'(pre)."""
+    M, N = dout.shape
+    K = weight.shape[1]
+    check(lib.gpt2_matmul_backward_input_gelu(_ptr(dinp), _ptr(dout), _ptr(weight), _ptr(pre), M, N, K,
+                                              PRECISIONS[precision], _stream_handle(stream)),
+          "gpt2_matmul_backward_input_gelu")
+
+
+def layer_check(stream=None):
+    """gpt2_layer_check: synchronise and raise if a single-layer kernel's bounded wait ran out."""
+    check(lib.gpt2_layer_check(_stream_handle(stream)), "gpt2_layer_check")
 
 
 def matmul_backward_scratch_bytes(M, N) -> int:

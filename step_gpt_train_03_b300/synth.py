@@ -64,6 +64,8 @@ class Workload:
 GPT2_124M = ModelShape(1024, 50257, 50304, 12, 12, 768)
 GPT2_350M = ModelShape(1024, 50257, 50304, 24, 16, 1024)
 TINY = ModelShape(32, 512, 512, 2, 4, 64)
+# the tiny model with one head of size 64, the head size of the bf16 (tensor-core) path
+TINY_HS64 = ModelShape(32, 512, 512, 2, 1, 64)
 
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", TINY, 2, 32, 0, "fp32", 1, tokens="uniform"),

@@ -41,8 +41,12 @@ def test_every_declared_symbol_is_exported(lib):
 def test_workspace_size_and_validation(lib):
     from step_gpt_train_03_b300 import synth
     n32 = lib.workspace_bytes(synth.TINY, 2, 32, "fp32")
-    n16 = lib.workspace_bytes(synth.TINY, 2, 32, "bf16")
+    n16 = lib.workspace_bytes(synth.TINY_HS64, 2, 32, "bf16")
     assert n32 > 0 and n16 > 0
+    # bf16 runs attention on the tensor cores, whose kernels take head size 64 only
+    with pytest.raises(lib.GPT2Error) as e:
+        lib.workspace_bytes(synth.TINY, 2, 32, "bf16")
+    assert e.value.status == 8
     big = lib.workspace_bytes(synth.GPT2_124M, 16, 1024, "bf16")
     assert 5e9 < big < 40e9
     bad = synth.ModelShape(32, 512, 500, 2, 4, 64)          # Vp < V

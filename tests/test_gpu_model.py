@@ -138,8 +138,9 @@ def test_gpt2_124m_fp32_free_running_ten_steps():
 
 
 def test_bf16_tiny_ten_steps():
-    """bf16 activations/weights with fp32 master weights and AdamW state, tiny model."""
-    shape = synth.TINY
+    """bf16 activations/weights with fp32 master weights and AdamW state, tiny model with
+    one head of size 64 (the tensor-core attention's head size)."""
+    shape = synth.TINY_HS64
     batches = synth.workload_batches(synth.WORKLOADS["tiny_fp32"], 10)
     hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
     _, lg, _ = run_gpu(shape, "bf16", 0, batches, hp)
@@ -156,9 +157,13 @@ def test_bf16_gpt2_124m_short_sequences_ten_steps():
     _, lg, gg = run_gpu(shape, "bf16", 2, batches, hp)
     _, lo, go = run_oracle(shape, 2, batches, hp, np.float32)
     assert max(abs(a - b) for a, b in zip(lg, lo)) <= LOSS_ABS_BF16, (lg, lo)
-    # bf16 gradients: not a spec bar, but a dropped term would show as O(1) error
+    # bf16 gradients against the fp32 oracle: each stored activation and activation
+    # gradient is rounded to bf16 (relative 2^-9 = 2e-3), and the backward chains about
+    # ten such roundings per layer through 12 layers; on this workload every tensor's
+    # normalised error measured <= 9.7e-3 (ln1w; most 5e-3..7e-3) on a B300.  The bound
+    # 2e-2 keeps a factor 2 over that; a dropped term or a wrong constant is O(0.1..1).
     errs = _grad_errors(gg[0], go[0])
-    assert max(errs.values()) < 0.1, errs
+    assert max(errs.values()) < 2e-2, errs
 
 
 def _golden(name):
@@ -212,7 +217,7 @@ def test_steps_are_bitwise_deterministic():
     """Two runs from the same state give bit-identical gradients (no float atomics)."""
     import torch
     for precision in ("fp32", "bf16"):
-        shape = synth.ModelShape(64, 512, 512, 2, 4, 64)
+        shape = synth.ModelShape(64, 512, 512, 2, 4 if precision == "fp32" else 1, 64)
         tok, tgt = synth.zipf_batches(512, 4, 64, 1, 4)[0]
         out = []
         for _ in range(2):
@@ -273,7 +278,7 @@ def test_graph_steps_match_eager_steps_bitwise(precision):
     shape; every step (learning rate changing each time, a batch-size change in the
     middle forcing a new capture) equals the kernel-by-kernel step bit for bit."""
     import torch
-    shape = synth.ModelShape(64, 512, 512, 2, 4, 64)
+    shape = synth.ModelShape(64, 512, 512, 2, 4 if precision == "fp32" else 1, 64)
     batches = synth.zipf_batches(512, 4, 64, 9, 11)
     g = gpu_model(shape, 4, 64, precision, 3)
     e = gpu_model(shape, 4, 64, precision, 3)

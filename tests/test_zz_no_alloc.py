@@ -43,12 +43,15 @@ def test_noalloc_layernorm_backward_matches_allocating_entry_point():
     ensure_built()
     import torch
     from step_gpt_train_03_b300 import gpt2lib as G
-    # two calls in a row, of different shapes, so stale scratch from the first would show
-    for N, C, seed in ((8192, 768, 2), (1000, 1024, 5)):
+    # calls in a row, of different shapes, so stale scratch from an earlier call would
+    # show; (4096, 2048) is the largest shape accepted at C = 2048 (its partial sums fill
+    # the array exactly) and runs the shared-memory pipelined kernel with one block per SM
+    for N, C, seed in ((8192, 768, 2), (1000, 1024, 5), (4096, 2048, 7), (8192, 768, 2)):
         args = _inputs(N, C, seed)
         scratch = torch.empty(G.layernorm_backward_scratch_bytes(N, C), dtype=torch.uint8, device="cuda")
         ref = _run(G.layernorm_backward, *args, scratch=scratch)
         got = _run(G.layernorm_backward_noalloc, *args)
+        G.layer_check()
         for r, g in zip(ref, got):
             assert norm_err(g, r) <= GRAD_TOL
 
@@ -57,11 +60,16 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     ensure_built()
     import torch
     from step_gpt_train_03_b300 import gpt2lib as G
-    N, C = 32768, 2048                     # needs 16 MiB of partials, the array holds 4 MiB
-    assert G.layernorm_backward_scratch_bytes(N, C) > G.NOALLOC_SCRATCH_BYTES
-    t = torch.zeros((N, C), device="cuda")
-    v = torch.zeros(C, device="cuda")
-    r = torch.ones(N, device="cuda")
-    with pytest.raises(G.GPT2Error) as e:
-        G.layernorm_backward_noalloc(t, v.clone(), v.clone(), t, t, v, r, r)
-    assert e.value.status == 1
+    # at C = 2048 the partials take min(ceil(N / 16), 296) blocks x 2C floats: 4 MiB at
+    # N = 4096 (accepted above), 4 MiB + 16 KiB at N = 4097, 4.625 MiB (296 blocks) from
+    # N = 4721 on
+    for N in (4097, 32768):
+        C = 2048
+        assert G.layernorm_backward_scratch_bytes(N, C) > G.NOALLOC_SCRATCH_BYTES
+        t = torch.zeros((N, C), device="cuda")
+        v = torch.zeros(C, device="cuda")
+        r = torch.ones(N, device="cuda")
+        with pytest.raises(G.GPT2Error) as e:
+            G.layernorm_backward_noalloc(t, v.clone(), v.clone(), t, t, v, r, r)
+        assert e.value.status == 1
+    assert G.layernorm_backward_scratch_bytes(4096, 2048) == G.NOALLOC_SCRATCH_BYTES
