@@ -314,23 +314,28 @@ def ours(args):
         # the library's whole-step call: one CUDA graph launch once the shape is captured
         m.step_device(toks[i], tgts[i], *hp, t, want_loss=False)
 
-    # warm-up: the first W-2 steps traced in full (every kernel class's share of the
-    # step, launched kernel by kernel), the last two untraced (the second captures the
-    # step graph that the timed region replays)
+    # warm-up (W >= 3 steps): one untraced step (the first step of the shape: lazy set-up,
+    # kernel by kernel), then W-2 steps traced in full (every kernel class's share of a
+    # warm step, launched kernel by kernel), then one untraced step that captures the
+    # step graph the timed region replays
     n_traced = max(1, args.warmup - 2)
+    G.profile_enable([])
+    with torch.cuda.stream(stream):
+        step(0, 1)
+    stream.synchronize()
     G.profile_enable(None)
     G.profile_reset()
     with torch.cuda.stream(stream):
-        for i in range(n_traced):
-            step(i, i + 1)
+        for i in range(1, 1 + n_traced):
+            step(i % n_batches, i + 1)
     stream.synchronize()
     m.check()
     warm_prof = G.profile_read()
     G.profile_reset()
     G.profile_enable([])
     with torch.cuda.stream(stream):
-        for i in range(n_traced, args.warmup):
-            step(i, i + 1)
+        for i in range(1 + n_traced, max(args.warmup, 2 + n_traced)):
+            step(i % n_batches, i + 1)
     stream.synchronize()
     m.check()
     shares = {k: v["ms"] for k, v in warm_prof.items()}
@@ -352,7 +357,7 @@ def ours(args):
     torch.cuda.synchronize()
     clocks.start()
     win_ms, win_clk = [], []
-    t_next = args.warmup
+    t_next = max(args.warmup, 2 + n_traced)
     for wi in range(max(1, args.windows)):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if wi > 0:

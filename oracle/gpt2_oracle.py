@@ -317,6 +317,101 @@ def sample_token(z, V, temperature, seed, b):
     return k, lo, float(c[k]), thr, float(c[-1])
 
 
+# --------------------------------------------------------------------------------------
+# fp8 (e4m3) quantization: the lower-precision variant (yinghuohong.cn article, section
+# "脚动完成每一个层前向/反向流传": precision planned to go from fp32 down to fp16 or lower)
+# --------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code):
+    """The real number an e4m3 byte stands for, from the format's definition: sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 is subnormal
+    (m/8 * 2^-6); S.1111.111 is NaN and there is no infinity, so the largest finite
+    magnitude is 1.75 * 2^8 = 448."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)])
+
+
+def e4m3_round(x):
+    """Round to the nearest e4m3 value, ties to the even mantissa, saturating at +-448
+    (finite inputs).  With e = floor(log2|x|) clamped to >= -6 (the subnormal range
+    shares the spacing of the smallest binade), the grid spacing is 2^(e-3)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    # log2 of values just below a power of two can land on it: correct by comparison
+    e = np.where(2.0 ** e > a, e - 1, e)
+    e = np.where(2.0 ** (e + 1) <= a, e + 1, e)
+    e = np.maximum(e, -6.0)
+    step = 2.0 ** (e - 3)
+    r = np.round(a / step) * step            # numpy rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.sign(x) * r
+
+
+def e4m3_encode(x):
+    """Codes (uint8) of e4m3_round(x): the sign bit of x (a negative value that rounds to
+    zero is -0) plus the index of the magnitude in the table of non-negative values
+    (which is increasing)."""
+    x = np.asarray(x, dtype=np.float64)
+    r = e4m3_round(x)
+    pos = E4M3_TABLE[:127]                    # codes 0x00..0x7E: 0 .. 448, increasing
+    idx = np.searchsorted(pos, np.abs(r))
+    return (idx | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def pow2_scale_exponent(amax):
+    """The largest k with amax * 2^k <= 448 (amax > 0 finite; 0 for amax == 0): a
+    power-of-two scale, so scaling and unscaling are exact.  With amax = f 2^e, f in
+    [0.5, 1): k = 9 - e if f <= 0.875 (448 = 0.875 2^9), else 8 - e."""
+    a = float(amax)
+    if a == 0.0:
+        return 0
+    f, e = math.frexp(a)
+    return (9 - e) if f <= 0.875 else (8 - e)
+
+
+def quantize_rows_e4m3(y):
+    """Row-wise scaling: for each row, k = pow2_scale_exponent(max |y|), values
+    e4m3_round(y * 2^k).  Returns (dequantized rows, codes, exponents k)."""
+    y = np.asarray(y)
+    rows = y.reshape(-1, y.shape[-1])
+    ks = np.array([pow2_scale_exponent(np.abs(r).max()) for r in rows])
+    scaled = rows * np.exp2(ks)[:, None]
+    q = e4m3_round(scaled)
+    deq = q * np.exp2(-ks)[:, None]
+    return deq.reshape(y.shape), e4m3_encode(scaled).reshape(y.shape), ks
+
+
+def quantize_tensor_e4m3(w):
+    """Tensor-wise scaling: k = pow2_scale_exponent(max |w|), values e4m3_round(w 2^k).
+    Returns (dequantized tensor, codes, k)."""
+    w = np.asarray(w)
+    k = pow2_scale_exponent(np.abs(w).max())
+    scaled = w * 2.0 ** k
+    return e4m3_round(scaled) * 2.0 ** -k, e4m3_encode(scaled), k
+
+
+def matmul_forward_fp8(x, w, bias):
+    """The fp8 linear layer: the input quantized row by row and the weight as one tensor
+    (power-of-two scales, e4m3 values), multiplied exactly, then unscaled; the bias is
+    added unquantized.  The backward of the layer is matmul_backward on the unquantized
+    input and weight (the quantization passes gradients straight through)."""
+    xq, _, _ = quantize_rows_e4m3(x)
+    wq, _, _ = quantize_tensor_e4m3(w)
+    return matmul_forward(xq, wq, bias)
+
+
 PARAM_FILE_MAGIC = 20240326
 PARAM_FILE_VERSION = 3
 
@@ -364,6 +459,9 @@ class GPT2Oracle:
         # the pre-softmax scores are part of the pages' activation list but the backward
         # does not read them; large runs may drop them to save host memory
         self.keep_preatt = True
+        # fp8 variant: the two products whose input is a layernorm output (qkv, fc) take
+        # e4m3 operands (matmul_forward_fp8); everything else as in the plain model
+        self.fp8 = False
 
     def _views(self, flat):
         out, off = {}, 0
@@ -396,12 +494,13 @@ class GPT2Oracle:
         a["encoded"] = x
         for l in range(L):
             ln1, m1, r1 = layernorm_forward(x, p["ln1w"][l], p["ln1b"][l])
-            qkv = matmul_forward(ln1, p["qkvw"][l], p["qkvb"][l])
+            mm_in = matmul_forward_fp8 if self.fp8 else matmul_forward
+            qkv = mm_in(ln1, p["qkvw"][l], p["qkvb"][l])
             atty, preatt, att = attention_forward(qkv, NH)
             attproj = matmul_forward(atty, p["attprojw"][l], p["attprojb"][l])
             res2 = residual_forward(x, attproj)
             ln2, m2, r2 = layernorm_forward(res2, p["ln2w"][l], p["ln2b"][l])
-            fch = matmul_forward(ln2, p["fcw"][l], p["fcb"][l])
+            fch = mm_in(ln2, p["fcw"][l], p["fcb"][l])
             g = gelu_forward(fch)
             fcproj = matmul_forward(g, p["fcprojw"][l], p["fcprojb"][l])
             res3 = residual_forward(res2, fcproj)

@@ -5,27 +5,30 @@
 // backward.  Per head: S = Q K^T / sqrt(64) over keys j <= t, P = softmax(S), O = P V;
 // the forward keeps O and each row's log-sum-exp only.
 //
-// Forward kernel, persistent, one CTA per SM, 320 threads; work item = (128-query
-// tile, batch*head), heaviest tiles (most keys) first:
-//   warp 0     TMA producer: Q tile (double-buffered across work items), then K and V
-//              tiles of 128 keys through a 4-slot ring
-//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M=128, N=128, K=64) into one of two
-//              TMEM S buffers, then O += P V (M=128, N=64, K=128) into the TMEM O buffer
-//   warps 2-9  softmax, two warps per query row quadrant (each takes half the keys of a
-//              tile): read the S row from TMEM, keep the running max / sum, write P
-//              (bf16) into one of two shared buffers for the P V product; at the end
-//              normalise O and write it with a TMA store, plus the row LSE
-// The softmax reads its 64 scores of an S row from TMEM once (the S buffer is released
-// right away, so S(j+2) can be computed while the softmax works on tile j), takes the
-// row max over the warp pair, then the exponentials from registers.
+// Forward kernel, persistent, one CTA per SM, 320 threads.  A work item is a pair of
+// 128-query tiles of one (batch, head): tile 2p+1 (slot A) and tile 2p (slot B), which
+// read the same key / value tiles 0..2p+1 (slot B stops one tile earlier), so each K
+// and V tile is loaded once for both.  Items go heaviest first, dealt to the CTAs in
+// snake order (forward in even rounds, backward in odd ones) to even out the tiles per
+// CTA.
+//   warp 0     TMA producer: the item's Q tiles (double-buffered across items), then
+//              K_j and V_j through a ring of AT_RING slots
+//   warp 1     TMEM owner and MMA issuer: S_X = Q_X K_j^T (M=128, N=128, K=64) into the
+//              slot's S buffer; O_X += P_X V_j (M=128, N=64, K=128) with P_X, the A
+//              operand, read from TMEM (no shared-memory traffic for it)
+//   warps 2-5  softmax of slot A, warps 6-9 softmax of slot B: one query row per
+//              thread (the warp's TMEM lane quadrant), all 128 keys of a tile; the row
+//              max is a thread's own, so no exchange between warps
+// The two softmax warpgroups work on different tiles and are not synchronised with each
+// other, so while one waits for its scores or finishes a tile, the other keeps the
+// exponential unit busy, and the tensor pipe always has the other slot's products.
 // The exponent reference of a row (its max so far) is only raised when a new score
 // exceeds it by more than 2^8: then, and only then, the row of O in TMEM is rescaled
-// (after waiting for the P V in flight).  Numerator and denominator always use the same
-// reference, so O / l is exact; p <= 256 stays far inside fp32 and bf16 range.  With P
-// double-buffered, the softmax of tile j+1 never waits for P V of tile j, and S(j+1) is
-// computed while the softmax works on tile j.  Every wait is bounded.
-// The tensor maps are 3-D (columns, T, B) so no tile ever reads or writes past its own
-// sequence.
+// (after the P V in flight has landed).  Numerator and denominator always use the same
+// reference, so O / l is exact; p <= 256 stays far inside fp32 and bf16 range.
+// TMEM (512 columns): S_A, S_B (128 each), O_A, O_B (64 each), P_A, P_B (bf16 pairs, 64
+// each).  Every wait is bounded.  The tensor maps are 3-D (columns, T, B) so no tile
+// ever reads or writes past its own sequence.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -39,13 +42,12 @@
 #include "tc_ptx.cuh"
 #include "../../include/gpt2.h"
 
-
 #define AT_HS 64
 #define AT_BM 128                  // queries per tile
 #define AT_BN 128                  // keys per tile
-#define AT_RING 4                  // K / V tile slots: K_{j+1} never waits on P V_{j-1}
+#define AT_RING 6                  // K / V tile slots of the forward
 #define AT_TILE_BYTES (128 * 64 * 2)
-#define AT_THREADS 320               // producer, MMA issuer, 8 compute warps (2 per TMEM lane quadrant)
+#define AT_THREADS 320             // producer, MMA issuer, 8 compute warps
 #define AT_LOG2E 1.4426950408889634f
 
 #define AT_RESCALE_LOG2 8.0f        // raise a row's exponent reference only past 2^8
@@ -59,16 +61,15 @@ __device__ __forceinline__ float ex2_fast(float x) {
 }
 
 struct AtSmem {
-    static constexpr int Q_OFF = 0;                                          // 2 x 16 KB
-    static constexpr int RING_OFF = Q_OFF + 2 * AT_TILE_BYTES;
-    static constexpr int P_OFF = RING_OFF + AT_RING * AT_TILE_BYTES;         // 2 x (2 x 16 KB)
-    static constexpr int O_OFF = P_OFF + 4 * AT_TILE_BYTES;                  // output staging
-    static constexpr int X_OFF = O_OFF + AT_TILE_BYTES;                      // row max / sum exchange
-    static constexpr int BAR_OFF = X_OFF + 3 * 1024;
-    // q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], s_free[2],
-    // p_full[2], o_done[2], o_free, done; then tmem address and abort flag
-    static constexpr int NBAR = 4 + 2 * AT_RING + 4 + 4 + 2;
+    static constexpr int Q_OFF = 0;                                          // [item parity][slot]
+    static constexpr int RING_OFF = Q_OFF + 4 * AT_TILE_BYTES;
+    static constexpr int O_OFF = RING_OFF + AT_RING * AT_TILE_BYTES;         // [slot] output staging
+    static constexpr int BAR_OFF = O_OFF + 2 * AT_TILE_BYTES;
+    // q_full[2], q_empty[2], ring_full[R], ring_empty[R]; per slot s_full, s_free,
+    // p_full, o_done, o_free; done; then tmem address and abort flag
+    static constexpr int NBAR = 4 + 2 * AT_RING + 10 + 1;
     static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
+    static_assert(TOTAL <= 232448, "shared memory of one CTA");
 };
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -82,26 +83,44 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
     uint64_t* q_empty = bars + 2;
     uint64_t* ring_full = bars + 4;
     uint64_t* ring_empty = ring_full + AT_RING;
-    uint64_t* s_full = ring_empty + AT_RING;
+    uint64_t* s_full = ring_empty + AT_RING;   // [slot]
     uint64_t* s_free = s_full + 2;
     uint64_t* p_full = s_free + 2;
     uint64_t* o_done = p_full + 2;
     uint64_t* o_free = o_done + 2;
-    uint64_t* done = o_free + 1;
+    uint64_t* done = o_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = B * NH;
     const int nqt = (Tn + AT_BM - 1) / AT_BM;
-    const int n_items = nqt * BH;
+    const int npairs = (nqt + 1) / 2;
+    const int n_items = npairs * BH;
+    const int G = gridDim.x, cta = blockIdx.x;
+    // the k-th item of this CTA (snake order), or -1
+    auto item_at = [&](int k) -> int {
+        const int it = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+        return it < n_items ? it : -1;
+    };
+    // item -> (pair p, b*h); tiles per slot: A = tile 2p+1 (when it exists), B = tile 2p
+    auto decode = [&](int it, int& p, int& bh, int& nkA, int& nkB) {
+        p = npairs - 1 - it / BH;
+        bh = it % BH;
+        nkA = (2 * p + 1 < nqt) ? 2 * p + 2 : 0;
+        nkB = 2 * p + 1;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
         for (int i = 0; i < AT_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 1); }
-        for (int i = 0; i < 2; i++) { mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 8); }
-        for (int i = 0; i < 2; i++) { mbar_init(&p_full[i], 8); mbar_init(&o_done[i], 1); }
-        mbar_init(o_free, 8);
+        for (int x = 0; x < 2; x++) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&s_free[x], 4);
+            mbar_init(&p_full[x], 4);
+            mbar_init(&o_done[x], 1);
+            mbar_init(&o_free[x], 4);
+        }
         mbar_init(done, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -117,21 +136,30 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t TM_S = tmem_base;          // S buffers at columns 0 and 128
-    const uint32_t TM_O = tmem_base + 256;    // O at columns 256..319
+    auto TM_S = [&](int x) { return tmem_base + x * AT_BN; };          // columns 0, 128
+    auto TM_O = [&](int x) { return tmem_base + 256 + x * AT_HS; };    // 256, 320
+    auto TM_P = [&](int x) { return tmem_base + 384 + x * 64; };       // 384, 448
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int rc = 0, local = 0;
+            int rc = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
-                const int qt = nqt - 1 - it / BH, bh = it % BH, b = bh / NH, h = bh % NH;
-                const int qb = local & 1;
-                if (!mbar_wait(&q_empty[qb], ((local >> 1) & 1) ^ 1, abort_flag, err)) break;
-                mbar_expect_tx(&q_full[qb], AT_TILE_BYTES);
-                tma_load_3d(smem + S::Q_OFF + qb * AT_TILE_BYTES, &tmQKV, &q_full[qb], h * AT_HS, qt * AT_BM, b);
-                const int nk = qt + 1;
+            for (int k = 0; ok; k++) {
+                const int it = item_at(k);
+                if (it < 0) break;
+                int p, bh, nkA, nkB;
+                decode(it, p, bh, nkA, nkB);
+                const int b = bh / NH, h = bh % NH;
+                const int qb = k & 1;
+                if (!mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1, abort_flag, err)) break;
+                mbar_expect_tx(&q_full[qb], (nkA ? 2 : 1) * AT_TILE_BYTES);
+                if (nkA)
+                    tma_load_3d(smem + S::Q_OFF + (qb * 2 + 0) * AT_TILE_BYTES, &tmQKV, &q_full[qb], h * AT_HS,
+                                (2 * p + 1) * AT_BM, b);
+                tma_load_3d(smem + S::Q_OFF + (qb * 2 + 1) * AT_TILE_BYTES, &tmQKV, &q_full[qb], h * AT_HS,
+                            2 * p * AT_BM, b);
+                const int nk = nkA ? nkA : nkB;
                 for (int j = 0; j < nk && ok; j++) {
                     for (int kv = 0; kv < 2; kv++, rc++) {
                         const int s = rc % AT_RING;
@@ -155,52 +183,65 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(AT_BM, AT_BN, false, false);
             constexpr uint32_t IDESC_O = idesc_bf16(AT_BM, AT_HS, false, true);
-            int rc = 0, sc = 0, pc = 0, local = 0;
+            int rc = 0;
+            int sn[2] = {0, 0}, pn[2] = {0, 0}, nitems[2] = {0, 0};   // per slot: S, P V, items so far
             bool ok = true;
-            // S = Q K^T for the K tile at ring index kidx into S buffer sc % 2
-            auto issue_s = [&](uint32_t q_addr, int kidx) -> bool {
-                const int sb = sc & 1, slot = kidx % AT_RING;
-                if (!mbar_wait(&s_free[sb], ((sc >> 1) & 1) ^ 1, abort_flag, err)) return false;
-                if (!mbar_wait(&ring_full[slot], (kidx / AT_RING) & 1, abort_flag, err)) return false;
-                tc_fence_after();
-                const uint32_t k_addr = smem_u32(smem + S::RING_OFF + slot * AT_TILE_BYTES);
+            for (int k = 0; ok; k++) {
+                const int it = item_at(k);
+                if (it < 0) break;
+                int p, bh, nkx[2];
+                decode(it, p, bh, nkx[0], nkx[1]);
+                const int nk = nkx[0] ? nkx[0] : nkx[1];
+                const int qb = k & 1;
+                if (!mbar_wait(&q_full[qb], (k >> 1) & 1, abort_flag, err)) break;
+                // K_j at ring index rc + 2j, V_j at rc + 2j + 1.  Order per j: S_A(j), S_B(j),
+                // then O_A += P_A(j-1) V_{j-1}, O_B += P_B(j-1) V_{j-1}
+                for (int j = 0; j <= nk && ok; j++) {
+                    if (j < nk) {
+                        const int kidx = rc + 2 * j, ks = kidx % AT_RING;
+                        if (!mbar_wait(&ring_full[ks], (kidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
+                        const uint32_t k_addr = smem_u32(smem + S::RING_OFF + ks * AT_TILE_BYTES);
+                        for (int x = 0; x < 2; x++) {
+                            if (j >= nkx[x]) continue;
+                            if (!mbar_wait(&s_free[x], (sn[x] & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t q_addr = smem_u32(smem + S::Q_OFF + (qb * 2 + x) * AT_TILE_BYTES);
 #pragma unroll
-                for (int k = 0; k < AT_HS / 16; k++)
-                    tc_mma(TM_S + sb * AT_BN, sdesc(q_addr + k * 32, 16, 1024), sdesc(k_addr + k * 32, 16, 1024),
-                           IDESC_S, k > 0 ? 1u : 0u);
-                tc_commit(&s_full[sb]);
-                tc_commit(&ring_empty[slot]);
-                sc++;
-                return true;
-            };
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, local++) {
-                const int qt = nqt - 1 - it / BH;
-                const int nk = qt + 1;
-                const int qb = local & 1;
-                if (!mbar_wait(&q_full[qb], (local >> 1) & 1, abort_flag, err)) break;
-                const uint32_t q_addr = smem_u32(smem + S::Q_OFF + qb * AT_TILE_BYTES);
-                // K_j sits at ring index rc + 2j, V_j at rc + 2j + 1
-                if (!issue_s(q_addr, rc)) break;
-                for (int j = 0; j < nk && ok; j++) {
-                    if (j + 1 < nk && !issue_s(q_addr, rc + 2 * (j + 1))) { ok = false; break; }
-                    if (j == nk - 1) tc_commit(&q_empty[qb]);   // Q buffer free once the last S completes
-                    // O += P_j V_j, P_j in buffer pc % 2
-                    const int vidx = rc + 2 * j + 1, vslot = vidx % AT_RING;
-                    const int pb = pc & 1;
-                    if (!mbar_wait(&ring_full[vslot], (vidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
-                    if (!mbar_wait(&p_full[pb], (pc >> 1) & 1, abort_flag, err)) { ok = false; break; }
-                    if (j == 0 && local > 0 && !mbar_wait(o_free, (local - 1) & 1, abort_flag, err)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t p_addr = smem_u32(smem + S::P_OFF + pb * 2 * AT_TILE_BYTES);
-                    const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vslot * AT_TILE_BYTES);
+                            for (int kk = 0; kk < AT_HS / 16; kk++)
+                                tc_mma(TM_S(x), sdesc(q_addr + kk * 32, 16, 1024), sdesc(k_addr + kk * 32, 16, 1024),
+                                       IDESC_S, kk > 0 ? 1u : 0u);
+                            tc_commit(&s_full[x]);
+                            sn[x]++;
+                        }
+                        if (!ok) break;
+                        tc_commit(&ring_empty[ks]);                      // K_j read by both products
+                        if (j == nk - 1) tc_commit(&q_empty[qb]);        // the item's Q tiles too
+                    }
+                    if (j >= 1) {
+                        const int jj = j - 1;
+                        const int vidx = rc + 2 * jj + 1, vs = vidx % AT_RING;
+                        if (!mbar_wait(&ring_full[vs], (vidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
+                        const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vs * AT_TILE_BYTES);
+                        for (int x = 0; x < 2; x++) {
+                            if (jj >= nkx[x]) continue;
+                            if (!mbar_wait(&p_full[x], pn[x] & 1, abort_flag, err)) { ok = false; break; }
+                            // the first P V of an item overwrites O: its last readout must be done
+                            if (jj == 0 && nitems[x] > 0 &&
+                                !mbar_wait(&o_free[x], (nitems[x] - 1) & 1, abort_flag, err)) { ok = false; break; }
+                            tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < AT_BN / 16; k++)
-                        tc_mma(TM_O, sdesc(p_addr + (k >> 2) * AT_TILE_BYTES + (k & 3) * 32, 16, 1024),
-                               sdesc(v_addr + k * 2048, 8192, 1024), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
-                    tc_commit(&o_done[pb]);
-                    tc_commit(&ring_empty[vslot]);
-                    pc++;
+                            for (int kk = 0; kk < AT_BN / 16; kk++)
+                                tc_mma_ts(TM_O(x), TM_P(x) + kk * 8, sdesc(v_addr + kk * 2048, 8192, 1024), IDESC_O,
+                                          (jj > 0 || kk > 0) ? 1u : 0u);
+                            tc_commit(&o_done[x]);
+                            pn[x]++;
+                        }
+                        if (!ok) break;
+                        tc_commit(&ring_empty[vs]);
+                    }
                 }
+                for (int x = 0; x < 2; x++)
+                    if (nkx[x]) nitems[x]++;
                 rc += 2 * nk;
             }
             tc_commit(done);
@@ -210,187 +251,182 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
         }
     } else {
         // ------------------------------------------------------------ softmax warps 2..9
-        // Two warps per TMEM lane quadrant: `half` picks columns [64*half, 64*half + 64) of
-        // every S tile (and [32*half, 32*half + 32) of O).  The pair swaps its row maxima
-        // through shared memory once per tile; the row sums stay split until the end.
-        const int lane_grp = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const int r = lane_grp * 32 + lane;                 // query row in the tile
+        const int x = (warp - 2) >> 2;                       // slot: 0 = A (warps 2-5), 1 = B
+        const int lane_grp = warp & 3;                       // TMEM lanes 32*lane_grp .. +31
+        const int r = lane_grp * 32 + lane;                  // query row in the tile
         const uint32_t lrow = (uint32_t)(lane_grp * 32) << 16;
-        uint8_t* obuf = smem + S::O_OFF;
-        float* xmax = reinterpret_cast<float*>(smem + S::X_OFF);   // [tile parity][half][128]
-        float* xsum = xmax + 512;                                   // [half][128]
-        const int pair_bar = 2 + lane_grp;                          // named barrier of the pair
-        const float sl2 = AT_LOG2E * 0.125f;                // log2(e) / sqrt(64)
-        int sc = 0, pc = 0, local = 0;
-        int seen0 = 0, seen1 = 0;                           // o_done phases observed, per P buffer
-        bool alive = true;
-        // wait until P V number `i` has completed (phases of each buffer are observed in order)
-        auto wait_pv = [&](int i) -> bool {
-            const int bb = i & 1, ph = i >> 1;
-            if ((bb ? seen1 : seen0) > ph) return true;
+        const int leader = 64 + 128 * x;                     // the warpgroup's store thread
+        const int wg_bar = 1 + x;                            // its named barrier (128 threads)
+        uint8_t* obuf = smem + S::O_OFF + x * AT_TILE_BYTES;
+        const float sl2 = AT_LOG2E * 0.125f;                 // log2(e) / sqrt(64)
+        int sn = 0, pn = 0, pv_seen = 0;
+        bool staged = false, alive = true;
+        auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
             int okw = 1;
-            if (lane == 0) okw = mbar_wait(&o_done[bb], ph & 1, abort_flag, err) ? 1 : 0;
+            if (lane == 0) okw = mbar_wait(bar, parity, abort_flag, err) ? 1 : 0;
             okw = __shfl_sync(0xffffffffu, okw, 0);
-            if (bb) seen1 = ph + 1; else seen0 = ph + 1;
             __syncwarp();
             return okw != 0;
         };
-        for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x, local++) {
-            const int qt = nqt - 1 - it / BH, bh = it % BH, b = bh / NH, h = bh % NH;
-            const int nk = qt + 1;
+        // wait until P V number n of this slot has completed (completions observed in order)
+        auto wait_pv = [&](int n) -> bool {
+            if (n < pv_seen) return true;
+            pv_seen = n + 1;
+            return wait_bar(&o_done[x], n & 1);
+        };
+        for (int k = 0; alive; k++) {
+            const int it = item_at(k);
+            if (it < 0) break;
+            int p, bh, nkA, nkB;
+            decode(it, p, bh, nkA, nkB);
+            const int nkx = x == 0 ? nkA : nkB;
+            if (nkx == 0) continue;                          // slot A of a last, odd tile
+            const int b = bh / NH, h = bh % NH;
+            const int qt = x == 0 ? 2 * p + 1 : 2 * p;
             const int q = qt * AT_BM + r;
-            const int pc0 = pc;                             // index of this item's first P V
-            float m = -INFINITY, l = 0.f;                   // exponent reference, partial running sum
-            for (int j = 0; j < nk; j++) {
-                const int sb = sc & 1;
-                int okw = 1;
-                if (lane == 0) okw = mbar_wait(&s_full[sb], (sc >> 1) & 1, abort_flag, err) ? 1 : 0;
-                okw = __shfl_sync(0xffffffffu, okw, 0);
-                if (!okw) { alive = false; break; }
-                __syncwarp();
-                tc_fence_after();
-                const uint32_t srow = TM_S + sb * AT_BN + lrow;
-                // keys after the query are masked on the diagonal tile: columns > lim
-                const int lim = (j == nk - 1) ? (q - j * AT_BN) : AT_BN;
-                const bool masked = lim < AT_BN;            // only the diagonal tile
-                // this warp's 64 scores of the row, read once; the S buffer is then free
-                uint32_t sr[64];
-                {
-                    uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                    uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                    tmem_ld32(srow + half * 64, s0);
-                    tmem_ld32(srow + half * 64 + 32, s1);
+            float m = -INFINITY, l = 0.f;                    // exponent reference, running sum
+            for (int j = 0; j < nkx; j++) {
+                // The row's 128 scores come in two halves of 64 (registers hold one half and
+                // its temporaries): the first half is read for its max only, the second is
+                // read and kept; after the second half's exponentials the first half is read
+                // again, and the S buffer is then free for S(j+1).
+                const bool diag = j == nkx - 1;              // keys after the query are masked
+                auto load_half = [&](int hf, uint32_t (&v)[2][32]) {
+                    tmem_ld32(TM_S(x) + lrow + hf * 64, v[0]);
+                    tmem_ld32(TM_S(x) + lrow + hf * 64 + 32, v[1]);
                     tmem_ld_wait();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[sb]);
-                if (masked) {
+                    if (diag) {
 #pragma unroll
-                    for (int i = 0; i < 64; i++)
-                        if (half * 64 + i > lim) sr[i] = __float_as_uint(-INFINITY);
-                }
-                // max over this warp's 64 columns, then over the pair
+                        for (int i = 0; i < 64; i++)
+                            if (hf * 64 + i > r) v[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+                    }
+                };
+                auto half_max = [&](const uint32_t (&v)[2][32]) -> float {
+                    float a0 = __uint_as_float(v[0][0]), a1 = __uint_as_float(v[0][1]);
+                    float a2 = __uint_as_float(v[1][0]), a3 = __uint_as_float(v[1][1]);
+#pragma unroll
+                    for (int i = 2; i < 32; i += 2) {
+                        a0 = fmax3(a0, __uint_as_float(v[0][i]), __uint_as_float(v[0][i + 1]));
+                        a2 = fmax3(a2, __uint_as_float(v[1][i]), __uint_as_float(v[1][i + 1]));
+                    }
+                    return fmax3(a0, a2, fmaxf(a1, a3));
+                };
+                float rs = 0.f;
+                // p = 2^(s sl2 - m) for one half: bf16 pairs into P (TMEM), partial row sum
+                auto exp_half = [&](int hf, const uint32_t (&v)[2][32], float mref) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; c8++) {
+                        float pv[16];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            const int e = c8 * 16 + i;
+                            const float2 a = __ffma2_rn(make_float2(__uint_as_float(v[e >> 5][e & 31]),
+                                                                    __uint_as_float(v[e >> 5][(e & 31) + 1])),
+                                                        make_float2(sl2, sl2), make_float2(-mref, -mref));
+                            pv[i] = ex2_fast(a.x);
+                            pv[i + 1] = ex2_fast(a.y);
+                        }
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
+                            pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        tmem_st8(TM_P(x) + lrow + hf * 32 + c8 * 8, pk);
+                        // pairwise tree sum; the levels with w >= 2 in packed pairs
+#pragma unroll
+                        for (int w = 8; w > 1; w >>= 1)
+#pragma unroll
+                            for (int i = 0; i < w; i += 2) {
+                                const float2 s2 = __fadd2_rn(make_float2(pv[i], pv[i + 1]),
+                                                             make_float2(pv[i + w], pv[i + w + 1]));
+                                pv[i] = s2.x;
+                                pv[i + 1] = s2.y;
+                            }
+                        rs += pv[0] + pv[1];
+                    }
+                };
+                if (!wait_bar(&s_full[x], sn & 1)) { alive = false; break; }
+                tc_fence_after();
                 float mx;
-                {
-                    // 64 -> 22 -> 8 -> 3 -> 1 with three-input maxima
-                    float a[22], b[8];
-#pragma unroll
-                    for (int i = 0; i < 21; i++)
-                        a[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]), __uint_as_float(sr[3 * i + 2]));
-                    a[21] = __uint_as_float(sr[63]);
-#pragma unroll
-                    for (int i = 0; i < 7; i++) b[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
-                    b[7] = a[21];
-                    mx = fmax3(fmax3(b[0], b[1], b[2]), fmax3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
-                }
-                mx *= sl2;                                  // scaling by sl2 > 0 keeps the max
-                float* xm = xmax + (sc & 1) * 256;
-                xm[half * 128 + r] = mx;
-                named_bar(pair_bar, 64);
-                mx = fmaxf(mx, xm[(half ^ 1) * 128 + r]);
-                // raise the reference only when needed; then O must be rescaled, after the
-                // P V still in flight for this item has landed
+                uint32_t sv[2][32];
+                load_half(0, sv);
+                mx = half_max(sv);
+                load_half(1, sv);
+                mx = fmaxf(mx, half_max(sv)) * sl2;          // scaling by sl2 > 0 keeps the max
                 const bool raise = mx > m + AT_RESCALE_LOG2;
                 const float m_new = raise ? mx : m;
-                const float corr = ex2_fast(m - m_new);     // 1 when unchanged, 0 on the first tile
+                const float corr = ex2_fast(m - m_new);      // 1 when unchanged, 0 on the first tile
                 if (__any_sync(0xffffffffu, raise && j > 0)) {
-                    if (!wait_pv(pc0 + j - 1)) { alive = false; break; }
+                    // rescale this warp's rows of O once the P V in flight has landed
+                    if (!wait_pv(pn - 1)) { alive = false; break; }
                     tc_fence_after();
-                    uint32_t rr[32];
-                    tmem_ld32(TM_O + lrow + half * 32, rr);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; i++) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
-                    tmem_st32(TM_O + lrow + half * 32, rr);
+                    for (int hh = 0; hh < 2; hh++) {
+                        uint32_t rr[32];
+                        tmem_ld32(TM_O(x) + lrow + hh * 32, rr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; i++) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
+                        tmem_st32(TM_O(x) + lrow + hh * 32, rr);
+                    }
                     tmem_st_wait();
                 }
                 m = m_new;
-                // the P buffer of this tile was last read by P V two tiles back
-                const int pb = pc & 1;
-                if (pc >= 2 && !wait_pv(pc - 2)) { alive = false; break; }
-                uint8_t* pbuf = smem + S::P_OFF + pb * 2 * AT_TILE_BYTES;
-                // p = 2^(s - m) (masked scores are -inf: p = 0), partial row sum, P into the
-                // swizzled A operand
-                float rs = 0.f;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; h2++) {
-                    const int c = half * 64 + h2 * 32;
-                    float p[32];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[h2 * 32 + i]), __uint_as_float(sr[h2 * 32 + i + 1])),
-                                                    make_float2(sl2, sl2), make_float2(-m, -m));
-                        p[i] = ex2_fast(a.x);
-                        p[i + 1] = ex2_fast(a.y);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const int ch = (c >> 3) + k;
-                        Vec<bf16> pv;
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) pv.set2(e, p[8 * k + e], p[8 * k + e + 1]);
-                        *reinterpret_cast<uint4*>(pbuf + (ch >> 3) * AT_TILE_BYTES + r * 128 +
-                                                  (((ch & 7) ^ (r & 7)) << 4)) = pv.v;
-                    }
-                    // pairwise tree sum; the levels with w >= 2 in packed pairs
-#pragma unroll
-                    for (int w = 16; w > 1; w >>= 1)
-#pragma unroll
-                        for (int i = 0; i < w; i += 2) {
-                            const float2 x = __fadd2_rn(make_float2(p[i], p[i + 1]), make_float2(p[i + w], p[i + w + 1]));
-                            p[i] = x.x;
-                            p[i + 1] = x.y;
-                        }
-                    rs += p[0] + p[1];
-                }
-                l = l * corr + rs;
-                fence_async_smem();
+                // P of this tile goes where the previous tile's P was read by P V
+                if (j > 0 && !wait_pv(pn - 1)) { alive = false; break; }
+                tc_fence_after();
+                exp_half(1, sv, m);
+                load_half(0, sv);
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[pb]);
-                sc++;
-                pc++;
+                if (lane == 0) mbar_arrive(&s_free[x]);
+                sn++;
+                exp_half(0, sv, m);
+                l = l * corr + rs;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[x]);
+                pn++;
             }
             if (!alive) break;
-            // the last P V of the item, then normalise and write this row of O
-            if (!wait_pv(pc - 1)) break;
+            // the item's last P V, then normalise and write this row of O
+            if (!wait_pv(pn - 1)) break;
             tc_fence_after();
-            float o[32];
-            {
+            float o[64];
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
                 uint32_t rr[32];
-                tmem_ld32(TM_O + lrow + half * 32, rr);
+                tmem_ld32(TM_O(x) + lrow + hh * 32, rr);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; i++) o[i] = __uint_as_float(rr[i]);
+                for (int i = 0; i < 32; i++) o[hh * 32 + i] = __uint_as_float(rr[i]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(o_free);
-            xsum[half * 128 + r] = l;
-            named_bar(pair_bar, 64);
-            const float lt = l + xsum[(half ^ 1) * 128 + r];
-            const float inv = 1.0f / lt;
-            // the previous item's O store must have finished reading the staging buffer
-            if (threadIdx.x == 64) bulk_wait_read<0>();
-            named_bar(1, 256);
+            if (lane == 0) mbar_arrive(&o_free[x]);
+            const float inv = 1.0f / l;
+            // the previous item's store must have finished reading the staging buffer
+            if (staged && threadIdx.x == leader) bulk_wait_read<0>();
+            named_bar(wg_bar, 128);
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int ch = half * 4 + k;
+            for (int ch = 0; ch < 8; ch++) {
                 Vec<bf16> ov;
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) ov.set2(e, o[8 * k + e] * inv, o[8 * k + e + 1] * inv);
+                for (int e = 0; e < 8; e += 2) ov.set2(e, o[8 * ch + e] * inv, o[8 * ch + e + 1] * inv);
                 *reinterpret_cast<uint4*>(obuf + r * 128 + ((ch ^ (r & 7)) << 4)) = ov.v;
             }
             fence_async_smem();
-            named_bar(1, 256);
-            if (threadIdx.x == 64) {
+            named_bar(wg_bar, 128);
+            if (threadIdx.x == leader) {
                 tma_store_3d(&tmO, obuf, h * AT_HS, qt * AT_BM, b);
                 bulk_commit();
             }
-            if (half == 0 && q < Tn) lse[(size_t)bh * Tn + q] = (m + log2f(lt)) / AT_LOG2E;
+            staged = true;
+            if (q < Tn) lse[(size_t)bh * Tn + q] = (m + log2f(l)) / AT_LOG2E;
         }
-        if (threadIdx.x == 64) bulk_wait<0>();
+        if (threadIdx.x == leader) bulk_wait<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -410,28 +446,31 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
 //   DQ   item = (128-query tile t, b*h); for every key tile u <= t:
 //          S = Q_t K_u^T, dP = dO_t V_u^T; P = 2^(S log2e/8 - LSE log2e), dS = P (dP - D)
 //          dQ += dS K_u;  then dQ / 8 to dqkv.
-// Warp 0 loads (the item's two row tiles once; the per-u tiles through a 3-stage ring
-// with, in DKV mode, that u's LSE and D vectors); warp 1 issues
-// the MMAs (the next S/dP pair is issued before the dV/dK (dQ) products of the current
-// one); warps 2-9 compute, two warps per TMEM lane quadrant, each on half the columns of
-// a tile (a TMEM lane is a key row in DKV mode, a query row in DQ mode).  The operands
-// the compute warps produce for the products are double-buffered, so tile u+1 is
-// computed while the products of tile u run: dS (dS^T) in shared memory and, in DKV
-// mode, P^T (bf16, two per 32-bit column) in TMEM, read there as the A operand of
-// dV += P^T dO_u.
+// Warp 0 loads (the item's two row tiles once; the per-u tiles through a ring with, in
+// DKV mode, that u's LSE and D vectors); warp 1 issues the MMAs (the next S/dP pair is
+// issued before the dV/dK (dQ) products of the current one); warps 2-9 compute, two warps
+// per TMEM lane quadrant, each on half the columns of a tile (a TMEM lane is a key row in
+// DKV mode, a query row in DQ mode).  The operands the compute warps produce for the
+// N = 64 products -- P^T and dS^T (DKV), dS (DQ), bf16 pairs -- go to TMEM and are read
+// there as the A operand, so those products fetch only their 64-wide B operand from
+// shared memory.  TMEM (512 columns): S (S^T) 128, dP (dP^T) 128, dV or dQ 64, dK 64, then
+// DKV: P^T 64 and dS^T 64 (single-buffered: the compute warps compute half a tile before
+// they need the buffer back); DQ: dS 2 x 64 (double-buffered).
 #define AB_STAGE_BYTES (2 * AT_TILE_BYTES + 1024)   // two tiles + LSE[128] + D[128]
 
 template <bool DKV>
 struct AbSmem {
-    static constexpr int RING = 3;
+    static constexpr int RING = 4;
     static constexpr int R_OFF = 0;                                        // 2 row tiles
     static constexpr int RING_OFF = R_OFF + 2 * AT_TILE_BYTES;
-    static constexpr int DS_OFF = RING_OFF + RING * AB_STAGE_BYTES;        // 2 x dS or dS^T, 32 KB each
-    static constexpr int BAR_OFF = DS_OFF + 4 * AT_TILE_BYTES;
+    static constexpr int STG_OFF = RING_OFF + RING * AB_STAGE_BYTES;       // output staging, 2 tiles
+    static constexpr int BAR_OFF = STG_OFF + 2 * AT_TILE_BYTES;
     // rr_full, rr_empty, ring_full[RING], ring_empty[RING], x_full, x_free, pds_full[2],
     // pds_free[2], acc_free, done; tmem address, abort flag
     static constexpr int NBAR = 2 + 2 * RING + 8;
     static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 1024;
+    static_assert(TOTAL <= 232448, "shared memory of one CTA");
+    static constexpr int NPB = DKV ? 1 : 2;          // P / dS buffers in TMEM
 };
 
 template <bool DKV>
@@ -494,9 +533,10 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // S (S^T), dP (dP^T), dV or dQ, dK, then (DKV) two P^T buffers of 64 columns
+    // S (S^T), dP (dP^T), dV or dQ, dK; then DKV: P^T, dS^T; DQ: dS[2]
     const uint32_t TM_X1 = tmem_base, TM_X2 = tmem_base + 128, TM_A1 = tmem_base + 256, TM_A2 = tmem_base + 320;
     const uint32_t TM_P = tmem_base + 384;
+    auto TM_DS = [&](int pb) { return tmem_base + (DKV ? 448 : 384 + 64 * pb); };
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
@@ -546,7 +586,6 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             constexpr uint32_t IDESC_X = idesc_bf16(AT_BM, AT_BN, false, false);
             constexpr uint32_t IDESC_A = idesc_bf16(AT_BM, AT_HS, false, true);
             const uint32_t r0 = smem_u32(smem + S::R_OFF), r1 = r0 + AT_TILE_BYTES;
-            const uint32_t dsbase = smem_u32(smem + S::DS_OFF);
             int rc = 0, xc = 0, gc = 0, local = 0;
             bool ok = true;
             // the S / dP pair for the ring stage of index `idx`
@@ -578,28 +617,25 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                     if (i == nu - 1) tc_commit(rr_empty);          // row tiles free after the last S / dP
                     const int slot = (rc + i) % AB_RING;
                     const uint32_t st = smem_u32(smem + S::RING_OFF + slot * AB_STAGE_BYTES);
-                    const int pb = gc & 1;                           // P / dS buffer of this tile
-                    const uint32_t dsbuf = dsbase + pb * 2 * AT_TILE_BYTES;
-                    if (!mbar_wait(&pds_full[pb], (gc >> 1) & 1, abort_flag, err)) { ok = false; break; }
+                    const int pb = gc % S::NPB;                      // P / dS buffer of this tile
+                    if (!mbar_wait(&pds_full[pb], (gc / S::NPB) & 1, abort_flag, err)) { ok = false; break; }
                     if (i == 0 && local > 0 && !mbar_wait(acc_free, (local - 1) & 1, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     if (DKV) {
-                        // dV += P^T dO_u (P^T from TMEM, 8 columns per 16 queries) ; dK += dS^T Q_u
-                        const uint32_t pt = TM_P + pb * 64;
+                        // dV += P^T dO_u ; dK += dS^T Q_u (A operands from TMEM, 8 columns per 16 queries)
 #pragma unroll
                         for (int k = 0; k < AT_BN / 16; k++) {
-                            const uint32_t aoff = (k >> 2) * AT_TILE_BYTES + (k & 3) * 32;
-                            tc_mma_ts(TM_A1, pt + k * 8, sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024), IDESC_A,
+                            tc_mma_ts(TM_A1, TM_P + k * 8, sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024), IDESC_A,
                                       (i > 0 || k > 0));
-                            tc_mma(TM_A2, sdesc(dsbuf + aoff, 16, 1024), sdesc(st + k * 2048, 8192, 1024), IDESC_A,
-                                   (i > 0 || k > 0));
+                            tc_mma_ts(TM_A2, TM_DS(pb) + k * 8, sdesc(st + k * 2048, 8192, 1024), IDESC_A,
+                                      (i > 0 || k > 0));
                         }
                     } else {
-                        // dQ += dS K_u
+                        // dQ += dS K_u (dS from TMEM)
 #pragma unroll
                         for (int k = 0; k < AT_BN / 16; k++)
-                            tc_mma(TM_A1, sdesc(dsbuf + (k >> 2) * AT_TILE_BYTES + (k & 3) * 32, 16, 1024),
-                                   sdesc(st + k * 2048, 8192, 1024), IDESC_A, (i > 0 || k > 0));
+                            tc_mma_ts(TM_A1, TM_DS(pb) + k * 8, sdesc(st + k * 2048, 8192, 1024), IDESC_A,
+                                      (i > 0 || k > 0));
                     }
                     tc_commit(&pds_free[pb]);
                     tc_commit(&ring_empty[slot]);
@@ -619,17 +655,10 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
         const int r = lane_grp * 32 + lane;                 // TMEM lane = row of the item's tile
         const uint32_t lrow = (uint32_t)(lane_grp * 32) << 16;
         const float sl2 = AT_LOG2E * 0.125f;
-        uint8_t* dsbase = smem + S::DS_OFF;
+        uint8_t* stg = smem + S::STG_OFF;
         int rc = 0, xc = 0, gc = 0, local = 0;
-        int pf_seen0 = 0, pf_seen1 = 0;                     // pds_free completions observed per buffer
-        int stg_pending = -1;                               // dS buffer an item's store may still be reading
-        // before this buffer is written again, the store issued from it has read it
-        auto stg_release = [&](int buf) {
-            if (stg_pending != buf) return;
-            if (threadIdx.x == 64) bulk_wait_read<0>();
-            named_bar(1, 256);
-            stg_pending = -1;
-        };
+        int pf_seen[2] = {0, 0};                            // pds_free completions observed per buffer
+        bool stg_pending = false;                           // an item's output store may still read stg
         bool alive = true;
         auto wait_one = [&](uint64_t* bar, uint32_t parity) -> bool {
             int okw = 1;
@@ -638,18 +667,13 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             __syncwarp();
             return okw != 0;
         };
-        // wait for the dV/dK (dQ) products of tile n: completion n >> 1 of buffer n & 1's
+        // wait for the dV/dK (dQ) products of tile n: completion n / NPB of buffer n % NPB's
         // barrier (each buffer's completions are observed in order)
         auto wait_pds_free = [&](int n) -> bool {
-            const int b = n & 1, need = (n >> 1) + 1;
-            if (b == 0) {
-                if (pf_seen0 >= need) return true;
-                pf_seen0 = need;
-            } else {
-                if (pf_seen1 >= need) return true;
-                pf_seen1 = need;
-            }
-            return wait_one(&pds_free[b], (n >> 1) & 1);
+            const int b = n % S::NPB, need = n / S::NPB + 1;
+            if (pf_seen[b] >= need) return true;
+            pf_seen[b] = need;
+            return wait_one(&pds_free[b], (n / S::NPB) & 1);
         };
         for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x, local++) {
             int t, bh, u0, u1;
@@ -667,15 +691,15 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 const uint8_t* st = smem + S::RING_OFF + (rc % AB_RING) * AB_STAGE_BYTES;
                 const float* Lv = reinterpret_cast<const float*>(st + 2 * AT_TILE_BYTES);
                 const float* Dv = Lv + 128;
-                const int pb = gc & 1;
-                uint8_t* dsbuf = dsbase + pb * 2 * AT_TILE_BYTES;
+                const int pb = gc % S::NPB;
 #pragma unroll 1
-                for (int c = half * 64; c < half * 64 + 64; c += 32) {
+                for (int ci = 0; ci < 2; ci++) {
+                    const int c = half * 64 + ci * 32;      // first column of this chunk
                     uint32_t s1[32], s2[32];
                     tmem_ld32(TM_X1 + lrow + c, s1);
                     tmem_ld32(TM_X2 + lrow + c, s2);
                     tmem_ld_wait();
-                    if (c == half * 64 + 32) {
+                    if (ci == 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(x_free);      // S / dP TMEM may be overwritten
@@ -722,33 +746,31 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                             ds[i + 1] = g.y;
                         }
                     }
-                    // the products of tile gc-2, and an item's output store, must have
-                    // finished reading this buffer
-                    if (c == half * 64 && gc >= 2 && !wait_pds_free(gc - 2)) { alive = false; break; }
-                    if (c == half * 64) stg_release(pb);
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const int ch = (c >> 3) + k;
-                        const int off = (ch >> 3) * AT_TILE_BYTES + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-                        Vec<bf16> dv;
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) dv.set2(e, ds[8 * k + e], ds[8 * k + e + 1]);
-                        *reinterpret_cast<uint4*>(dsbuf + off) = dv.v;
+                    // the products of tile gc - NPB must have read this tile's buffers (checked
+                    // once, after the first chunk's arithmetic)
+                    if (ci == 0 && gc >= S::NPB) {
+                        if (!wait_pds_free(gc - S::NPB)) { alive = false; break; }
+                        tc_fence_after();
                     }
+                    // bf16 pairs along the row: 16 TMEM columns per 32 values
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; k++) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(ds[2 * k], ds[2 * k + 1]);
+                        pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+                    }
+                    tmem_st16(TM_DS(pb) + lrow + (c >> 1), pk);
                     if (DKV) {
-                        // P^T row r, queries c..c+31: 16 columns of bf16 pairs
-                        uint32_t pk[16];
 #pragma unroll
                         for (int k = 0; k < 16; k++) {
                             __nv_bfloat162 h2 = __floats2bfloat162_rn(p[2 * k], p[2 * k + 1]);
                             pk[k] = *reinterpret_cast<uint32_t*>(&h2);
                         }
-                        tmem_st16(TM_P + pb * 64 + lrow + (c >> 1), pk);
+                        tmem_st16(TM_P + lrow + (c >> 1), pk);
                     }
                 }
                 if (!alive) break;
-                if (DKV) tmem_st_wait();
-                fence_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pds_full[pb]);
@@ -756,10 +778,6 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             if (!alive) break;
             // accumulators of the item: wait for its last products, read, release, store
             if (!wait_pds_free(gc - 1)) break;
-            // staging: the last tile's dS buffer (its products are done; the next item's
-            // first tile uses the other buffer)
-            uint8_t* stg = dsbase + ((gc - 1) & 1) * 2 * AT_TILE_BYTES;
-            stg_release((gc - 1) & 1);
             tc_fence_after();
             float a1[32], a2[32];
             {
@@ -778,7 +796,12 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free);
-            // stage in the (now idle) P / dS buffers, 128B-swizzled rows, then TMA-store
+            // the previous item's store must have finished reading the staging buffers
+            if (stg_pending) {
+                if (threadIdx.x == 64) bulk_wait_read<0>();
+                named_bar(1, 256);
+            }
+            // stage 128B-swizzled rows, then TMA-store
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 const int ch = half * 4 + k;
@@ -810,7 +833,7 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 }
                 bulk_commit();
             }
-            stg_pending = (gc - 1) & 1;   // read before that buffer is next written
+            stg_pending = true;
         }
         if (threadIdx.x == 64) bulk_wait<0>();
     }
@@ -867,7 +890,7 @@ int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const _
     if (C / NH != AT_HS || (((uintptr_t)qkv | (uintptr_t)out) & 15)) return GPT2_EUNSUPPORTED;
     CUtensorMap tq, to;
     if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&to, out, C, Tn, B, C)) return GPT2_EUNSUPPORTED;
-    const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
+    const int items = ((Tn + AT_BM - 1) / AT_BM + 1) / 2 * B * NH;      // pairs of query tiles
     const int grid = items < g_sms ? items : g_sms;
     attention_tc_forward_kernel<<<grid, AT_THREADS, AtSmem::TOTAL, s>>>(tq, to, lse, B, Tn, C, NH, err);
     rt_note_launches(1);
