@@ -450,7 +450,7 @@ def ours(args):
               f"of the same {args.steps} steps ({ms_traced / args.steps:.3f} ms/step with the events)")
     if d_fl > 0:
         achieved = d_fl / (d_ms / 1e3) / 1e12
-        if prec == "bf16":
+        if prec in ("bf16", "fp8"):
             # primary: the burst peak (measured at ~full clock, as these kernels run);
             # beside it the sustained peak (measured at a lower, power-capped clock) and
             # the burst peak scaled to the SM clock seen during the headline window
@@ -460,6 +460,9 @@ def ours(args):
                      "frac_clock_normalised": (achieved / (peak * sm_med / sm_max)) if sm_med else None,
                      "clock_normalisation": f"peak x {sm_med} / {sm_max} MHz (median SM clock of the headline window)"}
             peak_src = f"{src} bf16 burst (cuBLAS 8192^3, best of 10)"
+            if prec == "fp8":
+                peak_src += ("; the fp8 workload's matmul family mixes e4m3 (qkv, fc forward; nominal rate 2x bf16) "
+                             "and bf16 products, reported against the bf16 peak")
         else:
             # the fp32 path's matmuls run on the FP32 FMA units: 148 SMs x 128 lanes x 2 flops
             # at the 2032 MHz maximum SM clock
@@ -499,15 +502,17 @@ def ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prec == "bf16" else "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "fp8", "fp32": "f32"}[prec],
         "data": "synthetic (seeded Zipf s=1.1 int32 token stream, fresh batch per step; random-init weights)",
         "config": {"workload": w.name,
                    "shape": (f"L={w.shape.num_layers}, C={w.shape.channels}, NH={w.shape.num_heads}, "
                              f"V={w.shape.vocab_size} padded to {w.shape.padded_vocab_size}"),
                    "global_batch": B * world, "seq_len": T,
                    "parallelism": "replicas only" if world > 1 else "single GPU",
-                   "precision": ("bf16 weights/activations, fp32 master weights and AdamW state" if prec == "bf16"
-                                 else "fp32 throughout"),
+                   "precision": {"bf16": "bf16 weights/activations, fp32 master weights and AdamW state",
+                                 "fp8": ("e4m3 qkv and fc forward products (row-scaled layernorm outputs, tensor-scaled "
+                                         "weights); bf16 elsewhere; fp32 master weights and AdamW state"),
+                                 "fp32": "fp32 throughout"}[prec],
                    "l2": "no flush: the step's working set (GBs of activations) is far larger than the 126 MB L2"},
         "clocks": clk,
         "windows": {"n": len(win_ms), "steps_each": args.steps,

@@ -61,7 +61,17 @@ typedef struct {
  *            activation grads; matmuls and attention on the tcgen05 tensor cores with
  *            fp32 accumulation; fp32 master weights, parameter grads, AdamW state,
  *            layernorm statistics, softmax/loss arithmetic. */
-enum { GPT2_FP32 = 0, GPT2_BF16 = 1 };
+/* GPT2_FP8:  as GPT2_BF16, except that the two products whose input is a layernorm
+ *            output (the qkv and MLP-fc forward products) take e4m3 operands on the
+ *            tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation): the layernorm writes
+ *            its output also as e4m3 codes with one power-of-two scale per row (that row's
+ *            largest magnitude maps into the top binade, <= 448), the qkv and fc weights
+ *            have e4m3 shadows with one power-of-two scale per (tensor, layer), refreshed
+ *            from the fp32 master weights after every update.  The backward pass, the
+ *            other products and the LM head stay bf16 (the quantization passes gradients
+ *            straight through).  yinghuohong.cn llm.c article, section
+ *            "脚动完成每一个层前向/反向流传": precision taken from fp32 down to fp16 or lower. */
+enum { GPT2_FP32 = 0, GPT2_BF16 = 1, GPT2_FP8 = 2 };
 
 enum {
     GPT2_OK = 0,
@@ -253,6 +263,35 @@ int gpt2_layernorm_forward(float* out, float* mean, float* rstd, const float* in
 
 /* Scratch bytes gpt2_layernorm_backward needs for N rows of C. */
 size_t gpt2_layernorm_backward_scratch_bytes(int N, int C);
+
+/* The layernorm forward of the fp8 mode (fp32 tensors here): out, mean, rstd as
+ * gpt2_layernorm_forward, and out also as e4m3 codes (N, C bytes, 8-byte aligned) with
+ * row_deq[r] = 2^-k, k the largest integer with max_c |out[r, c]| * 2^k <= 448 (0 for an
+ * all-zero row, clamped to [-126, 126]); code = e4m3(out * 2^k), round to nearest even,
+ * saturating.  The codes are taken of the fp32 values. */
+int gpt2_layernorm_forward_fp8(float* out, uint8_t* codes, float* row_deq, float* mean, float* rstd,
+                               const float* inp, const float* weight, const float* bias, int N, int C,
+                               void* stream);
+
+/* Per-tensor e4m3 quantization of x (n fp32 values, n % 4 == 0, 16-byte aligned):
+ * codes (n bytes, 16-byte aligned) = e4m3(x * 2^k) and deq[0] = 2^-k with k as above for
+ * the tensor's largest |x| -- the fp8 mode's weight shadows.  amax_scratch: one device
+ * word, overwritten. */
+int gpt2_quantize_e4m3(uint8_t* codes, float* deq, unsigned* amax_scratch, const float* x, size_t n,
+                       void* stream);
+
+/* The fp8 mode's forward product: out (M,N) bf16 = epilogue((inp * inp_deq per row)
+ * (weight * weight_deq[0])^T + bias), inp (M,K) and weight (N,K) e4m3 codes, inp_deq (M)
+ * and weight_deq (1) fp32 device arrays, bias bf16 (nullable), epilogue and aux as
+ * gpt2_matmul_forward_fused.  K a multiple of 16, N of 8, 16-byte aligned operands. */
+int gpt2_matmul_forward_fp8(void* out, void* aux, const uint8_t* inp, const float* inp_deq,
+                            const uint8_t* weight, const float* weight_deq, const void* bias, int M, int N,
+                            int K, int epilogue, void* stream);
+
+/* fp8 mode: the model's e4m3 weight shadows.  which 0: qkvw (L, 3C, C bytes), 1: fcw
+ * (L, 4C, C); *deq points at L per-layer unscaling factors.  GPT2_ESTATE for another
+ * precision. */
+int gpt2_fp8_weights(GPT2* model, int which, uint8_t** codes, float** deq);
 
 /* Layernorm backward, fp32.  dinp += dx (accumulates); dweight += sum_rows dout*xhat;
  * dbias += sum_rows dout.  The column sums are deterministic (fixed-order two-stage

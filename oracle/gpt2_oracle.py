@@ -373,12 +373,14 @@ def e4m3_encode(x):
 def pow2_scale_exponent(amax):
     """The largest k with amax * 2^k <= 448 (amax > 0 finite; 0 for amax == 0): a
     power-of-two scale, so scaling and unscaling are exact.  With amax = f 2^e, f in
-    [0.5, 1): k = 9 - e if f <= 0.875 (448 = 0.875 2^9), else 8 - e."""
+    [0.5, 1): k = 9 - e if f <= 0.875 (448 = 0.875 2^9), else 8 - e; clamped to
+    [-126, 126] so that 2^k and 2^-k are normal fp32 numbers."""
     a = float(amax)
     if a == 0.0:
         return 0
     f, e = math.frexp(a)
-    return (9 - e) if f <= 0.875 else (8 - e)
+    k = (9 - e) if f <= 0.875 else (8 - e)
+    return max(-126, min(126, k))
 
 
 def quantize_rows_e4m3(y):

@@ -59,6 +59,8 @@ struct TcEpi {
     const bf16* bias;   // nullable
     void* aux;          // GELU pre-activation out / residual in / pre-activation in
     long ldo;           // row stride of out and aux (elements)
+    const float* a_deq; // e4m3 products: per-row unscaling factor of A (M floats)
+    const float* b_deq; // e4m3 products: unscaling factor of B (one float)
 };
 
 // Staging buffers per epilogue warp: four for the GELU epilogues of a CTA pair (two
@@ -106,7 +108,10 @@ __device__ __forceinline__ int stg_off(int r, int j) { return r * 64 + ((j ^ ((r
 // accumulator in both CTAs; each CTA's epilogue drains its own 128 rows of TMEM and
 // frees the accumulator on the leader's barrier.  Per CTA this halves the B operand
 // reads and shared-memory traffic of each MMA.  NACC accumulators of BN columns.
-template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1>
+// F8: e4m3 operands (kind::f8f6f4, K-major A and B only): a k-block is 128 elements, so
+// every byte offset, box and descriptor is that of the bf16 kernel; the epilogue
+// multiplies the accumulator by the row's A factor times the B factor.
+template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1, bool F8 = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux, int M, int N,
@@ -128,7 +133,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (M + TC_BM - 1) / TC_BM, n_tiles = (N + BN - 1) / BN;
-    const int nkb = (K + TC_BK - 1) / TC_BK;
+    constexpr int BKE = F8 ? 2 * TC_BK : TC_BK;        // elements per k-block (128 bytes)
+    static_assert(!F8 || (!A_MN && !B_MN), "e4m3 operands are K-major");
+    const int nkb = (K + BKE - 1) / BKE;
     const int kb_per = (nkb + splits - 1) / splits;
     const int m_groups = (m_tiles + CL - 1) / CL;
     const int units = m_groups * n_tiles * splits;
@@ -203,36 +210,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if constexpr (CL == 1) {
                         mbar_expect_tx(&full[s], S::STAGE_BYTES);
                         if (!A_MN) {
-                            tma_load_2d(a, &tmA, &full[s], kb * TC_BK, mt * TC_BM);
+                            tma_load_2d(a, &tmA, &full[s], kb * BKE, mt * TC_BM);
                         } else {
 #pragma unroll
                             for (int j = 0; j < TC_BM / 64; j++)
-                                tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * TC_BK);
+                                tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * BKE);
                         }
                         if (!B_MN) {
-                            tma_load_2d(b, &tmB, &full[s], kb * TC_BK, nb0);
+                            tma_load_2d(b, &tmB, &full[s], kb * BKE, nb0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BN / 64; j++)
-                                tma_load_2d(b + j * 8192, &tmB, &full[s], nb0 + j * 64, kb * TC_BK);
+                                tma_load_2d(b + j * 8192, &tmB, &full[s], nb0 + j * 64, kb * BKE);
                         }
                     } else {
                         // both CTAs' bytes are counted on the leader's barrier
                         const uint32_t fb = full_lead + s * 8;
                         if (leader) mbar_expect_tx(&full[s], CL * S::STAGE_BYTES);
                         if (!A_MN) {
-                            tma_load_2d_pair(a, &tmA, fb, kb * TC_BK, mt * TC_BM);
+                            tma_load_2d_pair(a, &tmA, fb, kb * BKE, mt * TC_BM);
                         } else {
 #pragma unroll
                             for (int j = 0; j < TC_BM / 64; j++)
-                                tma_load_2d_pair(a + j * 8192, &tmA, fb, mt * TC_BM + j * 64, kb * TC_BK);
+                                tma_load_2d_pair(a + j * 8192, &tmA, fb, mt * TC_BM + j * 64, kb * BKE);
                         }
                         if (!B_MN) {
-                            tma_load_2d_pair(b, &tmB, fb, kb * TC_BK, nb0);
+                            tma_load_2d_pair(b, &tmB, fb, kb * BKE, nb0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BH / 64; j++)
-                                tma_load_2d_pair(b + j * 8192, &tmB, fb, nb0 + j * 64, kb * TC_BK);
+                                tma_load_2d_pair(b + j * 8192, &tmB, fb, nb0 + j * 64, kb * BKE);
                         }
                     }
                 }
@@ -262,7 +269,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---------------------------------------------------------- MMA issuer
         // (in a pair only the leader's thread issues; its MMAs drive both tensor cores)
         if (lane == 0 && (CL == 1 || leader)) {
-            constexpr uint32_t IDESC = idesc_bf16(TC_BM * CL, BN, A_MN, B_MN);
+            constexpr uint32_t IDESC = F8 ? idesc_e4m3(TC_BM * CL, BN, A_MN, B_MN) : idesc_bf16(TC_BM * CL, BN, A_MN, B_MN);
             int it = 0, local = 0;
             bool ok = true;
             for (int u = ufirst; u < units && ok; u += ustep, local++) {
@@ -286,8 +293,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         // MN-major: 16 k-rows are two 1024-byte swizzle atoms
                         const uint64_t ad = A_MN ? sdesc(a + k * 2048, 8192, 1024) : sdesc(a + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? sdesc(b + k * 2048, 8192, 1024) : sdesc(b + k * 32, 16, 1024);
-                        if constexpr (CL == 1) tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
-                        else tc_mma_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        const uint32_t accf = (kb > kb0 || k > 0) ? 1u : 0u;
+                        if constexpr (F8) {
+                            if constexpr (CL == 1) tc_mma_f8(d_tmem, ad, bd, IDESC, accf);
+                            else tc_mma_pair_f8(d_tmem, ad, bd, IDESC, accf);
+                        } else {
+                            if constexpr (CL == 1) tc_mma(d_tmem, ad, bd, IDESC, accf);
+                            else tc_mma_pair(d_tmem, ad, bd, IDESC, accf);
+                        }
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs have read it
                     if constexpr (CL == 1) tc_commit(&empty[s]);
@@ -380,6 +393,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 float v2[64];
 #pragma unroll
                 for (int i = 0; i < 32; i++) { v2[i] = __uint_as_float(r0[i]); v2[32 + i] = __uint_as_float(r1[i]); }
+                if constexpr (F8) {
+                    // unscale: this lane's row factor times the weight's factor
+                    const int row = row0 + lane;
+                    const float sc = (row < M ? ep.a_deq[row] : 0.f) * ep.b_deq[0];
+#pragma unroll
+                    for (int i = 0; i < 64; i++) v2[i] *= sc;
+                }
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     float* v = v2 + 32 * h;
@@ -575,8 +595,10 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     cuuint64_t strides[1] = {ld * ebytes};
     cuuint32_t box[2] = {(cuuint32_t)(128 / ebytes), box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, ebytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt = ebytes == 2   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : ebytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -599,12 +621,12 @@ static bool make_epi_map(CUtensorMap* map, const void* base, uint64_t inner, uin
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1>
+template <int BN, int EPI, bool A_MN, bool B_MN, int CL = 1, bool F8 = false>
 static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                      const CUtensorMap& tx, int M, int N, int K, int splits, const TcEpi& ep, unsigned* err) {
     using SM = TcSmem<BN, CL, TcBufs<EPI, CL>::value>;
     static int max_clusters = 0;            // co-resident clusters of CL CTAs (0: not yet queried)
-    auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN, CL>;
+    auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN, CL, F8>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(TC_THREADS);
@@ -664,6 +686,38 @@ int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, c
         case EPI_RESID:
             return cl == 2 ? launch_tc<256, EPI_RESID, false, false, 2>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
                            : launch_tc<256, EPI_RESID, false, false, 1>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        default: return GPT2_EUNSUPPORTED;
+    }
+}
+
+int gemm_tc_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const float* inp_deq, const uint8_t* W,
+                        const float* w_deq, const bf16* bias, int M, int N, int K, int epi, bf16* aux, unsigned* err) {
+    // as gemm_tc_forward with e4m3 operands: K a multiple of 16 (16-byte rows for TMA)
+    if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
+    if (N % 8 || K % 16 || M < 1 || !inp_deq || !w_deq || !aligned16(out) || !aligned16(inp) || !aligned16(W) ||
+        (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
+        return GPT2_EUNSUPPORTED;
+    CUtensorMap ta, tb, to, tx;
+    const int cl = (N <= 768 && K <= 768) ? 1 : 2;
+    if (!make_map(&ta, inp, K, M, K, TC_BM, 1) || !make_map(&tb, W, K, N, K, 256 / cl, 1) ||
+        !make_epi_map(&to, out, N, M, N))
+        return GPT2_EUNSUPPORTED;
+    if (aux) {
+        if (!make_epi_map(&tx, aux, N, M, N)) return GPT2_EUNSUPPORTED;
+    } else {
+        tx = to;
+    }
+    TcEpi ep{out, bias, aux, (long)N, inp_deq, w_deq};
+    switch (epi) {
+        case EPI_STORE:
+            return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_STORE, false, false, 1, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_GELU:
+            return cl == 2 ? launch_tc<256, EPI_GELU, false, false, 2, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_GELU, false, false, 1, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
+        case EPI_RESID:
+            return cl == 2 ? launch_tc<256, EPI_RESID, false, false, 2, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
+                           : launch_tc<256, EPI_RESID, false, false, 1, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err);
         default: return GPT2_EUNSUPPORTED;
     }
 }

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stddef.h>
+#include <stdint.h>
 
 // 1 when the tensor-core kernels can run on the current device, else 0.
 int gemm_tc_available();
@@ -20,6 +21,13 @@ size_t gemm_tc_scratch_floats(size_t M, size_t N);
 int gemm_tc_forward(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* inp,
                     const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, int N, int K, int epi,
                     __nv_bfloat16* aux, unsigned* err);
+
+// The same with e4m3 operands (tcgen05 kind::f8f6f4): inp (M,K) and W (N,K) are e4m3 codes,
+// row m of inp stands for codes * inp_deq[m] and W for codes * w_deq[0]; the accumulator
+// is multiplied by both factors before the epilogue.  K a multiple of 16.
+int gemm_tc_forward_fp8(cudaStream_t s, __nv_bfloat16* out, const uint8_t* inp, const float* inp_deq,
+                        const uint8_t* W, const float* w_deq, const __nv_bfloat16* bias, int M, int N, int K,
+                        int epi, __nv_bfloat16* aux, unsigned* err);
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation).
 int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16* dout,

@@ -32,6 +32,12 @@
 
 static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
+#define RC(x)                          \
+    do {                               \
+        int rc_ = (x);                 \
+        if (rc_ != GPT2_OK) return rc_; \
+    } while (0)
+
 // ------------------------------------------------------------------ handle
 enum { P_WTE = 0, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB, P_LN2W, P_LN2B,
        P_FCW, P_FCB, P_FCPROJW, P_FCPROJB, P_LNFW, P_LNFB };
@@ -68,6 +74,14 @@ struct GPT2 {
     size_t red_arena_floats;
     int *tokens, *targets;             // staging copies of the last batch
     unsigned* err;
+    // fp8 mode: e4m3 copy of the layernorm output feeding the qkv / fc products (one
+    // layer at a time) with its per-row unscaling factors; e4m3 shadows of qkvw and fcw
+    // with per-(tensor, layer) factors and the amax words they are computed from
+    uint8_t* lnq;
+    float* lnq_deq;
+    uint8_t *wq_qkv, *wq_fc;
+    float* wq_deq;                     // [0, L): qkvw of layer l; [L, 2L): fcw of layer l
+    unsigned* wq_amax;
     // state
     int B, T;
     int have_fwd, have_targets;
@@ -82,10 +96,12 @@ struct GPT2 {
     long long g_kernels;
 };
 
+static int quantize_model_weights(GPT2* m);
+
 static const size_t kAlign = 1024;
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-static size_t act_elt(int prec) { return prec == GPT2_BF16 ? 2 : 4; }
+static size_t act_elt(int prec) { return prec == GPT2_FP32 ? 4 : 2; }   // bf16 and fp8 modes: bf16 activations
 
 // Walk the workspace layout: with base == nullptr only sizes are computed.
 static size_t plan(GPT2* m, char* base) {
@@ -104,7 +120,7 @@ static size_t plan(GPT2* m, char* base) {
     m->grads = (float*)take(nf * 4);
     m->m = (float*)take(nf * 4);
     m->v = (float*)take(nf * 4);
-    m->wbf = m->prec == GPT2_BF16 ? (bf16*)take(nf * 2) : nullptr;
+    m->wbf = m->prec != GPT2_FP32 ? (bf16*)take(nf * 2) : nullptr;
     m->encoded = take(BT * C * es);
     m->ln1 = take(L * BT * C * es);
     m->qkv = take(L * BT * 3 * C * es);
@@ -161,18 +177,32 @@ static size_t plan(GPT2* m, char* base) {
     m->tokens = (int*)take(BT * 4);
     m->targets = (int*)take(BT * 4);
     m->err = (unsigned*)take(16);
+    if (m->prec == GPT2_FP8) {
+        m->lnq = (uint8_t*)take(BT * C);
+        m->lnq_deq = (float*)take(BT * 4);
+        m->wq_qkv = (uint8_t*)take(L * 3 * C * C);
+        m->wq_fc = (uint8_t*)take(L * 4 * C * C);
+        m->wq_deq = (float*)take(2 * L * 4);
+        m->wq_amax = (unsigned*)take(align_up(2 * L * 4, 16));
+    } else {
+        m->lnq = nullptr;
+        m->lnq_deq = nullptr;
+        m->wq_qkv = m->wq_fc = nullptr;
+        m->wq_deq = nullptr;
+        m->wq_amax = nullptr;
+    }
     return align_up(off, kAlign);
 }
 
 static int validate_cfg(const GPT2Config* c, int maxB, int maxT, int prec) {
     if (!c) return GPT2_EINVAL;
-    if (prec != GPT2_FP32 && prec != GPT2_BF16) return GPT2_EINVAL;
+    if (prec != GPT2_FP32 && prec != GPT2_BF16 && prec != GPT2_FP8) return GPT2_EINVAL;
     if (c->num_layers < 1 || c->num_heads < 1 || c->channels < 64) return GPT2_EINVAL;
     if (c->channels % 64 != 0 || c->channels % c->num_heads != 0) return GPT2_EINVAL;
     if (c->channels > 2048) return GPT2_EUNSUPPORTED;
     if (c->channels / c->num_heads > ATT_MAX_HS || (c->channels / c->num_heads) % 8) return GPT2_EUNSUPPORTED;
     // bf16 runs every product on the tensor cores: attention there takes head size 64
-    if (prec == GPT2_BF16 && c->channels / c->num_heads != 64) return GPT2_EUNSUPPORTED;
+    if (prec != GPT2_FP32 && c->channels / c->num_heads != 64) return GPT2_EUNSUPPORTED;
     if (c->vocab_size < 1 || c->padded_vocab_size < c->vocab_size) return GPT2_EINVAL;
     if (c->padded_vocab_size % 64 != 0) return GPT2_EINVAL;
     if (c->max_seq_len < 1 || maxB < 1 || maxT < 1 || maxT > c->max_seq_len) return GPT2_EINVAL;
@@ -254,7 +284,7 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     m->ws_bytes = workspace_bytes;
     m->stream = (cudaStream_t)stream;
     // bf16 runs only on the tensor-core kernels; no other path is built for it
-    if (precision == GPT2_BF16 && (!gemm_tc_available() || !attention_tc_available())) {
+    if (precision != GPT2_FP32 && (!gemm_tc_available() || !attention_tc_available())) {
         free(m);
         return GPT2_EUNSUPPORTED;
     }
@@ -344,6 +374,7 @@ extern "C" int gpt2_sync_params(GPT2* m) {
         rt_note_launches(1);
         CK(cudaGetLastError());
     }
+    RC(quantize_model_weights(m));
     int rc = launch_zero(m->stream, m->m, m->n_flat * 4 * 2);   // m and v are adjacent
     return rc;
 }
@@ -354,7 +385,7 @@ extern "C" int gpt2_sample(GPT2* m, int pos, float temperature, unsigned long lo
     if (!m->have_fwd || m->have_targets) return GPT2_ESTATE;
     if (pos < 0 || pos >= m->T) return GPT2_EINVAL;
     const float inv = 1.0f / temperature;
-    if (m->prec == GPT2_BF16)
+    if (m->prec != GPT2_FP32)
         sample_kernel<bf16><<<m->B, SAMPLE_THREADS, 0, m->stream>>>(out, (const bf16*)m->logits, m->T, pos, m->V,
                                                                    m->Vp, inv, seed);
     else
@@ -443,6 +474,51 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
     }
     CK(cudaGetLastError());
     return GPT2_OK;
+}
+
+// Layernorm forward that also writes the e4m3 copy of its output (fp8 mode)
+template <typename T>
+static int ln_forward_q8(cudaStream_t s, T* out, float* mean, float* rstd, const T* inp, const T* w, const T* b,
+                         int N, int C, uint8_t* q, float* qdeq) {
+    constexpr int EPV = Vec<T>::N;
+    const int nv = ceil_div(C / EPV, 32);
+    dim3 grid(ceil_div(N, LN_WARPS));
+    ProfScope ps(s, PC_LAYERNORM_FWD, 0, 2.0 * N * C * sizeof(T) + 1.0 * N * C + 12.0 * N + 2.0 * C * sizeof(T));
+    rt_note_launches(1);
+    switch (nv) {
+#define LNQ_CASE(k) case k: layernorm_forward_kernel<T, k, true><<<grid, LN_WARPS * 32, 0, s>>>(out, mean, rstd, inp, w, b, N, C, q, qdeq); break;
+        LNQ_CASE(1) LNQ_CASE(2) LNQ_CASE(3) LNQ_CASE(4) LNQ_CASE(5) LNQ_CASE(6) LNQ_CASE(7) LNQ_CASE(8)
+        LNQ_CASE(9) LNQ_CASE(10) LNQ_CASE(11) LNQ_CASE(12) LNQ_CASE(13) LNQ_CASE(14) LNQ_CASE(15) LNQ_CASE(16)
+#undef LNQ_CASE
+        default: return GPT2_EUNSUPPORTED;
+    }
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+// Per-tensor e4m3 copies of `ntens` fp32 tensors of `len` elements each (len % 4 == 0),
+// back to back from w: codes into q, unscaling factors 2^-k into deq[0..ntens)
+static int quantize_tensors(cudaStream_t s, uint8_t* q, float* deq, unsigned* amax_bits, const float* w,
+                            size_t len, int ntens) {
+    ProfScope ps(s, PC_MISC, 0, 2.0 * 4.0 * len * ntens + 1.0 * len * ntens);
+    CK(cudaMemsetAsync(amax_bits, 0, sizeof(unsigned) * ntens, s));
+    const int gx = (int)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4 / std::max(1, ntens) + 1);
+    rt_note_launches(2);
+    absmax_tensors_kernel<<<dim3(gx, ntens), 256, 0, s>>>(amax_bits, w, len);
+    CK(cudaGetLastError());
+    quantize_tensors_kernel<<<dim3(gx, ntens), 256, 0, s>>>(q, deq, amax_bits, w, len);
+    CK(cudaGetLastError());
+    return GPT2_OK;
+}
+
+// fp8 mode: refresh the e4m3 shadows of qkvw and fcw from the fp32 master weights
+static int quantize_model_weights(GPT2* m) {
+    if (m->prec != GPT2_FP8) return GPT2_OK;
+    const size_t C = m->C;
+    int rc = quantize_tensors(m->stream, m->wq_qkv, m->wq_deq, m->wq_amax, m->params + m->poff[P_QKVW], 3 * C * C, m->L);
+    if (rc != GPT2_OK) return rc;
+    return quantize_tensors(m->stream, m->wq_fc, m->wq_deq + m->L, m->wq_amax + m->L, m->params + m->poff[P_FCW],
+                            4 * C * C, m->L);
 }
 
 // two resident blocks per SM on a 148-SM part; each warp then walks ~7 rows at N = 16384
@@ -615,6 +691,14 @@ static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T*
     }
 }
 
+// The forward product with e4m3 operands (fp8 mode): A row-scaled codes, W tensor-scaled
+static int mm_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const float* inp_deq, const uint8_t* W,
+                          const float* w_deq, const bf16* bias, int M, int N, int K, int epi, bf16* aux,
+                          unsigned* err) {
+    ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
+    return gemm_tc_forward_fp8(s, out, inp, inp_deq, W, w_deq, bias, M, N, K, epi, aux, err);
+}
+
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation of dinp's layer)
 template <typename T>
 static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N, int K, int epi,
@@ -706,11 +790,6 @@ static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const 
     }
 }
 
-#define RC(x)                          \
-    do {                               \
-        int rc_ = (x);                 \
-        if (rc_ != GPT2_OK) return rc_; \
-    } while (0)
 
 // ------------------------------------------------------------------ forward
 template <typename T>
@@ -720,6 +799,7 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
     const size_t BTmax = (size_t)m->maxB * m->maxT;
     const T* W = (sizeof(T) == 2) ? (const T*)m->wbf : (const T*)m->params;
     auto P = [&](int i) { return W + m->poff[i]; };
+    const bool fp8 = m->prec == GPT2_FP8;
     T* encoded = (T*)m->encoded;
     {
         constexpr int EPV = Vec<T>::N;
@@ -741,12 +821,26 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         T* res3 = (T*)m->res3 + l * BTmax * C;
         float* m1 = m->ln1_mean + l * BTmax; float* r1 = m->ln1_rstd + l * BTmax;
         float* m2 = m->ln2_mean + l * BTmax; float* r2 = m->ln2_rstd + l * BTmax;
-        RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
-        RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+        if (fp8) {
+            // fp8 mode: the layernorm also writes its output as row-scaled e4m3 codes, the
+            // qkv product reads them and the e4m3 weight shadow
+            RC(ln_forward_q8<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C, m->lnq, m->lnq_deq));
+            RC(mm_forward_fp8(s, (bf16*)qkv, m->lnq, m->lnq_deq, m->wq_qkv + (size_t)l * 3 * C * C, m->wq_deq + l,
+                              (const bf16*)(P(P_QKVB) + l * 3 * C), BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+        } else {
+            RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
+            RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+        }
         RC(attn_forward<T>(m, s, atty, qkv, l, B, Tn));
         RC(mm_forward<T>(s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x, m->err));
-        RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
-        RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err));
+        if (fp8) {
+            RC(ln_forward_q8<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C, m->lnq, m->lnq_deq));
+            RC(mm_forward_fp8(s, (bf16*)fchg, m->lnq, m->lnq_deq, m->wq_fc + (size_t)l * 4 * C * C, m->wq_deq + m->L + l,
+                              (const bf16*)(P(P_FCB) + l * 4 * C), BT, 4 * C, C, EPI_GELU, (bf16*)fch, m->err));
+        } else {
+            RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
+            RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err));
+        }
         RC(mm_forward<T>(s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2, m->err));
         x = res3;
     }
@@ -888,7 +982,7 @@ static int check_bt(GPT2* m, int B, int Tn) {
 static int forward_dispatch(GPT2* m, int B, int Tn, bool with_targets) {
     m->have_fwd = 0;
     m->have_targets = 0;
-    int rc = (m->prec == GPT2_BF16) ? forward_impl<bf16>(m, B, Tn, with_targets)
+    int rc = (m->prec != GPT2_FP32) ? forward_impl<bf16>(m, B, Tn, with_targets)
                                     : forward_impl<float>(m, B, Tn, with_targets);
     if (rc != GPT2_OK) return rc;
     m->B = B;
@@ -924,7 +1018,7 @@ extern "C" int gpt2_zero_grad(GPT2* m) {
 extern "C" int gpt2_backward(GPT2* m) {
     if (!m) return GPT2_EINVAL;
     if (!m->have_fwd || !m->have_targets) return GPT2_ESTATE;
-    int rc = (m->prec == GPT2_BF16) ? backward_impl<bf16>(m) : backward_impl<float>(m);
+    int rc = (m->prec != GPT2_FP32) ? backward_impl<bf16>(m) : backward_impl<float>(m);
     // the logits buffer now holds d loss/d logits and has been consumed
     m->have_fwd = 0;
     return rc;
@@ -957,7 +1051,7 @@ extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float ep
     adamw_kernel<<<a.grid, 256, 0, m->stream>>>(a.p, a.g, a.mm, a.vv, a.shadow, a.n4, a.lr, a.b1, a.b2, a.eps,
                                                 a.wd, a.bc1, a.bc2);
     CK(cudaGetLastError());
-    return GPT2_OK;
+    return quantize_model_weights(m);        // fp8 mode: the e4m3 weight shadows follow
 }
 
 // forward (with targets), zero_grad, backward and AdamW on the model's stream, as
@@ -1184,6 +1278,45 @@ static int epi_of(int epilogue) {
         case GPT2_EPI_RESIDUAL: return EPI_RESID;
         default: return -1;
     }
+}
+
+// ------------------------------------------------------------------ fp8 (single layer)
+extern "C" int gpt2_layernorm_forward_fp8(float* out, uint8_t* codes, float* row_deq, float* mean, float* rstd,
+                                          const float* inp, const float* weight, const float* bias, int N, int C,
+                                          void* stream) {
+    if (N < 0 || C < 8 || C % 8 || C > 2048) return GPT2_EINVAL;
+    if (N == 0) return GPT2_OK;
+    if (!out || !codes || !row_deq || !mean || !rstd || !inp || !weight || !bias) return GPT2_EINVAL;
+    if (((uintptr_t)codes & 7)) return GPT2_EINVAL;
+    return ln_forward_q8<float>((cudaStream_t)stream, out, mean, rstd, inp, weight, bias, N, C, codes, row_deq);
+}
+
+extern "C" int gpt2_quantize_e4m3(uint8_t* codes, float* deq, unsigned* amax_scratch, const float* x, size_t n,
+                                  void* stream) {
+    if (!codes || !deq || !amax_scratch || !x || n == 0 || n % 4) return GPT2_EINVAL;
+    if ((((uintptr_t)codes | (uintptr_t)x) & 15)) return GPT2_EINVAL;
+    return quantize_tensors((cudaStream_t)stream, codes, deq, amax_scratch, x, n, 1);
+}
+
+extern "C" int gpt2_matmul_forward_fp8(void* out, void* aux, const uint8_t* inp, const float* inp_deq,
+                                       const uint8_t* weight, const float* weight_deq, const void* bias, int M, int N,
+                                       int K, int epilogue, void* stream) {
+    const int epi = epi_of(epilogue);
+    if (!out || !inp || !inp_deq || !weight || !weight_deq || M < 0 || N <= 0 || K <= 0 || epi < 0) return GPT2_EINVAL;
+    if (epi != EPI_STORE && !aux) return GPT2_EINVAL;
+    if (M == 0) return GPT2_OK;
+    unsigned* err = nullptr;
+    RC(layer_err_word(&err));
+    return mm_forward_fp8((cudaStream_t)stream, (bf16*)out, inp, inp_deq, weight, weight_deq, (const bf16*)bias, M, N,
+                          K, epi, (bf16*)aux, err);
+}
+
+extern "C" int gpt2_fp8_weights(GPT2* m, int which, uint8_t** codes, float** deq) {
+    if (!m || !codes || !deq || (which != 0 && which != 1)) return GPT2_EINVAL;
+    if (m->prec != GPT2_FP8) return GPT2_ESTATE;
+    *codes = which == 0 ? m->wq_qkv : m->wq_fc;
+    *deq = m->wq_deq + (which == 0 ? 0 : m->L);
+    return GPT2_OK;
 }
 
 extern "C" int gpt2_matmul_forward_fused(void* out, void* aux, const void* inp, const void* weight,

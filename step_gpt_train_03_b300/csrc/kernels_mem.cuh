@@ -6,6 +6,8 @@
 // hand-written forward and backward).  Every reduction here runs in a fixed order, so
 // results are bitwise reproducible run to run (no floating-point atomics).
 #pragma once
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -247,17 +249,38 @@ __global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restri
     dwpe[idx] += s;
 }
 
+// ============================================================== e4m3 quantization
+// Power-of-two scales (so scaling and unscaling are exact): the largest k with
+// amax * 2^k <= 448, the largest e4m3 value.  With amax = f 2^e, f in [0.5, 1):
+// k = 9 - e if f <= 0.875 (448 = 0.875 2^9), else 8 - e; 0 for amax == 0; clamped to
+// [-126, 126] so that 2^k and 2^-k are normal floats.
+__device__ __forceinline__ int e4m3_scale_exp(float amax) {
+    if (!(amax > 0.f)) return 0;
+    int e;
+    const float f = frexpf(amax, &e);
+    const int k = (f <= 0.875f) ? 9 - e : 8 - e;
+    return max(-126, min(126, k));
+}
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
+// two values to e4m3 (round to nearest even, saturating at +-448): lo in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
 // ============================================================== layernorm
 #define LN_EPS 1e-5f
 #define LN_WARPS 8
 // One warp per row; the row lives in registers (NV 16-byte packets per lane).
 // mean = sum(x)/C; var = sum((x-mean)^2)/C (two passes over registers); rstd =
 // 1/sqrt(var + eps); out = (x-mean)*rstd*w + b.
-template <typename T, int NV>
+// Q8: also the row as e4m3 codes q (C bytes) of out * 2^k, k the power-of-two scale of
+// the row's largest |out| (taken before out is rounded to T), and qdeq[row] = 2^-k.
+template <typename T, int NV, bool Q8 = false>
 __global__ void __launch_bounds__(LN_WARPS * 32)
 layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* __restrict__ rstd,
                          const T* __restrict__ inp, const T* __restrict__ w,
-                         const T* __restrict__ b, int N, int C) {
+                         const T* __restrict__ b, int N, int C, uint8_t* __restrict__ q = nullptr,
+                         float* __restrict__ qdeq = nullptr) {
     constexpr int EPV = Vec<T>::N;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
@@ -279,28 +302,89 @@ layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* _
         }
     }
     const float m = warp_sum(s) / (float)C;
-    float q = 0.f;
+    float qs = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         if (lane + 32 * i < nvec) {
 #pragma unroll
-            for (int e = 0; e < EPV; e++) { float d = v[i][e] - m; q += d * d; }
+            for (int e = 0; e < EPV; e++) { float d = v[i][e] - m; qs += d * d; }
         }
     }
-    const float var = warp_sum(q) / (float)C;
+    const float var = warp_sum(qs) / (float)C;
     const float r = 1.0f / sqrtf(var + LN_EPS);
     T* o = out + (size_t)row * C;
+    float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         int vi = lane + 32 * i;
         if (vi < nvec) {
             Vec<T> wv = load_vec(w + vi * EPV), bv = load_vec(b + vi * EPV), ov;
 #pragma unroll
-            for (int e = 0; e < EPV; e++) ov.set(e, (v[i][e] - m) * r * wv.get(e) + bv.get(e));
+            for (int e = 0; e < EPV; e++) {
+                v[i][e] = (v[i][e] - m) * r * wv.get(e) + bv.get(e);
+                ov.set(e, v[i][e]);
+                if (Q8) amax = fmaxf(amax, fabsf(v[i][e]));
+            }
             store_vec(o + vi * EPV, ov);
         }
     }
+    if constexpr (Q8) {
+        const int k = e4m3_scale_exp(warp_max(amax));
+        const float sc = pow2f(k);
+        uint8_t* qr = q + (size_t)row * C;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            int vi = lane + 32 * i;
+            if (vi < nvec) {
+                uint32_t c[EPV / 4];
+#pragma unroll
+                for (int e = 0; e < EPV; e += 4)
+                    c[e / 4] = e4m3x2(v[i][e] * sc, v[i][e + 1] * sc) |
+                               (e4m3x2(v[i][e + 2] * sc, v[i][e + 3] * sc) << 16);
+                if constexpr (EPV == 8) *reinterpret_cast<uint2*>(qr + vi * EPV) = make_uint2(c[0], c[1]);
+                else *reinterpret_cast<uint32_t*>(qr + vi * EPV) = c[0];
+            }
+        }
+        if (lane == 0) qdeq[row] = pow2f(-k);
+    }
     if (lane == 0) { mean[row] = m; rstd[row] = r; }
+}
+
+// Per-tensor e4m3 quantization of fp32 weights: tensor t (blockIdx.y) is
+// [t * len, (t + 1) * len) of w.  First the largest |w| of each tensor (each block's
+// maximum folded in with an integer atomicMax on the float's bits: order-free, so
+// deterministic; amax_bits zeroed beforehand), then codes of w * 2^k and deq[t] = 2^-k.
+__global__ void absmax_tensors_kernel(unsigned* __restrict__ amax_bits, const float* __restrict__ w, size_t len) {
+    const float4* p = reinterpret_cast<const float4*>(w + (size_t)blockIdx.y * len);
+    const size_t n4 = len / 4;
+    float mx = 0.f;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = p[i];
+        mx = fmaxf(mx, fmax3(fabsf(a.x), fabsf(a.y), fmaxf(fabsf(a.z), fabsf(a.w))));
+    }
+    mx = warp_max(mx);
+    __shared__ float wm[32];
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < blockDim.x / 32 ? wm[threadIdx.x] : 0.f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) atomicMax(amax_bits + blockIdx.y, __float_as_uint(v));
+    }
+}
+__global__ void quantize_tensors_kernel(uint8_t* __restrict__ q, float* __restrict__ deq,
+                                        const unsigned* __restrict__ amax_bits, const float* __restrict__ w,
+                                        size_t len) {
+    const int k = e4m3_scale_exp(__uint_as_float(amax_bits[blockIdx.y]));
+    const float sc = pow2f(k);
+    const float4* p = reinterpret_cast<const float4*>(w + (size_t)blockIdx.y * len);
+    uint32_t* qo = reinterpret_cast<uint32_t*>(q + (size_t)blockIdx.y * len);
+    const size_t n4 = len / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = p[i];
+        qo[i] = e4m3x2(a.x * sc, a.y * sc) | (e4m3x2(a.z * sc, a.w * sc) << 16);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) deq[blockIdx.y] = pow2f(-k);
 }
 
 // Backward.  With xhat = (x-mean)*rstd, g = dy*w:

@@ -14,8 +14,8 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgpt2_b300.so")
 
-FP32, BF16 = 0, 1
-PRECISIONS = {"fp32": FP32, "bf16": BF16}
+FP32, BF16, FP8 = 0, 1, 2
+PRECISIONS = {"fp32": FP32, "bf16": BF16, "fp8": FP8}
 STATUS = {0: "GPT2_OK", 1: "GPT2_EINVAL", 2: "GPT2_ESTATE", 3: "GPT2_ECUDA", 4: "GPT2_ETOKEN",
           5: "GPT2_ENONFINITE", 6: "GPT2_ETIMEOUT", 7: "GPT2_ENOMEM", 8: "GPT2_EUNSUPPORTED",
           9: "GPT2_EIO"}
@@ -41,6 +41,10 @@ SIGNATURES = {
     "gpt2_param_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
     "gpt2_grad_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
     "gpt2_layer_check": (_i, [_vp]),
+    "gpt2_layernorm_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
+    "gpt2_quantize_e4m3": (_i, [_vp, _vp, _vp, _vp, _sz, _vp]),
+    "gpt2_matmul_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "gpt2_fp8_weights": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp)]),
     "gpt2_matmul_forward_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "gpt2_matmul_backward_input_gelu": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_set_stream": (_i, [_vp, _vp]),
@@ -321,6 +325,20 @@ class GPT2:
     def check(self):
         check(lib.gpt2_check(self.handle), "gpt2_check")
 
+    def fp8_weights(self, which: str):
+        """(codes uint8 (L, rows, C), deq fp32 (L,)) views of the fp8 mode's weight shadow of
+        'qkvw' or 'fcw'."""
+        import torch
+        codes, deq = ctypes.c_void_p(), ctypes.c_void_p()
+        check(lib.gpt2_fp8_weights(self.handle, 0 if which == "qkvw" else 1, ctypes.byref(codes), ctypes.byref(deq)),
+              "gpt2_fp8_weights")
+        L, C = self.shape.num_layers, self.shape.channels
+        rows = 3 * C if which == "qkvw" else 4 * C
+        base = self.workspace.data_ptr()
+        c_off, d_off = codes.value - base, deq.value - base
+        return (self.workspace[c_off:c_off + L * rows * C].view(L, rows, C),
+                self.workspace[d_off:d_off + 4 * L].view(torch.float32))
+
 
 # ---- observability -----------------------------------------------------------------------------
 def kernel_launches() -> int:
@@ -436,6 +454,29 @@ def matmul_backward_input_gelu(dinp, dout, weight, pre, precision, stream=None):
     check(lib.gpt2_matmul_backward_input_gelu(_ptr(dinp), _ptr(dout), _ptr(weight), _ptr(pre), M, N, K,
                                               PRECISIONS[precision], _stream_handle(stream)),
           "gpt2_matmul_backward_input_gelu")
+
+
+def layernorm_forward_fp8(out, codes, row_deq, mean, rstd, inp, weight, bias, stream=None):
+    """gpt2_layernorm_forward_fp8 (fp32 tensors, codes uint8 (N, C), row_deq fp32 (N))."""
+    N, C = inp.shape
+    check(lib.gpt2_layernorm_forward_fp8(_ptr(out), _ptr(codes), _ptr(row_deq), _ptr(mean), _ptr(rstd), _ptr(inp),
+                                         _ptr(weight), _ptr(bias), N, C, _stream_handle(stream)),
+          "gpt2_layernorm_forward_fp8")
+
+
+def quantize_e4m3(codes, deq, amax_scratch, x, stream=None):
+    """gpt2_quantize_e4m3: per-tensor e4m3 codes of the fp32 tensor x."""
+    check(lib.gpt2_quantize_e4m3(_ptr(codes), _ptr(deq), _ptr(amax_scratch), _ptr(x), x.numel(),
+                                 _stream_handle(stream)), "gpt2_quantize_e4m3")
+
+
+def matmul_forward_fp8(out, aux, inp, inp_deq, weight, weight_deq, bias, epilogue, stream=None):
+    """gpt2_matmul_forward_fp8: inp (M,K) and weight (N,K) e4m3 codes (uint8 tensors)."""
+    M, K = inp.shape
+    N = weight.shape[0]
+    check(lib.gpt2_matmul_forward_fp8(_ptr(out), _ptr(aux), _ptr(inp), _ptr(inp_deq), _ptr(weight),
+                                      _ptr(weight_deq), _ptr(bias), M, N, K, EPILOGUES[epilogue],
+                                      _stream_handle(stream)), "gpt2_matmul_forward_fp8")
 
 
 def layer_check(stream=None):

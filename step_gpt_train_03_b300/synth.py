@@ -76,6 +76,9 @@ WORKLOADS = {
                                          50, lr=6e-4, weight_decay=0.1),
     "gpt2_350m_bf16_b8_t1024": Workload("gpt2_350m_bf16_b8_t1024", GPT2_350M, 8, 1024, 3, "bf16",
                                         20, lr=3e-4, weight_decay=0.1),
+    # the 124M bf16 workload in the fp8 mode (e4m3 qkv and fc products)
+    "gpt2_124m_fp8_b16_t1024": Workload("gpt2_124m_fp8_b16_t1024", GPT2_124M, 16, 1024, 2, "fp8",
+                                        50, lr=6e-4, weight_decay=0.1),
 }
 
 

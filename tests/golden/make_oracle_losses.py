@@ -3,7 +3,8 @@
 Calls only the CPU oracle and the seeded input generators.  For the bf16 workloads the
 stored curve is the fp32 oracle's: the loss of each of the first ``n`` steps (the
 forward before that step's AdamW update) and the loss of one more forward after the
-n-th update.  Usage:
+n-th update.  For an fp8 workload the oracle runs in its fp8 mode (e4m3 qkv and fc
+products).  Usage:
 
     python tests/golden/make_oracle_losses.py gpt2_124m_bf16_b16_t1024 10
 """
@@ -25,6 +26,7 @@ def main(name, n):
     w = synth.WORKLOADS[name]
     o = O.from_shape(w.shape, np.float32)
     o.keep_preatt = False
+    o.fp8 = w.precision == "fp8"
     o.load(synth.init_params(w.shape, w.seed))
     batches = synth.workload_batches(w, n + 1)
     losses, secs = [], []
@@ -36,7 +38,7 @@ def main(name, n):
     final = o.forward(*batches[n])
     print(f"after {n} updates: loss {final:.6f}", flush=True)
     out = {
-        "workload": name, "oracle_dtype": "float32", "steps": n,
+        "workload": name, "oracle_dtype": "float32", "oracle_fp8": o.fp8, "steps": n,
         "losses": losses, "loss_after_updates": final,
         "note": "written by tests/golden/make_oracle_losses.py from the CPU oracle only",
     }
