@@ -177,6 +177,26 @@ int gpt2_backward(GPT2* model);
 int gpt2_update(GPT2* model, float lr, float beta1, float beta2, float eps,
                 float weight_decay, int t);
 
+/* The Muon optimizer (pimou.com article, sections "优化器的优势" and "相关技术的追溯":
+ * Muon orthogonalizes the update with Newton-Schulz iterations, after Bernstein &
+ * Newhouse 2024), for the bf16 and fp8 modes (GPT2_EUNSUPPORTED in fp32).  On each
+ * block matrix (qkvw, attprojw, fcw, fcprojw of every layer, one matrix per layer):
+ *   mom = momentum mom + g  (mom kept in the AdamW first-moment buffer of that matrix)
+ *   X = mom / ||mom||_F, then ns_iters times X <- 1.5 X - 0.5 X X^T X (in bf16 on the tensor
+ *   cores, fp32 accumulation; on the smaller Gram side)
+ *   p -= lr_muon (X + weight_decay p)
+ * and AdamW (lr, beta1, beta2, eps, weight_decay, t as gpt2_update) on every other
+ * parameter.  Then the bf16 (and fp8) weight shadows are refreshed. */
+int gpt2_update_muon(GPT2* model, float lr_muon, float momentum, int ns_iters, float lr, float beta1,
+                     float beta2, float eps, float weight_decay, int t);
+
+/* The Newton-Schulz iteration of gpt2_update_muon alone: out (r x c, bf16, device) =
+ * iters steps from G (r x c, fp32, device) / ||G||_F.  r, c multiples of 8; out, G and
+ * scratch 256-byte aligned; scratch >= gpt2_newton_schulz_scratch_bytes(r, c). */
+size_t gpt2_newton_schulz_scratch_bytes(int r, int c);
+int gpt2_newton_schulz(void* out, const float* G, int r, int c, int iters, void* scratch,
+                       size_t scratch_bytes, void* stream);
+
 /* One whole training step from HOST token buffers: copies tokens/targets (pinned host
  * memory recommended) to the device, runs forward, zero_grad, backward and update (as
  * one CUDA graph once the shape has been seen, see gpt2_step), and copies the mean loss

@@ -414,6 +414,60 @@ def matmul_forward_fp8(x, w, bias):
     return matmul_forward(xq, wq, bias)
 
 
+# --------------------------------------------------------------------------------------
+# Muon (pimou.com article, sections "优化器的优势" and "相关技术的追溯": the Muon optimizer
+# orthogonalizes with Newton-Schulz iterations after Bernstein & Newhouse (2024))
+# --------------------------------------------------------------------------------------
+MUON_TENSORS = ("qkvw", "attprojw", "fcw", "fcprojw")   # the 2-D matrices of every block
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), from the format's definition: the
+    top 16 bits of the float32 encoding, the dropped 16 bits rounded to nearest even.
+    Computed on the float32 value of x (finite inputs)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep = (b >> 16) & 1
+    b = (b + 0x7FFF + keep) >> 16 << 16
+    return (b & 0xFFFFFFFF).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def newton_schulz(G, iters, bf16=False):
+    """The cubic Newton-Schulz iteration towards the orthogonal polar factor of G: start
+    from X = G / ||G||_F (all singular values in (0, 1]), then `iters` times
+    X <- 1.5 X - 0.5 X X^T X, which maps each singular value s to 1.5 s - 0.5 s^3 and so
+    drives every nonzero one towards 1 while keeping the singular vectors.  Written on
+    the smaller Gram matrix: with S = X^T X (tall or square X) or X X^T (wide) and
+    T = 1.5 I - 0.5 S, X <- X T or T X (the same product).
+
+    bf16=True: the arithmetic of a bf16 implementation -- X, S and T rounded to bf16 where
+    it stores them (X after the normalization and after every step), the products and
+    sums exact.  Small singular values grow by 1.5 per step and so does the rounding in
+    their directions, so the bf16 iterate drifts from the exact one as steps are added."""
+    rnd = round_bf16 if bf16 else (lambda a: a)
+    X = np.asarray(G, dtype=np.float64)
+    nrm = np.sqrt((X * X).sum())
+    if nrm == 0.0:
+        return X.copy()
+    X = rnd(X / nrm)
+    tall = X.shape[0] >= X.shape[1]
+    n = X.shape[1] if tall else X.shape[0]
+    for _ in range(iters):
+        S = rnd(X.T @ X if tall else X @ X.T)
+        T = rnd(1.5 * np.eye(n) - 0.5 * S)
+        X = rnd(X @ T if tall else T @ X)
+    return X
+
+
+def muon_update(params, grads, mom, lr, momentum, weight_decay, iters):
+    """One Muon step on each matrix of MUON_TENSORS (per layer): mom <- momentum mom + g,
+    O = newton_schulz(mom), p <- p - lr (O + weight_decay p)."""
+    for name in MUON_TENSORS:
+        for l in range(params[name].shape[0]):
+            mom[name][l] = momentum * mom[name][l] + grads[name][l]
+            O = newton_schulz(mom[name][l], iters)
+            params[name][l] -= lr * (O + weight_decay * params[name][l])
+
+
 PARAM_FILE_MAGIC = 20240326
 PARAM_FILE_VERSION = 3
 
@@ -581,6 +635,23 @@ class GPT2Oracle:
     def update(self, lr, beta1, beta2, eps, weight_decay, t):
         adamw_update(self.flat, self.flat_grad, self.m, self.v, lr, beta1, beta2, eps,
                      weight_decay, t)
+
+    def update_muon(self, lr_muon, momentum, iters, lr, beta1, beta2, eps, weight_decay, t):
+        """Muon on the block matrices (momentum kept in the AdamW first-moment buffer of
+        those parameters), AdamW with (lr, beta1, beta2, eps, weight_decay) on every other
+        parameter; weight_decay also applies, decoupled, in the Muon step."""
+        other = np.ones(self.num_params, dtype=bool)
+        off = 0
+        for name in PARAM_ORDER:
+            n = self.sizes[name]
+            if name in MUON_TENSORS:
+                other[off:off + n] = False
+            off += n
+        idx = np.nonzero(other)[0]
+        p, g, m, v = self.flat[idx], self.flat_grad[idx], self.m[idx], self.v[idx]
+        adamw_update(p, g, m, v, lr, beta1, beta2, eps, weight_decay, t)
+        self.flat[idx], self.m[idx], self.v[idx] = p, m, v
+        muon_update(self.p, self.g, self._views(self.m), lr_muon, momentum, weight_decay, iters)
 
     def step(self, tokens, targets, lr, beta1, beta2, eps, weight_decay, t):
         loss = self.forward(tokens, targets)

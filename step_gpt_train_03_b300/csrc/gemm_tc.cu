@@ -722,6 +722,30 @@ int gemm_tc_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const flo
     }
 }
 
+int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16* B, bool b_mn, int M, int N, int K,
+                 unsigned* err) {
+    // out (M x N) = sum_k A(m,k) B(n,k): A K-major (M rows of K) or MN-major (K rows of M),
+    // B K-major (N rows of K) or MN-major (K rows of N)
+    if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
+    if (M % 8 || N % 8 || K % 8 || !aligned16(out) || !aligned16(A) || !aligned16(B)) return GPT2_EUNSUPPORTED;
+    const int cl = (N <= 768 && K <= 768) ? 1 : 2;
+    CUtensorMap ta, tb, to;
+    const bool ok_a = a_mn ? make_map(&ta, A, M, K, M, 64) : make_map(&ta, A, K, M, K, TC_BM);
+    const bool ok_b = b_mn ? make_map(&tb, B, N, K, N, 64) : make_map(&tb, B, K, N, K, 256 / cl);
+    if (!ok_a || !ok_b || !make_epi_map(&to, out, N, M, N)) return GPT2_EUNSUPPORTED;
+    TcEpi ep{out, nullptr, nullptr, (long)N};
+    if (!a_mn && !b_mn)
+        return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2>(s, ta, tb, to, to, M, N, K, 1, ep, err)
+                       : launch_tc<256, EPI_STORE, false, false, 1>(s, ta, tb, to, to, M, N, K, 1, ep, err);
+    if (!a_mn && b_mn)
+        return cl == 2 ? launch_tc<256, EPI_STORE, false, true, 2>(s, ta, tb, to, to, M, N, K, 1, ep, err)
+                       : launch_tc<256, EPI_STORE, false, true, 1>(s, ta, tb, to, to, M, N, K, 1, ep, err);
+    if (a_mn && b_mn)
+        return cl == 2 ? launch_tc<256, EPI_STORE, true, true, 2>(s, ta, tb, to, to, M, N, K, 1, ep, err)
+                       : launch_tc<256, EPI_STORE, true, true, 1>(s, ta, tb, to, to, M, N, K, 1, ep, err);
+    return GPT2_EUNSUPPORTED;
+}
+
 int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16* W, int M, int N, int K, int epi,
                         const bf16* aux, unsigned* err) {
     // dinp (M x K) = dout (M x N) W (N x K): contraction over N; A = dout K-major,

@@ -29,6 +29,12 @@ int gemm_tc_forward_fp8(cudaStream_t s, __nv_bfloat16* out, const uint8_t* inp, 
                         const uint8_t* W, const float* w_deq, const __nv_bfloat16* bias, int M, int N, int K,
                         int epi, __nv_bfloat16* aux, unsigned* err);
 
+// A plain bf16 product with bf16 output: out (M,N) = sum_k A(m,k) B(n,k), each operand
+// K-major (rows of K contiguous) or MN-major (rows of M or N contiguous, K rows); the
+// combination (A MN-major, B K-major) is not built.  M, N, K multiples of 8.
+int gemm_tc_bf16(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B,
+                 bool b_mn, int M, int N, int K, unsigned* err);
+
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation).
 int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16* dout,
                         const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux,

@@ -82,6 +82,10 @@ struct GPT2 {
     uint8_t *wq_qkv, *wq_fc;
     float* wq_deq;                     // [0, L): qkvw of layer l; [L, 2L): fcw of layer l
     unsigned* wq_amax;
+    // Muon (bf16 / fp8 modes): the normalized momentum of one tensor's L matrices (bf16),
+    // a ping-pong matrix, the Gram matrix S and T = 1.5 I - 0.5 S, sum-of-squares partials
+    bf16 *mu_x, *mu_xb, *mu_s, *mu_t;
+    float* mu_part;
     // state
     int B, T;
     int have_fwd, have_targets;
@@ -97,6 +101,7 @@ struct GPT2 {
 };
 
 static int quantize_model_weights(GPT2* m);
+static int layer_err_word(unsigned** out);
 
 static const size_t kAlign = 1024;
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -177,6 +182,16 @@ static size_t plan(GPT2* m, char* base) {
     m->tokens = (int*)take(BT * 4);
     m->targets = (int*)take(BT * 4);
     m->err = (unsigned*)take(16);
+    if (m->prec != GPT2_FP32) {
+        m->mu_x = (bf16*)take(L * 4 * C * C * 2);
+        m->mu_xb = (bf16*)take(4 * C * C * 2);
+        m->mu_s = (bf16*)take(C * C * 2);
+        m->mu_t = (bf16*)take(C * C * 2);
+        m->mu_part = (float*)take(L * MUON_NB * 4);
+    } else {
+        m->mu_x = m->mu_xb = m->mu_s = m->mu_t = nullptr;
+        m->mu_part = nullptr;
+    }
     if (m->prec == GPT2_FP8) {
         m->lnq = (uint8_t*)take(BT * C);
         m->lnq_deq = (float*)take(BT * 4);
@@ -1052,6 +1067,125 @@ extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float ep
                                                 a.wd, a.bc1, a.bc2);
     CK(cudaGetLastError());
     return quantize_model_weights(m);        // fp8 mode: the e4m3 weight shadows follow
+}
+
+// ------------------------------------------------------------------ Muon
+// pimou.com article, sections "优化器的优势" and "相关技术的追溯": the Muon optimizer,
+// orthogonalizing with Newton-Schulz iterations (after Bernstein & Newhouse, 2024).
+// X (r x c, bf16) <- `iters` cubic Newton-Schulz steps X <- X (1.5 I - 0.5 X^T X) (tall or
+// square) or (1.5 I - 0.5 X X^T) X (wide), on the tensor cores; X and xb ping-pong, the
+// result's buffer is returned in *res.
+static int newton_schulz_bf16(cudaStream_t s, bf16* X, bf16* xb, bf16* S, bf16* T, int r, int c, int iters,
+                              bf16** res, unsigned* err) {
+    const bool tall = r >= c;
+    const int n = tall ? c : r;
+    for (int k = 0; k < iters; k++) {
+        {
+            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * n * n * (tall ? r : c), 0);
+            // S = X^T X (A(i,k) = X[k][i] and B(j,k) = X[k][j], both MN-major) or X X^T
+            RC(tall ? gemm_tc_bf16(s, S, X, true, X, true, c, c, r, err)
+                    : gemm_tc_bf16(s, S, X, false, X, false, r, r, c, err));
+        }
+        rt_note_launches(1);
+        ns_affine_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz((size_t)n * n, 256), 592), 256, 0, s>>>(T, S, n);
+        CK(cudaGetLastError());
+        {
+            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * r * c * n, 0);
+            // xb = X T (B(j,k) = T[k][j], MN-major) or T X (B(j,k) = X[k][j], MN-major)
+            RC(tall ? gemm_tc_bf16(s, xb, X, false, T, true, r, c, c, err)
+                    : gemm_tc_bf16(s, xb, T, false, X, true, r, c, r, err));
+        }
+        std::swap(X, xb);
+    }
+    *res = X;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_update_muon(GPT2* m, float lr_muon, float momentum, int ns_iters, float lr, float beta1,
+                                float beta2, float eps, float wd, int t) {
+    if (!m || t < 1 || ns_iters < 0) return GPT2_EINVAL;
+    if (m->prec == GPT2_FP32) return GPT2_EUNSUPPORTED;
+    cudaStream_t s = m->stream;
+    const int L = m->L, C = m->C;
+    const int mu_idx[4] = {P_QKVW, P_ATTPROJW, P_FCW, P_FCPROJW};
+    const int mu_r[4] = {3 * C, C, 4 * C, C}, mu_c[4] = {C, C, C, 4 * C};
+    // AdamW over the flat ranges between the Muon tensors (gaps are zero and stay zero)
+    AdamArgs a;
+    adam_args(m, a, lr, beta1, beta2, eps, wd, t);
+    size_t start = 0;
+    for (int q = 0; q <= 4; q++) {
+        const size_t end = q < 4 ? m->poff[mu_idx[q]] : m->n_flat;
+        if (end > start) {
+            const size_t n4 = (end - start) / 4;
+            ProfScope ps(s, PC_ADAMW, 0, (double)(end - start) * 30.0);
+            rt_note_launches(1);
+            adamw_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 16), 256, 0, s>>>(
+                m->params + start, m->grads + start, m->m + start, m->v + start, m->wbf + start, n4, a.lr, a.b1, a.b2,
+                a.eps, a.wd, a.bc1, a.bc2);
+            CK(cudaGetLastError());
+        }
+        if (q < 4) start = m->poff[mu_idx[q]] + m->pnum[mu_idx[q]];
+    }
+    for (int q = 0; q < 4; q++) {
+        const size_t off = m->poff[mu_idx[q]], len = (size_t)mu_r[q] * mu_c[q];
+        float* mom = m->m + off;
+        {
+            ProfScope ps(s, PC_MISC, 0, 12.0 * L * len + 2.0 * L * len);
+            rt_note_launches(3);
+            const size_t n4 = L * len / 4;
+            muon_momentum_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 8), 256, 0, s>>>(
+                (float4*)mom, (const float4*)(m->grads + off), n4, momentum);
+            CK(cudaGetLastError());
+            sumsq_partial_kernel<<<dim3(MUON_NB, L), 256, 0, s>>>(m->mu_part, mom, len);
+            CK(cudaGetLastError());
+            scale_frobenius_bf16_kernel<<<dim3(std::max(1, 148 * 4 / L), L), 256, 0, s>>>(m->mu_x, mom, m->mu_part, len);
+            CK(cudaGetLastError());
+        }
+        for (int l = 0; l < L; l++) {
+            bf16* res = nullptr;
+            RC(newton_schulz_bf16(s, m->mu_x + l * len, m->mu_xb, m->mu_s, m->mu_t, mu_r[q], mu_c[q], ns_iters, &res,
+                                  m->err));
+            ProfScope ps(s, PC_MISC, 0, 14.0 * len);
+            rt_note_launches(1);
+            muon_apply_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4), 256, 0, s>>>(
+                (float4*)(m->params + off + l * len), res, m->wbf + off + l * len, len / 4, lr_muon, wd);
+            CK(cudaGetLastError());
+        }
+    }
+    return quantize_model_weights(m);
+}
+
+// The Newton-Schulz iteration alone (single layer): out (r x c, bf16) = `iters` cubic
+// steps from G (r x c, fp32) / ||G||_F.  scratch: gpt2_newton_schulz_scratch_bytes.
+extern "C" size_t gpt2_newton_schulz_scratch_bytes(int r, int c) {
+    if (r <= 0 || c <= 0) return 0;
+    const size_t n = (size_t)std::min(r, c);
+    return align_up((size_t)r * c * 2, 256) + 2 * align_up(n * n * 2, 256) + align_up(MUON_NB * 4, 256);
+}
+
+extern "C" int gpt2_newton_schulz(void* out, const float* G, int r, int c, int iters, void* scratch,
+                                  size_t scratch_bytes, void* stream) {
+    if (!out || !G || !scratch || r <= 0 || c <= 0 || iters < 0 || r % 8 || c % 8) return GPT2_EINVAL;
+    if (scratch_bytes < gpt2_newton_schulz_scratch_bytes(r, c)) return GPT2_EINVAL;
+    if ((((uintptr_t)out | (uintptr_t)G | (uintptr_t)scratch) & 255)) return GPT2_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t len = (size_t)r * c, n = (size_t)std::min(r, c);
+    char* sc = (char*)scratch;
+    bf16* xb = (bf16*)sc;
+    bf16* S = (bf16*)(sc + align_up(len * 2, 256));
+    bf16* T = (bf16*)((char*)S + align_up(n * n * 2, 256));
+    float* part = (float*)((char*)T + align_up(n * n * 2, 256));
+    unsigned* err = nullptr;
+    RC(layer_err_word(&err));
+    rt_note_launches(2);
+    sumsq_partial_kernel<<<dim3(MUON_NB, 1), 256, 0, s>>>(part, G, len);
+    CK(cudaGetLastError());
+    scale_frobenius_bf16_kernel<<<dim3(148, 1), 256, 0, s>>>((bf16*)out, G, part, len);
+    CK(cudaGetLastError());
+    bf16* res = nullptr;
+    RC(newton_schulz_bf16(s, (bf16*)out, xb, S, T, r, c, iters, &res, err));
+    if (res != (bf16*)out) CK(cudaMemcpyAsync(out, res, len * 2, cudaMemcpyDeviceToDevice, s));
+    return GPT2_OK;
 }
 
 // forward (with targets), zero_grad, backward and AdamW on the model's stream, as

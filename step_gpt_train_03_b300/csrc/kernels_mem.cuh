@@ -1127,3 +1127,78 @@ __global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restri
          i += (size_t)gridDim.x * blockDim.x)
         out[i] = __float2bfloat16_rn(in[i]);
 }
+
+// ============================================================== Muon
+// pimou.com article, sections "优化器的优势" and "相关技术的追溯": the Muon optimizer
+// orthogonalizes each block matrix's momentum with Newton-Schulz iterations.
+// mom = mu mom + g over the matrices' flat range (fp32)
+__global__ void muon_momentum_kernel(float4* __restrict__ mom, const float4* __restrict__ g, size_t n4, float mu) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        float4 a = mom[i];
+        const float4 b = g[i];
+        a.x = fmaf(mu, a.x, b.x); a.y = fmaf(mu, a.y, b.y); a.z = fmaf(mu, a.z, b.z); a.w = fmaf(mu, a.w, b.w);
+        mom[i] = a;
+    }
+}
+#define MUON_NB 64          // blocks per matrix of the sum-of-squares partials
+// partial[mat * MUON_NB + block] = sum of squares of the block's grid-stride slice of
+// matrix `mat` (blockIdx.y; matrices of `len` elements back to back), tree-added in a
+// fixed order
+__global__ void __launch_bounds__(256) sumsq_partial_kernel(float* __restrict__ partial, const float* __restrict__ x,
+                                                            size_t len) {
+    const float4* p = reinterpret_cast<const float4*>(x + (size_t)blockIdx.y * len);
+    float acc = 0.f;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < len / 4; i += (size_t)MUON_NB * blockDim.x) {
+        const float4 a = p[i];
+        acc = fmaf(a.x, a.x, acc); acc = fmaf(a.y, a.y, acc); acc = fmaf(a.z, a.z, acc); acc = fmaf(a.w, a.w, acc);
+    }
+    acc = warp_sum(acc);
+    __shared__ float ws[8];
+    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; w++) t += ws[w];
+        partial[(size_t)blockIdx.y * MUON_NB + blockIdx.x] = t;
+    }
+}
+// out = bf16(x / ||x||_F) for matrix blockIdx.y (0 where the norm is 0); every block sums
+// the matrix's MUON_NB partials in the same order, so all agree on the norm
+__global__ void __launch_bounds__(256) scale_frobenius_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ x,
+                                                                   const float* __restrict__ partial, size_t len) {
+    float ss = 0.f;
+    for (int b = 0; b < MUON_NB; b++) ss += partial[(size_t)blockIdx.y * MUON_NB + b];
+    const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    const float4* p = reinterpret_cast<const float4*>(x + (size_t)blockIdx.y * len);
+    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + (size_t)blockIdx.y * len);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < len / 4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = p[i];
+        o[2 * i] = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+        o[2 * i + 1] = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+    }
+}
+// T = 1.5 I - 0.5 S (n x n, bf16): the Newton-Schulz step X <- 1.5 X - 0.5 X S = X T
+__global__ void ns_affine_kernel(bf16* __restrict__ T, const bf16* __restrict__ S, int n) {
+    const size_t nn = (size_t)n * n;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nn; i += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / n), c = (int)(i % n);
+        T[i] = __float2bfloat16_rn((r == c ? 1.5f : 0.f) - 0.5f * __bfloat162float(S[i]));
+    }
+}
+// p -= lr (X + wd p); shadow (nullable) = bf16(p)
+__global__ void muon_apply_kernel(float4* __restrict__ p, const bf16* __restrict__ X, bf16* __restrict__ shadow,
+                                  size_t n4, float lr, float wd) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        float4 a = p[i];
+        const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(X) + 2 * i;
+        const float2 x0 = __bfloat1622float2(xp[0]), x1 = __bfloat1622float2(xp[1]);
+        a.x -= lr * (x0.x + wd * a.x); a.y -= lr * (x0.y + wd * a.y);
+        a.z -= lr * (x1.x + wd * a.z); a.w -= lr * (x1.y + wd * a.w);
+        p[i] = a;
+        if (shadow) {
+            __nv_bfloat162* sp = reinterpret_cast<__nv_bfloat162*>(shadow) + 2 * i;
+            sp[0] = __floats2bfloat162_rn(a.x, a.y);
+            sp[1] = __floats2bfloat162_rn(a.z, a.w);
+        }
+    }
+}

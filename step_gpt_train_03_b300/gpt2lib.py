@@ -41,6 +41,9 @@ SIGNATURES = {
     "gpt2_param_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
     "gpt2_grad_ptr": (_i, [_vp, ctypes.POINTER(_vp)]),
     "gpt2_layer_check": (_i, [_vp]),
+    "gpt2_update_muon": (_i, [_vp, _f, _f, _i, _f, _f, _f, _f, _f, _i]),
+    "gpt2_newton_schulz_scratch_bytes": (_sz, [_i, _i]),
+    "gpt2_newton_schulz": (_i, [_vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_layernorm_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_quantize_e4m3": (_i, [_vp, _vp, _vp, _vp, _sz, _vp]),
     "gpt2_matmul_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
@@ -251,6 +254,10 @@ class GPT2:
 
     def update(self, lr, beta1, beta2, eps, weight_decay, t):
         check(lib.gpt2_update(self.handle, lr, beta1, beta2, eps, weight_decay, t), "gpt2_update")
+
+    def update_muon(self, lr_muon, momentum, ns_iters, lr, beta1, beta2, eps, weight_decay, t):
+        check(lib.gpt2_update_muon(self.handle, lr_muon, momentum, ns_iters, lr, beta1, beta2, eps, weight_decay, t),
+              "gpt2_update_muon")
 
     def step(self, tokens, targets, lr, beta1, beta2, eps, weight_decay, t, want_loss=True):
         loss = self.forward(tokens, targets, want_loss)
@@ -477,6 +484,16 @@ def matmul_forward_fp8(out, aux, inp, inp_deq, weight, weight_deq, bias, epilogu
     check(lib.gpt2_matmul_forward_fp8(_ptr(out), _ptr(aux), _ptr(inp), _ptr(inp_deq), _ptr(weight),
                                       _ptr(weight_deq), _ptr(bias), M, N, K, EPILOGUES[epilogue],
                                       _stream_handle(stream)), "gpt2_matmul_forward_fp8")
+
+
+def newton_schulz(out, G, iters, stream=None):
+    """gpt2_newton_schulz: out (r, c) bf16 = iters Newton-Schulz steps from G (r, c) fp32."""
+    import torch
+    r, c = G.shape
+    nb = int(lib.gpt2_newton_schulz_scratch_bytes(r, c))
+    sc = torch.empty(nb, dtype=torch.uint8, device=G.device)
+    check(lib.gpt2_newton_schulz(_ptr(out), _ptr(G), r, c, iters, _ptr(sc), nb, _stream_handle(stream)),
+          "gpt2_newton_schulz")
 
 
 def layer_check(stream=None):
