@@ -970,7 +970,7 @@ static int backward_impl(GPT2* m) {
     CK(cudaGetLastError());
     encoder_backward_wte_final<<<ceil_div(BT, ENC_CHUNK), 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
     CK(cudaGetLastError());
-    encoder_backward_wpe<T><<<ceil_div(Tn * C, 256), 256, 0, s>>>(G(P_WPE), dresid, B, Tn, C);
+    encoder_backward_wpe<T><<<ceil_div(Tn * C / Vec<T>::N, 256), 256, 0, s>>>(G(P_WPE), dresid, B, Tn, C);
     CK(cudaGetLastError());
     return GPT2_OK;
 }

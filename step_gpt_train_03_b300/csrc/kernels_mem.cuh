@@ -238,15 +238,41 @@ __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float
 }
 
 // dwpe[t, :] += sum over b of dout[b, t, :], b in order.
+// One thread per 16-byte packet of a row (C a multiple of the packet): the B loads of a
+// packet are issued four at a time, then added in b order.
 template <typename T>
 __global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restrict__ dout,
                                      int B, int Tn, int C) {
-    size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (size_t)Tn * C) return;
-    int t = (int)(idx / C), c = (int)(idx % C);
-    float s = 0.f;
-    for (int b = 0; b < B; b++) s += to_f32(dout[((size_t)b * Tn + t) * C + c]);
-    dwpe[idx] += s;
+    constexpr int EPV = Vec<T>::N;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;     // packet index over (t, c)
+    if (idx >= (size_t)Tn * C / EPV) return;
+    const size_t off = idx * EPV;                                         // = t * C + c
+    float s[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; e++) s[e] = 0.f;
+    const size_t bstride = (size_t)Tn * C;
+    int b = 0;
+    for (; b + 3 < B; b += 4) {
+        Vec<T> a[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) a[k] = load_vec(dout + (size_t)(b + k) * bstride + off);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+            for (int e = 0; e < EPV; e++) s[e] += a[k].get(e);
+    }
+    for (; b < B; b++) {
+        Vec<T> a = load_vec(dout + (size_t)b * bstride + off);
+#pragma unroll
+        for (int e = 0; e < EPV; e++) s[e] += a.get(e);
+    }
+#pragma unroll
+    for (int q = 0; q < EPV / 4; q++) {
+        float4* d = reinterpret_cast<float4*>(dwpe + off) + q;
+        float4 v = *d;
+        v.x += s[4 * q]; v.y += s[4 * q + 1]; v.z += s[4 * q + 2]; v.w += s[4 * q + 3];
+        *d = v;
+    }
 }
 
 // ============================================================== e4m3 quantization

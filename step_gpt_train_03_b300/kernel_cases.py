@@ -5,6 +5,8 @@ times: the target of per-kernel Nsight Compute captures.
 
 With --time, the runs are timed with CUDA events (after the untimed ones) and the
 case's algorithmic work rate is printed (TFLOP/s for products, GB/s for layernorm).
+With --flush, each timed run is bracketed by its own events and preceded (outside the
+events) by a write of 256 MB, twice the 126 MB L2, so no input starts in L2.
 
 Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
   matmul_fc_forward       (16384 x 768) @ (3072 x 768)^T
@@ -28,6 +30,7 @@ def main(argv=None):
     ap.add_argument("case")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--time", action="store_true")
+    ap.add_argument("--flush", action="store_true")
     args = ap.parse_args(argv)
     import torch
     from step_gpt_train_03_b300 import gpt2lib as G
@@ -109,16 +112,29 @@ def main(argv=None):
     torch.cuda.synchronize()
     print(f"{case}: {args.iters} runs ok")
     if args.time:
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        for _ in range(args.iters):
-            run()
-        e.record()
-        e.synchronize()
-        sec = s.elapsed_time(e) / 1e3 / args.iters
+        if args.flush:
+            junk = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+            total = 0.0
+            for _ in range(args.iters):
+                junk.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                run()
+                e.record()
+                e.synchronize()
+                total += s.elapsed_time(e)
+            sec = total / 1e3 / args.iters
+        else:
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(args.iters):
+                run()
+            e.record()
+            e.synchronize()
+            sec = s.elapsed_time(e) / 1e3 / args.iters
         rate = (f"{work / sec / 1e12:.1f} TFLOP/s" if unit == "flop" else
                 f"{work / sec / 1e9:.0f} GB/s" if unit == "byte" else f"{work / sec:.0f} tokens/s")
-        print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic)")
+        print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic){', L2 flushed' if args.flush else ''}")
     return 0
 
 
