@@ -201,15 +201,17 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                         const int kidx = rc + 2 * j, ks = kidx % AT_RING;
                         if (!mbar_wait(&ring_full[ks], (kidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
                         const uint32_t k_addr = smem_u32(smem + S::RING_OFF + ks * AT_TILE_BYTES);
+                        #pragma unroll
                         for (int x = 0; x < 2; x++) {
                             if (j >= nkx[x]) continue;
                             if (!mbar_wait(&s_free[x], (sn[x] & 1) ^ 1, abort_flag, err)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t q_addr = smem_u32(smem + S::Q_OFF + (qb * 2 + x) * AT_TILE_BYTES);
+                            // descriptors of step kk: the start address field (bytes / 16) advances by 2
+                            const uint64_t qd = sdesc(q_addr, 16, 1024), kd = sdesc(k_addr, 16, 1024);
 #pragma unroll
                             for (int kk = 0; kk < AT_HS / 16; kk++)
-                                tc_mma(TM_S(x), sdesc(q_addr + kk * 32, 16, 1024), sdesc(k_addr + kk * 32, 16, 1024),
-                                       IDESC_S, kk > 0 ? 1u : 0u);
+                                tc_mma(TM_S(x), qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
                             tc_commit(&s_full[x]);
                             sn[x]++;
                         }
@@ -222,6 +224,7 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                         const int vidx = rc + 2 * jj + 1, vs = vidx % AT_RING;
                         if (!mbar_wait(&ring_full[vs], (vidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
                         const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vs * AT_TILE_BYTES);
+                        #pragma unroll
                         for (int x = 0; x < 2; x++) {
                             if (jj >= nkx[x]) continue;
                             if (!mbar_wait(&p_full[x], pn[x] & 1, abort_flag, err)) { ok = false; break; }
@@ -229,9 +232,10 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                             if (jj == 0 && nitems[x] > 0 &&
                                 !mbar_wait(&o_free[x], (nitems[x] - 1) & 1, abort_flag, err)) { ok = false; break; }
                             tc_fence_after();
+                            const uint64_t vd = sdesc(v_addr, 8192, 1024);    // step kk: + 2048 bytes
 #pragma unroll
                             for (int kk = 0; kk < AT_BN / 16; kk++)
-                                tc_mma_ts(TM_O(x), TM_P(x) + kk * 8, sdesc(v_addr + kk * 2048, 8192, 1024), IDESC_O,
+                                tc_mma_ts(TM_O(x), TM_P(x) + kk * 8, vd + 128 * kk, IDESC_O,
                                           (jj > 0 || kk > 0) ? 1u : 0u);
                             tc_commit(&o_done[x]);
                             pn[x]++;
@@ -240,6 +244,7 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                         tc_commit(&ring_empty[vs]);
                     }
                 }
+                #pragma unroll
                 for (int x = 0; x < 2; x++)
                     if (nkx[x]) nitems[x]++;
                 rc += 2 * nk;
@@ -595,13 +600,13 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 if (!mbar_wait(x_free, (xc & 1) ^ 1, abort_flag, err)) return false;
                 tc_fence_after();
                 const uint32_t st = smem_u32(smem + S::RING_OFF + slot * AB_STAGE_BYTES);
+                // descriptors of step k: the start address field (bytes / 16) advances by 2
+                const uint64_t d0 = sdesc(r0, 16, 1024), d1 = sdesc(r1, 16, 1024);
+                const uint64_t e0 = sdesc(st, 16, 1024), e1 = sdesc(st + AT_TILE_BYTES, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < AT_HS / 16; k++)
-                    tc_mma(TM_X1, sdesc(r0 + k * 32, 16, 1024), sdesc(st + k * 32, 16, 1024), IDESC_X, k > 0);
+                for (int k = 0; k < AT_HS / 16; k++) tc_mma(TM_X1, d0 + 2 * k, e0 + 2 * k, IDESC_X, k > 0);
 #pragma unroll
-                for (int k = 0; k < AT_HS / 16; k++)
-                    tc_mma(TM_X2, sdesc(r1 + k * 32, 16, 1024), sdesc(st + AT_TILE_BYTES + k * 32, 16, 1024), IDESC_X,
-                           k > 0);
+                for (int k = 0; k < AT_HS / 16; k++) tc_mma(TM_X2, d1 + 2 * k, e1 + 2 * k, IDESC_X, k > 0);
                 tc_commit(x_full);
                 xc++;
                 return true;
@@ -623,19 +628,18 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                     tc_fence_after();
                     if (DKV) {
                         // dV += P^T dO_u ; dK += dS^T Q_u (A operands from TMEM, 8 columns per 16 queries)
+                        const uint64_t bo = sdesc(st + AT_TILE_BYTES, 8192, 1024), bq = sdesc(st, 8192, 1024);
 #pragma unroll
-                        for (int k = 0; k < AT_BN / 16; k++) {
-                            tc_mma_ts(TM_A1, TM_P + k * 8, sdesc(st + AT_TILE_BYTES + k * 2048, 8192, 1024), IDESC_A,
-                                      (i > 0 || k > 0));
-                            tc_mma_ts(TM_A2, TM_DS(pb) + k * 8, sdesc(st + k * 2048, 8192, 1024), IDESC_A,
-                                      (i > 0 || k > 0));
+                        for (int k = 0; k < AT_BN / 16; k++) {      // step k: + 2048 bytes
+                            tc_mma_ts(TM_A1, TM_P + k * 8, bo + 128 * k, IDESC_A, (i > 0 || k > 0));
+                            tc_mma_ts(TM_A2, TM_DS(pb) + k * 8, bq + 128 * k, IDESC_A, (i > 0 || k > 0));
                         }
                     } else {
                         // dQ += dS K_u (dS from TMEM)
+                        const uint64_t bk = sdesc(st, 8192, 1024);
 #pragma unroll
                         for (int k = 0; k < AT_BN / 16; k++)
-                            tc_mma_ts(TM_A1, TM_DS(pb) + k * 8, sdesc(st + k * 2048, 8192, 1024), IDESC_A,
-                                      (i > 0 || k > 0));
+                            tc_mma_ts(TM_A1, TM_DS(pb) + k * 8, bk + 128 * k, IDESC_A, (i > 0 || k > 0));
                     }
                     tc_commit(&pds_free[pb]);
                     tc_commit(&ring_empty[slot]);

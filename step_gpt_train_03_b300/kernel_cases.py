@@ -6,7 +6,9 @@ times: the target of per-kernel Nsight Compute captures.
 With --time, the runs are timed with CUDA events (after the untimed ones) and the
 case's algorithmic work rate is printed (TFLOP/s for products, GB/s for layernorm).
 With --flush, each timed run is bracketed by its own events and preceded (outside the
-events) by a write of 256 MB, twice the 126 MB L2, so no input starts in L2.
+events) by a write of 256 MB, twice the 126 MB L2, so no input starts in L2 (the events
+then also time the launch).  With --rotate (layernorm cases), the runs go back to back
+over six copies of the per-row tensors, a working set larger than L2.
 
 Cases (B*T = 16384 rows, C = 768, NH = 12, Vp = 50304, bf16 unless stated):
   matmul_fc_forward       (16384 x 768) @ (3072 x 768)^T
@@ -31,6 +33,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--time", action="store_true")
     ap.add_argument("--flush", action="store_true")
+    ap.add_argument("--rotate", action="store_true")
     args = ap.parse_args(argv)
     import torch
     from step_gpt_train_03_b300 import gpt2lib as G
@@ -82,11 +85,31 @@ def main(argv=None):
         dw = torch.zeros(C, device=dev)
         db = torch.zeros(C, device=dev)
         sc = torch.empty(G.layernorm_backward_scratch_bytes(N, C), dtype=torch.uint8, device=dev)
+        # --rotate: six copies of every per-row tensor (6 x 4 x 25 MB > the 126 MB L2), used
+        # in turn, so back-to-back runs never find their inputs in L2
+        ncopy = 6 if args.rotate else 1
+        X = [x] + [x.clone() for _ in range(ncopy - 1)]
+        Y = [y] + [torch.empty_like(y) for _ in range(ncopy - 1)]
+        DY = [dy] + [dy.clone() for _ in range(ncopy - 1)]
+        DX = [dx] + [torch.zeros_like(dx) for _ in range(ncopy - 1)]
+        ST = [(mean, rstd)] + [(torch.empty_like(mean), torch.empty_like(rstd)) for _ in range(ncopy - 1)]
+        for i in range(1, ncopy):
+            G.layernorm_forward(Y[i], ST[i][0], ST[i][1], X[i], w, b)
+        ctr = [0]
+
+        def pick():
+            i = ctr[0] % ncopy
+            ctr[0] += 1
+            return i
         if case == "layernorm_backward_fp32":
-            run = lambda: G.layernorm_backward(dx, dw, db, dy, x, w, mean, rstd, sc)
+            def run():
+                i = pick()
+                G.layernorm_backward(DX[i], dw, db, DY[i], X[i], w, ST[i][0], ST[i][1], sc)
             work, unit = 4.0 * N * C * 4 + 8.0 * N, "byte"     # dy, x, dinp read; dinp written; stats
         else:
-            run = lambda: G.layernorm_forward(y, mean, rstd, x, w, b)
+            def run():
+                i = pick()
+                G.layernorm_forward(Y[i], ST[i][0], ST[i][1], X[i], w, b)
             work, unit = 2.0 * N * C * 4 + 8.0 * N, "byte"     # x read, y written; stats
     elif case in ("eval_124m", "sample_124m"):
         from step_gpt_train_03_b300 import synth
@@ -134,7 +157,7 @@ def main(argv=None):
             sec = s.elapsed_time(e) / 1e3 / args.iters
         rate = (f"{work / sec / 1e12:.1f} TFLOP/s" if unit == "flop" else
                 f"{work / sec / 1e9:.0f} GB/s" if unit == "byte" else f"{work / sec:.0f} tokens/s")
-        print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic){', L2 flushed' if args.flush else ''}")
+        print(f"{case}: {sec * 1e6:.1f} us per run, {rate} (algorithmic){', L2 flushed' if args.flush else ', 6 rotating input copies' if args.rotate else ''}")
     return 0
 
 
