@@ -537,15 +537,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 }
 
-// out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic)
+// out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic).  All
+// of a packet's partial loads (splits <= TC_MAX_SPLITS) are issued before the first add.
+#define TC_MAX_SPLITS 8
 __global__ void splitk_reduce_kernel(float* __restrict__ out, const float* __restrict__ part, size_t n4,
                                      int splits) {
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
+    float4 p[TC_MAX_SPLITS];
+#pragma unroll
+    for (int s = 0; s < TC_MAX_SPLITS; s++)
+        if (s < splits) p[s] = __ldcs(reinterpret_cast<const float4*>(part) + (size_t)s * n4 + i);
     float4 acc = reinterpret_cast<float4*>(out)[i];
-    for (int s = 0; s < splits; s++) {
-        float4 p = reinterpret_cast<const float4*>(part)[(size_t)s * n4 + i];
-        acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+#pragma unroll
+    for (int s = 0; s < TC_MAX_SPLITS; s++) {
+        if (s < splits) { acc.x += p[s].x; acc.y += p[s].y; acc.z += p[s].z; acc.w += p[s].w; }
     }
     reinterpret_cast<float4*>(out)[i] = acc;
 }
@@ -577,8 +583,7 @@ int gemm_tc_available() {
 }
 
 // Split-K is only used when a weight gradient has fewer 128x256 tiles than the GPU has
-// SMs, with at most 8 splits: its partials never exceed 8 x (SMs x one tile).
-#define TC_MAX_SPLITS 8
+// SMs, with at most TC_MAX_SPLITS splits: its partials never exceed 8 x (SMs x one tile).
 #define TC_SPLIT_SM_BOUND 160
 size_t gemm_tc_scratch_floats(size_t M, size_t N) {
     (void)M;
