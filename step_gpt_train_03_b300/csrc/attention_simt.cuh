@@ -15,6 +15,7 @@ template <typename T>
 __global__ void __launch_bounds__(ATT_WARPS * 32)
 attention_forward_simt(T* __restrict__ out, float* __restrict__ att, const T* __restrict__ qkv,
                        int B, int Tn, int C, int NH) {
+    pdl_wait();
     __shared__ float qs[ATT_WARPS][ATT_MAX_HS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * ATT_WARPS + warp;
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(ATT_WARPS * 32)
 attention_backward_ds(float* __restrict__ ds, const float* __restrict__ att,
                       const T* __restrict__ dout, const T* __restrict__ qkv,
                       int B, int Tn, int C, int NH) {
+    pdl_wait();
     __shared__ float dos[ATT_WARPS][ATT_MAX_HS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * ATT_WARPS + warp;
@@ -90,6 +92,7 @@ template <typename T>
 __global__ void __launch_bounds__(ATT_WARPS * 32)
 attention_backward_dq(T* __restrict__ dqkv, const float* __restrict__ ds, const T* __restrict__ qkv,
                       int B, int Tn, int C, int NH) {
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * ATT_WARPS + warp;
     if (gw >= B * NH * Tn) return;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(ATT_WARPS * 32)
 attention_backward_dkv(T* __restrict__ dqkv, const float* __restrict__ ds,
                        const float* __restrict__ att, const T* __restrict__ qkv,
                        const T* __restrict__ dout, int B, int Tn, int C, int NH) {
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * ATT_WARPS + warp;
     if (gw >= B * NH * Tn) return;

@@ -135,6 +135,10 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // set-up done (barriers, TMEM, descriptor prefetch): wait for the predecessor's
+    // results, and let the next kernel's CTAs launch onto SMs as ours retire
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem_base = *tmem_slot;
     auto TM_S = [&](int x) { return tmem_base + x * AT_BN; };          // columns 0, 128
     auto TM_O = [&](int x) { return tmem_base + 256 + x * AT_HS; };    // 256, 320
@@ -537,6 +541,10 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // set-up done (barriers, TMEM, descriptor prefetch): wait for the predecessor's
+    // results, and let the next kernel's CTAs launch onto SMs as ours retire
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem_base = *tmem_slot;
     // S (S^T), dP (dP^T), dV or dQ, dK; then DKV: P^T, dS^T; DQ: dS[2]
     const uint32_t TM_X1 = tmem_base, TM_X2 = tmem_base + 128, TM_A1 = tmem_base + 256, TM_A2 = tmem_base + 320;
@@ -896,7 +904,7 @@ int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const _
     if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&to, out, C, Tn, B, C)) return GPT2_EUNSUPPORTED;
     const int items = ((Tn + AT_BM - 1) / AT_BM + 1) / 2 * B * NH;      // pairs of query tiles
     const int grid = items < g_sms ? items : g_sms;
-    attention_tc_forward_kernel<<<grid, AT_THREADS, AtSmem::TOTAL, s>>>(tq, to, lse, B, Tn, C, NH, err);
+    launch_pdl(attention_tc_forward_kernel, grid, AT_THREADS, AtSmem::TOTAL, s, tq, to, lse, B, Tn, C, NH, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
@@ -922,6 +930,7 @@ static bool make_map_vec(CUtensorMap* map, const float* base, int Tn, int Tp, in
 __global__ void attention_rowdot_kernel(float* __restrict__ D, float* __restrict__ lse_pad,
                                         const float* __restrict__ lse, const bf16* __restrict__ dout,
                                         const bf16* __restrict__ out, int B, int Tn, int Tp, int C, int NH) {
+    pdl_wait();
     const int row = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 3);
     const int sub = threadIdx.x & 7;
     const bool valid = row < B * NH * Tn;
@@ -958,7 +967,7 @@ static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& 
     }
     const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
     const int grid = items < g_sms ? items : g_sms;
-    attention_tc_backward_kernel<DKV><<<grid, AT_THREADS, AbSmem<DKV>::TOTAL, s>>>(tq, tdo, tl, td, tdq, lse, D, B,
+    launch_pdl(attention_tc_backward_kernel<DKV>, grid, AT_THREADS, AbSmem<DKV>::TOTAL, s, tq, tdo, tl, td, tdq, lse, D, B,
                                                                                     Tn, Tp, C, NH, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
@@ -983,7 +992,7 @@ int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat
     const float* lse_k = lse_pad ? lse_pad : lse;
     if (!lse_pad && ((uintptr_t)lse & 15)) return GPT2_EUNSUPPORTED;
     const long long rows = (long long)B * NH * Tn;
-    attention_rowdot_kernel<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, s>>>(D, lse_pad, lse, dout, out, B, Tn, Tp,
+    launch_pdl(attention_rowdot_kernel, (unsigned)((rows * 8 + 255) / 256), 256, 0, s, D, lse_pad, lse, dout, out, B, Tn, Tp,
                                                                               C, NH);
     rt_note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return GPT2_ECUDA;

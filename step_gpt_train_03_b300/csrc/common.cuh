@@ -101,3 +101,33 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ size_t ceil_div_sz(size_t a, size_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ dependent launches
+// Every kernel of the library starts with pdl_wait(): launched with programmatic stream
+// serialization, a kernel may begin before its predecessor in the stream has finished,
+// and this waits until the predecessor has completed and its memory writes are visible
+// (launched normally, it returns at once).  Kernels whose CTAs are all resident from
+// their launch (the persistent tensor-core kernels) also call pdl_trigger() after their
+// set-up, letting the next kernel's CTAs launch onto SMs as they free up and do their
+// own set-up before they, in turn, wait.  Kernels with more CTAs than resident slots do
+// not trigger, so a waiting successor can never hold a slot one of their CTAs needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+#include <utility>
+// Launch `kern` with programmatic stream serialization allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}

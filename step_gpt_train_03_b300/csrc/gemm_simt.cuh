@@ -58,6 +58,7 @@ template <typename T, bool A_KC, bool B_KC, int EPI>
 __global__ void __launch_bounds__(SG_THREADS)
 gemm_simt_kernel(const T* __restrict__ A, const T* __restrict__ B, int M, int N, int K,
                  long lda, long ldb, EpiArgs ep) {
+    pdl_wait();
     __shared__ float As[SG_BK][SG_BM + 4];
     __shared__ float Bs[SG_BK][SG_BN + 4];
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
@@ -110,6 +111,6 @@ template <typename T, bool A_KC, bool B_KC, int EPI>
 static cudaError_t launch_gemm_simt(cudaStream_t s, const T* A, long lda, const T* B, long ldb,
                                     int M, int N, int K, const EpiArgs& ep) {
     dim3 grid(ceil_div(N, SG_BN), ceil_div(M, SG_BM));
-    gemm_simt_kernel<T, A_KC, B_KC, EPI><<<grid, SG_THREADS, 0, s>>>(A, B, M, N, K, lda, ldb, ep);
+    launch_pdl(gemm_simt_kernel<T, A_KC, B_KC, EPI>, grid, SG_THREADS, 0, s, A, B, M, N, K, lda, ldb, ep);
     return cudaGetLastError();
 }

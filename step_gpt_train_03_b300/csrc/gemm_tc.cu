@@ -179,6 +179,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     if (CL > 1) cluster_sync();        // the peer's barriers and TMEM address exist from here on
     tc_fence_after();
+    // set-up done (barriers, TMEM, descriptor prefetch): wait for the predecessor's
+    // results, and let the next kernel's CTAs launch onto SMs as ours retire
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem_base = *tmem_slot;
     // the pair's MMAs write one TMEM address in both CTAs: if the two allocations
     // differ, no work is done (both CTAs see the same two values and agree)
@@ -542,6 +546,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #define TC_MAX_SPLITS 8
 __global__ void splitk_reduce_kernel(float* __restrict__ out, const float* __restrict__ part, size_t n4,
                                      int splits) {
+    pdl_wait();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     float4 p[TC_MAX_SPLITS];
@@ -633,7 +638,7 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
     static int max_clusters = 0;            // co-resident clusters of CL CTAs (0: not yet queried)
     auto kern = gemm_tc_kernel<BN, EPI, A_MN, B_MN, CL, F8>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = SM::TOTAL;
     cfg.stream = s;
@@ -641,6 +646,8 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;    // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (max_clusters == 0) {
@@ -654,6 +661,7 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
     const int units = ((M + TC_BM - 1) / TC_BM + CL - 1) / CL * ((N + BN - 1) / BN) * splits;
     const int clusters = units < max_clusters ? units : max_clusters;
     cfg.gridDim = dim3(clusters * CL);
+    cfg.numAttrs = 2;
     // stream the larger operand once: m fastest when B (N x K) is larger than A (M x K)
     const int m_fast = N > M ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, to, tx, M, N, K, splits, m_fast, ep, err) != cudaSuccess)
@@ -827,7 +835,7 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
                      : launch_tc<256, TC_EPI_PARTIAL, true, true, 1>(s, ta, tb, to, to, N, K, M, splits, ep, err);
     if (rc != GPT2_OK) return rc;
     const size_t n4 = (size_t)N * K / 4;
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(dW, scratch, n4, splits);
+    launch_pdl(splitk_reduce_kernel, (unsigned)((n4 + 255) / 256), 256, 0, s, dW, scratch, n4, splits);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }

@@ -277,7 +277,7 @@ static int launch_zero(cudaStream_t s, void* p, size_t bytes) {
     if (n4 == 0) return GPT2_OK;
     int grid = (int)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 8);
     ProfScope ps(s, PC_MISC, 0, (double)bytes);
-    zero_kernel<<<grid, 256, 0, s>>>((float4*)p, n4);
+    launch_pdl(zero_kernel, grid, 256, 0, s, (float4*)p, n4);
     rt_note_launches(1);
     CK(cudaGetLastError());
     return GPT2_OK;
@@ -385,7 +385,7 @@ extern "C" void* gpt2_logits(GPT2* m) { return m ? m->logits : nullptr; }
 extern "C" int gpt2_sync_params(GPT2* m) {
     if (!m) return GPT2_EINVAL;
     if (m->wbf) {
-        f32_to_bf16_kernel<<<148 * 8, 256, 0, m->stream>>>(m->wbf, m->params, m->n_flat);
+        launch_pdl(f32_to_bf16_kernel, 148 * 8, 256, 0, m->stream, m->wbf, m->params, m->n_flat);
         rt_note_launches(1);
         CK(cudaGetLastError());
     }
@@ -401,10 +401,10 @@ extern "C" int gpt2_sample(GPT2* m, int pos, float temperature, unsigned long lo
     if (pos < 0 || pos >= m->T) return GPT2_EINVAL;
     const float inv = 1.0f / temperature;
     if (m->prec != GPT2_FP32)
-        sample_kernel<bf16><<<m->B, SAMPLE_THREADS, 0, m->stream>>>(out, (const bf16*)m->logits, m->T, pos, m->V,
+        launch_pdl(sample_kernel<bf16>, m->B, SAMPLE_THREADS, 0, m->stream, out, (const bf16*)m->logits, m->T, pos, m->V,
                                                                    m->Vp, inv, seed);
     else
-        sample_kernel<float><<<m->B, SAMPLE_THREADS, 0, m->stream>>>(out, (const float*)m->logits, m->T, pos, m->V,
+        launch_pdl(sample_kernel<float>, m->B, SAMPLE_THREADS, 0, m->stream, out, (const float*)m->logits, m->T, pos, m->V,
                                                                     m->Vp, inv, seed);
     rt_note_launches(1);
     CK(cudaGetLastError());
@@ -481,7 +481,7 @@ static int ln_forward(cudaStream_t s, T* out, float* mean, float* rstd, const T*
     ProfScope ps(s, PC_LAYERNORM_FWD, 0, 2.0 * N * C * sizeof(T) + 8.0 * N + 2.0 * C * sizeof(T));
     rt_note_launches(1);
     switch (nv) {
-#define LNF_CASE(k) case k: layernorm_forward_kernel<T, k><<<grid, LN_WARPS * 32, 0, s>>>(out, mean, rstd, inp, w, b, N, C); break;
+#define LNF_CASE(k) case k: launch_pdl(layernorm_forward_kernel<T, k>, grid, LN_WARPS * 32, 0, s, out, mean, rstd, inp, w, b, N, C, (uint8_t*)nullptr, (float*)nullptr); break;
         LNF_CASE(1) LNF_CASE(2) LNF_CASE(3) LNF_CASE(4) LNF_CASE(5) LNF_CASE(6) LNF_CASE(7) LNF_CASE(8)
         LNF_CASE(9) LNF_CASE(10) LNF_CASE(11) LNF_CASE(12) LNF_CASE(13) LNF_CASE(14) LNF_CASE(15) LNF_CASE(16)
 #undef LNF_CASE
@@ -501,7 +501,7 @@ static int ln_forward_q8(cudaStream_t s, T* out, float* mean, float* rstd, const
     ProfScope ps(s, PC_LAYERNORM_FWD, 0, 2.0 * N * C * sizeof(T) + 1.0 * N * C + 12.0 * N + 2.0 * C * sizeof(T));
     rt_note_launches(1);
     switch (nv) {
-#define LNQ_CASE(k) case k: layernorm_forward_kernel<T, k, true><<<grid, LN_WARPS * 32, 0, s>>>(out, mean, rstd, inp, w, b, N, C, q, qdeq); break;
+#define LNQ_CASE(k) case k: launch_pdl(layernorm_forward_kernel<T, k, true>, grid, LN_WARPS * 32, 0, s, out, mean, rstd, inp, w, b, N, C, q, qdeq); break;
         LNQ_CASE(1) LNQ_CASE(2) LNQ_CASE(3) LNQ_CASE(4) LNQ_CASE(5) LNQ_CASE(6) LNQ_CASE(7) LNQ_CASE(8)
         LNQ_CASE(9) LNQ_CASE(10) LNQ_CASE(11) LNQ_CASE(12) LNQ_CASE(13) LNQ_CASE(14) LNQ_CASE(15) LNQ_CASE(16)
 #undef LNQ_CASE
@@ -519,9 +519,9 @@ static int quantize_tensors(cudaStream_t s, uint8_t* q, float* deq, unsigned* am
     CK(cudaMemsetAsync(amax_bits, 0, sizeof(unsigned) * ntens, s));
     const int gx = (int)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4 / std::max(1, ntens) + 1);
     rt_note_launches(2);
-    absmax_tensors_kernel<<<dim3(gx, ntens), 256, 0, s>>>(amax_bits, w, len);
+    launch_pdl(absmax_tensors_kernel, dim3(gx, ntens), 256, 0, s, amax_bits, w, len);
     CK(cudaGetLastError());
-    quantize_tensors_kernel<<<dim3(gx, ntens), 256, 0, s>>>(q, deq, amax_bits, w, len);
+    launch_pdl(quantize_tensors_kernel, dim3(gx, ntens), 256, 0, s, q, deq, amax_bits, w, len);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
@@ -563,7 +563,7 @@ static int red_flush(cudaStream_t s, RedQueue& q) {
     if (q.n == 0) return GPT2_OK;
     ProfScope ps(s, PC_MISC, 0, 0);
     rt_note_launches(1);
-    column_reduce_batch_kernel<<<dim3(ceil_div(q.max_w, 32), q.n), 256, 0, s>>>(q.batch);
+    launch_pdl(column_reduce_batch_kernel, dim3(ceil_div(q.max_w, 32), q.n), 256, 0, s, q.batch);
     CK(cudaGetLastError());
     q.n = 0;
     q.used = 0;
@@ -575,9 +575,9 @@ static int red_flush(cudaStream_t s, RedQueue& q) {
 static void column_reduce_any(cudaStream_t s, float* out0, float* out1, int split, const float* partial, int G,
                               int W, float* out2) {
     if (W % 4 == 0 && ((uintptr_t)partial & 15) == 0)
-        column_reduce4_kernel<<<ceil_div(W, 32), 256, 0, s>>>(out0, out1, split, partial, G, W, out2);
+        launch_pdl(column_reduce4_kernel, ceil_div(W, 32), 256, 0, s, out0, out1, split, partial, G, W, out2);
     else
-        column_reduce_kernel<<<ceil_div(W, CR_COLS), CR_COLS * CR_GROUPS, 0, s>>>(out0, out1, split, partial, G, W, out2);
+        launch_pdl(column_reduce_kernel, ceil_div(W, CR_COLS), CR_COLS * CR_GROUPS, 0, s, out0, out1, split, partial, G, W, out2);
 }
 
 static int ln_backward_grid(int N) { return std::max(1, std::min(ceil_div(N, LN_WARPS * 2), 296)); }
@@ -599,14 +599,14 @@ static int ln_backward_launch(cudaStream_t s, int& G, T* dinp, float* partial, c
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pipe_smem) != cudaSuccess)
             return GPT2_ECUDA;
         if (pipe_smem > 113 * 1024) G = std::min(G, 148);     // one block per SM: a single wave
-        layernorm_backward_pipe_kernel<T, NV, SUM><<<G, LN_WARPS * 32, pipe_smem, s>>>(dinp, partial, dout, inp, w,
+        launch_pdl(layernorm_backward_pipe_kernel<T, NV, SUM>, G, LN_WARPS * 32, pipe_smem, s, dinp, partial, dout, inp, w,
                                                                                      mean, rstd, N, C, err);
     } else {
         const size_t smem = (SUM ? (3 + LN_WARPS) : 2) * C * sizeof(float);
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(layernorm_backward_kernel<T, NV, SUM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
-        layernorm_backward_kernel<T, NV, SUM><<<G, LN_WARPS * 32, smem, s>>>(dinp, partial, dout, inp, w, mean, rstd,
+        launch_pdl(layernorm_backward_kernel<T, NV, SUM>, G, LN_WARPS * 32, smem, s, dinp, partial, dout, inp, w, mean, rstd,
                                                                             N, C);
     }
     CK(cudaGetLastError());
@@ -668,8 +668,8 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
     ProfScope ps(s, PC_BIAS_GRAD, 0, (double)M * N * sizeof(T) + 8.0 * N);
     rt_note_launches(qpart ? 1 : 2);
     constexpr int EPV = Vec<T>::N;
-    if (N % EPV) colsum_partial_scalar_kernel<T><<<dim3(ceil_div(N, 128), R), 128, 0, s>>>(partial, x, M, N, rows);
-    else colsum_partial_kernel<T><<<dim3(ceil_div(N / EPV, 32), R), CS_WARPS * 32, 0, s>>>(partial, x, M, N, rows);
+    if (N % EPV) launch_pdl(colsum_partial_scalar_kernel<T>, dim3(ceil_div(N, 128), R), 128, 0, s, partial, x, M, N, rows);
+    else launch_pdl(colsum_partial_kernel<T>, dim3(ceil_div(N / EPV, 32), R), CS_WARPS * 32, 0, s, partial, x, M, N, rows);
     CK(cudaGetLastError());
     if (qpart) {
         q->push(partial, out, out, nullptr, N, R, N);
@@ -772,7 +772,7 @@ static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, in
     } else {
         float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
         int rows = B * NH * Tn;
-        attention_forward_simt<T><<<ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s>>>(out, att, qkv, B, Tn, C, NH);
+        launch_pdl(attention_forward_simt<T>, ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s, out, att, qkv, B, Tn, C, NH);
         rt_note_launches(1);
         CK(cudaGetLastError());
         return GPT2_OK;
@@ -795,11 +795,11 @@ static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const 
         int rows = B * NH * Tn;
         int grid = ceil_div(rows, ATT_WARPS);
         rt_note_launches(3);
-        attention_backward_ds<T><<<grid, ATT_WARPS * 32, 0, s>>>(m->datt, att, dout, qkv, B, Tn, C, NH);
+        launch_pdl(attention_backward_ds<T>, grid, ATT_WARPS * 32, 0, s, m->datt, att, dout, qkv, B, Tn, C, NH);
         CK(cudaGetLastError());
-        attention_backward_dq<T><<<grid, ATT_WARPS * 32, 0, s>>>(dqkv, m->datt, qkv, B, Tn, C, NH);
+        launch_pdl(attention_backward_dq<T>, grid, ATT_WARPS * 32, 0, s, dqkv, m->datt, qkv, B, Tn, C, NH);
         CK(cudaGetLastError());
-        attention_backward_dkv<T><<<grid, ATT_WARPS * 32, 0, s>>>(dqkv, m->datt, att, qkv, dout, B, Tn, C, NH);
+        launch_pdl(attention_backward_dkv<T>, grid, ATT_WARPS * 32, 0, s, dqkv, m->datt, att, qkv, dout, B, Tn, C, NH);
         CK(cudaGetLastError());
         return GPT2_OK;
     }
@@ -821,7 +821,7 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         size_t n = (size_t)BT * (C / EPV);
         ProfScope ps(s, PC_ENCODER_FWD, 0, 3.0 * BT * C * sizeof(T) + 4.0 * BT);
         rt_note_launches(1);
-        encoder_forward_kernel<T><<<(unsigned)ceil_div_sz(n, 256), 256, 0, s>>>(encoded, m->tokens, P(P_WTE), P(P_WPE), BT, Tn, C, m->V, m->err);
+        launch_pdl(encoder_forward_kernel<T>, (unsigned)ceil_div_sz(n, 256), 256, 0, s, encoded, m->tokens, P(P_WTE), P(P_WPE), BT, Tn, C, m->V, m->err);
         CK(cudaGetLastError());
     }
     const T* x = encoded;
@@ -865,10 +865,10 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         {
             ProfScope ps(s, PC_SOFTMAX_XENT, 0, 2.0 * BT * m->Vp * sizeof(T) + 12.0 * BT);
             rt_note_launches(2);
-            softmax_xent_kernel<T><<<BT, XENT_THREADS, 0, s>>>((T*)m->logits, m->losses, m->targets, m->V, m->Vp,
+            launch_pdl(softmax_xent_kernel<T>, BT, XENT_THREADS, 0, s, (T*)m->logits, m->losses, m->targets, m->V, m->Vp,
                                                                1.0f / (float)BT, m->err);
             CK(cudaGetLastError());
-            mean_loss_kernel<<<1, 1024, 0, s>>>(m->loss, m->losses, BT, m->err);
+            launch_pdl(mean_loss_kernel, 1, 1024, 0, s, m->loss, m->losses, BT, m->err);
             CK(cudaGetLastError());
         }
         // order the token positions by id now; the encoder backward consumes it.  One
@@ -882,11 +882,11 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         for (int p = 0; p < npass; p++) {
             unsigned* dst = ((npass - 1 - p) & 1) ? m->sort_tmp : m->sorted_keys;
             rt_note_launches(3);
-            radix_hist_kernel<<<nblk, RADIX_BLOCK, 0, s>>>(m->sort_hist, src, m->tokens, BT, m->V, 8 * p, nblk);
+            launch_pdl(radix_hist_kernel, nblk, RADIX_BLOCK, 0, s, m->sort_hist, src, m->tokens, BT, m->V, 8 * p, nblk);
             CK(cudaGetLastError());
-            radix_scan_kernel<<<1, RADIX_BLOCK, 0, s>>>(m->sort_hist, 256 * nblk);
+            launch_pdl(radix_scan_kernel, 1, RADIX_BLOCK, 0, s, m->sort_hist, 256 * nblk);
             CK(cudaGetLastError());
-            radix_scatter_kernel<<<nblk, RADIX_BLOCK, 0, s>>>(dst, src, m->tokens, m->sort_hist, BT, m->V, 8 * p, nblk);
+            launch_pdl(radix_scatter_kernel, nblk, RADIX_BLOCK, 0, s, dst, src, m->tokens, m->sort_hist, BT, m->V, 8 * p, nblk);
             CK(cudaGetLastError());
             src = dst;
         }
@@ -966,11 +966,11 @@ static int backward_impl(GPT2* m) {
     ProfScope ps(s, PC_ENCODER_BWD, 0, (double)BT * C * sizeof(T) + 8.0 * BT * C + 8.0 * Tn * C);
     rt_note_launches(3);
     const int enc_threads = std::min(256, ceil_div(C / Vec<T>::N, 32) * 32);
-    encoder_backward_wte_partial<T><<<ceil_div(BT, ENC_CHUNK), enc_threads, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, dresid, BT, C, m->V);
+    launch_pdl(encoder_backward_wte_partial<T>, ceil_div(BT, ENC_CHUNK), enc_threads, 0, s, G(P_WTE), m->enc_partial, m->sorted_keys, dresid, BT, C, m->V);
     CK(cudaGetLastError());
-    encoder_backward_wte_final<<<ceil_div(BT, ENC_CHUNK), 256, 0, s>>>(G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
+    launch_pdl(encoder_backward_wte_final, ceil_div(BT, ENC_CHUNK), 256, 0, s, G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
     CK(cudaGetLastError());
-    encoder_backward_wpe<T><<<ceil_div(Tn * C / Vec<T>::N, 256), 256, 0, s>>>(G(P_WPE), dresid, B, Tn, C);
+    launch_pdl(encoder_backward_wpe<T>, ceil_div(Tn * C / Vec<T>::N, 256), 256, 0, s, G(P_WPE), dresid, B, Tn, C);
     CK(cudaGetLastError());
     return GPT2_OK;
 }
@@ -1063,7 +1063,7 @@ extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float ep
     adam_args(m, a, lr, beta1, beta2, eps, wd, t);
     ProfScope ps(m->stream, PC_ADAMW, 0, (double)m->n_flat * (m->wbf ? 30.0 : 28.0));
     rt_note_launches(1);
-    adamw_kernel<<<a.grid, 256, 0, m->stream>>>(a.p, a.g, a.mm, a.vv, a.shadow, a.n4, a.lr, a.b1, a.b2, a.eps,
+    launch_pdl(adamw_kernel, a.grid, 256, 0, m->stream, a.p, a.g, a.mm, a.vv, a.shadow, a.n4, a.lr, a.b1, a.b2, a.eps,
                                                 a.wd, a.bc1, a.bc2);
     CK(cudaGetLastError());
     return quantize_model_weights(m);        // fp8 mode: the e4m3 weight shadows follow
@@ -1087,7 +1087,7 @@ static int newton_schulz_bf16(cudaStream_t s, bf16* X, bf16* xb, bf16* S, bf16* 
                     : gemm_tc_bf16(s, S, X, false, X, false, r, r, c, err));
         }
         rt_note_launches(1);
-        ns_affine_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz((size_t)n * n, 256), 592), 256, 0, s>>>(T, S, n);
+        launch_pdl(ns_affine_kernel, (unsigned)std::min<size_t>(ceil_div_sz((size_t)n * n, 256), 592), 256, 0, s, T, S, n);
         CK(cudaGetLastError());
         {
             ProfScope ps(s, PC_MATMUL_FWD, 2.0 * r * c * n, 0);
@@ -1119,7 +1119,7 @@ extern "C" int gpt2_update_muon(GPT2* m, float lr_muon, float momentum, int ns_i
             const size_t n4 = (end - start) / 4;
             ProfScope ps(s, PC_ADAMW, 0, (double)(end - start) * 30.0);
             rt_note_launches(1);
-            adamw_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 16), 256, 0, s>>>(
+            launch_pdl(adamw_kernel, (unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 16), 256, 0, s, 
                 m->params + start, m->grads + start, m->m + start, m->v + start, m->wbf + start, n4, a.lr, a.b1, a.b2,
                 a.eps, a.wd, a.bc1, a.bc2);
             CK(cudaGetLastError());
@@ -1133,12 +1133,12 @@ extern "C" int gpt2_update_muon(GPT2* m, float lr_muon, float momentum, int ns_i
             ProfScope ps(s, PC_MISC, 0, 12.0 * L * len + 2.0 * L * len);
             rt_note_launches(3);
             const size_t n4 = L * len / 4;
-            muon_momentum_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 8), 256, 0, s>>>(
+            launch_pdl(muon_momentum_kernel, (unsigned)std::min<size_t>(ceil_div_sz(n4, 256), 148 * 8), 256, 0, s, 
                 (float4*)mom, (const float4*)(m->grads + off), n4, momentum);
             CK(cudaGetLastError());
-            sumsq_partial_kernel<<<dim3(MUON_NB, L), 256, 0, s>>>(m->mu_part, mom, len);
+            launch_pdl(sumsq_partial_kernel, dim3(MUON_NB, L), 256, 0, s, m->mu_part, mom, len);
             CK(cudaGetLastError());
-            scale_frobenius_bf16_kernel<<<dim3(std::max(1, 148 * 4 / L), L), 256, 0, s>>>(m->mu_x, mom, m->mu_part, len);
+            launch_pdl(scale_frobenius_bf16_kernel, dim3(std::max(1, 148 * 4 / L), L), 256, 0, s, m->mu_x, mom, m->mu_part, len);
             CK(cudaGetLastError());
         }
         for (int l = 0; l < L; l++) {
@@ -1147,7 +1147,7 @@ extern "C" int gpt2_update_muon(GPT2* m, float lr_muon, float momentum, int ns_i
                                   m->err));
             ProfScope ps(s, PC_MISC, 0, 14.0 * len);
             rt_note_launches(1);
-            muon_apply_kernel<<<(unsigned)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4), 256, 0, s>>>(
+            launch_pdl(muon_apply_kernel, (unsigned)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4), 256, 0, s, 
                 (float4*)(m->params + off + l * len), res, m->wbf + off + l * len, len / 4, lr_muon, wd);
             CK(cudaGetLastError());
         }
@@ -1178,9 +1178,9 @@ extern "C" int gpt2_newton_schulz(void* out, const float* G, int r, int c, int i
     unsigned* err = nullptr;
     RC(layer_err_word(&err));
     rt_note_launches(2);
-    sumsq_partial_kernel<<<dim3(MUON_NB, 1), 256, 0, s>>>(part, G, len);
+    launch_pdl(sumsq_partial_kernel, dim3(MUON_NB, 1), 256, 0, s, part, G, len);
     CK(cudaGetLastError());
-    scale_frobenius_bf16_kernel<<<dim3(148, 1), 256, 0, s>>>((bf16*)out, G, part, len);
+    launch_pdl(scale_frobenius_bf16_kernel, dim3(148, 1), 256, 0, s, (bf16*)out, G, part, len);
     CK(cudaGetLastError());
     bf16* res = nullptr;
     RC(newton_schulz_bf16(s, (bf16*)out, xb, S, T, r, c, iters, &res, err));
@@ -1551,7 +1551,7 @@ extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, in
     }
     if (precision == GPT2_FP32) {
         const int rows = B * NH * Tn;
-        attention_forward_simt<float><<<ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s>>>(
+        launch_pdl(attention_forward_simt<float>, ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s, 
             (float*)out, lse, (const float*)qkv, B, Tn, C, NH);
         rt_note_launches(1);
         CK(cudaGetLastError());
@@ -1586,9 +1586,9 @@ extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void*
         const int grid = ceil_div(rows, ATT_WARPS);
         float* ds = (float*)scratch;
         rt_note_launches(3);
-        attention_backward_ds<float><<<grid, ATT_WARPS * 32, 0, s>>>(ds, lse, (const float*)dout, (const float*)qkv, B, Tn, C, NH);
-        attention_backward_dq<float><<<grid, ATT_WARPS * 32, 0, s>>>((float*)dqkv, ds, (const float*)qkv, B, Tn, C, NH);
-        attention_backward_dkv<float><<<grid, ATT_WARPS * 32, 0, s>>>((float*)dqkv, ds, lse, (const float*)qkv,
+        launch_pdl(attention_backward_ds<float>, grid, ATT_WARPS * 32, 0, s, ds, lse, (const float*)dout, (const float*)qkv, B, Tn, C, NH);
+        launch_pdl(attention_backward_dq<float>, grid, ATT_WARPS * 32, 0, s, (float*)dqkv, ds, (const float*)qkv, B, Tn, C, NH);
+        launch_pdl(attention_backward_dkv<float>, grid, ATT_WARPS * 32, 0, s, (float*)dqkv, ds, lse, (const float*)qkv,
                                                                    (const float*)dout, B, Tn, C, NH);
         CK(cudaGetLastError());
         return GPT2_OK;

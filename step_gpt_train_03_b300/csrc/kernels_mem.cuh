@@ -18,6 +18,7 @@ template <typename T>
 __global__ void encoder_forward_kernel(T* __restrict__ out, const int* __restrict__ tok,
                                        const T* __restrict__ wte, const T* __restrict__ wpe,
                                        int BT, int Tn, int C, int V, unsigned* err) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     const int vpr = C / EPV;
     size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -59,6 +60,7 @@ __device__ __forceinline__ unsigned radix_key(const unsigned* keys_in, const int
 __global__ void __launch_bounds__(RADIX_BLOCK)
 radix_hist_kernel(unsigned* __restrict__ hist, const unsigned* __restrict__ keys_in, const int* __restrict__ tok,
                   int BT, int V, int shift, int nblk) {
+    pdl_wait();
     __shared__ unsigned cnt[256];
     if (threadIdx.x < 256) cnt[threadIdx.x] = 0;
     __syncthreads();
@@ -69,6 +71,7 @@ radix_hist_kernel(unsigned* __restrict__ hist, const unsigned* __restrict__ keys
 }
 // exclusive scan of n counts, in place (one block, fixed order)
 __global__ void __launch_bounds__(RADIX_BLOCK) radix_scan_kernel(unsigned* __restrict__ hist, int n) {
+    pdl_wait();
     __shared__ unsigned wsum[32];
     const int per = (n + RADIX_BLOCK - 1) / RADIX_BLOCK;
     const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(RADIX_BLOCK) radix_scan_kernel(unsigned* __res
 __global__ void __launch_bounds__(RADIX_BLOCK)
 radix_scatter_kernel(unsigned* __restrict__ keys_out, const unsigned* __restrict__ keys_in, const int* __restrict__ tok,
                      const unsigned* __restrict__ hist, int BT, int V, int shift, int nblk) {
+    pdl_wait();
     __shared__ unsigned wcnt[RADIX_BLOCK / 32][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < (RADIX_BLOCK / 32) * 256; i += RADIX_BLOCK) (&wcnt[0][0])[i] = 0;
@@ -137,6 +141,7 @@ template <typename T>
 __global__ void encoder_backward_wte_partial(float* __restrict__ dwte, float* __restrict__ partial,
                                              const unsigned* __restrict__ sorted,
                                              const T* __restrict__ dout, int BT, int C, int V) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     constexpr int U = 8;
     __shared__ unsigned sk[ENC_CHUNK + 2];
@@ -197,6 +202,7 @@ __global__ void encoder_backward_wte_partial(float* __restrict__ dwte, float* __
 // start inside the run) in order.
 __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float* __restrict__ partial,
                                            const unsigned* __restrict__ sorted, int BT, int C, int V) {
+    pdl_wait();
     const int c0 = blockIdx.x * ENC_CHUNK;
     const int last = min(BT, c0 + ENC_CHUNK) - 1;
     if (last + 1 >= BT) return;                            // no later chunk
@@ -243,6 +249,7 @@ __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float
 template <typename T>
 __global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restrict__ dout,
                                      int B, int Tn, int C) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;     // packet index over (t, c)
     if (idx >= (size_t)Tn * C / EPV) return;
@@ -305,8 +312,9 @@ template <typename T, int NV, bool Q8 = false>
 __global__ void __launch_bounds__(LN_WARPS * 32)
 layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* __restrict__ rstd,
                          const T* __restrict__ inp, const T* __restrict__ w,
-                         const T* __restrict__ b, int N, int C, uint8_t* __restrict__ q = nullptr,
-                         float* __restrict__ qdeq = nullptr) {
+                         const T* __restrict__ b, int N, int C, uint8_t* __restrict__ q,
+                         float* __restrict__ qdeq) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
@@ -381,6 +389,7 @@ layernorm_forward_kernel(T* __restrict__ out, float* __restrict__ mean, float* _
 // maximum folded in with an integer atomicMax on the float's bits: order-free, so
 // deterministic; amax_bits zeroed beforehand), then codes of w * 2^k and deq[t] = 2^-k.
 __global__ void absmax_tensors_kernel(unsigned* __restrict__ amax_bits, const float* __restrict__ w, size_t len) {
+    pdl_wait();
     const float4* p = reinterpret_cast<const float4*>(w + (size_t)blockIdx.y * len);
     const size_t n4 = len / 4;
     float mx = 0.f;
@@ -401,6 +410,7 @@ __global__ void absmax_tensors_kernel(unsigned* __restrict__ amax_bits, const fl
 __global__ void quantize_tensors_kernel(uint8_t* __restrict__ q, float* __restrict__ deq,
                                         const unsigned* __restrict__ amax_bits, const float* __restrict__ w,
                                         size_t len) {
+    pdl_wait();
     const int k = e4m3_scale_exp(__uint_as_float(amax_bits[blockIdx.y]));
     const float sc = pow2f(k);
     const float4* p = reinterpret_cast<const float4*>(w + (size_t)blockIdx.y * len);
@@ -506,6 +516,7 @@ layernorm_backward_kernel(T* __restrict__ dinp, float* __restrict__ partial,
                           const T* __restrict__ dout, const T* __restrict__ inp,
                           const T* __restrict__ w, const float* __restrict__ mean,
                           const float* __restrict__ rstd, int N, int C) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     extern __shared__ float red[];   // 2C floats (SUM: 3C, then LN_WARPS rows of C)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -588,6 +599,7 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
                                const T* __restrict__ dout, const T* __restrict__ inp,
                                const T* __restrict__ w, const float* __restrict__ mean,
                                const float* __restrict__ rstd, int N, int C, unsigned* err) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     constexpr int W = SUM ? 3 : 2;
     extern __shared__ __align__(16) float red[];
@@ -716,6 +728,7 @@ layernorm_backward_pipe_kernel(T* __restrict__ dinp, float* __restrict__ partial
 __global__ void __launch_bounds__(CR_COLS * CR_GROUPS)
 column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
                      const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
+    pdl_wait();
     __shared__ float sm[CR_GROUPS][CR_COLS];
     const int c = threadIdx.x % CR_COLS, g = threadIdx.x / CR_COLS;
     const int w = blockIdx.x * CR_COLS + c;
@@ -780,6 +793,7 @@ __device__ __forceinline__ void column_reduce4_block(float* __restrict__ out0, f
 __global__ void __launch_bounds__(256)
 column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
                       const float* __restrict__ partial, int G, int W, float* __restrict__ out2 = nullptr) {
+    pdl_wait();
     column_reduce4_block(out0, out1, split, partial, G, W, out2, blockIdx.x);
 }
 
@@ -796,6 +810,7 @@ struct RedBatch {
     RedSeg seg[RED_MAX_SEGS];
 };
 __global__ void __launch_bounds__(256) column_reduce_batch_kernel(const __grid_constant__ RedBatch b) {
+    pdl_wait();
     const RedSeg& sg = b.seg[blockIdx.y];
     if ((int)blockIdx.x * 32 >= sg.W) return;
     column_reduce4_block(sg.out0, sg.out1, sg.split, sg.partial, sg.G, sg.W, sg.out2, blockIdx.x);
@@ -809,6 +824,7 @@ __global__ void __launch_bounds__(256) column_reduce_batch_kernel(const __grid_c
 template <typename T>
 __global__ void __launch_bounds__(CS_WARPS * 32)
 colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x, int M, int N, int rows_per_chunk) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     constexpr int U = 4;
     __shared__ float sm[CS_WARPS][EPV * 32];          // [warp][element][lane]: conflict-free
@@ -855,6 +871,7 @@ colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ x, int 
 template <typename T>
 __global__ void colsum_partial_scalar_kernel(float* __restrict__ partial, const T* __restrict__ x,
                                              int M, int N, int rows_per_chunk) {
+    pdl_wait();
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     const int r = blockIdx.y;
     if (n >= N) return;
@@ -892,6 +909,7 @@ template <typename T>
 __global__ void __launch_bounds__(XENT_THREADS)
 softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
                     const int* __restrict__ targets, int V, int Vp, float dloss, unsigned* err) {
+    pdl_wait();
     constexpr int EPV = Vec<T>::N;
     constexpr int NW = XENT_THREADS / 32;
     __shared__ float sm_m[NW], sm_s[NW];
@@ -1011,6 +1029,7 @@ softmax_xent_kernel(T* __restrict__ logits, float* __restrict__ losses,
 // Mean of n per-position losses, fixed order: thread i sums i, i+1024, ...; then a tree.
 __global__ void __launch_bounds__(1024)
 mean_loss_kernel(float* __restrict__ loss, const float* __restrict__ losses, int n, unsigned* err) {
+    pdl_wait();
     __shared__ float sm[32];
     float s = 0.f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) s += losses[i];
@@ -1050,6 +1069,7 @@ template <typename T>
 __global__ void __launch_bounds__(SAMPLE_THREADS)
 sample_kernel(int* __restrict__ out, const T* __restrict__ logits, int Tn, int pos, int V, int Vp,
               float inv_temp, unsigned long long seed) {
+    pdl_wait();
     __shared__ float s_red[32];
     __shared__ float s_pre[SAMPLE_THREADS];
     __shared__ int s_pick;
@@ -1112,6 +1132,7 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
                              float* __restrict__ m, float* __restrict__ v, bf16* __restrict__ shadow,
                              size_t n4, float lr, float b1, float b2, float eps, float wd,
                              float bc1, float bc2) {
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
         float4 pp = reinterpret_cast<float4*>(p)[i];
@@ -1143,12 +1164,14 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
 
 // ============================================================== small utilities
 __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, size_t n) {
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
         out[i] = __float2bfloat16_rn(in[i]);
@@ -1159,6 +1182,7 @@ __global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restri
 // orthogonalizes each block matrix's momentum with Newton-Schulz iterations.
 // mom = mu mom + g over the matrices' flat range (fp32)
 __global__ void muon_momentum_kernel(float4* __restrict__ mom, const float4* __restrict__ g, size_t n4, float mu) {
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         float4 a = mom[i];
         const float4 b = g[i];
@@ -1172,6 +1196,7 @@ __global__ void muon_momentum_kernel(float4* __restrict__ mom, const float4* __r
 // fixed order
 __global__ void __launch_bounds__(256) sumsq_partial_kernel(float* __restrict__ partial, const float* __restrict__ x,
                                                             size_t len) {
+    pdl_wait();
     const float4* p = reinterpret_cast<const float4*>(x + (size_t)blockIdx.y * len);
     float acc = 0.f;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < len / 4; i += (size_t)MUON_NB * blockDim.x) {
@@ -1192,6 +1217,7 @@ __global__ void __launch_bounds__(256) sumsq_partial_kernel(float* __restrict__ 
 // the matrix's MUON_NB partials in the same order, so all agree on the norm
 __global__ void __launch_bounds__(256) scale_frobenius_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ x,
                                                                    const float* __restrict__ partial, size_t len) {
+    pdl_wait();
     float ss = 0.f;
     for (int b = 0; b < MUON_NB; b++) ss += partial[(size_t)blockIdx.y * MUON_NB + b];
     const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
@@ -1205,6 +1231,7 @@ __global__ void __launch_bounds__(256) scale_frobenius_bf16_kernel(bf16* __restr
 }
 // T = 1.5 I - 0.5 S (n x n, bf16): the Newton-Schulz step X <- 1.5 X - 0.5 X S = X T
 __global__ void ns_affine_kernel(bf16* __restrict__ T, const bf16* __restrict__ S, int n) {
+    pdl_wait();
     const size_t nn = (size_t)n * n;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nn; i += (size_t)gridDim.x * blockDim.x) {
         const int r = (int)(i / n), c = (int)(i % n);
@@ -1214,6 +1241,7 @@ __global__ void ns_affine_kernel(bf16* __restrict__ T, const bf16* __restrict__ 
 // p -= lr (X + wd p); shadow (nullable) = bf16(p)
 __global__ void muon_apply_kernel(float4* __restrict__ p, const bf16* __restrict__ X, bf16* __restrict__ shadow,
                                   size_t n4, float lr, float wd) {
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         float4 a = p[i];
         const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(X) + 2 * i;
