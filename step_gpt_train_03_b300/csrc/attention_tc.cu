@@ -487,7 +487,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                              const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
                              const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
-                             const float* __restrict__ Dsum, int B, int Tn, int Tp, int C, int NH, unsigned* err) {
+                             const float* __restrict__ Dsum, float* __restrict__ bsum, int B, int Tn, int Tp, int C,
+                             int NH, unsigned* err) {
     using S = AbSmem<DKV>;
     constexpr int AB_RING = S::RING;
     extern __shared__ uint8_t smem_raw[];
@@ -846,6 +847,40 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 bulk_commit();
             }
             stg_pending = true;
+            if (bsum) {
+                // the qkv bias gradient: column sums of the staged (stored) tiles over 32
+                // rows, one partial row per (batch, row tile, row quarter).  Thread: a
+                // column pair of the dV or dK tile (dQ: warps 0-3 only) and a row quarter
+                const int ct = threadIdx.x - 64;                     // 0..255
+                const int tile = ct >> 7, quarter = (ct >> 5) & 3, cp = lane;
+                if (DKV || tile == 0) {
+                    const uint8_t* tb = stg + tile * AT_TILE_BYTES;
+                    // rows past T are left out (their staged values are not defined)
+                    const int nrow = Tn - t * AT_BM - quarter * 32;
+                    float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int hb = 0; hb < 2; hb++) {
+                        float2 p[16];
+#pragma unroll
+                        for (int k = 0; k < 16; k++) {
+                            const int i = hb * 16 + k, rr = quarter * 32 + i;
+                            const uint32_t u = *reinterpret_cast<const uint32_t*>(
+                                tb + rr * 128 + (((cp >> 2) ^ (rr & 7)) << 4) + (cp & 3) * 4);
+                            p[k] = i < nrow ? make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u))
+                                            : make_float2(0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                            for (int k = 0; k < w; k++) p[k] = __fadd2_rn(p[k], p[k + w]);
+                        acc2 = __fadd2_rn(acc2, p[0]);
+                    }
+                    // column offset within dqkv's row: dQ at 0, dK at C, dV at 2C
+                    const int part = DKV ? (tile == 0 ? 2 : 1) : 0;
+                    float* prow = bsum + ((size_t)(b * nt + t) * 4 + quarter) * 3 * C + part * C + h * AT_HS + 2 * cp;
+                    *reinterpret_cast<float2*>(prow) = acc2;
+                }
+            }
         }
         if (threadIdx.x == 64) bulk_wait<0>();
     }
@@ -956,8 +991,8 @@ __global__ void attention_rowdot_kernel(float* __restrict__ D, float* __restrict
 
 template <bool DKV>
 static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tl,
-                      const CUtensorMap& td, const CUtensorMap& tdq, const float* lse, const float* D, int B, int Tn,
-                      int Tp, int C, int NH, unsigned* err) {
+                      const CUtensorMap& td, const CUtensorMap& tdq, const float* lse, const float* D, float* bsum,
+                      int B, int Tn, int Tp, int C, int NH, unsigned* err) {
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(attention_tc_backward_kernel<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -967,8 +1002,8 @@ static int launch_bwd(cudaStream_t s, const CUtensorMap& tq, const CUtensorMap& 
     }
     const int items = ((Tn + AT_BM - 1) / AT_BM) * B * NH;
     const int grid = items < g_sms ? items : g_sms;
-    launch_pdl(attention_tc_backward_kernel<DKV>, grid, AT_THREADS, AbSmem<DKV>::TOTAL, s, tq, tdo, tl, td, tdq, lse, D, B,
-                                                                                    Tn, Tp, C, NH, err);
+    launch_pdl(attention_tc_backward_kernel<DKV>, grid, AT_THREADS, AbSmem<DKV>::TOTAL, s, tq, tdo, tl, td, tdq, lse, D, bsum,
+               B, Tn, Tp, C, NH, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
@@ -979,8 +1014,8 @@ size_t attention_tc_backward_scratch_floats(int B, int Tn, int NH) {
 }
 
 int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
-                          const __nv_bfloat16* out, const float* lse, float* scratch, int B, int Tn, int C, int NH,
-                          unsigned* err) {
+                          const __nv_bfloat16* out, const float* lse, float* scratch, float* bias_partial, int B,
+                          int Tn, int C, int NH, unsigned* err) {
     if (!attention_tc_available()) return GPT2_EUNSUPPORTED;
     if (C / NH != AT_HS || C % NH ||
         (((uintptr_t)qkv | (uintptr_t)dout | (uintptr_t)dqkv | (uintptr_t)out | (uintptr_t)scratch) & 15))
@@ -1001,7 +1036,7 @@ int attention_tc_backward(cudaStream_t s, __nv_bfloat16* dqkv, const __nv_bfloat
         !make_map_vec(&tl, lse_k, Tn, Tp, B * NH) || !make_map_vec(&td, D, Tn, Tp, B * NH) ||
         !make_map3(&tdq, dqkv, 3 * C, Tn, B, 3 * C))
         return GPT2_EUNSUPPORTED;
-    int rc = launch_bwd<true>(s, tq, tdo, tl, td, tdq, lse_k, D, B, Tn, Tp, C, NH, err);
+    int rc = launch_bwd<true>(s, tq, tdo, tl, td, tdq, lse_k, D, bias_partial, B, Tn, Tp, C, NH, err);
     if (rc != GPT2_OK) return rc;
-    return launch_bwd<false>(s, tq, tdo, tl, td, tdq, lse_k, D, B, Tn, Tp, C, NH, err);
+    return launch_bwd<false>(s, tq, tdo, tl, td, tdq, lse_k, D, bias_partial, B, Tn, Tp, C, NH, err);
 }

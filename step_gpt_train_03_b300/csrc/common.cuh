@@ -102,6 +102,25 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ size_t ceil_div_sz(size_t a, size_t b) { return (a + b - 1) / b; }
 
+// Column sums of a warp's 32 x 32 block, v[i] being column i of this lane's row: a
+// halving exchange (at width w, a lane keeps the half of its w pending columns that its
+// bit w selects and adds its partner's copy of that half), 31 shuffles per lane.  Returns
+// the sum over the 32 lanes of column `lane`; the order of the additions is fixed.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; i++) {
+            const float send = up ? v[i] : v[i + w];
+            const float keep = up ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
 // ------------------------------------------------------------------ dependent launches
 // Every kernel of the library starts with pdl_wait(): launched with programmatic stream
 // serialization, a kernel may begin before its predecessor in the stream has finished,

@@ -61,6 +61,8 @@ struct TcEpi {
     long ldo;           // row stride of out and aux (elements)
     const float* a_deq; // e4m3 products: per-row unscaling factor of A (M floats)
     const float* b_deq; // e4m3 products: unscaling factor of B (one float)
+    float* csum;        // GELU backward (nullable): column sums of the stored output over
+                        // each 32-row block, row r of a ceil(M/32) x N fp32 matrix
 };
 
 // Staging buffers per epilogue warp: four for the GELU epilogues of a CTA pair (two
@@ -460,6 +462,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         __syncwarp();
                         if (lane == 0 && col < N) { tma_store_2d(&tmOut, sb, col, yout); bulk_commit(); }
                         nbuf++;
+                        if (EPI == EPI_GELU_BWD && ep.csum) {
+                            // the bias gradient of the layer whose pre-activation this is:
+                            // this piece's 32 column sums over the warp's 32 rows, read
+                            // back from the staged (stored) values.  Lane: column pair
+                            // lane % 16 of the even (lane < 16) or odd rows
+                            const int cp = lane & 15, odd = lane >> 4;
+                            const int nrow = M - row0;
+                            float2 p[16];
+#pragma unroll
+                            for (int k = 0; k < 16; k++) {
+                                const int rr = 2 * k + odd;
+                                const uint32_t u = *reinterpret_cast<const uint32_t*>(sb + stg_off(rr, cp >> 2) + (cp & 3) * 4);
+                                p[k] = rr < nrow ? make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u))
+                                                 : make_float2(0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                                for (int k = 0; k < w; k++) p[k] = __fadd2_rn(p[k], p[k + w]);
+                            float2 acc2 = p[0];
+                            acc2.x += __shfl_xor_sync(0xffffffffu, acc2.x, 16);
+                            acc2.y += __shfl_xor_sync(0xffffffffu, acc2.y, 16);
+                            if (!odd && col + 2 * cp < N)
+                                *reinterpret_cast<float2*>(ep.csum + (size_t)(row0 >> 5) * N + col + 2 * cp) = acc2;
+                        }
                     } else {
                         if (col < N) {
                             add_bias(v, col);
@@ -760,7 +787,7 @@ int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16
 }
 
 int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16* W, int M, int N, int K, int epi,
-                        const bf16* aux, unsigned* err) {
+                        const bf16* aux, float* csum, unsigned* err) {
     // dinp (M x K) = dout (M x N) W (N x K): contraction over N; A = dout K-major,
     // B(k_out, n) = W[n][k_out] is MN-major (k_out contiguous)
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
@@ -775,7 +802,8 @@ int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16
     } else {
         tx = to;
     }
-    TcEpi ep{dinp, nullptr, (void*)aux, (long)K};
+    if (csum && epi != EPI_GELU_BWD) return GPT2_EINVAL;
+    TcEpi ep{dinp, nullptr, (void*)aux, (long)K, nullptr, nullptr, csum};
     const int cl = (N <= 768 && K <= 768) ? 1 : 2;      // as in the forward
     if (epi == EPI_GELU_BWD)
         return cl == 2 ? launch_tc<256, EPI_GELU_BWD, false, true, 2>(s, ta, tb, to, tx, M, K, N, 1, ep, err)

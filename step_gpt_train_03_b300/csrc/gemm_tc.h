@@ -36,9 +36,12 @@ int gemm_tc_bf16(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* A, boo
                  bool b_mn, int M, int N, int K, unsigned* err);
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation).
+// csum (nullable, EPI_GELU_BWD only): column sums of the stored dinp over each 32-row
+// block, row r of a ceil(M/32) x K fp32 matrix (whose column sums are the bias gradient
+// of the layer that produced the pre-activation).
 int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16* dout,
                         const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux,
-                        unsigned* err);
+                        float* csum, unsigned* err);
 
 // dW (N,K) fp32 += dout(M,N)^T inp (M,K).
 int gemm_tc_backward_dw(cudaStream_t s, float* dW, const __nv_bfloat16* dout, const __nv_bfloat16* inp,

@@ -169,10 +169,15 @@ static size_t plan(GPT2* m, char* base) {
     m->partials_floats = pf;
     m->partials = (float*)take(pf * 4);
     // deferred column sums: (2L+1) layernorm backwards of up to 3C-wide partials over at
-    // most 296 blocks, 2L bias gradients of up to 4C-wide partials over 128-row chunks
+    // most 296 blocks, L fc bias gradients of 4C-wide partials over 128-row chunks (or
+    // 32-row blocks from the bf16 GELU-backward output stage), and L qkv bias gradients of
+    // 3C-wide partials over 128-row chunks (or the 32-row blocks of the bf16 attention
+    // backward's output stage)
     {
         const size_t R = std::max<size_t>(1, std::min<size_t>(1024, (BT + 127) / 128));
-        m->red_arena_floats = (2 * L + 1) * 296 * 3 * C + 2 * L * R * 4 * C;
+        const size_t Ra = std::max<size_t>(R, (size_t)attention_tc_bias_partial_rows(m->maxB, m->maxT));
+        const size_t Rf = std::max<size_t>(R, (BT + 31) / 32);
+        m->red_arena_floats = (2 * L + 1) * 296 * 3 * C + L * Rf * 4 * C + L * Ra * 3 * C;
         m->red_arena = (float*)take(m->red_arena_floats * 4);
     }
     m->enc_partial = (float*)take(BT * C * 4);
@@ -715,15 +720,17 @@ static int mm_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const f
 }
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation of dinp's layer)
+// csum (bf16 only, nullable): see gemm_tc_backward_dx
 template <typename T>
 static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N, int K, int epi,
-                          const T* aux, unsigned* err) {
+                          const T* aux, unsigned* err, float* csum = nullptr) {
     ProfScope ps(s, PC_MATMUL_BWD_DX, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
-                                   (const bf16*)aux, err);
+                                   (const bf16*)aux, csum, err);
     } else {
         (void)err;
+        if (csum) return GPT2_EINVAL;
         EpiArgs ep{dinp, nullptr, (void*)aux, (long)K};
         cudaError_t e;
         rt_note_launches(1);
@@ -781,16 +788,17 @@ static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, in
 
 template <typename T>
 static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const T* qkv, const T* out,
-                         int l, int B, int Tn) {
+                         int l, int B, int Tn, float* bias_partial) {
     const int C = m->C, NH = m->NH;
     // dV, dP, dQ, dK: four causal-half products (the recomputed S is not counted)
     ProfScope ps(s, PC_ATTENTION_BWD, 2.0 * attn_fwd_flops(B, Tn, C), 0);
     if constexpr (sizeof(T) == 2) {
         const float* lse = m->lse + (size_t)l * m->maxB * NH * m->maxT;
         return attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
-                                     m->attn_scratch, B, Tn, C, NH, m->err);
+                                     m->attn_scratch, bias_partial, B, Tn, C, NH, m->err);
     } else {
         (void)out;
+        (void)bias_partial;
         const float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
         int rows = B * NH * Tn;
         int grid = ceil_div(rows, ATT_WARPS);
@@ -936,25 +944,34 @@ static int backward_impl(GPT2* m) {
         const T* fchg = (const T*)m->fchg + l * BTmax * 4 * C;
         const float* m1 = m->ln1_mean + l * BTmax; const float* r1 = m->ln1_rstd + l * BTmax;
         const float* m2 = m->ln2_mean + l * BTmax; const float* r2 = m->ln2_rstd + l * BTmax;
-        // MLP output projection (dresid = d res3)
-        RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err));
+        // MLP output projection (dresid = d res3); in bf16 its GELU-backward output stage
+        // also sums the columns of dfch for the fc bias gradient (a deferred sum)
+        const int frows = (int)ceil_div_sz(BT, 32);
+        float* fcb_part = sizeof(T) == 2 ? rq.take((size_t)frows * 4 * C) : nullptr;
+        RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err,
+                             fcb_part));
+        if (fcb_part) rq.push(fcb_part, G(P_FCB) + l * 4 * C, G(P_FCB) + l * 4 * C, nullptr, 4 * C, frows, 4 * C);
         RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err));
         // MLP input projection
         RC(mm_backward_dx<T>(s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr, m->err));
         RC(mm_backward_dw<T>(s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C, m->partials, m->partials_floats, m->err));
-        RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq));
+        if (!fcb_part) RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
                           G(P_ATTPROJB) + l * C, m->err, &rq));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
         RC(mm_backward_dx<T>(s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr, m->err));
         RC(mm_backward_dw<T>(s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C, m->partials, m->partials_floats, m->err));
-        // attention
-        RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn));
+        // attention; in bf16 its output stage also sums the columns of dqkv for the qkv
+        // bias gradient (reduced with the other deferred sums)
+        const int qrows = attention_tc_bias_partial_rows(B, Tn);
+        float* qkvb_part = sizeof(T) == 2 ? rq.take((size_t)qrows * 3 * C) : nullptr;
+        RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn, qkvb_part));
+        if (qkvb_part) rq.push(qkvb_part, G(P_QKVB) + l * 3 * C, G(P_QKVB) + l * 3 * C, nullptr, 3 * C, qrows, 3 * C);
         // qkv projection
         RC(mm_backward_dx<T>(s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
         RC(mm_backward_dw<T>(s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C, m->partials, m->partials_floats, m->err));
-        RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq));
+        if (!qkvb_part) RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq));
         // ln1 (dresid becomes d x_l)
         RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
                           l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err, &rq));   // d(res3) of layer l-1
@@ -1579,7 +1596,7 @@ extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void*
         unsigned* err = nullptr;
         RC(layer_err_word(&err));
         return attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
-                                     (float*)scratch, B, Tn, C, NH, err);
+                                     (float*)scratch, nullptr, B, Tn, C, NH, err);
     }
     if (precision == GPT2_FP32) {
         const int rows = B * NH * Tn;
