@@ -354,12 +354,15 @@ int gpt2_attention_forward(void* out, float* lse, const void* qkv, int B, int T,
                            int precision, void* stream);
 
 /* Backward: dqkv (B,T,3C) [overwritten] from dout (B,T,C) and the forward's qkv, out
- * and lse (fp32 path: probabilities).  scratch (device, 16-byte aligned): bf16 path the
+ * and lse (fp32 path: probabilities).  dbias (device fp32 (3C), nullable) += the column
+ * sums of dqkv over the B*T rows: the qkv bias gradient (bf16: summed from the stored
+ * bf16 dqkv in the kernels' output stage, 32 rows at a time, then in a fixed order).
+ * scratch (device, 16-byte aligned, gpt2_attention_backward_scratch_bytes): bf16 path the
  * fp32 row sums D = rowsum(dout * out) and, for T not a multiple of 4, a copy of the
- * LSE, each (B,NH,T rounded up to a multiple of 4); fp32 path (B,NH,T,T) fp32; size from
- * gpt2_attention_backward_scratch_bytes. */
-size_t gpt2_attention_backward_scratch_bytes(int B, int T, int NH, int precision);
-int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
+ * LSE, each (B,NH,T rounded up to a multiple of 4); fp32 path (B,NH,T,T) fp32; then the
+ * bias gradient's partial sums. */
+size_t gpt2_attention_backward_scratch_bytes(int B, int T, int C, int NH, int precision);
+int gpt2_attention_backward(void* dqkv, float* dbias, const void* dout, const void* qkv, const void* out,
                             const float* lse, int B, int T, int C, int NH, int precision,
                             void* scratch, size_t scratch_bytes, void* stream);
 
@@ -384,9 +387,16 @@ int gpt2_matmul_forward_fused(void* out, void* aux, const void* inp, const void*
 
 /* Input gradient of a matmul whose input was a GELU output, with the GELU backward fused:
  * dinp (M,K) = (dout (M,N) weight (N,K)) * gelu'(pre), pre (M,K) the GELU's stored input
- * (the model's MLP projection backward).  Types and limits as gpt2_matmul_forward. */
-int gpt2_matmul_backward_input_gelu(void* dinp, const void* dout, const void* weight, const void* pre,
-                                    int M, int N, int K, int precision, void* stream);
+ * (the model's MLP projection backward).  dbias (device fp32 (K), nullable) += the column
+ * sums of dinp: the bias gradient of the layer that produced `pre` (bf16: summed from the
+ * stored bf16 dinp in the product's output stage, 32 rows at a time, then in a fixed
+ * order); it needs `scratch` (device, 16-byte aligned,
+ * gpt2_matmul_backward_input_gelu_scratch_bytes), which is unused otherwise (nullable).
+ * Types and limits as gpt2_matmul_forward. */
+size_t gpt2_matmul_backward_input_gelu_scratch_bytes(int M, int K);
+int gpt2_matmul_backward_input_gelu(void* dinp, float* dbias, const void* dout, const void* weight,
+                                    const void* pre, int M, int N, int K, int precision, void* scratch,
+                                    size_t scratch_bytes, void* stream);
 
 /* Matmul backward: dinp (M,K) = dout (M,N) * weight (N,K)  [overwrites];
  * dweight (N,K, fp32) += dout^T * inp;  dbias (N, fp32, nullable) += column sums of

@@ -399,9 +399,9 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 if (lane == 0) mbar_arrive(&p_full[x]);
                 pn++;
             }
-            if (!alive) break;
             // the item's last P V, then normalise and write this row of O
-            if (!wait_pv(pn - 1)) break;
+            // (after an abort the reads below see whatever TMEM holds and nothing is stored)
+            const bool okw = alive && wait_pv(pn - 1);
             tc_fence_after();
             float o[64];
 #pragma unroll
@@ -414,11 +414,12 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[x]);
+            if (lane == 0 && okw) mbar_arrive(&o_free[x]);
             const float inv = 1.0f / l;
-            // the previous item's store must have finished reading the staging buffer
+            // the previous item's store must have finished reading the staging buffer; the
+            // warpgroup leaves together if any of its warps gave up waiting
             if (staged && threadIdx.x == leader) bulk_wait_read<0>();
-            named_bar(wg_bar, 128);
+            if (!named_bar_and(wg_bar, 128, okw)) break;
 #pragma unroll
             for (int ch = 0; ch < 8; ch++) {
                 Vec<bf16> ov;
@@ -788,9 +789,9 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pds_full[pb]);
             }
-            if (!alive) break;
             // accumulators of the item: wait for its last products, read, release, store
-            if (!wait_pds_free(gc - 1)) break;
+            // (after an abort the reads below see whatever TMEM holds and nothing is stored)
+            const bool okw = alive && wait_pds_free(gc - 1);
             tc_fence_after();
             float a1[32], a2[32];
             {
@@ -808,12 +809,11 @@ attention_tc_backward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_free);
-            // the previous item's store must have finished reading the staging buffers
-            if (stg_pending) {
-                if (threadIdx.x == 64) bulk_wait_read<0>();
-                named_bar(1, 256);
-            }
+            if (lane == 0 && okw) mbar_arrive(acc_free);
+            // the previous item's store must have finished reading the staging buffers; the
+            // compute warps leave together if any of them gave up waiting
+            if (stg_pending && threadIdx.x == 64) bulk_wait_read<0>();
+            if (!named_bar_and(1, 256, okw)) break;
             // stage 128B-swizzled rows, then TMA-store
 #pragma unroll
             for (int k = 0; k < 4; k++) {

@@ -1495,19 +1495,41 @@ extern "C" int gpt2_matmul_forward(void* out, const void* inp, const void* weigh
     return gpt2_matmul_forward_fused(out, nullptr, inp, weight, bias, M, N, K, GPT2_EPI_BIAS, precision, stream);
 }
 
-extern "C" int gpt2_matmul_backward_input_gelu(void* dinp, const void* dout, const void* weight, const void* pre,
-                                               int M, int N, int K, int precision, void* stream) {
+extern "C" size_t gpt2_matmul_backward_input_gelu_scratch_bytes(int M, int K) {
+    if (M <= 0 || K <= 0) return 0;
+    int R, rows;
+    colsum_shape(M, K, &R, &rows);
+    const size_t a = (size_t)R * K, b = (size_t)ceil_div(M, 32) * K;
+    return (a > b ? a : b) * sizeof(float);
+}
+
+extern "C" int gpt2_matmul_backward_input_gelu(void* dinp, float* dbias, const void* dout, const void* weight,
+                                               const void* pre, int M, int N, int K, int precision, void* scratch,
+                                               size_t scratch_bytes, void* stream) {
     if (!dinp || !dout || !weight || !pre || M < 0 || N <= 0 || K <= 0) return GPT2_EINVAL;
     if (M == 0) return GPT2_OK;
+    if (dbias && (!scratch || ((uintptr_t)scratch & 15) ||
+                  scratch_bytes < gpt2_matmul_backward_input_gelu_scratch_bytes(M, K)))
+        return GPT2_EINVAL;
     cudaStream_t s = (cudaStream_t)stream;
-    if (precision == GPT2_FP32)
-        return mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K,
-                                     EPI_GELU_BWD, (const float*)pre, nullptr);
+    float* part = dbias ? (float*)scratch : nullptr;
+    if (precision == GPT2_FP32) {
+        RC(mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_GELU_BWD,
+                                 (const float*)pre, nullptr));
+        if (dbias) RC(colsum<float>(s, dbias, (const float*)dinp, M, K, part, scratch_bytes / sizeof(float)));
+        return GPT2_OK;
+    }
     if (precision == GPT2_BF16) {
         unsigned* err = nullptr;
         RC(layer_err_word(&err));
-        return mm_backward_dx<bf16>(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_GELU_BWD,
-                                    (const bf16*)pre, err);
+        // the column sums come from the product's output stage, 32 rows at a time
+        RC(mm_backward_dx<bf16>(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)weight, M, N, K, EPI_GELU_BWD,
+                                (const bf16*)pre, err, part));
+        if (dbias) {
+            column_reduce_any(s, dbias, dbias, K, part, ceil_div(M, 32), K, nullptr);
+            CK(cudaGetLastError());
+        }
+        return GPT2_OK;
     }
     return GPT2_EINVAL;
 }
@@ -1577,26 +1599,46 @@ extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, in
     return GPT2_EINVAL;
 }
 
-extern "C" size_t gpt2_attention_backward_scratch_bytes(int B, int Tn, int NH, int precision) {
-    if (B < 1 || Tn < 1 || NH < 1) return 0;
-    const size_t rows = (size_t)B * NH * Tn;
-    return precision == GPT2_FP32 ? rows * Tn * sizeof(float)
-                                  : attention_tc_backward_scratch_floats(B, Tn, NH) * sizeof(float);
+// scratch of the attention backward: the kernels' own part (16-byte multiple), then the
+// partial column sums of dqkv for the bias gradient
+static size_t attn_bwd_own_floats(int B, int Tn, int NH, int precision) {
+    const size_t own = precision == GPT2_FP32 ? (size_t)B * NH * Tn * Tn : attention_tc_backward_scratch_floats(B, Tn, NH);
+    return (own + 3) / 4 * 4;
+}
+static size_t attn_bwd_bias_rows(int B, int Tn, int precision) {
+    if (precision == GPT2_FP32) {
+        int R, rows;
+        colsum_shape(B * Tn, 1, &R, &rows);
+        return (size_t)R;
+    }
+    return (size_t)attention_tc_bias_partial_rows(B, Tn);
 }
 
-extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void* qkv, const void* out,
+extern "C" size_t gpt2_attention_backward_scratch_bytes(int B, int Tn, int C, int NH, int precision) {
+    if (B < 1 || Tn < 1 || C < 1 || NH < 1) return 0;
+    return (attn_bwd_own_floats(B, Tn, NH, precision) + attn_bwd_bias_rows(B, Tn, precision) * 3 * C) * sizeof(float);
+}
+
+extern "C" int gpt2_attention_backward(void* dqkv, float* dbias, const void* dout, const void* qkv, const void* out,
                                        const float* lse, int B, int Tn, int C, int NH, int precision,
                                        void* scratch, size_t scratch_bytes, void* stream) {
     if (!dqkv || !dout || !qkv || !out || !lse || !scratch) return GPT2_EINVAL;
     if (!attn_args_ok(B, Tn, C, NH, GPT2_FP32)) return GPT2_EINVAL;
     if (!attn_args_ok(B, Tn, C, NH, precision)) return GPT2_EUNSUPPORTED;
-    if (scratch_bytes < gpt2_attention_backward_scratch_bytes(B, Tn, NH, precision)) return GPT2_EINVAL;
+    if (scratch_bytes < gpt2_attention_backward_scratch_bytes(B, Tn, C, NH, precision)) return GPT2_EINVAL;
     cudaStream_t s = (cudaStream_t)stream;
+    float* part = (float*)scratch + attn_bwd_own_floats(B, Tn, NH, precision);
+    const int prow = (int)attn_bwd_bias_rows(B, Tn, precision);
     if (precision == GPT2_BF16) {
         unsigned* err = nullptr;
         RC(layer_err_word(&err));
-        return attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
-                                     (float*)scratch, nullptr, B, Tn, C, NH, err);
+        RC(attention_tc_backward(s, (bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse,
+                                 (float*)scratch, dbias ? part : nullptr, B, Tn, C, NH, err));
+        if (dbias) {
+            column_reduce_any(s, dbias, dbias, 3 * C, part, prow, 3 * C, nullptr);
+            CK(cudaGetLastError());
+        }
+        return GPT2_OK;
     }
     if (precision == GPT2_FP32) {
         const int rows = B * NH * Tn;
@@ -1608,6 +1650,7 @@ extern "C" int gpt2_attention_backward(void* dqkv, const void* dout, const void*
         launch_pdl(attention_backward_dkv<float>, grid, ATT_WARPS * 32, 0, s, (float*)dqkv, ds, lse, (const float*)qkv,
                                                                    (const float*)dout, B, Tn, C, NH);
         CK(cudaGetLastError());
+        if (dbias) RC(colsum<float>(s, dbias, (const float*)dqkv, B * Tn, 3 * C, part, (size_t)prow * 3 * C));
         return GPT2_OK;
     }
     return GPT2_EINVAL;

@@ -287,6 +287,21 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// named barrier that also returns the AND of `v` over the `count` threads: warps that
+// share a barrier take an abort decision here together, so none is left waiting at a
+// later barrier for a warp that has left
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.and.pred p, %1, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(id), "r"((uint32_t)v), "r"(count)
+        : "memory");
+    return r != 0;
+}
 // 1-D bulk copy global -> shared (bytes a multiple of 16, both addresses 16-byte aligned)
 // completing on an mbarrier's transaction count
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -49,7 +49,8 @@ SIGNATURES = {
     "gpt2_matmul_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_fp8_weights": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp)]),
     "gpt2_matmul_forward_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
-    "gpt2_matmul_backward_input_gelu": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "gpt2_matmul_backward_input_gelu_scratch_bytes": (_sz, [_i, _i]),
+    "gpt2_matmul_backward_input_gelu": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_set_stream": (_i, [_vp, _vp]),
     "gpt2_num_parameters": (_i, [_vp, _psz, _psz]),
     "gpt2_param_tensor": (_i, [_vp, _i, _psz, _psz]),
@@ -88,8 +89,8 @@ SIGNATURES = {
     "gpt2_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
     "gpt2_layernorm_backward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_attention_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
-    "gpt2_attention_backward_scratch_bytes": (_sz, [_i, _i, _i, _i]),
-    "gpt2_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "gpt2_attention_backward_scratch_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "gpt2_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_matmul_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_matmul_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_matmul_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
@@ -423,15 +424,17 @@ def attention_forward(out, lse, qkv, NH, precision, stream=None):
                                      _stream_handle(stream)), "gpt2_attention_forward")
 
 
-def attention_backward_scratch_bytes(B, T, NH, precision) -> int:
-    return int(lib.gpt2_attention_backward_scratch_bytes(B, T, NH, PRECISIONS[precision]))
+def attention_backward_scratch_bytes(B, T, C, NH, precision) -> int:
+    return int(lib.gpt2_attention_backward_scratch_bytes(B, T, C, NH, PRECISIONS[precision]))
 
 
-def attention_backward(dqkv, dout, qkv, out, lse, NH, precision, scratch, stream=None):
+def attention_backward(dqkv, dout, qkv, out, lse, NH, precision, scratch, dbias=None, stream=None):
+    """gpt2_attention_backward: dqkv from dout; dbias (fp32 (3C), optional) += column sums of dqkv."""
     B, T, C3 = qkv.shape
-    check(lib.gpt2_attention_backward(_ptr(dqkv), _ptr(dout), _ptr(qkv), _ptr(out), _ptr(lse), B, T, C3 // 3, NH,
-                                      PRECISIONS[precision], _ptr(scratch), scratch.numel() * scratch.element_size(),
-                                      _stream_handle(stream)), "gpt2_attention_backward")
+    check(lib.gpt2_attention_backward(_ptr(dqkv), _ptr(dbias), _ptr(dout), _ptr(qkv), _ptr(out), _ptr(lse), B, T,
+                                      C3 // 3, NH, PRECISIONS[precision], _ptr(scratch),
+                                      scratch.numel() * scratch.element_size(), _stream_handle(stream)),
+          "gpt2_attention_backward")
 
 
 def matmul_forward(out, inp, weight, bias, precision, stream=None):
@@ -454,12 +457,18 @@ def matmul_forward_fused(out, aux, inp, weight, bias, epilogue, precision, strea
           "gpt2_matmul_forward_fused")
 
 
-def matmul_backward_input_gelu(dinp, dout, weight, pre, precision, stream=None):
-    """gpt2_matmul_backward_input_gelu: dinp = (dout weight) * gelu'(pre)."""
+def matmul_backward_input_gelu_scratch_bytes(M, K) -> int:
+    return int(lib.gpt2_matmul_backward_input_gelu_scratch_bytes(M, K))
+
+
+def matmul_backward_input_gelu(dinp, dout, weight, pre, precision, dbias=None, scratch=None, stream=None):
+    """gpt2_matmul_backward_input_gelu: dinp = (dout weight) * gelu'(pre); dbias (fp32 (K),
+    optional, with scratch) += column sums of dinp."""
     M, N = dout.shape
     K = weight.shape[1]
-    check(lib.gpt2_matmul_backward_input_gelu(_ptr(dinp), _ptr(dout), _ptr(weight), _ptr(pre), M, N, K,
-                                              PRECISIONS[precision], _stream_handle(stream)),
+    nbytes = scratch.numel() * scratch.element_size() if scratch is not None else 0
+    check(lib.gpt2_matmul_backward_input_gelu(_ptr(dinp), _ptr(dbias), _ptr(dout), _ptr(weight), _ptr(pre), M, N, K,
+                                              PRECISIONS[precision], _ptr(scratch), nbytes, _stream_handle(stream)),
           "gpt2_matmul_backward_input_gelu")
 
 

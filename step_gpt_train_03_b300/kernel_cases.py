@@ -68,7 +68,7 @@ def main(argv=None):
         else:
             dout = torch.randn(B, T, C, device=dev).to(bf)
             dqkv = torch.empty_like(qkv)
-            sc = torch.empty(G.attention_backward_scratch_bytes(B, T, NH, "bf16"), dtype=torch.uint8, device=dev)
+            sc = torch.empty(G.attention_backward_scratch_bytes(B, T, C, NH, "bf16"), dtype=torch.uint8, device=dev)
             run = lambda: G.attention_backward(dqkv, dout, qkv, out, lse, NH, "bf16", sc)
             work = 2 * work                                # dP, dV, dK, dQ (recomputed S not counted)
     elif case in ("layernorm_backward_fp32", "layernorm_forward_fp32"):

@@ -23,6 +23,10 @@ Tolerances (max |got - ref| / max |ref|), from the arithmetic:
   gelu' by up to ~5e-3; with the bf16 rounding of the result the bound is 1e-2.
 * fp32 weight gradients: fp32 accumulation over up to 16384 rows, split contractions
   added in a fixed order: 1e-4 (as the other fp32 gradient checks).
+* bias gradient summed in the GELU backward's output stage: against the exact (fp64)
+  column sums of the stored dinp it differs only by fp32 summation, relative ~1e-7:
+  bound 1e-5; against the oracle it carries dinp's errors, which average out over the
+  rows: bound GELU_BWD_TOL.
 """
 import numpy as np
 import pytest
@@ -120,11 +124,19 @@ def test_gelu_backward_input_gradient_full_size(G):
     w = (torch.randn(N, K, device="cuda", generator=g) / np.sqrt(N)).to(torch.bfloat16)
     pre = (1.5 * torch.randn(M, K, device="cuda", generator=g)).to(torch.bfloat16)
     dinp = torch.empty(M, K, device="cuda", dtype=torch.bfloat16)
-    G.matmul_backward_input_gelu(dinp, dout, w, pre, "bf16")
+    db0 = torch.randn(K, device="cuda", generator=g)
+    dbias = db0.clone()
+    sc = torch.empty(G.matmul_backward_input_gelu_scratch_bytes(M, K), dtype=torch.uint8, device="cuda")
+    G.matmul_backward_input_gelu(dinp, dout, w, pre, "bf16", dbias, sc)
     G.layer_check()
     ref = O.gelu_backward(_f64(dout) @ _f64(w), _f64(pre))
-    e = norm_err(_f64(dinp), ref)
+    got = _f64(dinp)
+    e = norm_err(got, ref)
     assert e <= GELU_BWD_TOL, e
+    # the fused bias gradient (added into dbias): the stored rows' column sums
+    db = (dbias - db0).double().cpu().numpy()
+    assert norm_err(db, got.sum(axis=0)) <= FP32_OUT_TOL
+    assert norm_err(db, ref.sum(axis=0)) <= GELU_BWD_TOL
 
 
 # ------------------------------------------------------------------ full-size weight gradients
@@ -200,10 +212,14 @@ def test_fused_epilogues_ragged_every_element(G, prec, M, N, K):
     w2 = (torch.randn(K, N, device="cuda", generator=g) / np.sqrt(K)).to(dt)
     p = (1.5 * torch.randn(M, N, device="cuda", generator=g)).to(dt)
     dinp = torch.empty(M, N, device="cuda", dtype=dt)
-    G.matmul_backward_input_gelu(dinp, dy, w2, p, prec)
+    dbias = torch.zeros(N, device="cuda")
+    sc = torch.empty(G.matmul_backward_input_gelu_scratch_bytes(M, N), dtype=torch.uint8, device="cuda")
+    G.matmul_backward_input_gelu(dinp, dy, w2, p, prec, dbias, sc)
     G.layer_check()
     ref = O.gelu_backward(_f64(dy) @ _f64(w2), _f64(p))
     assert norm_err(_f64(dinp), ref) <= (GELU_BWD_TOL if prec == "bf16" else FP32_OUT_TOL)
+    # bias gradient: the stored dinp's column sums (ragged row blocks and columns)
+    assert norm_err(dbias.double().cpu().numpy(), _f64(dinp).sum(axis=0)) <= FP32_OUT_TOL
 
 
 def test_bf16_shapes_off_the_tensor_core_path_are_refused(G):

@@ -156,14 +156,23 @@ def test_attention_forward_backward(L, B, T, NH, C, precision):
     lse = torch.empty((B, NH, T) if precision == "bf16" else (B, NH, T, T), device="cuda")
     L.attention_forward(out, lse, qkv_d, NH, precision)
     dqkv = torch.empty_like(qkv_d)
-    scratch = torch.empty(L.attention_backward_scratch_bytes(B, T, NH, precision), dtype=torch.uint8, device="cuda")
-    L.attention_backward(dqkv, dout_d, qkv_d, out, lse, NH, precision, scratch)
+    scratch = torch.empty(L.attention_backward_scratch_bytes(B, T, C, NH, precision), dtype=torch.uint8,
+                          device="cuda")
+    db0 = torch.as_tensor(rng.standard_normal(3 * C).astype(np.float32)).cuda()
+    dbias = db0.clone()
+    L.attention_backward(dqkv, dout_d, qkv_d, out, lse, NH, precision, scratch, dbias)
     torch.cuda.synchronize()
     ref_out, pre, att = O.attention_forward(q64, NH)
     ref_dqkv = O.attention_backward(d64, q64, att, NH)
     tol = ATT_TOL if precision == "bf16" else OUT_TOL
     assert norm_err(out.float().cpu().numpy(), ref_out) < tol
-    assert norm_err(dqkv.float().cpu().numpy(), ref_dqkv) < (tol if precision == "bf16" else GRAD_TOL)
+    got_dqkv = dqkv.float().cpu().numpy().astype(np.float64)
+    assert norm_err(got_dqkv, ref_dqkv) < (tol if precision == "bf16" else GRAD_TOL)
+    # the qkv bias gradient added into dbias: the stored dqkv's column sums (exact up to
+    # fp32 summation), and the oracle's within the dqkv tolerance
+    db = (dbias - db0).double().cpu().numpy()
+    assert norm_err(db, got_dqkv.reshape(-1, 3 * C).sum(axis=0)) < 1e-5
+    assert norm_err(db, ref_dqkv.reshape(-1, 3 * C).sum(axis=0)) < (tol if precision == "bf16" else GRAD_TOL)
     if precision == "bf16":
         m = pre.max(-1, keepdims=True)
         ref_lse = (m + np.log(np.exp(pre - m).sum(-1, keepdims=True)))[..., 0]
