@@ -62,7 +62,10 @@ def test_layernorm_standalone_workload(L):
     assert max(e["dx"], e["dw"], e["db"]) < 1e-5, e     # well inside the bar
 
 
-@pytest.mark.parametrize("N,C", [(1, 768), (13, 768), (8191, 768), (5, 8), (33, 64), (100, 2048), (7, 1000)])
+# (8000, 256) and (20000, 128): several rows per warp through the backward's pipelined
+# (shared-memory staged) form, so every stage is reused and every barrier phase flips
+@pytest.mark.parametrize("N,C", [(1, 768), (13, 768), (8191, 768), (5, 8), (33, 64), (100, 2048), (7, 1000),
+                                 (8000, 256), (20000, 128)])
 def test_layernorm_edge_shapes(L, N, C):
     e = _ln_case(L, N, C)
     for k in ("y", "mean", "rstd"):
