@@ -568,11 +568,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 }
 
-// out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic).  All
+// out[n][k] += sum_s part[s][n][k], s in order (split-K reduction, deterministic; with
+// `assign`, out = 0 + the same sum).  All
 // of a packet's partial loads (splits <= TC_MAX_SPLITS) are issued before the first add.
 #define TC_MAX_SPLITS 8
 __global__ void splitk_reduce_kernel(float* __restrict__ out, const float* __restrict__ part, size_t n4,
-                                     int splits) {
+                                     int splits, int assign) {
     pdl_wait();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
@@ -580,7 +581,8 @@ __global__ void splitk_reduce_kernel(float* __restrict__ out, const float* __res
 #pragma unroll
     for (int s = 0; s < TC_MAX_SPLITS; s++)
         if (s < splits) p[s] = __ldcs(reinterpret_cast<const float4*>(part) + (size_t)s * n4 + i);
-    float4 acc = reinterpret_cast<float4*>(out)[i];
+    // assign: the output's first write of the step (0 + the partials, in the same order)
+    float4 acc = assign ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<float4*>(out)[i];
 #pragma unroll
     for (int s = 0; s < TC_MAX_SPLITS; s++) {
         if (s < splits) { acc.x += p[s].x; acc.y += p[s].y; acc.z += p[s].z; acc.w += p[s].w; }
@@ -831,7 +833,7 @@ static int choose_splits(int tiles, int nkb, int slots) {
 }
 
 int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16* inp, int M, int N, int K,
-                        float* scratch, size_t scratch_floats, unsigned* err) {
+                        float* scratch, size_t scratch_floats, unsigned* err, bool assign) {
     // dW (N x K) += dout^T (N x M) inp (M x K): contraction over M; A(n, m) = dout[m][n]
     // and B(k, m) = inp[m][k] are both MN-major
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
@@ -854,6 +856,11 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
     if (splits == 1) {
         if (!make_epi_map(&to, dW, K, N, K, 4)) return GPT2_EUNSUPPORTED;
         TcEpi ep{dW, nullptr, nullptr, (long)K};
+        // assign: the tile is stored (the partial-tile epilogue with one split) instead of
+        // added by a TMA reduction -- the same values as adding into zeros
+        if (assign)
+            return cl == 2 ? launch_tc<256, TC_EPI_PARTIAL, true, true, 2>(s, ta, tb, to, to, N, K, M, 1, ep, err)
+                           : launch_tc<256, TC_EPI_PARTIAL, true, true, 1>(s, ta, tb, to, to, N, K, M, 1, ep, err);
         return cl == 2 ? launch_tc<256, EPI_ACC_F32, true, true, 2>(s, ta, tb, to, to, N, K, M, 1, ep, err)
                        : launch_tc<256, EPI_ACC_F32, true, true, 1>(s, ta, tb, to, to, N, K, M, 1, ep, err);
     }
@@ -863,7 +870,7 @@ int gemm_tc_backward_dw(cudaStream_t s, float* dW, const bf16* dout, const bf16*
                      : launch_tc<256, TC_EPI_PARTIAL, true, true, 1>(s, ta, tb, to, to, N, K, M, splits, ep, err);
     if (rc != GPT2_OK) return rc;
     const size_t n4 = (size_t)N * K / 4;
-    launch_pdl(splitk_reduce_kernel, (unsigned)((n4 + 255) / 256), 256, 0, s, dW, scratch, n4, splits);
+    launch_pdl(splitk_reduce_kernel, (unsigned)((n4 + 255) / 256), 256, 0, s, dW, scratch, n4, splits, assign ? 1 : 0);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }

@@ -43,6 +43,8 @@ int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16
                         const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux,
                         float* csum, unsigned* err);
 
-// dW (N,K) fp32 += dout(M,N)^T inp (M,K).
+// dW (N,K) fp32 += dout(M,N)^T inp (M,K); with `assign`, dW = the product (the same
+// values as adding into zeros).
 int gemm_tc_backward_dw(cudaStream_t s, float* dW, const __nv_bfloat16* dout, const __nv_bfloat16* inp,
-                        int M, int N, int K, float* scratch, size_t scratch_floats, unsigned* err);
+                        int M, int N, int K, float* scratch, size_t scratch_floats, unsigned* err,
+                        bool assign = false);

@@ -45,6 +45,7 @@ enum { P_WTE = 0, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
 struct GPT2 {
     GPT2Config cfg;
     int maxB, maxT, prec;
+    int overwrite;                     // the next backward's first write to each gradient stores (no clear before)
     int L, C, NH, V, Vp;
     size_t poff[GPT2_NUM_PARAM_TENSORS], pnum[GPT2_NUM_PARAM_TENSORS];
     size_t n_flat, n_real;
@@ -276,6 +277,7 @@ extern "C" int gpt2_workspace_bytes(const GPT2Config* cfg, int max_B, int max_T,
     return GPT2_OK;
 }
 
+static int launch_zero_floats(cudaStream_t s, float* p, size_t n);
 static int launch_zero(cudaStream_t s, void* p, size_t bytes) {
     // bytes is a multiple of 16 for every region this is used on
     size_t n4 = bytes / 16;
@@ -285,6 +287,11 @@ static int launch_zero(cudaStream_t s, void* p, size_t bytes) {
     launch_pdl(zero_kernel, grid, 256, 0, s, (float4*)p, n4);
     rt_note_launches(1);
     CK(cudaGetLastError());
+    return GPT2_OK;
+}
+// any float count and alignment (the short alignment gaps of the flat buffer)
+static int launch_zero_floats(cudaStream_t s, float* p, size_t n) {
+    CK(cudaMemsetAsync(p, 0, n * sizeof(float), s));
     return GPT2_OK;
 }
 
@@ -559,8 +566,8 @@ struct RedQueue {
         used += need;
         return p;
     }
-    void push(const float* partial, float* out0, float* out1, float* out2, int split, int G, int W) {
-        batch.seg[n++] = RedSeg{partial, out0, out1, out2, split, G, W, 0};
+    void push(const float* partial, float* out0, float* out1, float* out2, int split, int G, int W, bool assign = false) {
+        batch.seg[n++] = RedSeg{partial, out0, out1, out2, split, G, W, assign ? 1 : 0};
         max_w = std::max(max_w, W);
     }
 };
@@ -622,7 +629,7 @@ template <typename T>
 static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* dout, const T* inp,
                        const T* w, const float* mean, const float* rstd, int N, int C,
                        float* partial, size_t partial_floats, float* dsum = nullptr, unsigned* err = nullptr,
-                       RedQueue* q = nullptr) {
+                       RedQueue* q = nullptr, bool assign = false) {
     constexpr int EPV = Vec<T>::N;
     const int nv = ceil_div(C / EPV, 32);
     int G = ln_backward_grid(N);
@@ -647,8 +654,14 @@ static int ln_backward(cudaStream_t s, T* dinp, float* dw, float* db, const T* d
     }
     if (rc != GPT2_OK) return rc;
     if (qpart) {
-        q->push(partial, dw, db, dsum, C, G, W * C);         // G may have shrunk in the launcher
+        q->push(partial, dw, db, dsum, C, G, W * C, assign);         // G may have shrunk in the launcher
         return GPT2_OK;
+    }
+    // assign without a queue: the outputs are cleared, then the sums added
+    if (assign) {
+        RC(launch_zero(s, dw, (size_t)C * sizeof(float)));
+        RC(launch_zero(s, db, (size_t)C * sizeof(float)));
+        if (dsum) RC(launch_zero(s, dsum, (size_t)C * sizeof(float)));
     }
     column_reduce_any(s, dw, db, C, partial, G, W * C, dsum);
     CK(cudaGetLastError());
@@ -664,7 +677,7 @@ static void colsum_shape(int M, int N, int* R, int* rows) {
 
 template <typename T>
 static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* partial,
-                  size_t partial_floats, RedQueue* q = nullptr) {
+                  size_t partial_floats, RedQueue* q = nullptr, bool assign = false) {
     int R, rows;
     colsum_shape(M, N, &R, &rows);
     float* qpart = (q && N % 4 == 0) ? q->take((size_t)R * N) : nullptr;
@@ -677,9 +690,10 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
     else launch_pdl(colsum_partial_kernel<T>, dim3(ceil_div(N / EPV, 32), R), CS_WARPS * 32, 0, s, partial, x, M, N, rows);
     CK(cudaGetLastError());
     if (qpart) {
-        q->push(partial, out, out, nullptr, N, R, N);
+        q->push(partial, out, out, nullptr, N, R, N, assign);
         return GPT2_OK;
     }
+    if (assign) RC(launch_zero(s, out, (size_t)N * sizeof(float)));   // cleared, then added
     column_reduce_any(s, out, out, N, partial, R, N, nullptr);
     CK(cudaGetLastError());
     return GPT2_OK;
@@ -747,15 +761,16 @@ static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, in
 // tensor-core product split its contraction when the weight has few tiles
 template <typename T>
 static int mm_backward_dw(cudaStream_t s, float* dW, const T* dout, const T* inp, int M, int N, int K,
-                          float* partials, size_t partials_floats, unsigned* err) {
+                          float* partials, size_t partials_floats, unsigned* err, bool assign = false) {
     ProfScope ps(s, PC_MATMUL_BWD_DW, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, partials, partials_floats,
-                                   err);
+                                   err, assign);
     } else {
         (void)partials;
         (void)partials_floats;
         (void)err;
+        if (assign) RC(launch_zero(s, dW, (size_t)N * K * sizeof(float)));
         EpiArgs ep{dW, nullptr, nullptr, (long)K};
         // C(n, k) = sum_m dout[m][n] inp[m][k]: A(n, m) = dout[m*N + n], B(k, m) = inp[m*K + k]
         rt_note_launches(1);
@@ -916,6 +931,9 @@ static int backward_impl(GPT2* m) {
     T* dqkv = (T*)m->dqkv;
     T* dfch = (T*)m->dfch;
     const T* dlogits = (const T*)m->logits;
+    // overwrite: the gradients were not cleared for this backward; each one's first writer
+    // stores (the same values as adding into zeros) and what no writer covers is cleared
+    const bool ow = m->overwrite != 0;
     float* part = m->partials;
     const size_t pf = m->partials_floats;
     RedQueue rq;
@@ -926,13 +944,14 @@ static int backward_impl(GPT2* m) {
     rq.max_w = 0;
     // LM head (tied): dlnf = dlogits wte; dwte += dlogits^T lnf
     RC(mm_backward_dx<T>(s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr, m->err));
-    RC(mm_backward_dw<T>(s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C, m->partials, m->partials_floats, m->err));
+    RC(mm_backward_dw<T>(s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C, m->partials, m->partials_floats, m->err,
+                         ow));
     RC(launch_zero(s, dresid, (size_t)BT * C * sizeof(T)));
     const T* xlast = (const T*)m->res3 + (L - 1) * BTmax * C;
     // the updated residual gradient is d(res3) of the last layer: its column sums are
     // that layer's MLP-projection bias gradient
     RC(ln_backward<T>(s, dresid, G(P_LNFW), G(P_LNFB), dbufC, xlast, P(P_LNFW), m->lnf_mean, m->lnf_rstd, BT, C, part, pf,
-                      G(P_FCPROJB) + (L - 1) * C, m->err, &rq));
+                      G(P_FCPROJB) + (L - 1) * C, m->err, &rq, ow));
     for (int l = L - 1; l >= 0; l--) {
         const T* x_in = (l == 0) ? (const T*)m->encoded : (const T*)m->res3 + (l - 1) * BTmax * C;
         const T* ln1 = (const T*)m->ln1 + l * BTmax * C;
@@ -950,31 +969,31 @@ static int backward_impl(GPT2* m) {
         float* fcb_part = sizeof(T) == 2 ? rq.take((size_t)frows * 4 * C) : nullptr;
         RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err,
                              fcb_part));
-        if (fcb_part) rq.push(fcb_part, G(P_FCB) + l * 4 * C, G(P_FCB) + l * 4 * C, nullptr, 4 * C, frows, 4 * C);
-        RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err));
+        if (fcb_part) rq.push(fcb_part, G(P_FCB) + l * 4 * C, G(P_FCB) + l * 4 * C, nullptr, 4 * C, frows, 4 * C, ow);
+        RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err, ow));
         // MLP input projection
         RC(mm_backward_dx<T>(s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr, m->err));
-        RC(mm_backward_dw<T>(s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C, m->partials, m->partials_floats, m->err));
-        if (!fcb_part) RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq));
+        RC(mm_backward_dw<T>(s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C, m->partials, m->partials_floats, m->err, ow));
+        if (!fcb_part) RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq, ow));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
-                          G(P_ATTPROJB) + l * C, m->err, &rq));      // d(res2) column sums: attention-projection bias
+                          G(P_ATTPROJB) + l * C, m->err, &rq, ow));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
         RC(mm_backward_dx<T>(s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr, m->err));
-        RC(mm_backward_dw<T>(s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C, m->partials, m->partials_floats, m->err));
+        RC(mm_backward_dw<T>(s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C, m->partials, m->partials_floats, m->err, ow));
         // attention; in bf16 its output stage also sums the columns of dqkv for the qkv
         // bias gradient (reduced with the other deferred sums)
         const int qrows = attention_tc_bias_partial_rows(B, Tn);
         float* qkvb_part = sizeof(T) == 2 ? rq.take((size_t)qrows * 3 * C) : nullptr;
         RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn, qkvb_part));
-        if (qkvb_part) rq.push(qkvb_part, G(P_QKVB) + l * 3 * C, G(P_QKVB) + l * 3 * C, nullptr, 3 * C, qrows, 3 * C);
+        if (qkvb_part) rq.push(qkvb_part, G(P_QKVB) + l * 3 * C, G(P_QKVB) + l * 3 * C, nullptr, 3 * C, qrows, 3 * C, ow);
         // qkv projection
         RC(mm_backward_dx<T>(s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
-        RC(mm_backward_dw<T>(s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C, m->partials, m->partials_floats, m->err));
-        if (!qkvb_part) RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq));
+        RC(mm_backward_dw<T>(s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C, m->partials, m->partials_floats, m->err, ow));
+        if (!qkvb_part) RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq, ow));
         // ln1 (dresid becomes d x_l)
         RC(ln_backward<T>(s, dresid, G(P_LN1W) + l * C, G(P_LN1B) + l * C, dbufC, x_in, P(P_LN1W) + l * C, m1, r1, BT, C, part, pf,
-                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err, &rq));   // d(res3) of layer l-1
+                          l > 0 ? G(P_FCPROJB) + (l - 1) * C : nullptr, m->err, &rq, ow));   // d(res3) of layer l-1
         if (rq.n + 4 > RED_MAX_SEGS) RC(red_flush(s, rq));
     }
     // the deferred column sums (layernorm weight and bias gradients, linear biases)
@@ -987,8 +1006,20 @@ static int backward_impl(GPT2* m) {
     CK(cudaGetLastError());
     launch_pdl(encoder_backward_wte_final, ceil_div(BT, ENC_CHUNK), 256, 0, s, G(P_WTE), m->enc_partial, m->sorted_keys, BT, C, m->V);
     CK(cudaGetLastError());
-    launch_pdl(encoder_backward_wpe<T>, ceil_div(Tn * C / Vec<T>::N, 256), 256, 0, s, G(P_WPE), dresid, B, Tn, C);
+    launch_pdl(encoder_backward_wpe<T>, ceil_div(Tn * C / Vec<T>::N, 256), 256, 0, s, G(P_WPE), dresid, B, Tn, C,
+               ow ? 1 : 0);
     CK(cudaGetLastError());
+    if (ow) {
+        // what no writer covers: position rows past this T, and the alignment gaps of the
+        // flat buffer
+        const int Tw = m->cfg.max_seq_len;                 // rows of the position table
+        if (Tn < Tw) RC(launch_zero(s, G(P_WPE) + (size_t)Tn * C, (size_t)(Tw - Tn) * C * sizeof(float)));
+        for (int i = 0; i < GPT2_NUM_PARAM_TENSORS; i++) {
+            const size_t end = m->poff[i] + m->pnum[i];
+            const size_t next = i + 1 < GPT2_NUM_PARAM_TENSORS ? m->poff[i + 1] : m->n_flat;
+            if (next > end) RC(launch_zero_floats(s, m->grads + end, next - end));
+        }
+    }
     return GPT2_OK;
 }
 
@@ -1209,8 +1240,13 @@ extern "C" int gpt2_newton_schulz(void* out, const float* G, int r, int c, int i
 // launched one by one
 static int step_eager(GPT2* m, int B, int Tn, float lr, float b1, float b2, float eps, float wd, int t) {
     RC(forward_dispatch(m, B, Tn, true));
-    RC(gpt2_zero_grad(m));
-    RC(gpt2_backward(m));
+    // bf16 / fp8: no clear of the gradients; the backward's first write to each stores
+    // instead of adding (the same values), and it clears what no writer covers
+    if (m->prec == GPT2_FP32) RC(gpt2_zero_grad(m));
+    else m->overwrite = 1;
+    const int rc = gpt2_backward(m);
+    m->overwrite = 0;
+    RC(rc);
     return gpt2_update(m, lr, b1, b2, eps, wd, t);
 }
 

@@ -248,7 +248,7 @@ __global__ void encoder_backward_wte_final(float* __restrict__ dwte, const float
 // packet are issued four at a time, then added in b order.
 template <typename T>
 __global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restrict__ dout,
-                                     int B, int Tn, int C) {
+                                     int B, int Tn, int C, int assign) {
     pdl_wait();
     constexpr int EPV = Vec<T>::N;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;     // packet index over (t, c)
@@ -276,7 +276,7 @@ __global__ void encoder_backward_wpe(float* __restrict__ dwpe, const T* __restri
 #pragma unroll
     for (int q = 0; q < EPV / 4; q++) {
         float4* d = reinterpret_cast<float4*>(dwpe + off) + q;
-        float4 v = *d;
+        float4 v = assign ? make_float4(0.f, 0.f, 0.f, 0.f) : *d;
         v.x += s[4 * q]; v.y += s[4 * q + 1]; v.z += s[4 * q + 2]; v.w += s[4 * q + 3];
         *d = v;
     }
@@ -758,7 +758,7 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, int spl
 // (four loads in flight), then the 32 group sums of each column are added in group order.
 __device__ __forceinline__ void column_reduce4_block(float* __restrict__ out0, float* __restrict__ out1, int split,
                                                      const float* __restrict__ partial, int G, int W,
-                                                     float* __restrict__ out2, int bx) {
+                                                     float* __restrict__ out2, int bx, bool assign = false) {
     __shared__ float sm[32][33];
     const int p = threadIdx.x & 7, g = threadIdx.x >> 3;
     const int w = bx * 32 + p * 4;
@@ -785,9 +785,9 @@ __device__ __forceinline__ void column_reduce4_block(float* __restrict__ out0, f
         float acc = 0.f;
 #pragma unroll 8
         for (int k = 0; k < 32; k++) acc += sm[k][t];
-        if (wc < split) out0[wc] += acc;
-        else if (!out2 || wc < 2 * split) out1[wc - split] += acc;
-        else out2[wc - 2 * split] += acc;
+        // assign: the output's first write of the step (the same value as 0 + acc)
+        float* o = wc < split ? out0 + wc : (!out2 || wc < 2 * split) ? out1 + (wc - split) : out2 + (wc - 2 * split);
+        *o = assign ? acc : *o + acc;
     }
 }
 __global__ void __launch_bounds__(256)
@@ -803,7 +803,7 @@ column_reduce4_kernel(float* __restrict__ out0, float* __restrict__ out1, int sp
 struct RedSeg {
     const float* partial;
     float *out0, *out1, *out2;
-    int split, G, W, pad;
+    int split, G, W, assign;   // assign: store the sums instead of adding them
 };
 #define RED_MAX_SEGS 128
 struct RedBatch {
@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(256) column_reduce_batch_kernel(const __grid_c
     pdl_wait();
     const RedSeg& sg = b.seg[blockIdx.y];
     if ((int)blockIdx.x * 32 >= sg.W) return;
-    column_reduce4_block(sg.out0, sg.out1, sg.split, sg.partial, sg.G, sg.W, sg.out2, blockIdx.x);
+    column_reduce4_block(sg.out0, sg.out1, sg.split, sg.partial, sg.G, sg.W, sg.out2, blockIdx.x, sg.assign != 0);
 }
 
 // ============================================================== column sums (bias grads)

@@ -229,6 +229,30 @@ def test_steps_are_bitwise_deterministic():
         assert torch.equal(out[0], out[1]), precision
 
 
+@pytest.mark.parametrize("precision", ["bf16", "fp8"])
+def test_fused_step_stores_every_gradient(precision):
+    """gpt2_step does not clear the gradients: in its backward each gradient's first
+    writer stores instead of adding, and what no writer covers (the position rows past
+    T, alignment gaps) is cleared.  From a gradient buffer full of NaN, the fused step's
+    gradients -- eager, graph-capturing and graph-replayed calls -- equal those of
+    zero_grad + backward element for element, at a T shorter than the model's."""
+    import torch
+    shape = synth.TINY_HS64
+    tok, tgt = synth.uniform_tokens(shape.vocab_size, 2, 24, 5)
+    ref = gpu_model(shape, 2, 32, precision, 3)
+    ref.forward(dev_tokens(tok), dev_tokens(tgt))
+    ref.zero_grad()
+    ref.backward()
+    g_ref = ref.flat_grads().clone()
+    m = gpu_model(shape, 2, 32, precision, 3)
+    for call in range(3):
+        m.flat_grads().fill_(float("nan"))
+        m.step_device(dev_tokens(tok), dev_tokens(tgt), 0.0, 0.9, 0.999, 1e-8, 0.0, call + 1)
+        torch.cuda.synchronize()
+        g = m.flat_grads()
+        assert torch.equal(g, g_ref), (call, int(torch.isnan(g).sum()), float((g - g_ref).abs().nan_to_num(1e9).max()))
+
+
 def test_errors_are_reported_not_faulted():
     from step_gpt_train_03_b300.gpt2lib import GPT2Error
     shape = synth.TINY
