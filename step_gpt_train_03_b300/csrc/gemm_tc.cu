@@ -63,6 +63,10 @@ struct TcEpi {
     const float* b_deq; // e4m3 products: unscaling factor of B (one float)
     float* csum;        // GELU backward (nullable): column sums of the stored output over
                         // each 32-row block, row r of a ceil(M/32) x N fp32 matrix
+    // batched products (nb > 1): nb independent products whose operands and outputs are
+    // stacked along the rows of their tensor maps, batch element l's rows starting at
+    // l * a_rows (A), l * b_rows (B), l * o_rows (out)
+    int nb, a_rows, b_rows, o_rows;
 };
 
 // Staging buffers per epilogue warp: four for the GELU epilogues of a CTA pair (two
@@ -140,12 +144,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int nkb = (K + BKE - 1) / BKE;
     const int kb_per = (nkb + splits - 1) / splits;
     const int m_groups = (m_tiles + CL - 1) / CL;
-    const int units = m_groups * n_tiles * splits;
+    const int nbat = ep.nb > 1 ? ep.nb : 1;
+    const int upb = m_groups * n_tiles * splits;        // units per batch element
+    const int units = upb * nbat;
     const int crank = CL > 1 ? (int)cluster_rank() : 0;
     const bool leader = crank == 0;
     const int ustart = blockIdx.x / CL, ustep = gridDim.x / CL;    // this cluster's units
     constexpr uint16_t CMASK = (1u << CL) - 1;
-    auto decode = [&](int u, int& sp, int& mt, int& nt) {
+    // unit -> (split, m tile, n tile) of batch element u / upb (upb is a multiple of
+    // splits, so u % splits is the split in every role)
+    auto decode = [&](int u, int& sp, int& mt, int& nt, int& lb) {
+        lb = u / upb;
+        u -= lb * upb;
         sp = u % splits;
         const int tile = u / splits;
         const int mg = m_fast ? tile % m_groups : tile / n_tiles;
@@ -203,10 +213,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t full_lead = CL > 1 ? mapa_shared(full, 0) : 0;   // the leader's full[0]
             constexpr int BH = BN / CL;                                      // B rows (or columns) per CTA
             for (int u = ufirst; u < units && ok; u += ustep) {
-                int sp, mt, nt;
-                decode(u, sp, mt, nt);
+                int sp, mt, nt, lb;
+                decode(u, sp, mt, nt, lb);
                 const int kb0 = sp * kb_per, kb1 = min(nkb, kb0 + kb_per);
                 const int nb0 = nt * BN + crank * BH;                        // first B row of this CTA's share
+                const int ay = lb * ep.a_rows, by = lb * ep.b_rows;          // batch element's first rows
                 for (int kb = kb0; kb < kb1; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -216,36 +227,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if constexpr (CL == 1) {
                         mbar_expect_tx(&full[s], S::STAGE_BYTES);
                         if (!A_MN) {
-                            tma_load_2d(a, &tmA, &full[s], kb * BKE, mt * TC_BM);
+                            tma_load_2d(a, &tmA, &full[s], kb * BKE, ay + mt * TC_BM);
                         } else {
 #pragma unroll
                             for (int j = 0; j < TC_BM / 64; j++)
-                                tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, kb * BKE);
+                                tma_load_2d(a + j * 8192, &tmA, &full[s], mt * TC_BM + j * 64, ay + kb * BKE);
                         }
                         if (!B_MN) {
-                            tma_load_2d(b, &tmB, &full[s], kb * BKE, nb0);
+                            tma_load_2d(b, &tmB, &full[s], kb * BKE, by + nb0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BN / 64; j++)
-                                tma_load_2d(b + j * 8192, &tmB, &full[s], nb0 + j * 64, kb * BKE);
+                                tma_load_2d(b + j * 8192, &tmB, &full[s], nb0 + j * 64, by + kb * BKE);
                         }
                     } else {
                         // both CTAs' bytes are counted on the leader's barrier
                         const uint32_t fb = full_lead + s * 8;
                         if (leader) mbar_expect_tx(&full[s], CL * S::STAGE_BYTES);
                         if (!A_MN) {
-                            tma_load_2d_pair(a, &tmA, fb, kb * BKE, mt * TC_BM);
+                            tma_load_2d_pair(a, &tmA, fb, kb * BKE, ay + mt * TC_BM);
                         } else {
 #pragma unroll
                             for (int j = 0; j < TC_BM / 64; j++)
-                                tma_load_2d_pair(a + j * 8192, &tmA, fb, mt * TC_BM + j * 64, kb * BKE);
+                                tma_load_2d_pair(a + j * 8192, &tmA, fb, mt * TC_BM + j * 64, ay + kb * BKE);
                         }
                         if (!B_MN) {
-                            tma_load_2d_pair(b, &tmB, fb, kb * BKE, nb0);
+                            tma_load_2d_pair(b, &tmB, fb, kb * BKE, by + nb0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BH / 64; j++)
-                                tma_load_2d_pair(b + j * 8192, &tmB, fb, nb0 + j * 64, kb * BKE);
+                                tma_load_2d_pair(b + j * 8192, &tmB, fb, nb0 + j * 64, by + kb * BKE);
                         }
                     }
                 }
@@ -347,10 +358,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         auto aux_issue = [&](int g) {
             const int uu = ufirst + (g / NPC) * ustep, pc = g % NPC, kb = g % NB;
             if (lane == 0 && uu < units) {
-                int usp, umt, unt;
-                decode(uu, usp, umt, unt);
+                int usp, umt, unt, ulb;
+                decode(uu, usp, umt, unt, ulb);
                 const int col = unt * BN + cbase + pc * 32;
-                const int row0 = umt * TC_BM + lane_grp * 32;
+                const int row0 = ulb * ep.o_rows + umt * TC_BM + lane_grp * 32;
                 bulk_wait_read<NB - AHEAD - 1>();
                 aux_pend |= 1u << kb;
                 mbar_expect_tx(&auxb[kb], S::STG_BYTES);
@@ -374,8 +385,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if constexpr (AUX_IN)
             for (int g = 0; g < AHEAD; g++) aux_issue(g);
         for (int u = ufirst; u < units && alive; u += ustep, local++) {
-            int sp, mt, nt;
-            decode(u, sp, mt, nt);
+            int sp, mt, nt, lb;
+            decode(u, sp, mt, nt, lb);
             const int acc = local % NACC;
             const uint32_t aph = (local / NACC) & 1;
             // one lane waits; the warp then proceeds converged (tcgen05.ld is warp-wide)
@@ -386,7 +397,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __syncwarp();
             tc_fence_after();
             const int row0 = mt * TC_BM + lane_grp * 32;   // first of this warp's 32 rows
-            const int yout = (EPI == TC_EPI_PARTIAL) ? sp * M + row0 : row0;
+            const int oy = lb * ep.o_rows;                 // batch element's first output row
+            const int yout = ((EPI == TC_EPI_PARTIAL) ? sp * M + row0 : row0) + oy;
 #pragma unroll 1
             for (int pi = 0; pi < NPAIR && alive; pi++) {
                 const int c = cbase + pi * 64;
@@ -510,7 +522,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 }
                                 fence_async_smem();
                                 __syncwarp();
-                                if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0); bulk_commit(); }
+                                if (lane == 0) { tma_store_2d(&tmAux, sb, col, row0 + oy); bulk_commit(); }
                                 nbuf++;
                                 sb = stg + (nbuf % NB) * S::STG_BYTES;
                                 if (lane == 0) bulk_wait_read<NB - 1>();
@@ -687,7 +699,7 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return GPT2_ECUDA;
         max_clusters = n;
     }
-    const int units = ((M + TC_BM - 1) / TC_BM + CL - 1) / CL * ((N + BN - 1) / BN) * splits;
+    const int units = ((M + TC_BM - 1) / TC_BM + CL - 1) / CL * ((N + BN - 1) / BN) * splits * (ep.nb > 1 ? ep.nb : 1);
     const int clusters = units < max_clusters ? units : max_clusters;
     cfg.gridDim = dim3(clusters * CL);
     cfg.numAttrs = 2;
@@ -764,18 +776,27 @@ int gemm_tc_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const flo
     }
 }
 
-int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16* B, bool b_mn, int M, int N, int K,
-                 unsigned* err) {
-    // out (M x N) = sum_k A(m,k) B(n,k): A K-major (M rows of K) or MN-major (K rows of M),
-    // B K-major (N rows of K) or MN-major (K rows of N)
+int gemm_tc_bf16_batched(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16* B, bool b_mn, int M, int N,
+                         int K, int nb, unsigned* err) {
+    // out_l (M x N) = sum_k A_l(m,k) B_l(n,k), l < nb, each operand's nb matrices
+    // contiguous: A K-major (M rows of K) or MN-major (K rows of M), B K-major (N rows of K)
+    // or MN-major (K rows of N).  In the tensor maps the matrices are stacked along their
+    // rows, so with nb > 1 no tile may straddle two of them: M, N multiples of 256, K of 64.
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
-    if (M % 8 || N % 8 || K % 8 || !aligned16(out) || !aligned16(A) || !aligned16(B)) return GPT2_EUNSUPPORTED;
+    if (M % 8 || N % 8 || K % 8 || nb < 1 || !aligned16(out) || !aligned16(A) || !aligned16(B))
+        return GPT2_EUNSUPPORTED;
+    if (nb > 1 && (M % 256 || N % 256 || K % 64)) return GPT2_EUNSUPPORTED;
     const int cl = (N <= 768 && K <= 768) ? 1 : 2;
     CUtensorMap ta, tb, to;
-    const bool ok_a = a_mn ? make_map(&ta, A, M, K, M, 64) : make_map(&ta, A, K, M, K, TC_BM);
-    const bool ok_b = b_mn ? make_map(&tb, B, N, K, N, 64) : make_map(&tb, B, K, N, K, 256 / cl);
-    if (!ok_a || !ok_b || !make_epi_map(&to, out, N, M, N)) return GPT2_EUNSUPPORTED;
+    const uint64_t nbu = (uint64_t)nb;
+    const bool ok_a = a_mn ? make_map(&ta, A, M, K * nbu, M, 64) : make_map(&ta, A, K, M * nbu, K, TC_BM);
+    const bool ok_b = b_mn ? make_map(&tb, B, N, K * nbu, N, 64) : make_map(&tb, B, K, N * nbu, K, 256 / cl);
+    if (!ok_a || !ok_b || !make_epi_map(&to, out, N, M * nbu, N)) return GPT2_EUNSUPPORTED;
     TcEpi ep{out, nullptr, nullptr, (long)N};
+    ep.nb = nb;
+    ep.a_rows = a_mn ? K : M;
+    ep.b_rows = b_mn ? K : N;
+    ep.o_rows = M;
     if (!a_mn && !b_mn)
         return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2>(s, ta, tb, to, to, M, N, K, 1, ep, err)
                        : launch_tc<256, EPI_STORE, false, false, 1>(s, ta, tb, to, to, M, N, K, 1, ep, err);
@@ -786,6 +807,11 @@ int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16
         return cl == 2 ? launch_tc<256, EPI_STORE, true, true, 2>(s, ta, tb, to, to, M, N, K, 1, ep, err)
                        : launch_tc<256, EPI_STORE, true, true, 1>(s, ta, tb, to, to, M, N, K, 1, ep, err);
     return GPT2_EUNSUPPORTED;
+}
+
+int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16* B, bool b_mn, int M, int N, int K,
+                 unsigned* err) {
+    return gemm_tc_bf16_batched(s, out, A, a_mn, B, b_mn, M, N, K, 1, err);
 }
 
 int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16* W, int M, int N, int K, int epi,

@@ -32,6 +32,10 @@ int gemm_tc_forward_fp8(cudaStream_t s, __nv_bfloat16* out, const uint8_t* inp, 
 // A plain bf16 product with bf16 output: out (M,N) = sum_k A(m,k) B(n,k), each operand
 // K-major (rows of K contiguous) or MN-major (rows of M or N contiguous, K rows); the
 // combination (A MN-major, B K-major) is not built.  M, N, K multiples of 8.
+// nb such products at once, each operand's nb matrices contiguous (A_l = A + l M K, B_l =
+// B + l N K, out_l = out + l M N); for nb > 1, M and N multiples of 256 and K of 64.
+int gemm_tc_bf16_batched(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* A, bool a_mn,
+                         const __nv_bfloat16* B, bool b_mn, int M, int N, int K, int nb, unsigned* err);
 int gemm_tc_bf16(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B,
                  bool b_mn, int M, int N, int K, unsigned* err);
 

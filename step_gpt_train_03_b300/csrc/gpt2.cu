@@ -190,9 +190,9 @@ static size_t plan(GPT2* m, char* base) {
     m->err = (unsigned*)take(16);
     if (m->prec != GPT2_FP32) {
         m->mu_x = (bf16*)take(L * 4 * C * C * 2);
-        m->mu_xb = (bf16*)take(4 * C * C * 2);
-        m->mu_s = (bf16*)take(C * C * 2);
-        m->mu_t = (bf16*)take(C * C * 2);
+        m->mu_xb = (bf16*)take(L * 4 * C * C * 2);         // the iterates and Gram matrices of
+        m->mu_s = (bf16*)take(L * C * C * 2);              // all L layers of a tensor at once
+        m->mu_t = (bf16*)take(L * C * C * 2);
         m->mu_part = (float*)take(L * MUON_NB * 4);
     } else {
         m->mu_x = m->mu_xb = m->mu_s = m->mu_t = nullptr;
@@ -1123,25 +1123,28 @@ extern "C" int gpt2_update(GPT2* m, float lr, float beta1, float beta2, float ep
 // X (r x c, bf16) <- `iters` cubic Newton-Schulz steps X <- X (1.5 I - 0.5 X^T X) (tall or
 // square) or (1.5 I - 0.5 X X^T) X (wide), on the tensor cores; X and xb ping-pong, the
 // result's buffer is returned in *res.
-static int newton_schulz_bf16(cudaStream_t s, bf16* X, bf16* xb, bf16* S, bf16* T, int r, int c, int iters,
+// `iters` cubic Newton-Schulz steps on nb r x c bf16 matrices at once (X, xb: nb x r x c;
+// S, T: nb x n x n, n = min(r, c)); the products are batched over the nb matrices.
+static int newton_schulz_bf16(cudaStream_t s, bf16* X, bf16* xb, bf16* S, bf16* T, int r, int c, int nb, int iters,
                               bf16** res, unsigned* err) {
     const bool tall = r >= c;
     const int n = tall ? c : r;
     for (int k = 0; k < iters; k++) {
         {
-            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * n * n * (tall ? r : c), 0);
+            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * nb * n * n * (tall ? r : c), 0);
             // S = X^T X (A(i,k) = X[k][i] and B(j,k) = X[k][j], both MN-major) or X X^T
-            RC(tall ? gemm_tc_bf16(s, S, X, true, X, true, c, c, r, err)
-                    : gemm_tc_bf16(s, S, X, false, X, false, r, r, c, err));
+            RC(tall ? gemm_tc_bf16_batched(s, S, X, true, X, true, c, c, r, nb, err)
+                    : gemm_tc_bf16_batched(s, S, X, false, X, false, r, r, c, nb, err));
         }
         rt_note_launches(1);
-        launch_pdl(ns_affine_kernel, (unsigned)std::min<size_t>(ceil_div_sz((size_t)n * n, 256), 592), 256, 0, s, T, S, n);
+        launch_pdl(ns_affine_kernel, (unsigned)std::min<size_t>(ceil_div_sz((size_t)nb * n * n, 256), 592), 256, 0, s, T, S,
+                   n, nb);
         CK(cudaGetLastError());
         {
-            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * r * c * n, 0);
+            ProfScope ps(s, PC_MATMUL_FWD, 2.0 * nb * r * c * n, 0);
             // xb = X T (B(j,k) = T[k][j], MN-major) or T X (B(j,k) = X[k][j], MN-major)
-            RC(tall ? gemm_tc_bf16(s, xb, X, false, T, true, r, c, c, err)
-                    : gemm_tc_bf16(s, xb, T, false, X, true, r, c, r, err));
+            RC(tall ? gemm_tc_bf16_batched(s, xb, X, false, T, true, r, c, c, nb, err)
+                    : gemm_tc_bf16_batched(s, xb, T, false, X, true, r, c, r, nb, err));
         }
         std::swap(X, xb);
     }
@@ -1189,14 +1192,18 @@ extern "C" int gpt2_update_muon(GPT2* m, float lr_muon, float momentum, int ns_i
             launch_pdl(scale_frobenius_bf16_kernel, dim3(std::max(1, 148 * 4 / L), L), 256, 0, s, m->mu_x, mom, m->mu_part, len);
             CK(cudaGetLastError());
         }
-        for (int l = 0; l < L; l++) {
+        // all L layers' iterations batched in each product when no tile would straddle two
+        // layers' matrices (dimensions multiples of 256), else layer by layer
+        const bool batched = mu_r[q] % 256 == 0 && mu_c[q] % 256 == 0;
+        const int nl = batched ? L : 1;
+        for (int l0 = 0; l0 < L; l0 += nl) {
             bf16* res = nullptr;
-            RC(newton_schulz_bf16(s, m->mu_x + l * len, m->mu_xb, m->mu_s, m->mu_t, mu_r[q], mu_c[q], ns_iters, &res,
-                                  m->err));
-            ProfScope ps(s, PC_MISC, 0, 14.0 * len);
+            RC(newton_schulz_bf16(s, m->mu_x + l0 * len, m->mu_xb + l0 * len, m->mu_s, m->mu_t, mu_r[q], mu_c[q], nl,
+                                  ns_iters, &res, m->err));
+            ProfScope ps(s, PC_MISC, 0, 14.0 * nl * len);
             rt_note_launches(1);
-            launch_pdl(muon_apply_kernel, (unsigned)std::min<size_t>(ceil_div_sz(len / 4, 256), 148 * 4), 256, 0, s, 
-                (float4*)(m->params + off + l * len), res, m->wbf + off + l * len, len / 4, lr_muon, wd);
+            launch_pdl(muon_apply_kernel, (unsigned)std::min<size_t>(ceil_div_sz(nl * len / 4, 256), 148 * 4), 256, 0, s,
+                       (float4*)(m->params + off + l0 * len), res, m->wbf + off + l0 * len, nl * len / 4, lr_muon, wd);
             CK(cudaGetLastError());
         }
     }
@@ -1231,7 +1238,7 @@ extern "C" int gpt2_newton_schulz(void* out, const float* G, int r, int c, int i
     launch_pdl(scale_frobenius_bf16_kernel, dim3(148, 1), 256, 0, s, (bf16*)out, G, part, len);
     CK(cudaGetLastError());
     bf16* res = nullptr;
-    RC(newton_schulz_bf16(s, (bf16*)out, xb, S, T, r, c, iters, &res, err));
+    RC(newton_schulz_bf16(s, (bf16*)out, xb, S, T, r, c, 1, iters, &res, err));
     if (res != (bf16*)out) CK(cudaMemcpyAsync(out, res, len * 2, cudaMemcpyDeviceToDevice, s));
     return GPT2_OK;
 }

@@ -1230,11 +1230,12 @@ __global__ void __launch_bounds__(256) scale_frobenius_bf16_kernel(bf16* __restr
     }
 }
 // T = 1.5 I - 0.5 S (n x n, bf16): the Newton-Schulz step X <- 1.5 X - 0.5 X S = X T
-__global__ void ns_affine_kernel(bf16* __restrict__ T, const bf16* __restrict__ S, int n) {
+__global__ void ns_affine_kernel(bf16* __restrict__ T, const bf16* __restrict__ S, int n, int nb) {
     pdl_wait();
     const size_t nn = (size_t)n * n;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nn; i += (size_t)gridDim.x * blockDim.x) {
-        const int r = (int)(i / n), c = (int)(i % n);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nn * nb; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t j = i % nn;                       // element of matrix i / nn
+        const int r = (int)(j / n), c = (int)(j % n);
         T[i] = __float2bfloat16_rn((r == c ? 1.5f : 0.f) - 0.5f * __bfloat162float(S[i]));
     }
 }
