@@ -314,11 +314,8 @@ def ours(args):
 
     def step(i, t):
         if args.optimizer == "muon":
-            # forward, zero_grad, backward, then Muon + AdamW (launched kernel by kernel)
-            m.forward(toks[i], tgts[i], want_loss=False)
-            m.zero_grad()
-            m.backward()
-            m.update_muon(0.02, 0.95, 5, *hp[:4], hp[4], t)
+            # forward, backward, then Muon + AdamW: one CUDA graph launch once captured
+            m.step_muon_device(toks[i], tgts[i], 0.02, 0.95, 5, *hp, t, want_loss=False)
             return
         # the library's whole-step call: one CUDA graph launch once the shape is captured
         m.step_device(toks[i], tgts[i], *hp, t, want_loss=False)

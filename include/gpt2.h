@@ -215,8 +215,18 @@ int gpt2_step(GPT2* model, const int32_t* tokens, const int32_t* targets, int B,
               float lr, float beta1, float beta2, float eps, float weight_decay, int t,
               float* loss_out);
 
-/* Enable (1, the default) or disable (0) the step graph of gpt2_step / gpt2_step_host;
- * disabling frees a captured graph.  GPT2_EINVAL for a NULL model. */
+/* The step of gpt2_step with the update of gpt2_update_muon (same arguments; bf16 and fp8
+ * models, GPT2_EUNSUPPORTED in fp32): forward, backward and the Muon + AdamW update, as
+ * one CUDA graph once the shape has been seen.  A graph serves one (B, T) and one set of
+ * Muon constants (ns_iters, lr_muon, momentum, weight_decay): a step with other values
+ * runs kernel by kernel and the next one is captured anew; lr, beta1, beta2, eps and t
+ * are set on the graph's AdamW nodes before each launch. */
+int gpt2_step_muon(GPT2* model, const int32_t* tokens, const int32_t* targets, int B, int T,
+                   float lr_muon, float momentum, int ns_iters, float lr, float beta1, float beta2,
+                   float eps, float weight_decay, int t, float* loss_out);
+
+/* Enable (1, the default) or disable (0) the step graph of gpt2_step / gpt2_step_host /
+ * gpt2_step_muon; disabling frees a captured graph.  GPT2_EINVAL for a NULL model. */
 int gpt2_set_graphs(GPT2* model, int enable);
 
 /* Next-token sampling (the llm.c article's training run: after training, the program

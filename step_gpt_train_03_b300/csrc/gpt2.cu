@@ -90,14 +90,24 @@ struct GPT2 {
     // state
     int B, T;
     int have_fwd, have_targets;
-    // the whole step as one CUDA graph, captured for (gB, gT) on the second step of that
-    // shape; the AdamW node's scalars are set before each launch
+    // the whole step as one CUDA graph, captured for (gB, gT) and the optimizer (g_opt:
+    // 0 AdamW, 1 Muon with its constants) on the second step of that shape; the scalars
+    // of its AdamW nodes (one per flat range they update) are set before each launch
     int use_graph, g_seen;
     int gB, gT;
+    int g_opt, g_ns;
+    float g_lrmu, g_mu, g_wdmu;
     cudaStream_t cap_stream;           // private stream the step is captured on
     cudaGraph_t graph;
     cudaGraphExec_t gexec;
-    cudaGraphNode_t g_adam;
+    int g_nadam;
+    cudaGraphNode_t g_adam[8];
+    float* ga_p[8];                    // each AdamW node's range: pointers, float4 count, grid
+    const float* ga_g[8];
+    float *ga_m[8], *ga_v[8];
+    bf16* ga_sh[8];
+    size_t ga_n4[8];
+    unsigned ga_grid[8];
     long long g_kernels;
 };
 
@@ -321,7 +331,7 @@ extern "C" int gpt2_build(const GPT2Config* cfg, int max_B, int max_T, int preci
     m->cap_stream = nullptr;
     m->graph = nullptr;
     m->gexec = nullptr;
-    m->g_adam = nullptr;
+    m->g_nadam = 0;
     m->g_kernels = 0;
     int rc = launch_zero(m->stream, m->params, (size_t)m->n_flat * 4 * 4);   // params, grads, m, v
     if (rc == GPT2_OK) rc = launch_zero(m->stream, m->err, 16);
@@ -337,7 +347,7 @@ static void drop_graph(GPT2* m) {
     if (m->graph) cudaGraphDestroy(m->graph);
     m->gexec = nullptr;
     m->graph = nullptr;
-    m->g_adam = nullptr;
+    m->g_nadam = 0;
     m->g_seen = 0;
 }
 
@@ -1245,7 +1255,16 @@ extern "C" int gpt2_newton_schulz(void* out, const float* G, int r, int c, int i
 
 // forward (with targets), zero_grad, backward and AdamW on the model's stream, as
 // launched one by one
-static int step_eager(GPT2* m, int B, int Tn, float lr, float b1, float b2, float eps, float wd, int t) {
+// the optimizer of a fused step: AdamW, or Muon on the block matrices with AdamW on the rest
+struct StepHp {
+    int opt;                           // 0 AdamW, 1 Muon
+    float lr, b1, b2, eps, wd;
+    int t;
+    float lr_mu, mu;                   // Muon
+    int ns;
+};
+
+static int step_eager(GPT2* m, int B, int Tn, const StepHp& hp) {
     RC(forward_dispatch(m, B, Tn, true));
     // bf16 / fp8: no clear of the gradients; the backward's first write to each stores
     // instead of adding (the same values), and it clears what no writer covers
@@ -1254,14 +1273,15 @@ static int step_eager(GPT2* m, int B, int Tn, float lr, float b1, float b2, floa
     const int rc = gpt2_backward(m);
     m->overwrite = 0;
     RC(rc);
-    return gpt2_update(m, lr, b1, b2, eps, wd, t);
+    if (hp.opt == 1) return gpt2_update_muon(m, hp.lr_mu, hp.mu, hp.ns, hp.lr, hp.b1, hp.b2, hp.eps, hp.wd, hp.t);
+    return gpt2_update(m, hp.lr, hp.b1, hp.b2, hp.eps, hp.wd, hp.t);
 }
 
 // Capture the step for (B, Tn) into a graph and find its AdamW node.  Lazy set-up
 // (function attributes, occupancy queries) has already run in an earlier eager step.
 // The capture runs on a private stream (the caller's may be the legacy default stream,
 // which cannot be captured); the graph is then launched into the caller's stream.
-static int capture_step(GPT2* m, int B, int Tn) {
+static int capture_step(GPT2* m, int B, int Tn, StepHp hp) {
     drop_graph(m);
     if (!m->cap_stream) CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
     const long long n0 = rt_launches();
@@ -1273,7 +1293,10 @@ static int capture_step(GPT2* m, int B, int Tn) {
         g_last_cuda_error = cb;
         return GPT2_ECUDA;
     }
-    int rc = step_eager(m, B, Tn, 0.f, 0.9f, 0.999f, 1e-8f, 0.f, 1);
+    // the AdamW scalars captured here are replaced before every launch
+    hp.lr = 0.f;
+    hp.t = 1;
+    int rc = step_eager(m, B, Tn, hp);
     cudaGraph_t g = nullptr;
     cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &g);
     m->stream = user;
@@ -1287,21 +1310,33 @@ static int capture_step(GPT2* m, int B, int Tn) {
     cudaGraphGetNodes(g, nullptr, &nn);
     std::vector<cudaGraphNode_t> nodes(nn);
     cudaGraphGetNodes(g, nodes.data(), &nn);
-    cudaGraphNode_t adam = nullptr;
+    // the AdamW nodes, each with the pointers and float4 count of its range
+    int na = 0;
+    bool too_many = false;
     for (cudaGraphNode_t nd : nodes) {
         cudaGraphNodeType ty;
         if (cudaGraphNodeGetType(nd, &ty) != cudaSuccess || ty != cudaGraphNodeTypeKernel) continue;
         cudaKernelNodeParams kp;
-        if (cudaGraphKernelNodeGetParams(nd, &kp) == cudaSuccess && kp.func == (void*)adamw_kernel) adam = nd;
+        if (cudaGraphKernelNodeGetParams(nd, &kp) != cudaSuccess || kp.func != (void*)adamw_kernel) continue;
+        if (na == 8) { too_many = true; break; }
+        m->g_adam[na] = nd;
+        m->ga_p[na] = *(float**)kp.kernelParams[0];
+        m->ga_g[na] = *(const float**)kp.kernelParams[1];
+        m->ga_m[na] = *(float**)kp.kernelParams[2];
+        m->ga_v[na] = *(float**)kp.kernelParams[3];
+        m->ga_sh[na] = *(bf16**)kp.kernelParams[4];
+        m->ga_n4[na] = *(size_t*)kp.kernelParams[5];
+        m->ga_grid[na] = kp.gridDim.x;
+        na++;
     }
     cudaGraphExec_t ex = nullptr;
-    if (!adam || cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    if (na == 0 || too_many || cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
         cudaGraphDestroy(g);
         return GPT2_ECUDA;
     }
     m->graph = g;
     m->gexec = ex;
-    m->g_adam = adam;
+    m->g_nadam = na;
     m->g_kernels = captured;
     m->gB = B;
     m->gT = Tn;
@@ -1311,32 +1346,49 @@ static int capture_step(GPT2* m, int B, int Tn) {
 // One training step on the batch already in m->tokens / m->targets.  With graphs on and
 // the tracer off: the first step of a shape runs eagerly, the second captures the step,
 // and from then on each step is one graph launch with this step's AdamW scalars.
-static int run_step(GPT2* m, int B, int Tn, float lr, float b1, float b2, float eps, float wd, int t) {
-    if (!m->use_graph || rt_tracing_on()) return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
-    if (m->gexec && (m->gB != B || m->gT != Tn)) drop_graph(m);
+static int run_step(GPT2* m, int B, int Tn, const StepHp& hp) {
+    if (!m->use_graph || rt_tracing_on()) return step_eager(m, B, Tn, hp);
+    // a graph serves one shape and one optimizer (Muon: with its constants)
+    const bool same = m->gB == B && m->gT == Tn && m->g_opt == hp.opt &&
+                      (hp.opt == 0 || (m->g_ns == hp.ns && m->g_lrmu == hp.lr_mu && m->g_mu == hp.mu &&
+                                       m->g_wdmu == hp.wd));
+    if (m->gexec && !same) drop_graph(m);
     if (!m->gexec) {
-        if (!m->g_seen || m->gB != B || m->gT != Tn) {
+        if (!m->g_seen || !same) {
             m->g_seen = 1;
             m->gB = B;
             m->gT = Tn;
-            return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
+            m->g_opt = hp.opt;
+            m->g_ns = hp.ns;
+            m->g_lrmu = hp.lr_mu;
+            m->g_mu = hp.mu;
+            m->g_wdmu = hp.wd;
+            return step_eager(m, B, Tn, hp);
         }
-        int rc = capture_step(m, B, Tn);
+        int rc = capture_step(m, B, Tn, hp);
         if (rc != GPT2_OK) {                    // no graph for this model: stay eager
             m->use_graph = 0;
-            return step_eager(m, B, Tn, lr, b1, b2, eps, wd, t);
+            return step_eager(m, B, Tn, hp);
         }
     }
-    AdamArgs a;
-    adam_args(m, a, lr, b1, b2, eps, wd, t);
-    cudaKernelNodeParams kp = {};
-    kp.func = (void*)adamw_kernel;
-    kp.gridDim = dim3(a.grid);
-    kp.blockDim = dim3(256);
-    kp.sharedMemBytes = 0;
-    kp.kernelParams = a.kp;
-    kp.extra = nullptr;
-    CK(cudaGraphExecKernelNodeSetParams(m->gexec, m->g_adam, &kp));
+    for (int i = 0; i < m->g_nadam; i++) {
+        AdamArgs a;
+        adam_args(m, a, hp.lr, hp.b1, hp.b2, hp.eps, hp.wd, hp.t);
+        a.p = m->ga_p[i];
+        a.g = m->ga_g[i];
+        a.mm = m->ga_m[i];
+        a.vv = m->ga_v[i];
+        a.shadow = m->ga_sh[i];
+        a.n4 = m->ga_n4[i];
+        cudaKernelNodeParams kp = {};
+        kp.func = (void*)adamw_kernel;
+        kp.gridDim = dim3(m->ga_grid[i]);
+        kp.blockDim = dim3(256);
+        kp.sharedMemBytes = 0;
+        kp.kernelParams = a.kp;
+        kp.extra = nullptr;
+        CK(cudaGraphExecKernelNodeSetParams(m->gexec, m->g_adam[i], &kp));
+    }
     CK(cudaGraphLaunch(m->gexec, m->stream));
     rt_note_launches(m->g_kernels);
     m->B = B;
@@ -1360,7 +1412,7 @@ extern "C" int gpt2_step(GPT2* m, const int32_t* tokens, const int32_t* targets,
     const size_t BT = (size_t)B * Tn;
     CK(cudaMemcpyAsync(m->tokens, tokens, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
     CK(cudaMemcpyAsync(m->targets, targets, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
-    RC(run_step(m, B, Tn, lr, beta1, beta2, eps, wd, t));
+    RC(run_step(m, B, Tn, StepHp{0, lr, beta1, beta2, eps, wd, t, 0.f, 0.f, 0}));
     if (!loss_out) return GPT2_OK;
     float l = -1.f;
     CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
@@ -1377,7 +1429,25 @@ extern "C" int gpt2_step_host(GPT2* m, const int32_t* tokens_host, const int32_t
     const size_t BT = (size_t)B * Tn;
     CK(cudaMemcpyAsync(m->tokens, tokens_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
     CK(cudaMemcpyAsync(m->targets, targets_host, BT * 4, cudaMemcpyHostToDevice, m->stream));
-    RC(run_step(m, B, Tn, lr, beta1, beta2, eps, wd, t));
+    RC(run_step(m, B, Tn, StepHp{0, lr, beta1, beta2, eps, wd, t, 0.f, 0.f, 0}));
+    float l = -1.f;
+    CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+    int rc = read_error(m);
+    *loss_out = l;
+    return rc;
+}
+
+extern "C" int gpt2_step_muon(GPT2* m, const int32_t* tokens, const int32_t* targets, int B, int Tn, float lr_muon,
+                              float momentum, int ns_iters, float lr, float beta1, float beta2, float eps, float wd,
+                              int t, float* loss_out) {
+    if (!m || !tokens || !targets || t < 1 || ns_iters < 0) return GPT2_EINVAL;
+    if (m->prec == GPT2_FP32) return GPT2_EUNSUPPORTED;
+    RC(check_bt(m, B, Tn));
+    const size_t BT = (size_t)B * Tn;
+    CK(cudaMemcpyAsync(m->tokens, tokens, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    CK(cudaMemcpyAsync(m->targets, targets, BT * 4, cudaMemcpyDeviceToDevice, m->stream));
+    RC(run_step(m, B, Tn, StepHp{1, lr, beta1, beta2, eps, wd, t, lr_muon, momentum, ns_iters}));
+    if (!loss_out) return GPT2_OK;
     float l = -1.f;
     CK(cudaMemcpyAsync(&l, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
     int rc = read_error(m);

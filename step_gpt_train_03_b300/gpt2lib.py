@@ -65,6 +65,7 @@ SIGNATURES = {
     "gpt2_update": (_i, [_vp, _f, _f, _f, _f, _f, _i]),
     "gpt2_step_host": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
     "gpt2_step": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
+    "gpt2_step_muon": (_i, [_vp, _vp, _vp, _i, _i, _f, _f, _i, _f, _f, _f, _f, _f, _i, ctypes.POINTER(_f)]),
     "gpt2_set_graphs": (_i, [_vp, _i]),
     "gpt2_sample": (_i, [_vp, _i, _f, ctypes.c_ulonglong, _vp]),
     "gpt2_save_params": (_i, [_vp, ctypes.c_char_p]),
@@ -283,6 +284,17 @@ class GPT2:
         loss = ctypes.c_float(0.0)
         check(lib.gpt2_step(self.handle, _ptr(tokens), _ptr(targets), B, T, lr, beta1, beta2, eps,
                             weight_decay, t, ctypes.byref(loss) if want_loss else None), "gpt2_step")
+        return loss.value if want_loss else None
+
+    def step_muon_device(self, tokens, targets, lr_muon, momentum, ns_iters, lr, beta1, beta2, eps, weight_decay, t,
+                         want_loss=False):
+        """Whole Muon step from int32 CUDA tensors (B, T) through gpt2_step_muon (a CUDA graph
+        once the shape has been seen).  Returns the mean loss (synchronises) when want_loss."""
+        B, T = tokens.shape
+        loss = ctypes.c_float(0.0)
+        check(lib.gpt2_step_muon(self.handle, _ptr(tokens), _ptr(targets), B, T, lr_muon, momentum, ns_iters, lr,
+                                 beta1, beta2, eps, weight_decay, t, ctypes.byref(loss) if want_loss else None),
+              "gpt2_step_muon")
         return loss.value if want_loss else None
 
     def sample(self, pos: int, temperature: float, seed: int, out=None):

@@ -125,3 +125,25 @@ def test_muon_gpt2_124m_short_sequences(G):
     hp = dict(lr_muon=0.02, mu=0.95, iters=5, lr=6e-4, wd=0.0)
     _, _, lg, lo = _muon_run(shape, 2, 128, batches, hp)
     assert max(abs(a - b) for a, b in zip(lg, lo)) <= LOSS_ABS, (lg, lo)
+
+
+@pytest.mark.parametrize("shape", [synth.TINY_HS64, synth.ModelShape(64, 512, 512, 2, 4, 256)],
+                         ids=["layer-by-layer", "batched"])
+def test_muon_graph_steps_match_eager_steps_bitwise(G, shape):
+    """gpt2_step_muon replays one captured CUDA graph (forward, backward, Muon + AdamW)
+    per shape and Muon constants; every step -- the AdamW learning rate changing each
+    time, a Muon momentum change in the middle forcing a new capture -- equals the
+    kernel-by-kernel step bit for bit.  The C = 256 shape takes the batched Newton-Schulz
+    products (all matrix sides multiples of 256), the tiny one the layer-by-layer path."""
+    import torch
+    batches = synth.zipf_batches(shape.vocab_size, 2, 32, 8, 13)
+    g = gpu_model(shape, 2, 32, "bf16", 4)
+    e = gpu_model(shape, 2, 32, "bf16", 4)
+    e.set_graphs(False)
+    for i, (tok, tgt) in enumerate(batches):
+        tk, tg = dev_tokens(tok), dev_tokens(tgt)
+        lr, mom = 1e-3 * (1 + 0.1 * i), (0.95 if i < 4 else 0.9)
+        lg = g.step_muon_device(tk, tg, 0.02, mom, 5, lr, 0.9, 0.95, 1e-8, 0.1, i + 1, want_loss=True)
+        le = e.step_muon_device(tk, tg, 0.02, mom, 5, lr, 0.9, 0.95, 1e-8, 0.1, i + 1, want_loss=True)
+        assert lg == le, (i, lg, le)
+        assert torch.equal(g.flat_params(), e.flat_params()), i
