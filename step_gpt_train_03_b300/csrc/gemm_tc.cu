@@ -67,6 +67,9 @@ struct TcEpi {
     // stacked along the rows of their tensor maps, batch element l's rows starting at
     // l * a_rows (A), l * b_rows (B), l * o_rows (out)
     int nb, a_rows, b_rows, o_rows;
+    // GELU epilogues: with gelu_deriv the forward keeps gelu'(h) instead of h in aux, and
+    // the input-gradient product multiplies by aux as it is (already the derivative)
+    int gelu_deriv;
 };
 
 // Staging buffers per epilogue warp: four for the GELU epilogues of a CTA pair (two
@@ -465,7 +468,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                             for (int e = 0; e < 8; e += 2) {
                                 const float2 x = a.get2(e), acc2 = make_float2(v[8 * j + e], v[8 * j + e + 1]);
-                                const float2 r = (EPI == EPI_RESID) ? __fadd2_rn(acc2, x) : __fmul2_rn(acc2, gelu_grad2_fast(x));
+                                const float2 r = (EPI == EPI_RESID) ? __fadd2_rn(acc2, x)
+                                                 : __fmul2_rn(acc2, ep.gelu_deriv ? x : gelu_grad2_fast(x));
                                 o.set2(e, r.x, r.y);
                             }
                             *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
@@ -506,18 +510,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             if (lane == 0) bulk_wait_read<NB - 1>();
                             __syncwarp();
                             if constexpr (EPI == EPI_GELU) {
-                                // pre-activation out first, then the activation into the other buffer
+                                // pre-activation (or its GELU derivative) out first, then the
+                                // activation into the other buffer; both of the rounded (bf16)
+                                // pre-activation
 #pragma unroll
                                 for (int j = 0; j < 4; j++) {
                                     Vec<bf16> o;
 #pragma unroll
                                     for (int e = 0; e < 8; e += 2) o.set2(e, v[8 * j + e], v[8 * j + e + 1]);
-                                    *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+                                    if (ep.gelu_deriv) {
+                                        Vec<bf16> dv;
 #pragma unroll
-                                    for (int e = 0; e < 8; e += 2) {
-                                        const float2 g = gelu2_fast(o.get2(e));      // of the stored pre-activation
-                                        v[8 * j + e] = g.x;
-                                        v[8 * j + e + 1] = g.y;
+                                        for (int e = 0; e < 8; e += 2) {
+                                            float2 g, d;
+                                            gelu_and_grad2_fast(o.get2(e), g, d);
+                                            v[8 * j + e] = g.x;
+                                            v[8 * j + e + 1] = g.y;
+                                            dv.set2(e, d.x, d.y);
+                                        }
+                                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = dv.v;
+                                    } else {
+                                        *reinterpret_cast<uint4*>(sb + stg_off(lane, j)) = o.v;
+#pragma unroll
+                                        for (int e = 0; e < 8; e += 2) {
+                                            const float2 g = gelu2_fast(o.get2(e));      // of the stored pre-activation
+                                            v[8 * j + e] = g.x;
+                                            v[8 * j + e + 1] = g.y;
+                                        }
                                     }
                                 }
                                 fence_async_smem();
@@ -712,7 +731,7 @@ static int launch_tc(cudaStream_t s, const CUtensorMap& ta, const CUtensorMap& t
 }
 
 int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, const bf16* bias, int M, int N,
-                    int K, int epi, bf16* aux, unsigned* err) {
+                    int K, int epi, bf16* aux, unsigned* err, bool gelu_deriv) {
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
     if (N % 8 || K % 8 || M < 1 || !aligned16(out) || !aligned16(inp) || !aligned16(W) ||
         (bias && !aligned16(bias)) || (aux && !aligned16(aux)))
@@ -730,6 +749,7 @@ int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, c
         tx = to;
     }
     TcEpi ep{out, bias, aux, (long)N};
+    ep.gelu_deriv = gelu_deriv ? 1 : 0;
     switch (epi) {
         case EPI_STORE:
             return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
@@ -745,7 +765,8 @@ int gemm_tc_forward(cudaStream_t s, bf16* out, const bf16* inp, const bf16* W, c
 }
 
 int gemm_tc_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const float* inp_deq, const uint8_t* W,
-                        const float* w_deq, const bf16* bias, int M, int N, int K, int epi, bf16* aux, unsigned* err) {
+                        const float* w_deq, const bf16* bias, int M, int N, int K, int epi, bf16* aux, unsigned* err,
+                        bool gelu_deriv) {
     // as gemm_tc_forward with e4m3 operands: K a multiple of 16 (16-byte rows for TMA)
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
     if (N % 8 || K % 16 || M < 1 || !inp_deq || !w_deq || !aligned16(out) || !aligned16(inp) || !aligned16(W) ||
@@ -762,6 +783,7 @@ int gemm_tc_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const flo
         tx = to;
     }
     TcEpi ep{out, bias, aux, (long)N, inp_deq, w_deq};
+    ep.gelu_deriv = gelu_deriv ? 1 : 0;
     switch (epi) {
         case EPI_STORE:
             return cl == 2 ? launch_tc<256, EPI_STORE, false, false, 2, true>(s, ta, tb, to, tx, M, N, K, 1, ep, err)
@@ -815,7 +837,7 @@ int gemm_tc_bf16(cudaStream_t s, bf16* out, const bf16* A, bool a_mn, const bf16
 }
 
 int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16* W, int M, int N, int K, int epi,
-                        const bf16* aux, float* csum, unsigned* err) {
+                        const bf16* aux, float* csum, unsigned* err, bool gelu_deriv) {
     // dinp (M x K) = dout (M x N) W (N x K): contraction over N; A = dout K-major,
     // B(k_out, n) = W[n][k_out] is MN-major (k_out contiguous)
     if (!gemm_tc_available()) return GPT2_EUNSUPPORTED;
@@ -832,6 +854,7 @@ int gemm_tc_backward_dx(cudaStream_t s, bf16* dinp, const bf16* dout, const bf16
     }
     if (csum && epi != EPI_GELU_BWD) return GPT2_EINVAL;
     TcEpi ep{dinp, nullptr, (void*)aux, (long)K, nullptr, nullptr, csum};
+    ep.gelu_deriv = gelu_deriv ? 1 : 0;
     const int cl = (N <= 768 && K <= 768) ? 1 : 2;      // as in the forward
     if (epi == EPI_GELU_BWD)
         return cl == 2 ? launch_tc<256, EPI_GELU_BWD, false, true, 2>(s, ta, tb, to, tx, M, K, N, 1, ep, err)

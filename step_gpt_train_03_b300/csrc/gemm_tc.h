@@ -18,16 +18,18 @@ size_t gemm_tc_scratch_floats(size_t M, size_t N);
 
 // out (M,N) = inp (M,K) W(N,K)^T + bias, with epilogue epi (EpiKind): aux is the GELU
 // pre-activation output (EPI_GELU) or the residual input (EPI_RESID).
+// gelu_deriv (EPI_GELU): aux receives gelu'(h) instead of h (for the fused input-gradient
+// product of gemm_tc_backward_dx with gelu_deriv).
 int gemm_tc_forward(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* inp,
                     const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, int N, int K, int epi,
-                    __nv_bfloat16* aux, unsigned* err);
+                    __nv_bfloat16* aux, unsigned* err, bool gelu_deriv = false);
 
 // The same with e4m3 operands (tcgen05 kind::f8f6f4): inp (M,K) and W (N,K) are e4m3 codes,
 // row m of inp stands for codes * inp_deq[m] and W for codes * w_deq[0]; the accumulator
 // is multiplied by both factors before the epilogue.  K a multiple of 16.
 int gemm_tc_forward_fp8(cudaStream_t s, __nv_bfloat16* out, const uint8_t* inp, const float* inp_deq,
                         const uint8_t* W, const float* w_deq, const __nv_bfloat16* bias, int M, int N, int K,
-                        int epi, __nv_bfloat16* aux, unsigned* err);
+                        int epi, __nv_bfloat16* aux, unsigned* err, bool gelu_deriv = false);
 
 // A plain bf16 product with bf16 output: out (M,N) = sum_k A(m,k) B(n,k), each operand
 // K-major (rows of K contiguous) or MN-major (rows of M or N contiguous, K rows); the
@@ -42,10 +44,11 @@ int gemm_tc_bf16(cudaStream_t s, __nv_bfloat16* out, const __nv_bfloat16* A, boo
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation).
 // csum (nullable, EPI_GELU_BWD only): column sums of the stored dinp over each 32-row
 // block, row r of a ceil(M/32) x K fp32 matrix (whose column sums are the bias gradient
-// of the layer that produced the pre-activation).
+// of the layer that produced the pre-activation).  gelu_deriv (EPI_GELU_BWD): aux holds
+// gelu'(h) (from gemm_tc_forward with gelu_deriv), dinp = (dout W) * aux.
 int gemm_tc_backward_dx(cudaStream_t s, __nv_bfloat16* dinp, const __nv_bfloat16* dout,
                         const __nv_bfloat16* W, int M, int N, int K, int epi, const __nv_bfloat16* aux,
-                        float* csum, unsigned* err);
+                        float* csum, unsigned* err, bool gelu_deriv = false);
 
 // dW (N,K) fp32 += dout(M,N)^T inp (M,K); with `assign`, dW = the product (the same
 // values as adding into zeros).

@@ -714,11 +714,11 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
 // the FMA kernel.  `err` (device, nullable) is the error word of bounded waits.
 template <typename T>
 static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T* bias, int M, int N, int K,
-                      int epi, void* aux, unsigned* err) {
+                      int epi, void* aux, unsigned* err, bool gelu_deriv = false) {
     ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias, M, N, K, epi,
-                               (bf16*)aux, err);
+                               (bf16*)aux, err, gelu_deriv);
     } else {
         (void)err;
         EpiArgs ep{out, bias, aux, (long)N};
@@ -738,20 +738,20 @@ static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T*
 // The forward product with e4m3 operands (fp8 mode): A row-scaled codes, W tensor-scaled
 static int mm_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const float* inp_deq, const uint8_t* W,
                           const float* w_deq, const bf16* bias, int M, int N, int K, int epi, bf16* aux,
-                          unsigned* err) {
+                          unsigned* err, bool gelu_deriv = false) {
     ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
-    return gemm_tc_forward_fp8(s, out, inp, inp_deq, W, w_deq, bias, M, N, K, epi, aux, err);
+    return gemm_tc_forward_fp8(s, out, inp, inp_deq, W, w_deq, bias, M, N, K, epi, aux, err, gelu_deriv);
 }
 
 // dinp (M,K) = dout (M,N) W (N,K); epi EPI_STORE or EPI_GELU_BWD (aux = pre-activation of dinp's layer)
 // csum (bf16 only, nullable): see gemm_tc_backward_dx
 template <typename T>
 static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N, int K, int epi,
-                          const T* aux, unsigned* err, float* csum = nullptr) {
+                          const T* aux, unsigned* err, float* csum = nullptr, bool gelu_deriv = false) {
     ProfScope ps(s, PC_MATMUL_BWD_DX, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
-                                   (const bf16*)aux, csum, err);
+                                   (const bf16*)aux, csum, err, gelu_deriv);
     } else {
         (void)err;
         if (csum) return GPT2_EINVAL;
@@ -884,10 +884,12 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
         if (fp8) {
             RC(ln_forward_q8<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C, m->lnq, m->lnq_deq));
             RC(mm_forward_fp8(s, (bf16*)fchg, m->lnq, m->lnq_deq, m->wq_fc + (size_t)l * 4 * C * C, m->wq_deq + m->L + l,
-                              (const bf16*)(P(P_FCB) + l * 4 * C), BT, 4 * C, C, EPI_GELU, (bf16*)fch, m->err));
+                              (const bf16*)(P(P_FCB) + l * 4 * C), BT, 4 * C, C, EPI_GELU, (bf16*)fch, m->err, true));
         } else {
             RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
-            RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err));
+            // bf16: fch keeps gelu'(h) (what the backward needs) instead of h
+            RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err,
+                             sizeof(T) == 2));
         }
         RC(mm_forward<T>(s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2, m->err));
         x = res3;
@@ -978,7 +980,7 @@ static int backward_impl(GPT2* m) {
         const int frows = (int)ceil_div_sz(BT, 32);
         float* fcb_part = sizeof(T) == 2 ? rq.take((size_t)frows * 4 * C) : nullptr;
         RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err,
-                             fcb_part));
+                             fcb_part, sizeof(T) == 2));
         if (fcb_part) rq.push(fcb_part, G(P_FCB) + l * 4 * C, G(P_FCB) + l * 4 * C, nullptr, 4 * C, frows, 4 * C, ow);
         RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err, ow));
         // MLP input projection

@@ -132,6 +132,18 @@ __device__ __forceinline__ float2 gelu2_fast(float2 x) {
     const float2 hx = __fmul2_rn(x, make_float2(0.5f, 0.5f));
     return __ffma2_rn(hx, th, hx);
 }
+// GELU and its derivative together, sharing the tanh (the two functions above and below)
+__device__ __forceinline__ void gelu_and_grad2_fast(float2 x, float2& g, float2& d) {
+    const float2 u = __fmul2_rn(x, x);
+    const float2 a = gelu_arg2(x, u);
+    const float2 th = make_float2(tanh_fast(a.x), tanh_fast(a.y));
+    const float2 one = make_float2(1.0f, 1.0f), half = make_float2(0.5f, 0.5f);
+    const float2 hx = __fmul2_rn(x, half);
+    g = __ffma2_rn(hx, th, hx);
+    const float2 sech2 = __ffma2_rn(make_float2(-th.x, -th.y), th, one);
+    const float2 dg = __ffma2_rn(make_float2(1.5f * GELU_C1, 1.5f * GELU_C1), u, make_float2(0.5f * GELU_K0, 0.5f * GELU_K0));
+    d = __ffma2_rn(__fmul2_rn(x, sech2), dg, __ffma2_rn(half, th, half));
+}
 __device__ __forceinline__ float2 gelu_grad2_fast(float2 x) {
     const float2 u = __fmul2_rn(x, x);
     const float2 g = gelu_arg2(x, u);
