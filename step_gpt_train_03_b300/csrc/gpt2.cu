@@ -714,7 +714,8 @@ static int colsum(cudaStream_t s, float* out, const T* x, int M, int N, float* p
 // the FMA kernel.  `err` (device, nullable) is the error word of bounded waits.
 template <typename T>
 static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T* bias, int M, int N, int K,
-                      int epi, void* aux, unsigned* err, bool gelu_deriv = false) {
+                      int epi, void* aux, unsigned* err, bool gelu_deriv = false, float* scratch = nullptr,
+                      size_t scratch_floats = 0) {
     ProfScope ps(s, PC_MATMUL_FWD, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_forward(s, (bf16*)out, (const bf16*)inp, (const bf16*)W, (const bf16*)bias, M, N, K, epi,
@@ -725,9 +726,15 @@ static int mm_forward(cudaStream_t s, T* out, const T* inp, const T* W, const T*
         cudaError_t e;
         rt_note_launches(1);
         switch (epi) {
-            case EPI_STORE: e = launch_gemm_simt<T, true, true, EPI_STORE>(s, inp, K, W, K, M, N, K, ep); break;
-            case EPI_GELU: e = launch_gemm_simt<T, true, true, EPI_GELU>(s, inp, K, W, K, M, N, K, ep); break;
-            case EPI_RESID: e = launch_gemm_simt<T, true, true, EPI_RESID>(s, inp, K, W, K, M, N, K, ep); break;
+            case EPI_STORE:
+                e = launch_gemm_simt<T, true, true, EPI_STORE>(s, inp, K, W, K, M, N, K, ep, scratch, scratch_floats);
+                break;
+            case EPI_GELU:
+                e = launch_gemm_simt<T, true, true, EPI_GELU>(s, inp, K, W, K, M, N, K, ep, scratch, scratch_floats);
+                break;
+            case EPI_RESID:
+                e = launch_gemm_simt<T, true, true, EPI_RESID>(s, inp, K, W, K, M, N, K, ep, scratch, scratch_floats);
+                break;
             default: return GPT2_EINVAL;
         }
         CK(e);
@@ -747,7 +754,8 @@ static int mm_forward_fp8(cudaStream_t s, bf16* out, const uint8_t* inp, const f
 // csum (bf16 only, nullable): see gemm_tc_backward_dx
 template <typename T>
 static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, int M, int N, int K, int epi,
-                          const T* aux, unsigned* err, float* csum = nullptr, bool gelu_deriv = false) {
+                          const T* aux, unsigned* err, float* csum = nullptr, bool gelu_deriv = false,
+                          float* scratch = nullptr, size_t scratch_floats = 0) {
     ProfScope ps(s, PC_MATMUL_BWD_DX, 2.0 * M * N * K, 0);
     if constexpr (sizeof(T) == 2) {
         return gemm_tc_backward_dx(s, (bf16*)dinp, (const bf16*)dout, (const bf16*)W, M, N, K, epi,
@@ -759,8 +767,10 @@ static int mm_backward_dx(cudaStream_t s, T* dinp, const T* dout, const T* W, in
         cudaError_t e;
         rt_note_launches(1);
         // C(m, k) = sum_n dout[m][n] W[n][k]: A K-contig over n (lda = N), B(k, n) = W[n*K + k]
-        if (epi == EPI_GELU_BWD) e = launch_gemm_simt<T, true, false, EPI_GELU_BWD>(s, dout, N, W, K, M, K, N, ep);
-        else if (epi == EPI_STORE) e = launch_gemm_simt<T, true, false, EPI_STORE>(s, dout, N, W, K, M, K, N, ep);
+        if (epi == EPI_GELU_BWD)
+            e = launch_gemm_simt<T, true, false, EPI_GELU_BWD>(s, dout, N, W, K, M, K, N, ep, scratch, scratch_floats);
+        else if (epi == EPI_STORE)
+            e = launch_gemm_simt<T, true, false, EPI_STORE>(s, dout, N, W, K, M, K, N, ep, scratch, scratch_floats);
         else return GPT2_EINVAL;
         CK(e);
         return GPT2_OK;
@@ -777,14 +787,12 @@ static int mm_backward_dw(cudaStream_t s, float* dW, const T* dout, const T* inp
         return gemm_tc_backward_dw(s, dW, (const bf16*)dout, (const bf16*)inp, M, N, K, partials, partials_floats,
                                    err, assign);
     } else {
-        (void)partials;
-        (void)partials_floats;
         (void)err;
         if (assign) RC(launch_zero(s, dW, (size_t)N * K * sizeof(float)));
         EpiArgs ep{dW, nullptr, nullptr, (long)K};
         // C(n, k) = sum_m dout[m][n] inp[m][k]: A(n, m) = dout[m*N + n], B(k, m) = inp[m*K + k]
         rt_note_launches(1);
-        CK((launch_gemm_simt<T, false, false, EPI_ACC_F32>(s, dout, N, inp, K, N, K, M, ep)));
+        CK((launch_gemm_simt<T, false, false, EPI_ACC_F32>(s, dout, N, inp, K, N, K, M, ep, partials, partials_floats)));
         return GPT2_OK;
     }
 }
@@ -877,10 +885,12 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
                               (const bf16*)(P(P_QKVB) + l * 3 * C), BT, 3 * C, C, EPI_STORE, nullptr, m->err));
         } else {
             RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
-            RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+            RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err,
+                             false, m->partials, m->partials_floats));
         }
         RC(attn_forward<T>(m, s, atty, qkv, l, B, Tn));
-        RC(mm_forward<T>(s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x, m->err));
+        RC(mm_forward<T>(s, res2, atty, P(P_ATTPROJW) + (size_t)l * C * C, P(P_ATTPROJB) + l * C, BT, C, C, EPI_RESID, (void*)x, m->err,
+                         false, m->partials, m->partials_floats));
         if (fp8) {
             RC(ln_forward_q8<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C, m->lnq, m->lnq_deq));
             RC(mm_forward_fp8(s, (bf16*)fchg, m->lnq, m->lnq_deq, m->wq_fc + (size_t)l * 4 * C * C, m->wq_deq + m->L + l,
@@ -889,13 +899,15 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
             RC(ln_forward<T>(s, ln2, m2, r2, res2, P(P_LN2W) + l * C, P(P_LN2B) + l * C, BT, C));
             // bf16: fch keeps gelu'(h) (what the backward needs) instead of h
             RC(mm_forward<T>(s, fchg, ln2, P(P_FCW) + (size_t)l * 4 * C * C, P(P_FCB) + l * 4 * C, BT, 4 * C, C, EPI_GELU, fch, m->err,
-                             sizeof(T) == 2));
+                             sizeof(T) == 2, m->partials, m->partials_floats));
         }
-        RC(mm_forward<T>(s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2, m->err));
+        RC(mm_forward<T>(s, res3, fchg, P(P_FCPROJW) + (size_t)l * 4 * C * C, P(P_FCPROJB) + l * C, BT, C, 4 * C, EPI_RESID, res2, m->err,
+                         false, m->partials, m->partials_floats));
         x = res3;
     }
     RC(ln_forward<T>(s, (T*)m->lnf, m->lnf_mean, m->lnf_rstd, x, P(P_LNFW), P(P_LNFB), BT, C));
-    RC(mm_forward<T>(s, (T*)m->logits, (const T*)m->lnf, P(P_WTE), (const T*)nullptr, BT, m->Vp, C, EPI_STORE, nullptr, m->err));
+    RC(mm_forward<T>(s, (T*)m->logits, (const T*)m->lnf, P(P_WTE), (const T*)nullptr, BT, m->Vp, C, EPI_STORE, nullptr, m->err,
+                     false, m->partials, m->partials_floats));
     if (with_targets) {
         {
             ProfScope ps(s, PC_SOFTMAX_XENT, 0, 2.0 * BT * m->Vp * sizeof(T) + 12.0 * BT);
@@ -955,7 +967,8 @@ static int backward_impl(GPT2* m) {
     rq.n = 0;
     rq.max_w = 0;
     // LM head (tied): dlnf = dlogits wte; dwte += dlogits^T lnf
-    RC(mm_backward_dx<T>(s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr, m->err));
+    RC(mm_backward_dx<T>(s, dbufC, dlogits, P(P_WTE), BT, m->Vp, C, EPI_STORE, nullptr, m->err, nullptr, false,
+                         m->partials, m->partials_floats));
     RC(mm_backward_dw<T>(s, G(P_WTE), dlogits, (const T*)m->lnf, BT, m->Vp, C, m->partials, m->partials_floats, m->err,
                          ow));
     RC(launch_zero(s, dresid, (size_t)BT * C * sizeof(T)));
@@ -980,18 +993,20 @@ static int backward_impl(GPT2* m) {
         const int frows = (int)ceil_div_sz(BT, 32);
         float* fcb_part = sizeof(T) == 2 ? rq.take((size_t)frows * 4 * C) : nullptr;
         RC(mm_backward_dx<T>(s, dfch, dresid, P(P_FCPROJW) + (size_t)l * 4 * C * C, BT, C, 4 * C, EPI_GELU_BWD, fch, m->err,
-                             fcb_part, sizeof(T) == 2));
+                             fcb_part, sizeof(T) == 2, m->partials, m->partials_floats));
         if (fcb_part) rq.push(fcb_part, G(P_FCB) + l * 4 * C, G(P_FCB) + l * 4 * C, nullptr, 4 * C, frows, 4 * C, ow);
         RC(mm_backward_dw<T>(s, G(P_FCPROJW) + (size_t)l * 4 * C * C, dresid, fchg, BT, C, 4 * C, m->partials, m->partials_floats, m->err, ow));
         // MLP input projection
-        RC(mm_backward_dx<T>(s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dx<T>(s, dbufC, dfch, P(P_FCW) + (size_t)l * 4 * C * C, BT, 4 * C, C, EPI_STORE, nullptr, m->err,
+                             nullptr, false, m->partials, m->partials_floats));
         RC(mm_backward_dw<T>(s, G(P_FCW) + (size_t)l * 4 * C * C, dfch, ln2, BT, 4 * C, C, m->partials, m->partials_floats, m->err, ow));
         if (!fcb_part) RC(colsum<T>(s, G(P_FCB) + l * 4 * C, dfch, BT, 4 * C, part, pf, &rq, ow));
         // ln2 (adds into dresid: d res2 = d res3 + LN2 backward)
         RC(ln_backward<T>(s, dresid, G(P_LN2W) + l * C, G(P_LN2B) + l * C, dbufC, res2, P(P_LN2W) + l * C, m2, r2, BT, C, part, pf,
                           G(P_ATTPROJB) + l * C, m->err, &rq, ow));      // d(res2) column sums: attention-projection bias
         // attention output projection (dresid = d res2)
-        RC(mm_backward_dx<T>(s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dx<T>(s, dbufC, dresid, P(P_ATTPROJW) + (size_t)l * C * C, BT, C, C, EPI_STORE, nullptr, m->err,
+                             nullptr, false, m->partials, m->partials_floats));
         RC(mm_backward_dw<T>(s, G(P_ATTPROJW) + (size_t)l * C * C, dresid, atty, BT, C, C, m->partials, m->partials_floats, m->err, ow));
         // attention; in bf16 its output stage also sums the columns of dqkv for the qkv
         // bias gradient (reduced with the other deferred sums)
@@ -1000,7 +1015,8 @@ static int backward_impl(GPT2* m) {
         RC(attn_backward<T>(m, s, dqkv, dbufC, qkv, atty, l, B, Tn, qkvb_part));
         if (qkvb_part) rq.push(qkvb_part, G(P_QKVB) + l * 3 * C, G(P_QKVB) + l * 3 * C, nullptr, 3 * C, qrows, 3 * C, ow);
         // qkv projection
-        RC(mm_backward_dx<T>(s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err));
+        RC(mm_backward_dx<T>(s, dbufC, dqkv, P(P_QKVW) + (size_t)l * 3 * C * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err,
+                             nullptr, false, m->partials, m->partials_floats));
         RC(mm_backward_dw<T>(s, G(P_QKVW) + (size_t)l * 3 * C * C, dqkv, ln1, BT, 3 * C, C, m->partials, m->partials_floats, m->err, ow));
         if (!qkvb_part) RC(colsum<T>(s, G(P_QKVB) + l * 3 * C, dqkv, BT, 3 * C, part, pf, &rq, ow));
         // ln1 (dresid becomes d x_l)
@@ -1630,7 +1646,8 @@ extern "C" int gpt2_matmul_backward_input_gelu(void* dinp, float* dbias, const v
     float* part = dbias ? (float*)scratch : nullptr;
     if (precision == GPT2_FP32) {
         RC(mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_GELU_BWD,
-                                 (const float*)pre, nullptr));
+                                 (const float*)pre, nullptr, nullptr, false, (float*)scratch,
+                                 scratch ? scratch_bytes / sizeof(float) : 0));
         if (dbias) RC(colsum<float>(s, dbias, (const float*)dinp, M, K, part, scratch_bytes / sizeof(float)));
         return GPT2_OK;
     }
@@ -1668,8 +1685,8 @@ extern "C" int gpt2_matmul_backward(void* dinp, float* dweight, float* dbias, co
     size_t pf = scratch_bytes / sizeof(float);
     if (precision == GPT2_FP32) {
         RC(mm_backward_dx<float>(s, (float*)dinp, (const float*)dout, (const float*)weight, M, N, K, EPI_STORE,
-                                 nullptr, nullptr));
-        RC(mm_backward_dw<float>(s, dweight, (const float*)dout, (const float*)inp, M, N, K, nullptr, 0, nullptr));
+                                 nullptr, nullptr, nullptr, false, part, pf));
+        RC(mm_backward_dw<float>(s, dweight, (const float*)dout, (const float*)inp, M, N, K, part, pf, nullptr));
         if (dbias) RC(colsum<float>(s, dbias, (const float*)dout, M, N, part, pf));
         return GPT2_OK;
     }

@@ -116,7 +116,8 @@ def _mm_case(L, M, N, K, precision, seed=0):
     }
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (64, 64, 64), (257, 130, 72), (1000, 768, 768)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (64, 64, 64), (257, 130, 72), (1000, 768, 768),
+                                   (300, 1030, 516)])
 def test_matmul_fp32(L, M, N, K):
     e = _mm_case(L, M, N, K, "fp32")
     assert max(e.values()) < OUT_TOL, e
