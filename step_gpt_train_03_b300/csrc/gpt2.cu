@@ -811,8 +811,7 @@ static int attn_forward(GPT2* m, cudaStream_t s, T* out, const T* qkv, int l, in
         return attention_tc_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, m->err);
     } else {
         float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
-        int rows = B * NH * Tn;
-        launch_pdl(attention_forward_simt<T>, ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s, out, att, qkv, B, Tn, C, NH);
+        launch_pdl(attention_forward_simt<T>, att_simt_grid(B, NH, Tn), ATT_WARPS * 32, 0, s, out, att, qkv, B, Tn, C, NH);
         rt_note_launches(1);
         CK(cudaGetLastError());
         return GPT2_OK;
@@ -833,8 +832,7 @@ static int attn_backward(GPT2* m, cudaStream_t s, T* dqkv, const T* dout, const 
         (void)out;
         (void)bias_partial;
         const float* att = m->att + (size_t)l * m->maxB * NH * m->maxT * m->maxT;
-        int rows = B * NH * Tn;
-        int grid = ceil_div(rows, ATT_WARPS);
+        const int grid = att_simt_grid(B, NH, Tn);
         rt_note_launches(3);
         launch_pdl(attention_backward_ds<T>, grid, ATT_WARPS * 32, 0, s, m->datt, att, dout, qkv, B, Tn, C, NH);
         CK(cudaGetLastError());
@@ -1721,8 +1719,7 @@ extern "C" int gpt2_attention_forward(void* out, float* lse, const void* qkv, in
         return attention_tc_forward(s, (bf16*)out, lse, (const bf16*)qkv, B, Tn, C, NH, err);
     }
     if (precision == GPT2_FP32) {
-        const int rows = B * NH * Tn;
-        launch_pdl(attention_forward_simt<float>, ceil_div(rows, ATT_WARPS), ATT_WARPS * 32, 0, s, 
+        launch_pdl(attention_forward_simt<float>, att_simt_grid(B, NH, Tn), ATT_WARPS * 32, 0, s,
             (float*)out, lse, (const float*)qkv, B, Tn, C, NH);
         rt_note_launches(1);
         CK(cudaGetLastError());
@@ -1773,8 +1770,7 @@ extern "C" int gpt2_attention_backward(void* dqkv, float* dbias, const void* dou
         return GPT2_OK;
     }
     if (precision == GPT2_FP32) {
-        const int rows = B * NH * Tn;
-        const int grid = ceil_div(rows, ATT_WARPS);
+        const int grid = att_simt_grid(B, NH, Tn);
         float* ds = (float*)scratch;
         rt_note_launches(3);
         launch_pdl(attention_backward_ds<float>, grid, ATT_WARPS * 32, 0, s, ds, lse, (const float*)dout, (const float*)qkv, B, Tn, C, NH);
