@@ -55,56 +55,65 @@ __device__ __forceinline__ void epi_apply(const EpiArgs& ep, int m, int n, float
 
 // Tiles of 128 x 128 outputs, 256 threads with 8 x 8 outputs each (rows ty*4 + i and
 // 64 + ty*4 + i, columns likewise, so every shared-memory read is a float4 that the
-// warp reads conflict-free), K in steps of 8 through two shared-memory buffers: the next
-// step's operands are loaded into registers while the current one is multiplied.
+// warp reads conflict-free), K in steps of SG_BK through two shared-memory buffers:
+// the next step's operands are loaded into registers while the current one is
+// multiplied.
 // When the tiles do not fill the SMs, the contraction is split into S ranges of whole
 // K steps: split z writes its fp32 partial tile to scratch and a second kernel adds the
 // S partials in order z = 0..S-1 and applies the epilogue (deterministic).  A product
 // that neither fills the SMs nor splits (K too short, no scratch) runs on 64 x 64 tiles.
 #define SG_BM 128
 #define SG_BN 128
-#define SG_BK 8
+#ifndef SG_BK
+#define SG_BK 16                  // 124M fp32 B4 T64 step: 8.75 ms; 9.40 at 8, 8.97 at 32
+#endif
+#define SG_NL (SG_BK / 8)         // 16-byte packets per thread per operand and K step
 #define SG_PAD 4                  // row padding: conflict-free transposed stores
 #define SG_THREADS 256
 #define SG_MAX_SPLITS 32
+#ifndef SG_SPLIT_BLOCKS
+#define SG_SPLIT_BLOCKS 4         // blocks per SM that the splits aim for
+#endif
 
-// One K step of a 128-row operand tile: 4 elements per thread.  K-contiguous source
-// (X[r * ld + k]): thread t takes row t / 2, k = 4 (t % 2) .. +3; R-contiguous source
-// (X[k * ld + r]): k = t / 32, rows 4 (t % 32) .. +3.  VEC: 16-byte loads (the caller
-// checked alignment, ld % 4 and the contiguous extent % 4); elements past R or K are 0.
+// One K step of a 128-row operand tile: SG_NL packets of 4 elements per thread, packet
+// e = t + 256 l.  K-contiguous source (X[r * ld + k]): row e / (SG_BK / 4), k =
+// 4 (e % (SG_BK / 4)) .. +3; R-contiguous source (X[k * ld + r]): k = e / 32, rows
+// 4 (e % 32) .. +3.  VEC: 16-byte loads (the caller checked alignment, ld % 4 and the
+// contiguous extent % 4); elements past R or K are 0.
 template <typename T, bool KC, bool VEC>
 __device__ __forceinline__ void sg_load(const T* __restrict__ X, long ld, int r0, int R, int k0, int K, int t,
-                                        float (&v)[4]) {
-    if constexpr (KC) {
-        const int r = r0 + (t >> 1), k = k0 + 4 * (t & 1);
+                                        float (&v)[SG_NL][4]) {
+#pragma unroll
+    for (int l = 0; l < SG_NL; l++) {
+        const int e = t + SG_THREADS * l;
+        const int r = r0 + (KC ? e / (SG_BK / 4) : 4 * (e % 32));
+        const int k = k0 + (KC ? 4 * (e % (SG_BK / 4)) : e / 32);
         if constexpr (VEC) {
             float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < R && k < K) q = *reinterpret_cast<const float4*>(X + (size_t)r * ld + k);
-            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+            if (r < R && k < K)
+                q = *reinterpret_cast<const float4*>(X + (KC ? (size_t)r * ld + k : (size_t)k * ld + r));
+            v[l][0] = q.x; v[l][1] = q.y; v[l][2] = q.z; v[l][3] = q.w;
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; i++) v[i] = (r < R && k + i < K) ? to_f32(X[(size_t)r * ld + k + i]) : 0.f;
-        }
-    } else {
-        const int k = k0 + (t >> 5), r = r0 + 4 * (t & 31);
-        if constexpr (VEC) {
-            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (k < K && r < R) q = *reinterpret_cast<const float4*>(X + (size_t)k * ld + r);
-            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; i++) v[i] = (k < K && r + i < R) ? to_f32(X[(size_t)k * ld + r + i]) : 0.f;
+            for (int i = 0; i < 4; i++) {
+                const int ri = KC ? r : r + i, ki = KC ? k + i : k;
+                v[l][i] = (ri < R && ki < K) ? to_f32(X[KC ? (size_t)ri * ld + ki : (size_t)ki * ld + ri]) : 0.f;
+            }
         }
     }
 }
 template <bool KC>
-__device__ __forceinline__ void sg_store(float (*S)[SG_BM + SG_PAD], int t, const float (&v)[4]) {
-    if constexpr (KC) {
-        const int r = t >> 1, k = 4 * (t & 1);
+__device__ __forceinline__ void sg_store(float (*S)[SG_BM + SG_PAD], int t, const float (&v)[SG_NL][4]) {
 #pragma unroll
-        for (int i = 0; i < 4; i++) S[k + i][r] = v[i];
-    } else {
-        *reinterpret_cast<float4*>(&S[t >> 5][4 * (t & 31)]) = make_float4(v[0], v[1], v[2], v[3]);
+    for (int l = 0; l < SG_NL; l++) {
+        const int e = t + SG_THREADS * l;
+        if constexpr (KC) {
+            const int r = e / (SG_BK / 4), k = 4 * (e % (SG_BK / 4));
+#pragma unroll
+            for (int i = 0; i < 4; i++) S[k + i][r] = v[l][i];
+        } else {
+            *reinterpret_cast<float4*>(&S[e / 32][4 * (e % 32)]) = make_float4(v[l][0], v[l][1], v[l][2], v[l][3]);
+        }
     }
 }
 
@@ -122,7 +131,7 @@ gemm_simt_kernel(const T* __restrict__ A, const T* __restrict__ B, int M, int N,
     const int nk = (K + SG_BK - 1) / SG_BK;
     const int kt0 = (int)((long)nk * blockIdx.z / gridDim.z), kt1 = (int)((long)nk * (blockIdx.z + 1) / gridDim.z);
     float acc[8][8] = {};
-    float ra[4], rb[4];
+    float ra[SG_NL][4], rb[SG_NL][4];
     if (kt0 < kt1) {
         sg_load<T, A_KC, VEC>(A, lda, m0, M, kt0 * SG_BK, K, tid, ra);
         sg_load<T, B_KC, VEC>(B, ldb, n0, N, kt0 * SG_BK, K, tid, rb);
@@ -265,14 +274,14 @@ static int sg_num_sms() {
     return n;
 }
 
-// Contraction splits: about two blocks per SM when the tiles alone give fewer, each
-// split at least 16 K steps, bounded by the scratch (S partial M x N tiles)
+// Contraction splits: about SG_SPLIT_BLOCKS blocks per SM when the tiles alone give
+// fewer, each split at least 128 of K, bounded by the scratch (S partial M x N tiles)
 static int sg_splits(int M, int N, int K, size_t scratch_floats) {
     const long tiles = (long)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
-    const long want = 2L * sg_num_sms();
+    const long want = (long)SG_SPLIT_BLOCKS * sg_num_sms();
     if (tiles >= want || scratch_floats == 0) return 1;
     long S = (want + tiles - 1) / tiles;
-    S = std::min<long>(S, ((K + SG_BK - 1) / SG_BK) / 16);
+    S = std::min<long>(S, K / 128);
     S = std::min<long>(S, SG_MAX_SPLITS);
     S = std::min<long>(S, (long)(scratch_floats / ((size_t)M * N)));
     return S > 1 ? (int)S : 1;
