@@ -116,11 +116,35 @@ def _mm_case(L, M, N, K, precision, seed=0):
     }
 
 
+# fp32 shapes reach every form of the FMA product: 64 x 64 tiles (few tiles, no split),
+# 128 x 128 tiles with 16-byte or scalar loads, with and without a split contraction
+# (1000 x 768 x 768 and 300 x 1030 x 516 split the input and weight gradients;
+# 2100 x 1300 x 130 runs the forward on 128 x 128 tiles with scalar loads, unsplit)
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (64, 64, 64), (257, 130, 72), (1000, 768, 768),
-                                   (300, 1030, 516)])
+                                   (300, 1030, 516), (2100, 1300, 130)])
 def test_matmul_fp32(L, M, N, K):
     e = _mm_case(L, M, N, K, "fp32")
     assert max(e.values()) < OUT_TOL, e
+
+
+def test_matmul_fp32_split_is_deterministic(L):
+    """The split contraction adds its partials in a fixed order: two runs agree bit for bit."""
+    import torch
+    M, N, K = 300, 1030, 516
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(M, K, generator=g).cuda()
+    w = torch.randn(N, K, generator=g).cuda()
+    dy = torch.randn(M, N, generator=g).cuda()
+    scratch = torch.empty(L.matmul_backward_scratch_bytes(M, N), dtype=torch.uint8, device="cuda")
+    runs = []
+    for _ in range(2):
+        dx = torch.empty(M, K, device="cuda")
+        dW = torch.zeros(N, K, device="cuda")
+        dB = torch.zeros(N, device="cuda")
+        L.matmul_backward(dx, dW, dB, dy, x, w, "fp32", scratch)
+        torch.cuda.synchronize()
+        runs.append((dx.cpu(), dW.cpu()))
+    assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
 
 
 # bf16: fp32 accumulation of exact bf16 products, output rounded to bf16 (relative 2^-9),
