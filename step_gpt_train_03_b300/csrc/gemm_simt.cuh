@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(256) gemm_simt_splitk_reduce(const float* __re
     epi_apply<T, EPI>(ep, (int)(idx / N), (int)(idx % N), acc);
 }
 
+// SM count of the device current at the first call: it only steers the split choice
 static int sg_num_sms() {
     static const int n = [] {
         int dev = 0, v = 0;

@@ -883,6 +883,8 @@ static int forward_impl(GPT2* m, int B, int Tn, bool with_targets) {
                               (const bf16*)(P(P_QKVB) + l * 3 * C), BT, 3 * C, C, EPI_STORE, nullptr, m->err));
         } else {
             RC(ln_forward<T>(s, ln1, m1, r1, x, P(P_LN1W) + l * C, P(P_LN1B) + l * C, BT, C));
+            // fp32: m->partials doubles as the split-contraction scratch of the FMA products
+            // (every other user of it consumes its partials before the next kernel)
             RC(mm_forward<T>(s, qkv, ln1, P(P_QKVW) + (size_t)l * 3 * C * C, P(P_QKVB) + l * 3 * C, BT, 3 * C, C, EPI_STORE, nullptr, m->err,
                              false, m->partials, m->partials_floats));
         }
