@@ -5,7 +5,7 @@
 // backward.  Per head: S = Q K^T / sqrt(64) over keys j <= t, P = softmax(S), O = P V;
 // the forward keeps O and each row's log-sum-exp only.
 //
-// Forward kernel, persistent, one CTA per SM, 320 threads.  A work item is a pair of
+// Forward kernel, persistent, one CTA per SM, 352 threads.  A work item is a pair of
 // 128-query tiles of one (batch, head): tile 2p+1 (slot A) and tile 2p (slot B), which
 // read the same key / value tiles 0..2p+1 (slot B stops one tile earlier), so each K
 // and V tile is loaded once for both.  Items go heaviest first, dealt to the CTAs in
@@ -13,9 +13,11 @@
 // CTA.
 //   warp 0     TMA producer: the item's Q tiles (double-buffered across items), then
 //              K_j and V_j through a ring of AT_RING slots
-//   warp 1     TMEM owner and MMA issuer: S_X = Q_X K_j^T (M=128, N=128, K=64) into the
-//              slot's S buffer; O_X += P_X V_j (M=128, N=64, K=128) with P_X, the A
-//              operand, read from TMEM (no shared-memory traffic for it)
+//   warp 1     TMEM owner and slot A's MMA issuer, warp 10 slot B's: S_X = Q_X K_j^T
+//              (M=128, N=128, K=64) into the slot's S buffer; O_X += P_X V_j (M=128,
+//              N=64, K=128) with P_X, the A operand, read from TMEM (no shared-memory
+//              traffic for it); one issuing thread per slot, so neither slot's products
+//              wait behind the other's in a single thread's instruction stream
 //   warps 2-5  softmax of slot A, warps 6-9 softmax of slot B: one query row per
 //              thread (the warp's TMEM lane quadrant), all 128 keys of a tile; the row
 //              max is a thread's own, so no exchange between warps
@@ -47,7 +49,8 @@
 #define AT_BN 128                  // keys per tile
 #define AT_RING 6                  // K / V tile slots of the forward
 #define AT_TILE_BYTES (128 * 64 * 2)
-#define AT_THREADS 320             // producer, MMA issuer, 8 compute warps
+#define AT_THREADS 320             // backward: loads, MMA issuer, 8 compute warps
+#define AT_FWD_WARPS 11            // forward: producer, MMA issuer A, 8 softmax warps, MMA issuer B
 #define AT_LOG2E 1.4426950408889634f
 
 #define AT_RESCALE_LOG2 8.0f        // raise a row's exponent reference only past 2^8
@@ -72,7 +75,7 @@ struct AtSmem {
     static_assert(TOTAL <= 232448, "shared memory of one CTA");
 };
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(AT_FWD_WARPS * 32, 1)
 attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmO,
                             float* __restrict__ lse, int B, int Tn, int C, int NH, unsigned* err) {
     using S = AtSmem;
@@ -112,8 +115,8 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
     };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
-        for (int i = 0; i < AT_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 1); }
+        for (int i = 0; i < 2; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 2); }
+        for (int i = 0; i < AT_RING; i++) { mbar_init(&ring_full[i], 1); mbar_init(&ring_empty[i], 2); }
         for (int x = 0; x < 2; x++) {
             mbar_init(&s_full[x], 1);
             mbar_init(&s_free[x], 4);
@@ -121,7 +124,7 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
             mbar_init(&o_done[x], 1);
             mbar_init(&o_free[x], 4);
         }
-        mbar_init(done, 1);
+        mbar_init(done, 2);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmQKV);
@@ -182,13 +185,17 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                     if (clock64() - t0 > TC_WAIT_LIMIT) { raise_error(err, ERRBIT_TIMEOUT); break; }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == AT_FWD_WARPS - 1) {
+        // ------------------------------------------------------------ MMA issuers
+        // warp 1 issues slot A's products, the last warp slot B's: S_x = Q_x K_j^T, then
+        // O_x += P_x V_{j-1}.  Both walk every K / V stage of the item (slot B has one key
+        // tile fewer) and commit the shared ring, Q and done barriers once each (those
+        // count two arrivals), so a stage is released when both slots' products are done.
         if (lane == 0) {
+            const int x = warp == 1 ? 0 : 1;
             constexpr uint32_t IDESC_S = idesc_bf16(AT_BM, AT_BN, false, false);
             constexpr uint32_t IDESC_O = idesc_bf16(AT_BM, AT_HS, false, true);
-            int rc = 0;
-            int sn[2] = {0, 0}, pn[2] = {0, 0}, nitems[2] = {0, 0};   // per slot: S, P V, items so far
+            int rc = 0, sn = 0, pn = 0, nitems = 0;      // this slot's S, P V, items so far
             bool ok = true;
             for (int k = 0; ok; k++) {
                 const int it = item_at(k);
@@ -196,20 +203,19 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                 int p, bh, nkx[2];
                 decode(it, p, bh, nkx[0], nkx[1]);
                 const int nk = nkx[0] ? nkx[0] : nkx[1];
+                const int nkm = nkx[x];                      // this slot's key tiles (0: none)
                 const int qb = k & 1;
                 if (!mbar_wait(&q_full[qb], (k >> 1) & 1, abort_flag, err)) break;
-                // K_j at ring index rc + 2j, V_j at rc + 2j + 1.  Order per j: S_A(j), S_B(j),
-                // then O_A += P_A(j-1) V_{j-1}, O_B += P_B(j-1) V_{j-1}
+                // K_j at ring index rc + 2j, V_j at rc + 2j + 1.  Order per j: S_x(j), then
+                // O_x += P_x(j-1) V_{j-1}
                 for (int j = 0; j <= nk && ok; j++) {
                     if (j < nk) {
                         const int kidx = rc + 2 * j, ks = kidx % AT_RING;
                         if (!mbar_wait(&ring_full[ks], (kidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
-                        const uint32_t k_addr = smem_u32(smem + S::RING_OFF + ks * AT_TILE_BYTES);
-                        #pragma unroll
-                        for (int x = 0; x < 2; x++) {
-                            if (j >= nkx[x]) continue;
-                            if (!mbar_wait(&s_free[x], (sn[x] & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+                        if (j < nkm) {
+                            if (!mbar_wait(&s_free[x], (sn & 1) ^ 1, abort_flag, err)) { ok = false; break; }
                             tc_fence_after();
+                            const uint32_t k_addr = smem_u32(smem + S::RING_OFF + ks * AT_TILE_BYTES);
                             const uint32_t q_addr = smem_u32(smem + S::Q_OFF + (qb * 2 + x) * AT_TILE_BYTES);
                             // descriptors of step kk: the start address field (bytes / 16) advances by 2
                             const uint64_t qd = sdesc(q_addr, 16, 1024), kd = sdesc(k_addr, 16, 1024);
@@ -217,40 +223,34 @@ attention_tc_forward_kernel(const __grid_constant__ CUtensorMap tmQKV, const __g
                             for (int kk = 0; kk < AT_HS / 16; kk++)
                                 tc_mma(TM_S(x), qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
                             tc_commit(&s_full[x]);
-                            sn[x]++;
+                            sn++;
                         }
-                        if (!ok) break;
-                        tc_commit(&ring_empty[ks]);                      // K_j read by both products
-                        if (j == nk - 1) tc_commit(&q_empty[qb]);        // the item's Q tiles too
+                        tc_commit(&ring_empty[ks]);                  // K_j read by this slot's products
+                        if (j == nk - 1) tc_commit(&q_empty[qb]);    // and its Q tile
                     }
                     if (j >= 1) {
                         const int jj = j - 1;
                         const int vidx = rc + 2 * jj + 1, vs = vidx % AT_RING;
                         if (!mbar_wait(&ring_full[vs], (vidx / AT_RING) & 1, abort_flag, err)) { ok = false; break; }
-                        const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vs * AT_TILE_BYTES);
-                        #pragma unroll
-                        for (int x = 0; x < 2; x++) {
-                            if (jj >= nkx[x]) continue;
-                            if (!mbar_wait(&p_full[x], pn[x] & 1, abort_flag, err)) { ok = false; break; }
+                        if (jj < nkm) {
+                            if (!mbar_wait(&p_full[x], pn & 1, abort_flag, err)) { ok = false; break; }
                             // the first P V of an item overwrites O: its last readout must be done
-                            if (jj == 0 && nitems[x] > 0 &&
-                                !mbar_wait(&o_free[x], (nitems[x] - 1) & 1, abort_flag, err)) { ok = false; break; }
+                            if (jj == 0 && nitems > 0 &&
+                                !mbar_wait(&o_free[x], (nitems - 1) & 1, abort_flag, err)) { ok = false; break; }
                             tc_fence_after();
+                            const uint32_t v_addr = smem_u32(smem + S::RING_OFF + vs * AT_TILE_BYTES);
                             const uint64_t vd = sdesc(v_addr, 8192, 1024);    // step kk: + 2048 bytes
 #pragma unroll
                             for (int kk = 0; kk < AT_BN / 16; kk++)
                                 tc_mma_ts(TM_O(x), TM_P(x) + kk * 8, vd + 128 * kk, IDESC_O,
                                           (jj > 0 || kk > 0) ? 1u : 0u);
                             tc_commit(&o_done[x]);
-                            pn[x]++;
+                            pn++;
                         }
-                        if (!ok) break;
                         tc_commit(&ring_empty[vs]);
                     }
                 }
-                #pragma unroll
-                for (int x = 0; x < 2; x++)
-                    if (nkx[x]) nitems[x]++;
+                if (nkm) nitems++;
                 rc += 2 * nk;
             }
             tc_commit(done);
@@ -939,7 +939,7 @@ int attention_tc_forward(cudaStream_t s, __nv_bfloat16* out, float* lse, const _
     if (!make_map3(&tq, qkv, 3 * C, Tn, B, 3 * C) || !make_map3(&to, out, C, Tn, B, C)) return GPT2_EUNSUPPORTED;
     const int items = ((Tn + AT_BM - 1) / AT_BM + 1) / 2 * B * NH;      // pairs of query tiles
     const int grid = items < g_sms ? items : g_sms;
-    launch_pdl(attention_tc_forward_kernel, grid, AT_THREADS, AtSmem::TOTAL, s, tq, to, lse, B, Tn, C, NH, err);
+    launch_pdl(attention_tc_forward_kernel, grid, AT_FWD_WARPS * 32, AtSmem::TOTAL, s, tq, to, lse, B, Tn, C, NH, err);
     rt_note_launches(1);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ECUDA;
 }
