@@ -169,7 +169,8 @@ ATT_TOL = 2e-2
 @pytest.mark.parametrize("B,T,NH,C,precision", [(2, 64, 4, 256, "bf16"), (1, 200, 2, 128, "bf16"),
                                                 (2, 1024, 12, 768, "bf16"), (3, 37, 2, 128, "bf16"),
                                                 (2, 131, 1, 64, "bf16"), (1, 1, 1, 64, "bf16"),
-                                                (2, 40, 4, 64, "fp32"), (1, 129, 2, 128, "fp32")])
+                                                (2, 40, 4, 64, "fp32"), (1, 129, 2, 128, "fp32"),
+                                                (1, 70, 1, 128, "fp32"), (2, 33, 1, 8, "fp32")])
 def test_attention_forward_backward(L, B, T, NH, C, precision):
     import torch
     rng = np.random.default_rng(B * 1000 + T)
